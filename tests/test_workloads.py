@@ -1,0 +1,56 @@
+"""The mask generators encode each family's semantics exactly.
+
+The dense expansion of the generated vectors (the oracle's 1x1 tile map) must
+equal the family's semantic predicate, built from the drawn structure.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from sparse_masked_attention_gb300 import workloads as W
+
+
+@pytest.mark.parametrize("name", sorted(W.CONFIGS))
+def test_config_mask_matches_semantics(name):
+    cfg = W.CONFIGS[name]
+    N = min(cfg["N"], 3000)
+    mask = W.make_mask(cfg, seed=0, N=N, B=min(cfg["B"], 2))
+    for b in range(len(mask.meta)):
+        cls, visible = oracle.tilemap(N, mask.slice(b), mask.causal, tq=1, tk=1)
+        sem = W.dense_semantic(mask, b)
+        np.testing.assert_array_equal(cls == oracle.TILE_SKIP, sem)
+        assert not sem.all(axis=1).any()
+
+
+def test_three_documents_partition():
+    rng = np.random.default_rng(0)
+    lens = W.three_documents(rng, 256)
+    assert len(lens) == 3 and sum(lens) == 256 and min(lens) >= 1
+
+
+def test_uniform_lengths_cover_exactly():
+    rng = np.random.default_rng(0)
+    lens = W.uniform_lengths(rng, 512, 4096, 8192)
+    assert sum(lens) == 8192 and all(1 <= x <= 4096 for x in lens)
+    assert all(x >= 512 for x in lens[:-1])
+
+
+def test_block_sparse_fraction_near_target():
+    N = 128 * 64
+    mask = W.block_sparse(N, np.random.default_rng(0))
+    runs = mask.meta[0]["runs"]
+    masked = sum((r1[1] - r1[0]) + (r2[1] - r2[0]) for r1, r2 in runs)
+    cand = sum(64 - 1 - kb for kb in range(64))
+    assert abs(masked / cand - 0.3) < 0.02
+    # the diagonal block is never masked
+    for kb, (r1, r2) in enumerate(runs):
+        assert r1[0] > kb or r1[0] == r1[1]
+        assert r2[0] > kb or r2[0] == r2[1]
+
+
+def test_inputs_are_seeded():
+    a = W.make_inputs(1, 16, 2, 8, 8, seed=3)
+    b = W.make_inputs(1, 16, 2, 8, 8, seed=3)
+    for x, y in zip(a, b):
+        assert x.dtype.is_floating_point and x.shape[-1] == 8
+        assert bool((x == y).all())
