@@ -1,0 +1,435 @@
+"""Benchmark: effective TFLOP/s of masked attention (forward + backward) on GB300.
+
+One step is one pass of the whole path over one batch: the tile map, the
+forward, and the backward (tile map, preprocess, key-side and query-side
+gradient kernels).  Effective FLOPs count unmasked (i, j) pairs only:
+2(d+dv) per pair for the forward and 8d+6dv per pair for forward + backward.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+    python bench.py --impl reference ...   # the fp64 CPU oracle, timed on host cores
+
+Under torchrun every rank runs an independent replica of the workload (the
+path shards over (batch, head) with no exchange).  The value is the total
+over all ranks, divided by the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+DEFAULT_WORKLOAD = "share_question"
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--fwd-only", action="store_true", help="time the forward pass alone")
+    return ap.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi samples during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, flag in zip(names, parts[5:9]):
+                if flag.lower() == "active":
+                    reasons.add(n)
+        sm.sort()
+        return {"sm_mhz": sm[len(sm) // 2] if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- workload
+def flops_per_pair(d, dv):
+    return {"fwd": 2 * (d + dv), "bwd": 2 * (3 * d + 2 * dv), "fwd+bwd": 8 * d + 6 * dv}
+
+
+def kernel_names(d, dv):
+    fwd = ["classify", "lists", "fwd"]
+    bwd = ["classify", "lists", "bwd_preprocess"]
+    bwd += ["bwd_dkdv_dv", "bwd_dkdv_dk"] if (d == 256 and dv == 256) else ["bwd_dkdv"]
+    bwd += ["bwd_dq"]
+    return fwd, bwd
+
+
+def kernel_alg_flops_per_pair(name, d, dv):
+    """Algorithmic FLOPs per unmasked pair credited to each kernel.  The
+    key-side kernel does the S/dP recomputation and the dK/dV products the
+    backward needs once; the query-side kernel is credited with dQ only (its S
+    and dP are a second recomputation)."""
+    return {"fwd": 2 * (d + dv), "bwd_dkdv": 2 * (2 * d + 2 * dv), "bwd_dq": 2 * d,
+            "bwd_dkdv_dv": 2 * (d + dv) + 2 * dv, "bwd_dkdv_dk": 2 * d + 2 * dv + 2 * d}.get(name, 0)
+
+
+def setup(cfg, seed, device):
+    import torch
+    from sparse_masked_attention_gb300 import attention as fm
+    from sparse_masked_attention_gb300 import workloads as W
+    B, H, N, d, dv = cfg["B"], cfg["H"], cfg["N"], cfg["d"], cfg["dv"]
+    q, k, v, do = W.make_inputs(B, N, H, d, dv, seed=seed, device=device)
+    mask = W.make_mask(cfg, seed=seed)
+    vec = [None if getattr(mask, n) is None else torch.from_numpy(getattr(mask, n)).to(device)
+           for n in ("lts", "lte", "uts", "ute")]
+    U = fm.count_unmasked(N, B, H, *vec, causal=mask.causal, device=device)
+    torch.cuda.synchronize()
+    u_heads = int(U.sum().item()) * H  # one mask per sample, shared by the H heads
+    return q, k, v, do, mask, vec, u_heads
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+    from sparse_masked_attention_gb300 import attention as fm
+    from sparse_masked_attention_gb300 import workloads as W
+
+    torch.cuda.set_device(local_rank)
+    device = torch.device("cuda", local_rank)
+    cfg = dict(W.CONFIGS[args.workload])
+    B, H, N, d, dv = cfg["B"], cfg["H"], cfg["N"], cfg["d"], cfg["dv"]
+    has_bwd = "bwd" in cfg["passes"] and not args.fwd_only
+    det = bool(cfg.get("deterministic", False))
+    q, k, v, do, mask, vec, U = setup(cfg, seed=rank, device=device)
+    fpp = flops_per_pair(d, dv)
+    step_flops = U * (fpp["fwd+bwd"] if has_bwd else fpp["fwd"])
+    fwd_names, bwd_names = kernel_names(d, dv)
+
+    o = torch.empty((B, N, H, dv), dtype=torch.bfloat16, device=device)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=device)
+    dq, dk, dvv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws_f = torch.empty(fm.workspace_size(B, H, 1, N, d, dv, False), dtype=torch.uint8,
+                       device=device)
+    ws_b = torch.empty(fm.workspace_size(B, H, 1, N, d, dv, True, det), dtype=torch.uint8,
+                       device=device)
+    stream = torch.cuda.current_stream()
+
+    def make_events(n):
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+        for e in evs:
+            e.record(stream)  # creates the underlying cudaEvent_t
+        return evs
+
+    K = args.steps
+    ev_f = [make_events(2 * len(fwd_names)) for _ in range(K)]
+    ev_b = [make_events(2 * len(bwd_names)) for _ in range(K)] if has_bwd else []
+    torch.cuda.synchronize()
+    opt_f = [fm.make_options(kernel_events=[e.cuda_event for e in evs]) for evs in ev_f]
+    opt_b = [fm.make_options(det, kernel_events=[e.cuda_event for e in evs]) for evs in ev_b]
+    plain_f = fm.make_options()
+    plain_b = fm.make_options(det)
+
+    def step(i=None):
+        fm.fwd(q, k, v, *vec, causal=mask.causal, out=o, lse=lse, workspace=ws_f,
+               options=plain_f if i is None else opt_f[i])
+        if has_bwd:
+            fm.bwd(q, k, v, o, lse, do, *vec, causal=mask.causal, deterministic=det, dq=dq,
+                   dk=dk, dv=dvv, workspace=ws_b, options=plain_b if i is None else opt_b[i])
+
+    for _ in range(args.warmup):
+        step()
+    fm.get_error()
+
+    sampler = ClockSampler(local_rank) if rank == 0 else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.5)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    start.record(stream)
+    for i in range(K):
+        step(i)
+    end.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop() if sampler else None
+    fm.get_error()
+    ms_total = start.elapsed_time(end)
+    if world > 1:
+        t = torch.tensor([ms_total], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_total = float(t.item())
+    ms_step = ms_total / K
+
+    # per-kernel durations from the library's event pairs
+    per_kernel = {}
+    for evs_list, names in ((ev_f, fwd_names), (ev_b, bwd_names)):
+        for evs in evs_list:
+            for j, name in enumerate(names):
+                key = ("fwd:" if names is fwd_names else "bwd:") + name
+                per_kernel.setdefault(key, []).append(evs[2 * j].elapsed_time(evs[2 * j + 1]))
+    avg = {k_: sum(v_) / len(v_) for k_, v_ in per_kernel.items()}
+    dominant = max(avg, key=avg.get)
+    dom_name = dominant.split(":", 1)[1]
+    pk, src = peaks()
+    alg = U * kernel_alg_flops_per_pair(dom_name, d, dv)
+    achieved = alg / (avg[dominant] * 1e-3) / 1e12
+    roofline = {"bound": "tensor", "kernel": dom_name, "achieved": round(achieved, 2),
+                "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": round(achieved / pk["bf16_tflops"], 4),
+                "frac_sustained": round(achieved / pk["bf16_tflops_sustained"], 4),
+                "peak_source": f"{src} burst bf16 (sustained {pk['bf16_tflops_sustained']})",
+                "traffic": None, "avg_ms": round(avg[dominant], 4)}
+
+    # forward alone, same inputs (event pairs of the forward calls)
+    fwd_ms = sum(avg[f"fwd:{n}"] for n in fwd_names)
+    value = step_flops / (ms_step * 1e-3) / 1e12 * world
+    launches = K * (len(fwd_names) + (len(bwd_names) if has_bwd else 0))
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(q, k, v, do, vec, mask, cfg, has_bwd, det, args, step_flops, world, device)
+
+    result = {
+        "metric": "masked-attn effective TFLOP/s fwd+bwd" if has_bwd else
+                  "masked-attn effective TFLOP/s fwd",
+        "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": args.workload, "B": B, "H": H, "N": N, "d": d, "dv": dv,
+                   "mask": cfg["mask"], "passes": "fwd+bwd" if has_bwd else "fwd",
+                   "deterministic": det, "unmasked_pairs": U,
+                   "l2": "inputs larger than L2 (q, k, v, dO each "
+                         f"{B * N * H * d * 2 / 2**20:.0f} MiB > 129 MB)",
+                   "parallelism": f"replicas x{world}"},
+        "fwd_tflops": round(U * fpp["fwd"] / (fwd_ms * 1e-3) / 1e12, 3),
+        "fwd_frac_of_peak": round(U * fpp["fwd"] / (fwd_ms * 1e-3) / 1e12 / pk["bf16_tflops"], 4),
+        "frac_of_peak": round(value / world / pk["bf16_tflops"], 4),
+        "kernel_ms": {k_: round(v_, 4) for k_, v_ in avg.items()},
+        "roofline": roofline,
+        "gpu_launches": launches,
+        "clocks": clocks,
+        "e2e": e2e,
+    }
+    return result
+
+
+def run_e2e(q, k, v, do, vec, mask, cfg, has_bwd, det, args, step_flops, world, device):
+    """Same step through the public API with pinned host buffers; the H2D copies
+    of q, k, v, dO and the mask vectors and the D2H read of the results are
+    inside the timed region."""
+    import torch
+    from sparse_masked_attention_gb300 import attention as fm
+    host_in = [t.cpu().pin_memory() for t in (q, k, v, do)]
+    host_vec = [None if t is None else t.cpu().pin_memory() for t in vec]
+    dev_in = [torch.empty_like(t) for t in (q, k, v, do)]
+    dev_vec = [None if t is None else torch.empty_like(t) for t in vec]
+    outs_dev = None
+    h2d = sum(t.numel() * t.element_size() for t in host_in[: (4 if has_bwd else 3)])
+    h2d += sum(t.numel() * t.element_size() for t in host_vec if t is not None)
+    B, H, N, d, dv = cfg["B"], cfg["H"], cfg["N"], cfg["d"], cfg["dv"]
+    out_shapes = [(B, N, H, dv)] + ([(B, N, H, d), (B, N, H, d), (B, N, H, dv)] if has_bwd else [])
+    host_out = [torch.empty(s, dtype=torch.bfloat16).pin_memory() for s in out_shapes]
+    d2h = sum(t.numel() * t.element_size() for t in host_out)
+
+    def step():
+        for hsrc, ddst in zip(host_in, dev_in):
+            ddst.copy_(hsrc, non_blocking=True)
+        for hsrc, ddst in zip(host_vec, dev_vec):
+            if hsrc is not None:
+                ddst.copy_(hsrc, non_blocking=True)
+        o, lse = fm.fwd(dev_in[0], dev_in[1], dev_in[2], *dev_vec, causal=mask.causal)
+        outs = [o]
+        if has_bwd:
+            outs += list(fm.bwd(dev_in[0], dev_in[1], dev_in[2], o, lse, dev_in[3], *dev_vec,
+                                causal=mask.causal, deterministic=det))
+        for hdst, dsrc in zip(host_out, outs):
+            hdst.copy_(dsrc, non_blocking=True)
+
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    K = max(1, min(args.steps, 5))
+    s.record()
+    for _ in range(K):
+        step()
+    e.record()
+    torch.cuda.synchronize()
+    ms = s.elapsed_time(e) / K
+    return {"value": round(step_flops / (ms * 1e-3) / 1e12 * world, 3), "unit": "TFLOP/s",
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "ms_per_step": round(ms, 3)}
+
+
+# ----------------------------------------------------------- CPU (oracle) side
+def oracle_sample(cfg, n_rows, seed=0):
+    """Leading n x n block of (batch 0, head 0).  The sample's mask is the
+    workload's own mask restricted to rows and keys [0, n)."""
+    import numpy as np
+    from sparse_masked_attention_gb300 import workloads as W
+    d, dv = cfg["d"], cfg["dv"]
+    N = cfg["N"]
+    n = min(n_rows, N)
+    mask = W.make_mask(cfg, seed=seed)
+    sl = mask.slice(0)
+    sub = {k_: (None if v_ is None else np.ascontiguousarray(v_[:n])) for k_, v_ in sl.items()}
+    rng = np.random.default_rng(seed)
+    to_bf16 = lambda a: (a.astype(np.float32).view(np.uint32) & 0xFFFF0000).view(np.float32)
+    q, k, v, do = (to_bf16(rng.standard_normal((n, c))).astype(np.float64)
+                   for c in (d, d, dv, dv))
+    return q, k, v, do, sub, mask.causal, n
+
+
+def time_oracle(cfg, n_rows, has_bwd):
+    import oracle
+    q, k, v, do, sub, causal, n = oracle_sample(cfg, n_rows)
+    d, dv = cfg["d"], cfg["dv"]
+    U = oracle.count_unmasked(n, sub, causal)
+    t0 = time.perf_counter()
+    oracle.attention_fwd(q, k, v, sub, causal)
+    if has_bwd:
+        oracle.attention_bwd(q, k, v, do, sub, causal)
+    dt = time.perf_counter() - t0
+    fpp = flops_per_pair(d, dv)["fwd+bwd" if has_bwd else "fwd"]
+    return U * fpp / dt / 1e12, dt, U, n
+
+
+def cpu_baseline(cfg, has_bwd, n_rows=8192):
+    import oracle
+    tflops, dt, U, n = time_oracle(cfg, n_rows, has_bwd)
+    return {"value": round(tflops, 6), "unit": "TFLOP/s", "cores": oracle.num_threads(),
+            "kind": "oracle",
+            "sample": f"leading {n}x{n} block of batch 0, head 0 ({U} unmasked pairs), "
+                      f"{'fwd+bwd' if has_bwd else 'fwd'} in fp64, {dt:.2f} s"}
+
+
+def run_reference(args):
+    from sparse_masked_attention_gb300 import workloads as W
+    import oracle
+    cfg = dict(W.CONFIGS[args.workload])
+    has_bwd = "bwd" in cfg["passes"] and not args.fwd_only
+    n_rows = 4096
+    for _ in range(args.warmup):
+        time_oracle(cfg, 1024, has_bwd)
+    total_t, total_f = 0.0, 0.0
+    U = n = 0
+    for _ in range(args.steps):
+        tflops, dt, U, n = time_oracle(cfg, n_rows, has_bwd)
+        total_t += dt
+        total_f += tflops * 1e12 * dt
+    value = total_f / total_t / 1e12
+    line = {
+        "impl": "reference",
+        "metric": "masked-attn effective TFLOP/s fwd+bwd" if has_bwd else
+                  "masked-attn effective TFLOP/s fwd",
+        "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(total_t / args.steps * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": args.workload, "B": cfg["B"], "H": cfg["H"], "N": cfg["N"],
+                   "d": cfg["d"], "dv": cfg["dv"], "mask": cfg["mask"],
+                   "passes": "fwd+bwd" if has_bwd else "fwd"},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s",
+                         "cores": oracle.num_threads(), "kind": "oracle",
+                         "sample": f"each step: leading {n}x{n} block of batch 0, head 0 "
+                                   f"({U} unmasked pairs)"},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    return line
+
+
+def main():
+    args = parse()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+    import torch
+    import torch.distributed as dist
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    result = run_ours(args, rank, world, local_rank)
+    if rank == 0 and not args.no_cpu_baseline:
+        from sparse_masked_attention_gb300 import workloads as W
+        cfg = W.CONFIGS[args.workload]
+        result["cpu_baseline"] = cpu_baseline(cfg, "bwd" in cfg["passes"] and not args.fwd_only)
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,161 @@
+/*
+ * flashmask.h -- C ABI of libflashmask: exact masked attention with a
+ * column-wise sparse mask, forward and backward, on one sm_103a GPU.
+ *
+ * Method (FlashMask README, "Formulation"):
+ *     O = softmax(Q K^T * scale + M) V,      scale = 1/sqrt(d) by default,
+ * d is the head dim of Q and K; V may have its own head dim dv.
+ *
+ * Mask (FlashMask README, "Overview"; FlashMask-3 abstract): for every key
+ * column j, four int32 query-row boundaries LTS_j, LTE_j, UTS_j, UTE_j.
+ * Query row i is masked in column j (M_ij = -inf) when
+ *     LTS_j <= i < LTE_j   or   UTS_j <= i < UTE_j   or   (causal and i < j).
+ * Boundaries are clamped to [0, N], which does not change the mask; start >= end
+ * is an empty interval.  A NULL pair (both pointers NULL) is an empty interval;
+ * exactly one NULL pointer of a pair is an error.
+ *
+ * Sparsity skipping ("FlashMask: Efficient and Rich Mask Extension of
+ * FlashAttention", abstract): 128 x 128 tiles whose elements are all masked are
+ * never computed, and the result is exact.
+ *
+ * Conventions shared by every entry point:
+ *   - Device pointers are owned by the caller.  The library never allocates,
+ *     frees or synchronises, except flashmask_get_error, which synchronises
+ *     its stream.
+ *   - Work is enqueued on `stream` (a cudaStream_t, NULL = legacy default
+ *     stream), and the call returns at once.
+ *   - Errors are returned as fm_status; nothing is thrown and nothing is
+ *     printed.
+ *   - Layouts, row-major and contiguous:
+ *       q, k: [B, N, H, d] bf16;  v, o, dout, dv: [B, N, H, dv] bf16;
+ *       dq, dk: [B, N, H, d] bf16;  lse: [B, H, N] fp32 (natural log);
+ *       mask vectors: [B, Hm, N] int32 with Hm in {1, H}.  Hm = 1 shares one
+ *       mask among all heads; otherwise head h uses mask head h.
+ *   - Pointers must be 16-byte aligned.
+ *   - Rows whose every key is masked give O = 0 and LSE = -inf, and they add
+ *     nothing to any gradient.
+ *   - Supported (d, dv): (64, 64), (128, 128), (192, 128), (256, 256).
+ *   - Nq = Nk = N.  1 <= N <= 2^24.
+ */
+#ifndef FLASHMASK_H
+#define FLASHMASK_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    FM_OK = 0,
+    FM_ERR_INVALID_ARG = 1,     /* NULL/unaligned pointer, bad size or flag        */
+    FM_ERR_UNSUPPORTED = 2,     /* (d, dv) pair or device not supported            */
+    FM_ERR_WORKSPACE = 3,       /* workspace NULL, unaligned or smaller than needed */
+    FM_ERR_CUDA = 4,            /* a CUDA runtime/driver call failed               */
+    FM_ERR_DEVICE_TIMEOUT = 5   /* a kernel gave up on a bounded wait              */
+} fm_status;
+
+/* Problem shape.  scale <= 0 selects the default 1/sqrt(d). */
+typedef struct {
+    int B, H, Hm, N, d, dv;
+    float scale;
+    int causal;
+} fm_problem;
+
+/* Options.  deterministic: the backward adds every partial sum in a fixed
+ * order, so dQ/dK/dV are bit-identical from run to run.  debug_bounds is
+ * reserved and must be 0.  wait_timeout_ns bounds every wait on the device;
+ * 0 selects 1 s.
+ * kernel_events (optional, may be NULL): an array of n_kernel_events
+ * cudaEvent_t handles owned by the caller.  The call records
+ * kernel_events[2i] on `stream` just before its i-th kernel launch and
+ * kernel_events[2i+1] just after it.  Events beyond the array are skipped.
+ * Kernel order: fwd = classify, lists, attention; bwd = classify, lists,
+ * preprocess, key-side gradient (twice when d = dv = 256), query-side gradient.
+ * A NULL options pointer selects all defaults. */
+typedef struct {
+    int deterministic;
+    int debug_bounds;
+    unsigned long long wait_timeout_ns;
+    void **kernel_events;
+    int n_kernel_events;
+} fm_options;
+
+/* Tile classes written by flashmask_classify (128 x 128 tiles). */
+#define FM_TILE_SKIP 0      /* every in-range element masked */
+#define FM_TILE_PARTIAL 1   /* some, not all, masked         */
+#define FM_TILE_UNMASKED 2  /* no element masked             */
+
+/*
+ * Bytes of device workspace that flashmask_fwd (is_bwd = 0),
+ * flashmask_bwd (is_bwd = 1), flashmask_classify and flashmask_count_unmasked
+ * need for this problem.  Returns 0 for an invalid problem.
+ * The workspace must be 256-byte aligned.
+ */
+size_t flashmask_workspace_size(const fm_problem *p, const fm_options *opt, int is_bwd);
+
+/*
+ * Forward (FlashMask README, "Formulation").  Writes o [B,N,H,dv] bf16 and
+ * lse [B,H,N] fp32, with LSE_i = log sum_j exp(scale q_i.k_j + M_ij).
+ * Tiles that are fully masked are skipped, and the mask is applied only on
+ * partial tiles.
+ */
+fm_status flashmask_fwd(const fm_problem *p, const fm_options *opt,
+                        const void *q, const void *k, const void *v,
+                        const int32_t *lts, const int32_t *lte,
+                        const int32_t *uts, const int32_t *ute,
+                        void *o, float *lse,
+                        void *workspace, size_t ws_bytes, void *stream);
+
+/*
+ * Backward, the derivative of the forward above.  P is rebuilt from lse.
+ * o and lse must be the forward's outputs for the same inputs.  dout has the
+ * layout of o.  Writes dq, dk [B,N,H,d] and dv [B,N,H,dv] bf16.  These are the
+ * gradients of sum(dout * O) with respect to q, k and v.
+ */
+fm_status flashmask_bwd(const fm_problem *p, const fm_options *opt,
+                        const void *q, const void *k, const void *v,
+                        const void *o, const float *lse, const void *dout,
+                        const int32_t *lts, const int32_t *lte,
+                        const int32_t *uts, const int32_t *ute,
+                        void *dq, void *dk, void *dv,
+                        void *workspace, size_t ws_bytes, void *stream);
+
+/*
+ * Tile map (the sparsity-skipping step of the FlashMask abstract).  Writes
+ * tile_class [B*Hm, T, T] uint8 with T = ceil(N/128).  Entry [bm, qt, kt]
+ * gives the class of query rows [128 qt, 128 qt + 128) and key columns
+ * [128 kt, 128 kt + 128), counting only elements inside [0, N).
+ */
+fm_status flashmask_classify(const fm_problem *p,
+                             const int32_t *lts, const int32_t *lte,
+                             const int32_t *uts, const int32_t *ute,
+                             uint8_t *tile_class,
+                             void *workspace, size_t ws_bytes, void *stream);
+
+/*
+ * Number of unmasked (i, j) pairs of each mask head, summed over all columns.
+ * Writes counts [B*Hm] uint64 (device memory).  This is the work the
+ * effective-FLOP figures count.
+ */
+fm_status flashmask_count_unmasked(const fm_problem *p,
+                                   const int32_t *lts, const int32_t *lte,
+                                   const int32_t *uts, const int32_t *ute,
+                                   unsigned long long *counts, void *stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the library's device error
+ * word.  Returns FM_ERR_DEVICE_TIMEOUT if a kernel gave up on a bounded wait
+ * since the last call, FM_ERR_CUDA if the stream itself failed, else FM_OK.
+ */
+fm_status flashmask_get_error(void *stream);
+
+/* Static text for a status code. */
+const char *flashmask_error_string(fm_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FLASHMASK_H */

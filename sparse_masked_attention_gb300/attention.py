@@ -1,0 +1,198 @@
+"""PyTorch front end over the C ABI.
+
+torch supplies device memory and the current stream; the work runs in the
+CUDA library through ``binding``.  Layouts follow the C ABI:
+q, k ``[B, N, H, d]``; v ``[B, N, H, dv]`` (bf16, contiguous); mask vectors
+``[B, Hm, N]`` int32 with ``Hm`` in ``{1, H}``; lse ``[B, H, N]`` fp32.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+from typing import Optional
+
+import torch
+
+from . import binding as _b
+
+
+class FlashMaskError(RuntimeError):
+    pass
+
+
+def _check(status: int, what: str):
+    if status != _b.FM_OK:
+        raise FlashMaskError(f"{what}: {_b.flashmask_error_string(status)} (status {status})")
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream
+
+
+def _mask_args(masks, B: int, H: int, N: int, device):
+    """Validate the four boundary vectors; returns (Hm, [ptr x 4], keep-alive)."""
+    Hm = None
+    keep = []
+    for name, t in zip(("lts", "lte", "uts", "ute"), masks):
+        if t is None:
+            keep.append(None)
+            continue
+        if t.dtype != torch.int32 or t.device != device or not t.is_contiguous():
+            raise FlashMaskError(f"{name} must be a contiguous int32 tensor on {device}")
+        if t.dim() != 3 or t.shape[0] != B or t.shape[2] != N or t.shape[1] not in (1, H):
+            raise FlashMaskError(f"{name} must have shape [B, 1 or H, N], got {tuple(t.shape)}")
+        if Hm is not None and t.shape[1] != Hm:
+            raise FlashMaskError("all mask vectors must share the same head count")
+        Hm = t.shape[1]
+        keep.append(t)
+    return (Hm or 1), [_ptr(t) for t in keep], keep
+
+
+def make_problem(B, H, Hm, N, d, dv, scale, causal) -> _b.fm_problem:
+    return _b.fm_problem(B, H, Hm, N, d, dv, float(scale if scale is not None else 0.0),
+                         int(bool(causal)))
+
+
+def make_options(deterministic=False, wait_timeout_ns=0, kernel_events=None) -> _b.fm_options:
+    """kernel_events: optional list of raw cudaEvent_t handles (ints), recorded in
+    pairs around each kernel launch of the call."""
+    opt = _b.fm_options(int(bool(deterministic)), 0, int(wait_timeout_ns), None, 0)
+    if kernel_events:
+        arr = (ctypes.c_void_p * len(kernel_events))(*kernel_events)
+        opt.kernel_events = ctypes.cast(arr, ctypes.POINTER(ctypes.c_void_p))
+        opt.n_kernel_events = len(kernel_events)
+        opt._keep = arr
+    return opt
+
+
+def _check_qkv(q, k, v):
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous() or t.dim() != 4:
+            raise FlashMaskError(f"{name} must be a contiguous 4-D bf16 CUDA tensor [B,N,H,dim]")
+    B, N, H, d = q.shape
+    if k.shape != (B, N, H, d) or v.shape[:3] != (B, N, H):
+        raise FlashMaskError("q, k, v shapes disagree")
+    return B, N, H, d, v.shape[3]
+
+
+def workspace_size(B, H, Hm, N, d, dv, is_bwd: bool, deterministic=False) -> int:
+    prob = make_problem(B, H, Hm, N, d, dv, None, False)
+    n = _b.flashmask_workspace_size(prob, make_options(deterministic), int(is_bwd))
+    if n == 0:
+        raise FlashMaskError("invalid problem for workspace query")
+    return n
+
+
+def fwd(q, k, v, lts=None, lte=None, uts=None, ute=None, causal=False, scale=None,
+        out=None, lse=None, workspace=None, stream=None, options=None):
+    """Masked attention forward; returns (o [B,N,H,dv] bf16, lse [B,H,N] fp32)."""
+    B, N, H, d, dv = _check_qkv(q, k, v)
+    Hm, mp, _keep = _mask_args((lts, lte, uts, ute), B, H, N, q.device)
+    prob = make_problem(B, H, Hm, N, d, dv, scale, causal)
+    opt = make_options() if options is None else options
+    if out is None:
+        out = torch.empty((B, N, H, dv), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    ws_bytes = _b.flashmask_workspace_size(prob, opt, 0)
+    if workspace is None:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
+    st = _b.flashmask_fwd(prob, opt, q.data_ptr(), k.data_ptr(), v.data_ptr(), *mp,
+                          out.data_ptr(), lse.data_ptr(), workspace.data_ptr(),
+                          workspace.numel(), _stream(stream))
+    _check(st, "flashmask_fwd")
+    return out, lse
+
+
+def bwd(q, k, v, o, lse, dout, lts=None, lte=None, uts=None, ute=None, causal=False,
+        scale=None, deterministic=False, dq=None, dk=None, dv=None, workspace=None,
+        stream=None, options=None):
+    """Masked attention backward; returns (dq, dk, dv) in bf16."""
+    B, N, H, d, dvd = _check_qkv(q, k, v)
+    for name, t, shape in (("o", o, (B, N, H, dvd)), ("dout", dout, (B, N, H, dvd))):
+        if t.dtype != torch.bfloat16 or not t.is_contiguous() or tuple(t.shape) != shape:
+            raise FlashMaskError(f"{name} must be contiguous bf16 {shape}")
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, N) or not lse.is_contiguous():
+        raise FlashMaskError("lse must be contiguous fp32 [B, H, N]")
+    Hm, mp, _keep = _mask_args((lts, lte, uts, ute), B, H, N, q.device)
+    prob = make_problem(B, H, Hm, N, d, dvd, scale, causal)
+    opt = make_options(deterministic) if options is None else options
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    ws_bytes = _b.flashmask_workspace_size(prob, opt, 1)
+    if workspace is None:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
+    st = _b.flashmask_bwd(prob, opt, q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                          lse.data_ptr(), dout.data_ptr(), *mp, dq.data_ptr(), dk.data_ptr(),
+                          dv.data_ptr(), workspace.data_ptr(), workspace.numel(),
+                          _stream(stream))
+    _check(st, "flashmask_bwd")
+    return dq, dk, dv
+
+
+def classify(N, B=1, H=1, lts=None, lte=None, uts=None, ute=None, causal=False, device="cuda",
+             stream=None):
+    """Tile map [B*Hm, T, T] uint8 (0 skip, 1 partial, 2 unmasked) of 128x128 tiles."""
+    device = torch.device(device)
+    Hm, mp, _keep = _mask_args((lts, lte, uts, ute), B, H, N, device)
+    prob = make_problem(B, H, Hm, N, 128, 128, None, causal)
+    T = -(-N // 128)
+    out = torch.empty((B * Hm, T, T), dtype=torch.uint8, device=device)
+    ws_bytes = _b.flashmask_workspace_size(prob, None, 0)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=device)
+    st = _b.flashmask_classify(prob, *mp, out.data_ptr(), ws.data_ptr(), ws.numel(),
+                               _stream(stream))
+    _check(st, "flashmask_classify")
+    return out
+
+
+def count_unmasked(N, B=1, H=1, lts=None, lte=None, uts=None, ute=None, causal=False,
+                   device="cuda", stream=None):
+    """Unmasked (i, j) pairs per mask head: int64 tensor [B*Hm] on the device."""
+    device = torch.device(device)
+    Hm, mp, _keep = _mask_args((lts, lte, uts, ute), B, H, N, device)
+    prob = make_problem(B, H, Hm, N, 128, 128, None, causal)
+    out = torch.empty((B * Hm,), dtype=torch.int64, device=device)
+    st = _b.flashmask_count_unmasked(prob, *mp, out.data_ptr(), _stream(stream))
+    _check(st, "flashmask_count_unmasked")
+    return out
+
+
+def get_error(stream=None):
+    """Synchronise the stream and raise if a kernel gave up on a bounded wait."""
+    _check(_b.flashmask_get_error(_stream(stream)), "device")
+
+
+class FlashMaskAttention(torch.autograd.Function):
+    """Autograd wrapper: forward and backward both run in the CUDA library."""
+
+    @staticmethod
+    def forward(ctx, q, k, v, lts, lte, uts, ute, causal, scale, deterministic):
+        o, lse = fwd(q, k, v, lts, lte, uts, ute, causal, scale)
+        ctx.save_for_backward(q, k, v, o, lse, lts, lte, uts, ute)
+        ctx.causal, ctx.scale, ctx.deterministic = causal, scale, deterministic
+        return o
+
+    @staticmethod
+    def backward(ctx, do):
+        q, k, v, o, lse, lts, lte, uts, ute = ctx.saved_tensors
+        dq, dk, dv = bwd(q, k, v, o, lse, do.contiguous(), lts, lte, uts, ute, ctx.causal,
+                         ctx.scale, ctx.deterministic)
+        return dq, dk, dv, None, None, None, None, None, None, None
+
+
+def flashmask_attention(q, k, v, lts=None, lte=None, uts=None, ute=None, causal=False,
+                        scale=None, deterministic=False):
+    """O = softmax(Q K^T * scale + M) V with the column-wise mask; differentiable."""
+    return FlashMaskAttention.apply(q, k, v, lts, lte, uts, ute, causal, scale, deterministic)
+
+
+def default_scale(d: int) -> float:
+    return 1.0 / math.sqrt(d)

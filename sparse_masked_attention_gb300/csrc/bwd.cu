@@ -1,0 +1,742 @@
+// bwd.cu -- backward of FlashMask masked attention on tcgen05 tensor cores.
+//
+// The derivative of O = softmax(Q K^T * scale + M) V (FlashMask README,
+// "Formulation").  P is rebuilt from the forward's LSE:
+//   P = exp(S * scale - LSE),  dP = dO V^T,  D_i = sum_c dO_ic O_ic,
+//   dS = P * (dP - D),  dQ = scale dS K,  dK = scale dS^T Q,  dV = P^T dO.
+// The backward walks the same tile map as the forward: fully masked tiles are
+// skipped, and the mask is applied elementwise only on partial tiles.
+//
+// Three kernels:
+//   preprocess   D (fp32) and the log2-domain LSE per row, padded to whole
+//                tiles; padding rows and fully masked rows get LSE = +inf, so
+//                their P is 0.
+//   dq kernel    one CTA per 128-row query tile walks its key tiles:
+//                S = Q K^T, dP = dO V^T (SS MMAs); dS -> shared memory (bf16);
+//                dQ += dS K (SS MMA).  Writes dQ once, in a fixed order.
+//   dkdv kernel  one CTA per 128-key tile walks its query tiles:
+//                S^T = K Q^T, dP^T = V dO^T (SS MMAs); P^T and dS^T -> TMEM
+//                as bf16; dV += P^T dO and dK += dS^T Q (TS MMAs).
+// No atomics are used, so every gradient is bit-reproducible.  For
+// d = dv = 256 the accumulators dK and dV do not fit in TMEM together, so
+// the dkdv kernel runs twice: once for dV, once for dK.
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include "fm_device.cuh"
+#include "fm_internal.h"
+
+namespace fm {
+
+static __device__ unsigned g_err_bwd;
+
+namespace {
+
+__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, uint64_t tmo,
+                                          volatile int *abort) {
+    const bool ok = mbar_wait(bar, parity, tmo, abort, &g_err_bwd);
+    return __all_sync(0xffffffffu, ok);
+}
+
+__device__ __forceinline__ void store_row_bf16(__nv_bfloat16 *dst, const float (&v)[32],
+                                               float mul) {
+    uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        uint4 w;
+        w.x = pack_bf16(v[q * 8 + 0] * mul, v[q * 8 + 1] * mul);
+        w.y = pack_bf16(v[q * 8 + 2] * mul, v[q * 8 + 3] * mul);
+        w.z = pack_bf16(v[q * 8 + 4] * mul, v[q * 8 + 5] * mul);
+        w.w = pack_bf16(v[q * 8 + 6] * mul, v[q * 8 + 7] * mul);
+        d4[q] = w;
+    }
+}
+
+// ---------------------------------------------------------------- preprocess
+// 16 threads per row; each takes 8 consecutive bf16 of dO and O at a time.
+__global__ void __launch_bounds__(256) preprocess_kernel(
+    int N, int H, int dv, int Npad, int rows_total, const __nv_bfloat16 *__restrict__ o,
+    const __nv_bfloat16 *__restrict__ dout, const float *__restrict__ lse,
+    float *__restrict__ lse2, float *__restrict__ delta) {
+    const int r0 = blockIdx.x * 16 + (threadIdx.x >> 4);  // over B*H*Npad
+    const int t = threadIdx.x & 15;
+    const bool valid = r0 < rows_total;
+    const int r = valid ? r0 : 0;
+    const int bh = r / Npad, i = r % Npad;
+    const int b = bh / H, h = bh % H;
+    float acc = 0.f;
+    if (valid && i < N) {
+        const size_t base = ((static_cast<size_t>(b) * N + i) * H + h) * dv;
+        for (int c = t * 8; c < dv; c += 128) {
+            const uint4 a = *reinterpret_cast<const uint4 *>(o + base + c);
+            const uint4 g = *reinterpret_cast<const uint4 *>(dout + base + c);
+            const __nv_bfloat162 *a2 = reinterpret_cast<const __nv_bfloat162 *>(&a);
+            const __nv_bfloat162 *g2 = reinterpret_cast<const __nv_bfloat162 *>(&g);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float2 fa = __bfloat1622float2(a2[e]);
+                const float2 fg = __bfloat1622float2(g2[e]);
+                acc = fmaf(fa.x, fg.x, acc);
+                acc = fmaf(fa.y, fg.y, acc);
+            }
+        }
+    }
+#pragma unroll
+    for (int off = 8; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off, 16);
+    if (valid && t == 0) {
+        float l2 = INFINITY;
+        if (i < N) {
+            const float l = lse[static_cast<size_t>(bh) * N + i];
+            l2 = (l == -INFINITY) ? INFINITY : l * 1.4426950408889634f;
+        }
+        lse2[r] = l2;
+        delta[r] = i < N ? acc : 0.f;
+    }
+}
+
+struct BwdParams {
+    const int4 *vec;
+    const int *list;  // fwd list (dq kernel) or bwd list (dkdv kernel)
+    const int *cnt;
+    const float *lse2;
+    const float *delta;
+    __nv_bfloat16 *dq, *dk, *dv;
+    int N, H, Hm, T, Npad, causal;
+    float sl2;    // scale * log2(e)
+    float scale;
+    uint64_t timeout_ns;
+};
+
+// ------------------------------------------------------------------ dq kernel
+template <int D_, int DV_, int BN_, int ST_>
+struct DqCfg {
+    static constexpr int D = D_, DV = DV_, BN = BN_, ST = ST_;
+    static constexpr int BM = 128;
+    static constexpr int SUB = TILE / BN;
+    static constexpr int Q_BYTES = BM * D * 2;
+    static constexpr int DO_BYTES = BM * DV * 2;
+    static constexpr int K_BYTES = BN * D * 2;
+    static constexpr int V_BYTES = BN * DV * 2;
+    static constexpr int DS_BYTES = BM * BN * 2;
+    static constexpr int OFF_Q = 0;
+    static constexpr int OFF_DO = OFF_Q + Q_BYTES;
+    static constexpr int OFF_DS = OFF_DO + DO_BYTES;
+    static constexpr int OFF_K = OFF_DS + DS_BYTES;
+    static constexpr int OFF_V = OFF_K + ST * K_BYTES;
+    static constexpr int OFF_BAR = OFF_V + ST * V_BYTES;
+    // q_full, kv_full[ST], kv_empty[ST], s_full, ds_full, dq_done
+    static constexpr int NBAR = 1 + 2 * ST + 3;
+    static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+    static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
+    static constexpr int TM_S = 0, TM_DP = BN, TM_DQ = 2 * BN;
+    static constexpr int TM_COLS = 512;
+    static constexpr int THREADS = 192;
+    static_assert(TM_DQ + D <= TM_COLS, "TMEM budget");
+    static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+};
+
+template <class C>
+__global__ void __launch_bounds__(C::THREADS, 1)
+    dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+              const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+              const BwdParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t *sQ = smem + C::OFF_Q, *sDO = smem + C::OFF_DO, *sDS = smem + C::OFF_DS;
+    uint8_t *sK = smem + C::OFF_K, *sV = smem + C::OFF_V;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
+    uint64_t *q_full = bars, *kv_full = bars + 1, *kv_empty = kv_full + C::ST;
+    uint64_t *s_full = kv_empty + C::ST, *ds_full = s_full + 1, *dq_done = ds_full + 1;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
+    volatile int *abort = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int qt = p.T - 1 - static_cast<int>(blockIdx.x);
+    const int h = blockIdx.y, b = blockIdx.z;
+    const int bm = b * p.Hm + (p.Hm == 1 ? 0 : h);
+    const int n_entries = p.cnt[static_cast<size_t>(bm) * p.T + qt];
+    const int *entries = p.list + (static_cast<size_t>(bm) * p.T + qt) * p.T;
+    // After a bounded wait gave up anywhere, later CTAs do no work.
+    const int n = (*reinterpret_cast<volatile unsigned *>(&g_err_bwd) != 0) ? 0
+                                                                            : n_entries * C::SUB;
+    const uint64_t tmo = p.timeout_ns;
+
+    if (threadIdx.x == 0) {
+        mbar_init(q_full, 1);
+        for (int i = 0; i < C::ST; ++i) {
+            mbar_init(&kv_full[i], 1);
+            mbar_init(&kv_empty[i], 1);
+        }
+        mbar_init(s_full, 1);
+        mbar_init(ds_full, 128);
+        mbar_init(dq_done, 1);
+        *abort = 0;
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, C::TM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    auto key0_of = [&](int u) {
+        return (entries[u / C::SUB] >> 1) * TILE + (u % C::SUB) * C::BN;
+    };
+
+    if (warp == 0) {
+        if (lane == 0 && n > 0) {
+            prefetch_tmap(&tm_q);
+            prefetch_tmap(&tm_k);
+            prefetch_tmap(&tm_v);
+            prefetch_tmap(&tm_do);
+            mbar_arrive_expect_tx(q_full, C::Q_BYTES + C::DO_BYTES);
+#pragma unroll
+            for (int c = 0; c < C::D / 64; ++c)
+                tma_load_4d(sQ + c * C::BM * 128, &tm_q, q_full, c * 64, h, qt * TILE, b);
+#pragma unroll
+            for (int c = 0; c < C::DV / 64; ++c)
+                tma_load_4d(sDO + c * C::BM * 128, &tm_do, q_full, c * 64, h, qt * TILE, b);
+            for (int u = 0; u < n; ++u) {
+                const int s = u % C::ST;
+                if (u >= C::ST &&
+                    !mbar_wait(&kv_empty[s], ((u / C::ST) - 1) & 1, tmo, abort, &g_err_bwd))
+                    break;
+                mbar_arrive_expect_tx(&kv_full[s], C::K_BYTES + C::V_BYTES);
+                const int key0 = key0_of(u);
+#pragma unroll
+                for (int c = 0; c < C::D / 64; ++c)
+                    tma_load_4d(sK + s * C::K_BYTES + c * C::BN * 128, &tm_k, &kv_full[s],
+                                c * 64, h, key0, b);
+#pragma unroll
+                for (int c = 0; c < C::DV / 64; ++c)
+                    tma_load_4d(sV + s * C::V_BYTES + c * C::BN * 128, &tm_v, &kv_full[s],
+                                c * 64, h, key0, b);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0 && n > 0) {
+            constexpr uint32_t IDESC_S = idesc_bf16(128, C::BN, false, false);
+            constexpr uint32_t IDESC_DQ = idesc_bf16(128, C::D, false, true);
+            const uint32_t q_addr = smem_u32(sQ), do_addr = smem_u32(sDO);
+            const uint32_t ds_addr = smem_u32(sDS);
+            const uint32_t k_addr = smem_u32(sK), v_addr = smem_u32(sV);
+            auto issue_s_dp = [&](int u) -> bool {
+                const int s = u % C::ST;
+                if (!mbar_wait(&kv_full[s], (u / C::ST) & 1, tmo, abort, &g_err_bwd)) return false;
+                tc_fence_after();
+#pragma unroll
+                for (int k = 0; k < C::D / 16; ++k) {
+                    const uint64_t ad =
+                        sdesc_sw128(q_addr + (k / 4) * (C::BM * 128) + (k % 4) * 32, 16, 1024);
+                    const uint64_t bd = sdesc_sw128(
+                        k_addr + s * C::K_BYTES + (k / 4) * (C::BN * 128) + (k % 4) * 32, 16, 1024);
+                    mma_ss(tmem + C::TM_S, ad, bd, IDESC_S, k > 0 ? 1u : 0u);
+                }
+#pragma unroll
+                for (int k = 0; k < C::DV / 16; ++k) {
+                    const uint64_t ad =
+                        sdesc_sw128(do_addr + (k / 4) * (C::BM * 128) + (k % 4) * 32, 16, 1024);
+                    const uint64_t bd = sdesc_sw128(
+                        v_addr + s * C::V_BYTES + (k / 4) * (C::BN * 128) + (k % 4) * 32, 16, 1024);
+                    mma_ss(tmem + C::TM_DP, ad, bd, IDESC_S, k > 0 ? 1u : 0u);
+                }
+                mma_commit(s_full);
+                return true;
+            };
+            bool ok = mbar_wait(q_full, 0, tmo, abort, &g_err_bwd);
+            if (ok) ok = issue_s_dp(0);
+            for (int u = 0; u < n && ok; ++u) {
+                if (!mbar_wait(ds_full, u & 1, tmo, abort, &g_err_bwd)) break;
+                tc_fence_after();
+                const int s = u % C::ST;
+                // dQ += dS K_u: A = dS (K-major, BN keys), B = K_u (MN-major over d).
+#pragma unroll
+                for (int k = 0; k < C::BN / 16; ++k) {
+                    const uint64_t ad =
+                        sdesc_sw128(ds_addr + (k / 4) * (C::BM * 128) + (k % 4) * 32, 16, 1024);
+                    const uint64_t bd =
+                        sdesc_sw128(k_addr + s * C::K_BYTES + k * 2048, C::BN * 128, 1024);
+                    mma_ss(tmem + C::TM_DQ, ad, bd, IDESC_DQ, (u > 0 || k > 0) ? 1u : 0u);
+                }
+                mma_commit(&kv_empty[s]);
+                if (u + 1 < n) ok = issue_s_dp(u + 1);
+            }
+            mma_commit(dq_done);
+        }
+    } else {
+        // compute warpgroup: thread = query row
+        const int quad = warp & 3;
+        const int row = quad * 32 + lane;
+        const int grow = qt * TILE + row;
+        const uint32_t lane_base = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+        const size_t bh = static_cast<size_t>(b) * p.H + h;
+        const float lse2 = p.lse2[bh * p.Npad + grow];
+        const float Drow = p.delta[bh * p.Npad + grow];
+        const int4 *vec = p.vec + static_cast<size_t>(bm) * p.Npad;
+        // dS row r of the K-major swizzled tile: 16-byte chunk c of 64-column
+        // box kb lives at kb*BM*128 + r*128 + ((c ^ (r & 7)) * 16).
+        uint8_t *ds_row = sDS + row * 128;
+        for (int u = 0; u < n; ++u) {
+            if (!warp_wait(s_full, u & 1, tmo, abort)) break;
+            tc_fence_after();
+            float pr[C::BN];
+#pragma unroll
+            for (int c = 0; c < C::BN / 32; ++c) {
+                uint32_t r[32];
+                tmem_ld32(lane_base + C::TM_S + c * 32, r);
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    pr[c * 32 + i] = ex2(__uint_as_float(r[i]) * p.sl2 - lse2);
+            }
+            if (entries[u / C::SUB] & 1) {
+                const int key0 = key0_of(u);
+#pragma unroll
+                for (int jj = 0; jj < C::BN; ++jj) {
+                    const int4 cv = __ldg(vec + key0 + jj);
+                    if (masked_at(grow, key0 + jj, cv, p.causal)) pr[jj] = 0.f;
+                }
+            }
+#pragma unroll
+            for (int c = 0; c < C::BN / 32; ++c) {
+                uint32_t r[32];
+                tmem_ld32(lane_base + C::TM_DP + c * 32, r);
+                // 32 columns = 4 chunks of 8 bf16 in box (c*32)/64
+                const int box = (c * 32) / 64;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int col = c * 32 + q * 8;
+                    uint4 w;
+                    float d8[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        d8[e] = pr[col + e] * (__uint_as_float(r[q * 8 + e]) - Drow);
+                    w.x = pack_bf16(d8[0], d8[1]);
+                    w.y = pack_bf16(d8[2], d8[3]);
+                    w.z = pack_bf16(d8[4], d8[5]);
+                    w.w = pack_bf16(d8[6], d8[7]);
+                    const int chunk = (col % 64) / 8;
+                    *reinterpret_cast<uint4 *>(ds_row + box * C::BM * 128 +
+                                               ((chunk ^ (row & 7)) * 16)) = w;
+                }
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(ds_full);
+        }
+        if (n > 0) warp_wait(dq_done, 0, tmo, abort);
+        tc_fence_after();
+        __nv_bfloat16 *dst =
+            p.dq + ((static_cast<size_t>(b) * p.N + grow) * p.H + h) * static_cast<size_t>(C::D);
+#pragma unroll 1
+        for (int c = 0; c < C::D / 32; ++c) {
+            uint32_t r[32];
+            tmem_ld32(lane_base + C::TM_DQ + c * 32, r);
+            float v[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = n > 0 ? __uint_as_float(r[i]) : 0.f;
+            if (grow < p.N) store_row_bf16(dst + c * 32, v, p.scale);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, C::TM_COLS);
+    }
+}
+
+// ---------------------------------------------------------------- dkdv kernel
+template <int D_, int DV_, int BM_, int ST_, bool DK_, bool DV_ON_>
+struct DkdvCfg {
+    static constexpr int D = D_, DV = DV_, BM = BM_, ST = ST_;
+    static constexpr bool DO_DK = DK_, DO_DV = DV_ON_;
+    static constexpr int BN = 128;            // keys per CTA (TMEM lanes)
+    static constexpr int SUB = TILE / BM;     // query sub-tiles per list entry
+    static constexpr bool NEED_V = DO_DK;     // V only feeds dP^T
+    static constexpr int K_BYTES = BN * D * 2;
+    static constexpr int V_BYTES = NEED_V ? BN * DV * 2 : 0;
+    static constexpr int Q_BYTES = BM * D * 2;
+    static constexpr int DO_BYTES = BM * DV * 2;
+    static constexpr int STAGE_BYTES = Q_BYTES + DO_BYTES + 2 * BM * 4;
+    static constexpr int OFF_K = 0;
+    static constexpr int OFF_V = OFF_K + K_BYTES;
+    static constexpr int OFF_ST = OFF_V + V_BYTES;
+    static constexpr int ST_Q = 0, ST_DO = Q_BYTES, ST_LSE = Q_BYTES + DO_BYTES,
+                         ST_D = ST_LSE + BM * 4;
+    static constexpr int STAGE_STRIDE = (STAGE_BYTES + 1023) / 1024 * 1024;
+    static constexpr int OFF_BAR = OFF_ST + ST * STAGE_STRIDE;
+    // kv_full, q_full[ST], q_empty[ST], s_full, p_full, ds_full, done
+    static constexpr int NBAR = 1 + 2 * ST + 4;
+    static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+    static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
+    static constexpr int TM_DK = 0;
+    static constexpr int TM_DV = DO_DK ? D : 0;
+    static constexpr int TM_S = TM_DV + (DO_DV ? DV : 0);
+    static constexpr int TM_DP = TM_S + BM;
+    static constexpr int TM_END = TM_DP + (DO_DK ? BM : 0);
+    static constexpr int TM_COLS = 512;
+    static constexpr int THREADS = 192;
+    static_assert(TM_END <= TM_COLS, "TMEM budget");
+    static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+    static_assert(D <= 256 && DV <= 256 && BM % 32 == 0, "MMA shape");
+};
+
+template <class C>
+__global__ void __launch_bounds__(C::THREADS, 1)
+    dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                const __grid_constant__ CUtensorMap tm_v,
+                const __grid_constant__ CUtensorMap tm_do, const BwdParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t *sK = smem + C::OFF_K, *sV = smem + C::OFF_V, *sST = smem + C::OFF_ST;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
+    uint64_t *kv_full = bars, *q_full = bars + 1, *q_empty = q_full + C::ST;
+    uint64_t *s_full = q_empty + C::ST, *p_full = s_full + 1, *ds_full = p_full + 1,
+             *done = ds_full + 1;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
+    volatile int *abort = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int kt = blockIdx.x;
+    const int h = blockIdx.y, b = blockIdx.z;
+    const int bm = b * p.Hm + (p.Hm == 1 ? 0 : h);
+    const int n_entries = p.cnt[static_cast<size_t>(bm) * p.T + kt];
+    const int *entries = p.list + (static_cast<size_t>(bm) * p.T + kt) * p.T;
+    // After a bounded wait gave up anywhere, later CTAs do no work.
+    const int n = (*reinterpret_cast<volatile unsigned *>(&g_err_bwd) != 0) ? 0
+                                                                            : n_entries * C::SUB;
+    const uint64_t tmo = p.timeout_ns;
+    const size_t bh = static_cast<size_t>(b) * p.H + h;
+
+    if (threadIdx.x == 0) {
+        mbar_init(kv_full, 1);
+        for (int i = 0; i < C::ST; ++i) {
+            mbar_init(&q_full[i], 1);
+            mbar_init(&q_empty[i], 1);
+        }
+        mbar_init(s_full, 1);
+        mbar_init(p_full, 128);
+        mbar_init(ds_full, 128);
+        mbar_init(done, 1);
+        *abort = 0;
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, C::TM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    auto q0_of = [&](int u) { return (entries[u / C::SUB] >> 1) * TILE + (u % C::SUB) * C::BM; };
+
+    if (warp == 0) {
+        if (lane == 0 && n > 0) {
+            prefetch_tmap(&tm_q);
+            prefetch_tmap(&tm_k);
+            prefetch_tmap(&tm_do);
+            mbar_arrive_expect_tx(kv_full, C::K_BYTES + C::V_BYTES);
+#pragma unroll
+            for (int c = 0; c < C::D / 64; ++c)
+                tma_load_4d(sK + c * C::BN * 128, &tm_k, kv_full, c * 64, h, kt * TILE, b);
+            if constexpr (C::NEED_V) {
+                prefetch_tmap(&tm_v);
+#pragma unroll
+                for (int c = 0; c < C::DV / 64; ++c)
+                    tma_load_4d(sV + c * C::BN * 128, &tm_v, kv_full, c * 64, h, kt * TILE, b);
+            }
+            for (int u = 0; u < n; ++u) {
+                const int s = u % C::ST;
+                if (u >= C::ST &&
+                    !mbar_wait(&q_empty[s], ((u / C::ST) - 1) & 1, tmo, abort, &g_err_bwd))
+                    break;
+                uint8_t *stg = sST + s * C::STAGE_STRIDE;
+                mbar_arrive_expect_tx(&q_full[s], C::STAGE_BYTES);
+                const int q0 = q0_of(u);
+#pragma unroll
+                for (int c = 0; c < C::D / 64; ++c)
+                    tma_load_4d(stg + C::ST_Q + c * C::BM * 128, &tm_q, &q_full[s], c * 64, h, q0,
+                                b);
+#pragma unroll
+                for (int c = 0; c < C::DV / 64; ++c)
+                    tma_load_4d(stg + C::ST_DO + c * C::BM * 128, &tm_do, &q_full[s], c * 64, h,
+                                q0, b);
+                bulk_load(stg + C::ST_LSE, p.lse2 + bh * p.Npad + q0, C::BM * 4, &q_full[s]);
+                bulk_load(stg + C::ST_D, p.delta + bh * p.Npad + q0, C::BM * 4, &q_full[s]);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0 && n > 0) {
+            constexpr uint32_t IDESC_S = idesc_bf16(128, C::BM, false, false);
+            constexpr uint32_t IDESC_DV = idesc_bf16(128, C::DV, false, true);
+            constexpr uint32_t IDESC_DK = idesc_bf16(128, C::D, false, true);
+            const uint32_t k_addr = smem_u32(sK), v_addr = smem_u32(sV);
+            const uint32_t st_addr = smem_u32(sST);
+            bool ok = mbar_wait(kv_full, 0, tmo, abort, &g_err_bwd);
+            for (int u = 0; u < n && ok; ++u) {
+                const int s = u % C::ST;
+                const uint32_t stg = st_addr + s * C::STAGE_STRIDE;
+                if (!mbar_wait(&q_full[s], (u / C::ST) & 1, tmo, abort, &g_err_bwd)) break;
+                tc_fence_after();
+                // S^T = K Q^T
+#pragma unroll
+                for (int k = 0; k < C::D / 16; ++k) {
+                    const uint64_t ad =
+                        sdesc_sw128(k_addr + (k / 4) * (C::BN * 128) + (k % 4) * 32, 16, 1024);
+                    const uint64_t bd = sdesc_sw128(
+                        stg + C::ST_Q + (k / 4) * (C::BM * 128) + (k % 4) * 32, 16, 1024);
+                    mma_ss(tmem + C::TM_S, ad, bd, IDESC_S, k > 0 ? 1u : 0u);
+                }
+                if constexpr (C::DO_DK) {
+                    // dP^T = V dO^T
+#pragma unroll
+                    for (int k = 0; k < C::DV / 16; ++k) {
+                        const uint64_t ad = sdesc_sw128(
+                            v_addr + (k / 4) * (C::BN * 128) + (k % 4) * 32, 16, 1024);
+                        const uint64_t bd = sdesc_sw128(
+                            stg + C::ST_DO + (k / 4) * (C::BM * 128) + (k % 4) * 32, 16, 1024);
+                        mma_ss(tmem + C::TM_DP, ad, bd, IDESC_S, k > 0 ? 1u : 0u);
+                    }
+                }
+                mma_commit(s_full);
+                if constexpr (C::DO_DV) {
+                    if (!mbar_wait(p_full, u & 1, tmo, abort, &g_err_bwd)) break;
+                    tc_fence_after();
+                    // dV += P^T dO: A = P^T (TMEM, bf16), B = dO (MN-major over dv)
+#pragma unroll
+                    for (int k = 0; k < C::BM / 16; ++k) {
+                        const uint64_t bd =
+                            sdesc_sw128(stg + C::ST_DO + k * 2048, C::BM * 128, 1024);
+                        mma_ts(tmem + C::TM_DV, tmem + C::TM_S + k * 8, bd, IDESC_DV,
+                               (u > 0 || k > 0) ? 1u : 0u);
+                    }
+                }
+                if constexpr (C::DO_DK) {
+                    if (!mbar_wait(ds_full, u & 1, tmo, abort, &g_err_bwd)) break;
+                    tc_fence_after();
+                    // dK += dS^T Q: A = dS^T (TMEM, bf16), B = Q (MN-major over d)
+#pragma unroll
+                    for (int k = 0; k < C::BM / 16; ++k) {
+                        const uint64_t bd =
+                            sdesc_sw128(stg + C::ST_Q + k * 2048, C::BM * 128, 1024);
+                        mma_ts(tmem + C::TM_DK, tmem + C::TM_DP + k * 8, bd, IDESC_DK,
+                               (u > 0 || k > 0) ? 1u : 0u);
+                    }
+                } else {
+                    // S^T is read back before P^T is written; keep the order
+                    // "compute done with S^T" -> next S^T explicit.
+                    if (!mbar_wait(ds_full, u & 1, tmo, abort, &g_err_bwd)) break;
+                }
+                mma_commit(&q_empty[s]);
+            }
+            mma_commit(done);
+        }
+    } else {
+        // compute warpgroup: thread = key column (TMEM lane)
+        const int quad = warp & 3;
+        const int row = quad * 32 + lane;
+        const int gkey = kt * TILE + row;
+        const uint32_t lane_base = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+        const int4 cv = p.vec[static_cast<size_t>(bm) * p.Npad + gkey];
+        for (int u = 0; u < n; ++u) {
+            const int s = u % C::ST;
+            const uint8_t *stg = sST + s * C::STAGE_STRIDE;
+            const float *slse = reinterpret_cast<const float *>(stg + C::ST_LSE);
+            const float *sd = reinterpret_cast<const float *>(stg + C::ST_D);
+            if (!warp_wait(s_full, u & 1, tmo, abort)) break;
+            tc_fence_after();
+            const int q0 = q0_of(u);
+            const bool need_mask = entries[u / C::SUB] & 1;
+            float pr[C::BM];
+#pragma unroll
+            for (int c = 0; c < C::BM / 32; ++c) {
+                uint32_t r[32];
+                tmem_ld32(lane_base + C::TM_S + c * 32, r);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const int qi = c * 32 + i;
+                    float v = ex2(__uint_as_float(r[i]) * p.sl2 - slse[qi]);
+                    if (need_mask && masked_at(q0 + qi, gkey, cv, p.causal)) v = 0.f;
+                    pr[qi] = v;
+                }
+            }
+            if constexpr (C::DO_DV) {
+#pragma unroll
+                for (int c = 0; c < C::BM / 64; ++c) {
+                    uint32_t r[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) r[i] = pack_bf16(pr[c * 64 + 2 * i], pr[c * 64 + 2 * i + 1]);
+                    tmem_st32(lane_base + C::TM_S + c * 32, r);
+                }
+                tmem_st_wait();
+                tc_fence_before();
+                mbar_arrive(p_full);
+            }
+            if constexpr (C::DO_DK) {
+#pragma unroll
+                for (int c = 0; c < C::BM / 32; ++c) {
+                    uint32_t r[32];
+                    tmem_ld32(lane_base + C::TM_DP + c * 32, r);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const int qi = c * 32 + i;
+                        pr[qi] = pr[qi] * (__uint_as_float(r[i]) - sd[qi]);
+                    }
+                }
+#pragma unroll
+                for (int c = 0; c < C::BM / 64; ++c) {
+                    uint32_t r[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) r[i] = pack_bf16(pr[c * 64 + 2 * i], pr[c * 64 + 2 * i + 1]);
+                    tmem_st32(lane_base + C::TM_DP + c * 32, r);
+                }
+                tmem_st_wait();
+            }
+            tc_fence_before();
+            mbar_arrive(ds_full);
+        }
+        if (n > 0) warp_wait(done, 0, tmo, abort);
+        tc_fence_after();
+        const bool store = gkey < p.N;
+        const size_t rowoff = (static_cast<size_t>(b) * p.N + gkey) * p.H + h;
+        if constexpr (C::DO_DK) {
+#pragma unroll 1
+            for (int c = 0; c < C::D / 32; ++c) {
+                uint32_t r[32];
+                tmem_ld32(lane_base + C::TM_DK + c * 32, r);
+                float v[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) v[i] = n > 0 ? __uint_as_float(r[i]) : 0.f;
+                if (store) store_row_bf16(p.dk + rowoff * C::D + c * 32, v, p.scale);
+            }
+        }
+        if constexpr (C::DO_DV) {
+#pragma unroll 1
+            for (int c = 0; c < C::DV / 32; ++c) {
+                uint32_t r[32];
+                tmem_ld32(lane_base + C::TM_DV + c * 32, r);
+                float v[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) v[i] = n > 0 ? __uint_as_float(r[i]) : 0.f;
+                if (store) store_row_bf16(p.dv + rowoff * C::DV + c * 32, v, 1.0f);
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, C::TM_COLS);
+    }
+}
+
+BwdParams make_params(const Geometry &g, const Workspace &ws, const BwdArgs &a, bool dq_side) {
+    BwdParams p;
+    p.vec = ws.vec;
+    p.list = dq_side ? ws.fwd_list : ws.bwd_list;
+    p.cnt = dq_side ? ws.fwd_cnt : ws.bwd_cnt;
+    p.lse2 = ws.lse2;
+    p.delta = ws.delta;
+    p.dq = static_cast<__nv_bfloat16 *>(a.dq);
+    p.dk = static_cast<__nv_bfloat16 *>(a.dk);
+    p.dv = static_cast<__nv_bfloat16 *>(a.dv);
+    p.N = g.N;
+    p.H = g.H;
+    p.Hm = g.Hm;
+    p.T = g.T;
+    p.Npad = g.Npad;
+    p.causal = g.causal;
+    p.sl2 = g.scale * 1.4426950408889634f;
+    p.scale = g.scale;
+    p.timeout_ns = g.timeout_ns;
+    return p;
+}
+
+template <class C>
+cudaError_t launch_dq(const Geometry &g, const Workspace &ws, const BwdArgs &a, cudaStream_t st) {
+    auto kern = dq_kernel<C>;
+    cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    dim3 grid(g.T, g.H, g.B);
+    kern<<<grid, C::THREADS, C::SMEM_BYTES, st>>>(*a.tm_q_dq, *a.tm_k_dq, *a.tm_v_dq,
+                                                  *a.tm_do_dq, make_params(g, ws, a, true));
+    return cudaGetLastError();
+}
+
+template <class C>
+cudaError_t launch_dkdv(const Geometry &g, const Workspace &ws, const BwdArgs &a,
+                        cudaStream_t st) {
+    auto kern = dkdv_kernel<C>;
+    cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    dim3 grid(g.T, g.H, g.B);
+    kern<<<grid, C::THREADS, C::SMEM_BYTES, st>>>(*a.tm_q, *a.tm_k, *a.tm_v, *a.tm_do,
+                                                  make_params(g, ws, a, false));
+    return cudaGetLastError();
+}
+
+template <class KV, class DQ>
+cudaError_t launch_pair(const Geometry &g, const Workspace &ws, const BwdArgs &a, cudaStream_t st,
+                        Recorder &rec) {
+    rec.before(st);
+    cudaError_t e = launch_dkdv<KV>(g, ws, a, st);
+    rec.after(st);
+    if (e != cudaSuccess) return e;
+    rec.before(st);
+    e = launch_dq<DQ>(g, ws, a, st);
+    rec.after(st);
+    return e;
+}
+
+}  // namespace
+
+cudaError_t launch_bwd(const Geometry &g, const Workspace &ws, const BwdArgs &a,
+                       cudaStream_t st, Recorder &rec) {
+    const int rows_total = g.B * g.H * g.Npad;
+    rec.before(st);
+    preprocess_kernel<<<(rows_total + 15) / 16, 256, 0, st>>>(
+        g.N, g.H, g.dv, g.Npad, rows_total, static_cast<const __nv_bfloat16 *>(a.o),
+        static_cast<const __nv_bfloat16 *>(a.dout), a.lse, ws.lse2, ws.delta);
+    rec.after(st);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    if (g.d == 64 && g.dv == 64)
+        return launch_pair<DkdvCfg<64, 64, 128, 3, true, true>, DqCfg<64, 64, 128, 3>>(g, ws, a,
+                                                                                     st, rec);
+    if (g.d == 128 && g.dv == 128)
+        return launch_pair<DkdvCfg<128, 128, 128, 2, true, true>, DqCfg<128, 128, 128, 2>>(
+            g, ws, a, st, rec);
+    if (g.d == 192 && g.dv == 128)
+        return launch_pair<DkdvCfg<192, 128, 64, 2, true, true>, DqCfg<192, 128, 64, 2>>(
+            g, ws, a, st, rec);
+    if (g.d == 256 && g.dv == 256) {
+        rec.before(st);
+        e = launch_dkdv<DkdvCfg<256, 256, 64, 2, false, true>>(g, ws, a, st);
+        rec.after(st);
+        if (e != cudaSuccess) return e;
+        return launch_pair<DkdvCfg<256, 256, 64, 1, true, false>, DqCfg<256, 256, 64, 1>>(
+            g, ws, a, st, rec);
+    }
+    return cudaErrorInvalidValue;
+}
+
+unsigned read_clear_error_bwd() {
+    unsigned v = 0, zero = 0;
+    if (cudaMemcpyFromSymbol(&v, g_err_bwd, sizeof(v)) != cudaSuccess) return 0;
+    if (v) cudaMemcpyToSymbol(g_err_bwd, &zero, sizeof(zero));
+    return v;
+}
+
+}  // namespace fm

@@ -1,0 +1,222 @@
+// classify.cu -- the tile map: which 128x128 (query-tile, key-tile) blocks are
+// fully masked (skipped), partially masked (mask applied elementwise) or
+// unmasked.  This is the sparsity skipping of "FlashMask: Efficient and Rich
+// Mask Extension of FlashAttention" (abstract) on the column-wise boundaries
+// of the FlashMask README ("Overview").
+//
+// One CTA per (mask head, key tile).  Its 128 threads each own one key column.
+// The CTA first reduces the per-tile min/max of the four boundary vectors.
+// Those eight numbers settle most tiles at once.  A tile they leave open gets
+// an exact per-column test: each column's masked rows form the union of at most
+// three intervals ([0, j) for the causal flag, LT, UT).  The map is therefore
+// exact, never just conservative.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "fm_device.cuh"
+#include "fm_internal.h"
+
+namespace fm {
+
+static __device__ unsigned g_err_classify;
+
+namespace {
+
+__device__ __forceinline__ int clampN(int x, int N) { return x < 0 ? 0 : (x > N ? N : x); }
+
+// Does [a, b) meet [r0, r1)?
+__device__ __forceinline__ bool meets(int a, int b, int r0, int r1) {
+    return max(a, r0) < min(b, r1);
+}
+
+// Does the union of [0, cj) (cj = j under the causal flag, else 0),
+// [c.x, c.y) and [c.z, c.w) cover [r0, r1)?
+__device__ __forceinline__ bool covers(int cj, int4 c, int r0, int r1) {
+    int reach = r0;
+#pragma unroll
+    for (int round = 0; round < 3; ++round) {
+        if (0 <= reach && cj > reach) reach = cj;
+        if (c.x <= reach && c.y > reach) reach = c.y;
+        if (c.z <= reach && c.w > reach) reach = c.w;
+    }
+    return reach >= r1;
+}
+
+__device__ __forceinline__ int block_min(int v, int *red) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = min(v, __shfl_xor_sync(0xffffffffu, v, o));
+    __syncthreads();
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+    __syncthreads();
+    return min(min(red[0], red[1]), min(red[2], red[3]));
+}
+
+__device__ __forceinline__ int block_max(int v, int *red) {
+    return -block_min(-v, red);
+}
+
+__global__ void __launch_bounds__(128) classify_kernel(
+    int N, int T, int Npad, int Hm, int causal, const int32_t *__restrict__ lts,
+    const int32_t *__restrict__ lte, const int32_t *__restrict__ uts,
+    const int32_t *__restrict__ ute, int4 *__restrict__ vec, uint8_t *__restrict__ cls,
+    int *__restrict__ bwd_list, int *__restrict__ bwd_cnt) {
+    __shared__ int red[4];
+    const int kt = blockIdx.x;
+    const int bm = blockIdx.y;  // b * Hm + hm
+    const int j = kt * TILE + threadIdx.x;
+    const bool in_range = j < N;
+    const size_t row = static_cast<size_t>(bm) * N;
+
+    int4 c;
+    if (in_range) {
+        c.x = lts ? clampN(lts[row + j], N) : N;
+        c.y = lte ? clampN(lte[row + j], N) : N;
+        c.z = uts ? clampN(uts[row + j], N) : 0;
+        c.w = ute ? clampN(ute[row + j], N) : 0;
+    } else {
+        c = make_int4(0, N, 0, 0);  // padding column: masked for every row
+    }
+    vec[static_cast<size_t>(bm) * Npad + j] = c;
+
+    // Per-tile min/max over in-range columns (padding columns are neutral).
+    const int BIG = 0x7fffffff;
+    const int mn_lts = block_min(in_range ? c.x : BIG, red);
+    const int mx_lts = block_max(in_range ? c.x : -BIG, red);
+    const int mn_lte = block_min(in_range ? c.y : BIG, red);
+    const int mx_lte = block_max(in_range ? c.y : -BIG, red);
+    const int mn_uts = block_min(in_range ? c.z : BIG, red);
+    const int mx_uts = block_max(in_range ? c.z : -BIG, red);
+    const int mn_ute = block_min(in_range ? c.w : BIG, red);
+    const int mx_ute = block_max(in_range ? c.w : -BIG, red);
+    const int j_first = kt * TILE;
+    const int j_last = min(kt * TILE + TILE, N) - 1;
+    const bool tail_kt = (N % TILE) != 0 && kt == T - 1;
+    const int cj = causal ? j : 0;
+
+    int count = 0;
+    int *my_list = bwd_list + (static_cast<size_t>(bm) * T + kt) * T;
+    for (int qt = 0; qt < T; ++qt) {
+        const int r0 = qt * TILE;
+        const int r1 = min(r0 + TILE, N);
+        int klass = -1;
+        // All columns covered by one mechanism alone.
+        if ((causal && j_first >= r1) || (mx_lts <= r0 && mn_lte >= r1) ||
+            (mx_uts <= r0 && mn_ute >= r1)) {
+            klass = FM_TILE_SKIP;
+        } else if ((!causal || j_last <= r0) && (mn_lts >= r1 || mx_lte <= r0) &&
+                   (mn_uts >= r1 || mx_ute <= r0)) {
+            // No mechanism reaches into the tile.
+            klass = FM_TILE_UNMASKED;
+        } else {
+            const bool col_cov = !in_range || covers(cj, c, r0, r1);
+            const bool col_touch =
+                in_range && ((causal && j > r0) || meets(c.x, c.y, r0, r1) || meets(c.z, c.w, r0, r1));
+            const int all_cov = __syncthreads_and(col_cov);
+            const int any_touch = __syncthreads_or(col_touch);
+            klass = all_cov ? FM_TILE_SKIP : (any_touch ? FM_TILE_PARTIAL : FM_TILE_UNMASKED);
+        }
+        if (threadIdx.x == 0) {
+            cls[(static_cast<size_t>(bm) * T + qt) * T + kt] = static_cast<uint8_t>(klass);
+            if (klass != FM_TILE_SKIP)
+                my_list[count] = (qt << 1) | ((klass == FM_TILE_PARTIAL || tail_kt) ? 1 : 0);
+        }
+        count += (klass != FM_TILE_SKIP);
+    }
+    if (threadIdx.x == 0) bwd_cnt[static_cast<size_t>(bm) * T + kt] = count;
+}
+
+// One warp per (mask head, q-tile): ordered list of its non-skipped k-tiles.
+__global__ void __launch_bounds__(128) fwd_lists_kernel(int N, int T, int rows,
+                                                        const uint8_t *__restrict__ cls,
+                                                        int *__restrict__ fwd_list,
+                                                        int *__restrict__ fwd_cnt) {
+    const int r = blockIdx.x * 4 + (threadIdx.x >> 5);  // (bm * T + qt)
+    const int lane = threadIdx.x & 31;
+    if (r >= rows) return;
+    const uint8_t *src = cls + static_cast<size_t>(r) * T;
+    int *dst = fwd_list + static_cast<size_t>(r) * T;
+    const bool has_tail = (N % TILE) != 0;
+    int count = 0;
+    for (int k0 = 0; k0 < T; k0 += 32) {
+        const int kt = k0 + lane;
+        const int c = kt < T ? src[kt] : FM_TILE_SKIP;
+        const bool keep = c != FM_TILE_SKIP;
+        const unsigned ballot = __ballot_sync(0xffffffffu, keep);
+        if (keep) {
+            const int pos = count + __popc(ballot & ((1u << lane) - 1u));
+            const bool need = c == FM_TILE_PARTIAL || (has_tail && kt == T - 1);
+            dst[pos] = (kt << 1) | (need ? 1 : 0);
+        }
+        count += __popc(ballot);
+    }
+    if (lane == 0) fwd_cnt[r] = count;
+}
+
+// Unmasked pairs per mask head: sum over columns of N - |masked rows of j|.
+__global__ void __launch_bounds__(1024) count_kernel(int N, int causal,
+                                                     const int32_t *__restrict__ lts,
+                                                     const int32_t *__restrict__ lte,
+                                                     const int32_t *__restrict__ uts,
+                                                     const int32_t *__restrict__ ute,
+                                                     unsigned long long *__restrict__ out) {
+    __shared__ unsigned long long red[32];
+    const int bm = blockIdx.x;
+    const size_t row = static_cast<size_t>(bm) * N;
+    unsigned long long acc = 0;
+    for (int j = threadIdx.x; j < N; j += blockDim.x) {
+        // Three intervals on [0, N): causal [0, j), LT, UT; measure of the union
+        // by inclusion-exclusion.
+        const int a0 = 0, b0 = causal ? j : 0;
+        const int a1 = lts ? clampN(lts[row + j], N) : N, b1 = lte ? clampN(lte[row + j], N) : N;
+        const int a2 = uts ? clampN(uts[row + j], N) : 0, b2 = ute ? clampN(ute[row + j], N) : 0;
+        auto len = [](int a, int b) { return b > a ? b - a : 0; };
+        auto len2 = [&](int a, int b, int c, int d) { return len(max(a, c), min(b, d)); };
+        const int s1 = len(a0, b0) + len(a1, b1) + len(a2, b2);
+        const int s2 = len2(a0, b0, a1, b1) + len2(a0, b0, a2, b2) + len2(a1, b1, a2, b2);
+        const int s3 = len(max(a0, max(a1, a2)), min(b0, min(b1, b2)));
+        acc += static_cast<unsigned long long>(N - (s1 - s2 + s3));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = acc;
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        unsigned long long v = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0ull;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        if (threadIdx.x == 0) out[bm] = v;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_classify(const Geometry &g, const MaskPtrs &m, const Workspace &ws,
+                            cudaStream_t st) {
+    dim3 grid(g.T, g.B * g.Hm);
+    classify_kernel<<<grid, 128, 0, st>>>(g.N, g.T, g.Npad, g.Hm, g.causal, m.lts, m.lte, m.uts,
+                                          m.ute, ws.vec, ws.cls, ws.bwd_list, ws.bwd_cnt);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_fwd_lists(const Geometry &g, const Workspace &ws, cudaStream_t st) {
+    const int rows = g.B * g.Hm * g.T;
+    fwd_lists_kernel<<<(rows + 3) / 4, 128, 0, st>>>(g.N, g.T, rows, ws.cls, ws.fwd_list,
+                                                     ws.fwd_cnt);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_count(const Geometry &g, const MaskPtrs &m, unsigned long long *counts,
+                         cudaStream_t st) {
+    count_kernel<<<g.B * g.Hm, 1024, 0, st>>>(g.N, g.causal, m.lts, m.lte, m.uts, m.ute,
+                                               counts);
+    return cudaGetLastError();
+}
+
+unsigned read_clear_error_classify() {
+    unsigned v = 0, zero = 0;
+    if (cudaMemcpyFromSymbol(&v, g_err_classify, sizeof(v)) != cudaSuccess) return 0;
+    if (v) cudaMemcpyToSymbol(g_err_classify, &zero, sizeof(zero));
+    return v;
+}
+
+}  // namespace fm

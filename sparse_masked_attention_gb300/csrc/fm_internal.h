@@ -1,0 +1,92 @@
+// fm_internal.h -- host-side structures shared by the library's translation
+// units: problem geometry, the workspace layout and the kernel launchers.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "flashmask.h"
+
+namespace fm {
+
+constexpr int TILE = 128;  // tile edge of the tile map and of the list entries
+
+struct Geometry {
+    int B, H, Hm, N, d, dv;
+    int T;       // ceil(N / 128)
+    int Npad;    // T * 128
+    float scale;
+    int causal;
+    uint64_t timeout_ns;
+    int deterministic;
+};
+
+// Normalised mask boundaries per key column: (LTS, LTE, UTS, UTE) clamped to
+// [0, N]; absent intervals empty; padding columns j >= N masked for every row.
+struct Workspace {
+    int4 *vec;         // [B*Hm][Npad]
+    uint8_t *cls;      // [B*Hm][T][T] tile classes
+    int *fwd_list;     // [B*Hm][T][T] per q-tile: (kt << 1) | needs_mask
+    int *fwd_cnt;      // [B*Hm][T]
+    int *bwd_list;     // [B*Hm][T][T] per k-tile: (qt << 1) | needs_mask
+    int *bwd_cnt;      // [B*Hm][T]
+    float *lse2;       // [B*H][Npad] log2-domain LSE, +inf for empty / padding rows
+    float *delta;      // [B*H][Npad] D_i = sum_c dO_ic O_ic
+};
+
+// Optional per-kernel event recording (fm_options.kernel_events).
+struct Recorder {
+    cudaEvent_t *ev = nullptr;
+    int n = 0;
+    int i = 0;
+    void before(cudaStream_t s) {
+        if (ev && 2 * i + 1 < n) cudaEventRecord(ev[2 * i], s);
+    }
+    void after(cudaStream_t s) {
+        if (ev && 2 * i + 1 < n) cudaEventRecord(ev[2 * i + 1], s);
+        ++i;
+    }
+};
+
+// Lays the workspace out from `base` (may be nullptr to size it); returns bytes.
+size_t carve_workspace(const Geometry &g, bool bwd, void *base, Workspace *ws);
+
+struct MaskPtrs {
+    const int32_t *lts, *lte, *uts, *ute;
+};
+
+// classify.cu
+cudaError_t launch_classify(const Geometry &g, const MaskPtrs &m, const Workspace &ws,
+                            cudaStream_t st);
+cudaError_t launch_fwd_lists(const Geometry &g, const Workspace &ws, cudaStream_t st);
+cudaError_t launch_count(const Geometry &g, const MaskPtrs &m, unsigned long long *counts,
+                         cudaStream_t st);
+unsigned read_clear_error_classify();
+
+// fwd.cu
+struct FwdArgs {
+    const CUtensorMap *tm_q, *tm_k, *tm_v;
+    void *o;
+    float *lse;
+};
+cudaError_t launch_fwd(const Geometry &g, const Workspace &ws, const FwdArgs &a,
+                       cudaStream_t st);
+unsigned read_clear_error_fwd();
+
+// bwd.cu
+struct BwdArgs {
+    // key-side (dK/dV) kernel maps: q/dO boxes of its query sub-tile, k/v of 128 rows
+    const CUtensorMap *tm_q, *tm_k, *tm_v, *tm_do;
+    // query-side (dQ) kernel maps: q/dO boxes of 128 rows, k/v of its key sub-tile
+    const CUtensorMap *tm_q_dq, *tm_k_dq, *tm_v_dq, *tm_do_dq;
+    const void *o, *dout;
+    const float *lse;
+    void *dq, *dk, *dv;
+};
+cudaError_t launch_bwd(const Geometry &g, const Workspace &ws, const BwdArgs &a,
+                       cudaStream_t st, Recorder &rec);
+unsigned read_clear_error_bwd();
+
+}  // namespace fm

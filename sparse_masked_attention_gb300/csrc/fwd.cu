@@ -1,0 +1,435 @@
+// fwd.cu -- forward of FlashMask masked attention on tcgen05 tensor cores.
+//
+//   O = softmax(Q K^T * scale + M) V        (FlashMask README, "Formulation")
+//
+// One CTA owns one 128-row query tile of one (batch, head).  It walks only
+// the key tiles the tile map kept for that query tile ("skip unnecessary
+// computation", FlashMask abstract).  Roles, by warp:
+//   warp 0      TMA producer: Q once, then K and V tiles into shared-memory rings
+//   warp 1      allocates TMEM; lane 0 issues every tcgen05.mma
+//   warps 2..   NWG softmax warpgroups.  Thread t of a group owns query row t,
+//               which is TMEM lane t.
+// With NWG = 2, the two groups take alternate key tiles of the same query
+// tile.  Each group keeps its own running max, running sum and O accumulator
+// in TMEM.  The two halves are merged in the epilogue.  While one group runs
+// exp2 on its S tile, the tensor core works on the other group's tiles.
+//
+// Per key tile u, owned by group w:
+//   S_w  = Q K_u^T                (SS MMA, fp32 in TMEM)
+//   softmax thread: S -> registers; apply the mask elementwise on partial
+//   tiles only; online max/sum in the log2 domain with exp2; P -> TMEM as
+//   bf16, in place of S; the O_w rescale is deferred until the max has grown
+//   by more than 2^8
+//   O_w += P V_u                  (TS MMA: P read from TMEM, V from smem)
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include "fm_device.cuh"
+#include "fm_internal.h"
+
+namespace fm {
+
+static __device__ unsigned g_err_fwd;
+
+namespace {
+
+struct FwdParams {
+    const int4 *vec;
+    const int *list;
+    const int *cnt;
+    __nv_bfloat16 *o;
+    float *lse;
+    int N, H, Hm, T, Npad, causal;
+    float sl2;  // scale * log2(e)
+    uint64_t timeout_ns;
+};
+
+template <int D_, int DV_, int BN_, int NWG_, int NSB_, int KS_, int VS_>
+struct FwdCfg {
+    static constexpr int D = D_, DV = DV_, BN = BN_, NWG = NWG_, NSB = NSB_, KS = KS_, VS = VS_;
+    static constexpr int BM = 128;
+    static constexpr int SUB = TILE / BN;  // key sub-tiles per list entry
+    static constexpr int Q_BYTES = BM * D * 2;
+    static constexpr int K_BYTES = BN * D * 2;
+    static constexpr int V_BYTES = BN * DV * 2;
+    static constexpr int OFF_Q = 0;
+    static constexpr int OFF_K = OFF_Q + Q_BYTES;
+    static constexpr int OFF_V = OFF_K + KS * K_BYTES;
+    static constexpr int OFF_BAR = OFF_V + VS * V_BYTES;
+    // q_full, k_full[KS], k_empty[KS], v_full[VS], v_empty[VS],
+    // s_full[NWG*NSB], p_full[NWG*NSB], pv_done[NWG*2]
+    static constexpr int NBAR = 1 + 2 * KS + 2 * VS + 2 * NWG * NSB + 2 * NWG;
+    static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+    static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
+    static constexpr int TM_O = 0;
+    static constexpr int TM_S = NWG * DV;
+    static constexpr int TM_COLS = 512;
+    static constexpr int THREADS = 64 + NWG * 128;
+    static_assert(TM_S + NWG * NSB * BN <= TM_COLS, "TMEM budget");
+    static_assert(D % 64 == 0 && DV % 64 == 0 && (BN == 64 || BN == 128), "tile shape");
+    static_assert(DV <= 256 && BN % 32 == 0, "MMA shape");
+    static_assert(NWG * 128 * 2 * 4 <= K_BYTES, "merge statistics alias K stage 0");
+    static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+};
+
+// Warp-uniform bounded wait: every lane polls, the warp agrees on the result.
+__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, uint64_t tmo,
+                                          volatile int *abort) {
+    const bool ok = mbar_wait(bar, parity, tmo, abort, &g_err_fwd);
+    return __all_sync(0xffffffffu, ok);
+}
+
+template <class C>
+__global__ void __launch_bounds__(C::THREADS, 1)
+    fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+               const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t *sQ = smem + C::OFF_Q;
+    uint8_t *sK = smem + C::OFF_K;
+    uint8_t *sV = smem + C::OFF_V;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
+    uint64_t *q_full = bars;
+    uint64_t *k_full = q_full + 1;
+    uint64_t *k_empty = k_full + C::KS;
+    uint64_t *v_full = k_empty + C::KS;
+    uint64_t *v_empty = v_full + C::VS;
+    uint64_t *s_full = v_empty + C::VS;
+    uint64_t *p_full = s_full + C::NWG * C::NSB;
+    uint64_t *pv_done = p_full + C::NWG * C::NSB;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
+    volatile int *abort = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int qt = p.T - 1 - static_cast<int>(blockIdx.x);  // heaviest query tiles first
+    const int h = blockIdx.y, b = blockIdx.z;
+    const int bm = b * p.Hm + (p.Hm == 1 ? 0 : h);
+    const int n_entries = p.cnt[static_cast<size_t>(bm) * p.T + qt];
+    const int *entries = p.list + (static_cast<size_t>(bm) * p.T + qt) * p.T;
+    // key tiles of BN columns; none after a bounded wait gave up anywhere
+    const int n = (*reinterpret_cast<volatile unsigned *>(&g_err_fwd) != 0) ? 0
+                                                                            : n_entries * C::SUB;
+    const uint64_t tmo = p.timeout_ns;
+
+    if (threadIdx.x == 0) {
+        mbar_init(q_full, 1);
+        for (int i = 0; i < C::KS; ++i) {
+            mbar_init(&k_full[i], 1);
+            mbar_init(&k_empty[i], 1);
+        }
+        for (int i = 0; i < C::VS; ++i) {
+            mbar_init(&v_full[i], 1);
+            mbar_init(&v_empty[i], 1);
+        }
+        for (int i = 0; i < C::NWG * C::NSB; ++i) {
+            mbar_init(&s_full[i], 1);
+            mbar_init(&p_full[i], 128);
+        }
+        for (int i = 0; i < C::NWG * 2; ++i) mbar_init(&pv_done[i], 1);
+        *abort = 0;
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, C::TM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    auto key0_of = [&](int u) {
+        return (entries[u / C::SUB] >> 1) * TILE + (u % C::SUB) * C::BN;
+    };
+    constexpr int L = C::NWG * C::NSB;  // S tiles in flight
+
+    if (warp == 0) {
+        // ------------------------------------------------------ TMA producer
+        if (lane == 0 && n > 0) {
+            prefetch_tmap(&tm_q);
+            prefetch_tmap(&tm_k);
+            prefetch_tmap(&tm_v);
+            mbar_arrive_expect_tx(q_full, C::Q_BYTES);
+#pragma unroll
+            for (int c = 0; c < C::D / 64; ++c)
+                tma_load_4d(sQ + c * C::BM * 128, &tm_q, q_full, c * 64, h, qt * TILE, b);
+            auto load_k = [&](int u) -> bool {
+                const int s = u % C::KS;
+                if (u >= C::KS &&
+                    !mbar_wait(&k_empty[s], ((u / C::KS) - 1) & 1, tmo, abort, &g_err_fwd))
+                    return false;
+                mbar_arrive_expect_tx(&k_full[s], C::K_BYTES);
+                const int key0 = key0_of(u);
+#pragma unroll
+                for (int c = 0; c < C::D / 64; ++c)
+                    tma_load_4d(sK + s * C::K_BYTES + c * C::BN * 128, &tm_k, &k_full[s], c * 64,
+                                h, key0, b);
+                return true;
+            };
+            auto load_v = [&](int u) -> bool {
+                const int s = u % C::VS;
+                if (u >= C::VS &&
+                    !mbar_wait(&v_empty[s], ((u / C::VS) - 1) & 1, tmo, abort, &g_err_fwd))
+                    return false;
+                mbar_arrive_expect_tx(&v_full[s], C::V_BYTES);
+                const int key0 = key0_of(u);
+#pragma unroll
+                for (int c = 0; c < C::DV / 64; ++c)
+                    tma_load_4d(sV + s * C::V_BYTES + c * C::BN * 128, &tm_v, &v_full[s], c * 64,
+                                h, key0, b);
+                return true;
+            };
+            bool ok = true;
+            for (int u = 0; u < L && u < n && ok; ++u) ok = load_k(u);
+            for (int u = 0; u < n && ok; ++u) {
+                ok = load_v(u);
+                if (ok && u + L < n) ok = load_k(u + L);
+            }
+        }
+    } else if (warp == 1) {
+        // --------------------------------------------------- tcgen05 issuer
+        if (lane == 0 && n > 0) {
+            constexpr uint32_t IDESC_S = idesc_bf16(128, C::BN, false, false);
+            constexpr uint32_t IDESC_PV = idesc_bf16(128, C::DV, false, true);
+            const uint32_t q_addr = smem_u32(sQ);
+            const uint32_t k_addr = smem_u32(sK);
+            const uint32_t v_addr = smem_u32(sV);
+            auto issue_s = [&](int u) -> bool {
+                const int w = u % C::NWG, lu = u / C::NWG, sb = w * C::NSB + lu % C::NSB;
+                const int s = u % C::KS;
+                if (!mbar_wait(&k_full[s], (u / C::KS) & 1, tmo, abort, &g_err_fwd)) return false;
+                tc_fence_after();
+                const uint32_t d_tmem = tmem + C::TM_S + sb * C::BN;
+#pragma unroll
+                for (int k = 0; k < C::D / 16; ++k) {
+                    const uint64_t ad =
+                        sdesc_sw128(q_addr + (k / 4) * (C::BM * 128) + (k % 4) * 32, 16, 1024);
+                    const uint64_t bd = sdesc_sw128(
+                        k_addr + s * C::K_BYTES + (k / 4) * (C::BN * 128) + (k % 4) * 32, 16, 1024);
+                    mma_ss(d_tmem, ad, bd, IDESC_S, k > 0 ? 1u : 0u);
+                }
+                mma_commit(&k_empty[s]);
+                mma_commit(&s_full[sb]);
+                return true;
+            };
+            bool ok = mbar_wait(q_full, 0, tmo, abort, &g_err_fwd);
+            for (int u = 0; u < L && u < n && ok; ++u) ok = issue_s(u);
+            for (int u = 0; u < n && ok; ++u) {
+                const int w = u % C::NWG, lu = u / C::NWG, sb = w * C::NSB + lu % C::NSB;
+                if (!mbar_wait(&p_full[sb], (lu / C::NSB) & 1, tmo, abort, &g_err_fwd)) break;
+                const int vs = u % C::VS;
+                if (!mbar_wait(&v_full[vs], (u / C::VS) & 1, tmo, abort, &g_err_fwd)) break;
+                tc_fence_after();
+                const uint32_t o_tmem = tmem + C::TM_O + w * C::DV;
+                const uint32_t p_tmem = tmem + C::TM_S + sb * C::BN;
+#pragma unroll
+                for (int k = 0; k < C::BN / 16; ++k) {
+                    const uint64_t bd =
+                        sdesc_sw128(v_addr + vs * C::V_BYTES + k * 2048, C::BN * 128, 1024);
+                    mma_ts(o_tmem, p_tmem + k * 8, bd, IDESC_PV, (lu > 0 || k > 0) ? 1u : 0u);
+                }
+                mma_commit(&v_empty[vs]);
+                mma_commit(&pv_done[w * 2 + (lu & 1)]);
+                if (u + L < n) ok = issue_s(u + L);
+            }
+        }
+    } else {
+        // ------------------------------------------------ softmax warpgroups
+        const int wg = (warp - 2) >> 2;
+        const int quad = warp & 3;
+        const int row = quad * 32 + lane;
+        const int grow = qt * TILE + row;
+        const uint32_t lane_base = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+        const int n_my = n > wg ? (n - wg + C::NWG - 1) / C::NWG : 0;
+        const float NEG_INF = -INFINITY;
+        const int4 *vec = p.vec + static_cast<size_t>(bm) * p.Npad;
+        float m_ref = NEG_INF, l_sum = 0.f;
+
+        for (int lu = 0; lu < n_my; ++lu) {
+            const int u = lu * C::NWG + wg;
+            const int sb = wg * C::NSB + lu % C::NSB;
+            if (!warp_wait(&s_full[sb], (lu / C::NSB) & 1, tmo, abort)) break;
+            tc_fence_after();
+            float x[C::BN];
+            const uint32_t s_addr = lane_base + C::TM_S + sb * C::BN;
+#pragma unroll
+            for (int c = 0; c < C::BN / 32; ++c) {
+                uint32_t r[32];
+                tmem_ld32(s_addr + c * 32, r);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) x[c * 32 + i] = __uint_as_float(r[i]) * p.sl2;
+            }
+            if (entries[u / C::SUB] & 1) {
+                const int key0 = key0_of(u);
+#pragma unroll
+                for (int jj = 0; jj < C::BN; ++jj) {
+                    const int4 cv = __ldg(vec + key0 + jj);
+                    if (masked_at(grow, key0 + jj, cv, p.causal)) x[jj] = NEG_INF;
+                }
+            }
+            float mx = NEG_INF;
+#pragma unroll
+            for (int jj = 0; jj < C::BN; ++jj) mx = fmaxf(mx, x[jj]);
+            const float m_new = fmaxf(m_ref, mx);
+            const bool need = (m_ref != NEG_INF) && (m_new > m_ref + 8.0f);
+            if (m_ref == NEG_INF) m_ref = m_new;
+            if (__any_sync(0xffffffffu, need)) {
+                // O_w holds the sum over this group's earlier tiles; rescale it.
+                const float alpha = need ? ex2(m_ref - m_new) : 1.0f;
+                if (need) m_ref = m_new;
+                l_sum *= alpha;
+                const int pl = lu - 1;
+                if (!warp_wait(&pv_done[wg * 2 + (pl & 1)], (pl >> 1) & 1, tmo, abort)) break;
+                tc_fence_after();
+                const uint32_t o_addr = lane_base + C::TM_O + wg * C::DV;
+#pragma unroll
+                for (int c = 0; c < C::DV / 32; ++c) {
+                    uint32_t r[32];
+                    tmem_ld32(o_addr + c * 32, r);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+                    tmem_st32(o_addr + c * 32, r);
+                }
+            }
+            const float m_use = (m_ref == NEG_INF) ? 0.0f : m_ref;
+#pragma unroll
+            for (int c = 0; c < C::BN / 64; ++c) {
+                uint32_t r[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const float p0 = ex2(x[c * 64 + 2 * i] - m_use);
+                    const float p1 = ex2(x[c * 64 + 2 * i + 1] - m_use);
+                    l_sum += p0 + p1;
+                    r[i] = pack_bf16(p0, p1);
+                }
+                tmem_st32(s_addr + c * 32, r);
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(&p_full[sb]);
+        }
+
+        // ------------------------------------------------------- epilogue
+        if (n_my > 0) {
+            const int pl = n_my - 1;
+            warp_wait(&pv_done[wg * 2 + (pl & 1)], (pl >> 1) & 1, tmo, abort);
+        }
+        tc_fence_after();
+        __nv_bfloat16 *orow =
+            p.o + ((static_cast<size_t>(b) * p.N + grow) * p.H + h) * static_cast<size_t>(C::DV);
+        const bool store = grow < p.N;
+        float m_all = m_ref, l_all = l_sum, a0 = 1.f, a1 = 0.f;
+        float l0 = l_sum, l1 = 0.f;
+        int c_begin = 0, c_end = C::DV / 32;
+        if constexpr (C::NWG == 2) {
+            float *stats = reinterpret_cast<float *>(sK);  // K stage 0 is idle by now
+            stats[(wg * 128 + row) * 2 + 0] = m_ref;
+            stats[(wg * 128 + row) * 2 + 1] = l_sum;
+            tc_fence_before();
+            named_bar_sync(1, 256);
+            tc_fence_after();
+            const float mA = stats[row * 2 + 0], lA = stats[row * 2 + 1];
+            const float mB = stats[(128 + row) * 2 + 0], lB = stats[(128 + row) * 2 + 1];
+            m_all = fmaxf(mA, mB);
+            a0 = lA > 0.f ? ex2(mA - m_all) : 0.f;
+            a1 = lB > 0.f ? ex2(mB - m_all) : 0.f;
+            l0 = lA;
+            l1 = lB;
+            l_all = a0 * lA + a1 * lB;
+            c_begin = wg * (C::DV / 64);
+            c_end = c_begin + C::DV / 64;
+        }
+        const float inv = l_all > 0.f ? 1.0f / l_all : 0.f;
+        for (int c = c_begin; c < c_end; ++c) {
+            uint32_t r0[32];
+            tmem_ld32(lane_base + C::TM_O + c * 32, r0);
+            float o[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = l0 > 0.f ? a0 * __uint_as_float(r0[i]) : 0.f;
+            if constexpr (C::NWG == 2) {
+                uint32_t r1[32];
+                tmem_ld32(lane_base + C::TM_O + C::DV + c * 32, r1);
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    o[i] += l1 > 0.f ? a1 * __uint_as_float(r1[i]) : 0.f;
+            }
+            if (store) {
+                uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
+#pragma unroll
+                for (int v = 0; v < 4; ++v) {
+                    uint4 w;
+                    w.x = pack_bf16(o[v * 8 + 0] * inv, o[v * 8 + 1] * inv);
+                    w.y = pack_bf16(o[v * 8 + 2] * inv, o[v * 8 + 3] * inv);
+                    w.z = pack_bf16(o[v * 8 + 4] * inv, o[v * 8 + 5] * inv);
+                    w.w = pack_bf16(o[v * 8 + 6] * inv, o[v * 8 + 7] * inv);
+                    dst[v] = w;
+                }
+            }
+        }
+        if (wg == 0 && store) {
+            const float ln2 = 0.69314718055994530942f;
+            p.lse[(static_cast<size_t>(b) * p.H + h) * p.N + grow] =
+                l_all > 0.f ? (m_all + lg2(l_all)) * ln2 : NEG_INF;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, C::TM_COLS);
+    }
+}
+
+template <class C>
+cudaError_t launch_cfg(const Geometry &g, const Workspace &ws, const FwdArgs &a,
+                       cudaStream_t st) {
+    FwdParams p;
+    p.vec = ws.vec;
+    p.list = ws.fwd_list;
+    p.cnt = ws.fwd_cnt;
+    p.o = static_cast<__nv_bfloat16 *>(a.o);
+    p.lse = a.lse;
+    p.N = g.N;
+    p.H = g.H;
+    p.Hm = g.Hm;
+    p.T = g.T;
+    p.Npad = g.Npad;
+    p.causal = g.causal;
+    p.sl2 = g.scale * 1.4426950408889634f;
+    p.timeout_ns = g.timeout_ns;
+    auto kern = fwd_kernel<C>;
+    cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    dim3 grid(g.T, g.H, g.B);
+    kern<<<grid, C::THREADS, C::SMEM_BYTES, st>>>(*a.tm_q, *a.tm_k, *a.tm_v, p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd(const Geometry &g, const Workspace &ws, const FwdArgs &a,
+                       cudaStream_t st) {
+    if (g.d == 64 && g.dv == 64) return launch_cfg<FwdCfg<64, 64, 128, 2, 1, 3, 3>>(g, ws, a, st);
+    if (g.d == 128 && g.dv == 128)
+        return launch_cfg<FwdCfg<128, 128, 128, 2, 1, 3, 3>>(g, ws, a, st);
+    if (g.d == 192 && g.dv == 128)
+        return launch_cfg<FwdCfg<192, 128, 128, 2, 1, 2, 2>>(g, ws, a, st);
+    if (g.d == 256 && g.dv == 256)
+        return launch_cfg<FwdCfg<256, 256, 64, 1, 2, 2, 2>>(g, ws, a, st);
+    return cudaErrorInvalidValue;
+}
+
+unsigned read_clear_error_fwd() {
+    unsigned v = 0, zero = 0;
+    if (cudaMemcpyFromSymbol(&v, g_err_fwd, sizeof(v)) != cudaSuccess) return 0;
+    if (v) cudaMemcpyToSymbol(g_err_fwd, &zero, sizeof(zero));
+    return v;
+}
+
+}  // namespace fm

@@ -1,0 +1,93 @@
+"""Host-side checks of the C ABI (no GPU needed).
+
+The library loads and exports every function that include/flashmask.h
+declares.  Its host-only logic answers without touching a device: workspace
+sizing, status strings, and argument validation that fails before any CUDA
+call.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+from sparse_masked_attention_gb300 import binding as B
+from sparse_masked_attention_gb300 import build as build_mod
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build_mod.build()
+    return B.load()
+
+
+def _declared():
+    text = open(os.path.join(ROOT, "include", "flashmask.h")).read()
+    return sorted(set(re.findall(r"\b(flashmask_\w+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = _declared()
+    assert len(names) >= 7
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in flashmask.h but not exported"
+    assert set(names) == set(B.EXPORTS)
+
+
+def test_error_strings(lib):
+    for s in range(6):
+        assert B.flashmask_error_string(s)
+    assert B.flashmask_error_string(99) == "unknown status"
+
+
+def _prob(**kw):
+    p = dict(B=1, H=2, Hm=1, N=1000, d=128, dv=128, scale=0.0, causal=1)
+    p.update(kw)
+    return B.fm_problem(**p)
+
+
+def test_workspace_size_host_only(lib):
+    fwd = B.flashmask_workspace_size(_prob(), None, 0)
+    bwd = B.flashmask_workspace_size(_prob(), None, 1)
+    T = 8
+    # normalised vectors + tile map + two lists + counts, each 256-byte aligned
+    assert fwd >= 1024 * 16 + T * T + 2 * T * T * 4 + 2 * T * 4
+    assert bwd >= fwd + 2 * 2 * 1024 * 4
+    assert fwd % 256 == 0 and bwd % 256 == 0
+
+
+@pytest.mark.parametrize("kw", [dict(N=0), dict(B=0), dict(Hm=3), dict(causal=2),
+                                dict(d=96, dv=96), dict(d=128, dv=64), dict(scale=float("nan"))])
+def test_invalid_problems_have_no_workspace(lib, kw):
+    assert B.flashmask_workspace_size(_prob(**kw), None, 0) == 0
+
+
+def test_invalid_args_rejected_before_cuda(lib):
+    p = _prob()
+    st = B.flashmask_fwd(p, None, None, None, None, None, None, None, None, None, None, None, 0,
+                         None)
+    assert st == B.FM_ERR_INVALID_ARG
+    # misaligned pointer
+    st = B.flashmask_fwd(p, None, 8, 16, 16, None, None, None, None, 16, 16, 256, 1 << 20, None)
+    assert st == B.FM_ERR_INVALID_ARG
+    st = B.flashmask_bwd(p, None, *([None] * 14), 0, None)
+    assert st == B.FM_ERR_INVALID_ARG
+    # unsupported head dims, all pointers plausible
+    p2 = _prob(d=96, dv=96)
+    st = B.flashmask_fwd(p2, None, 256, 256, 256, None, None, None, None, 256, 256, 256, 1 << 30,
+                         None)
+    assert st == B.FM_ERR_UNSUPPORTED
+    # half-given interval pair
+    st = B.flashmask_fwd(p, None, 256, 256, 256, 256, None, None, None, 256, 256, 256, 1 << 30,
+                         None)
+    assert st == B.FM_ERR_INVALID_ARG
+    # workspace too small
+    st = B.flashmask_fwd(p, None, 256, 256, 256, None, None, None, None, 256, 256, 256, 16, None)
+    assert st == B.FM_ERR_WORKSPACE
+    # reserved option
+    opt = B.fm_options(0, 1, 0, None, 0)
+    st = B.flashmask_fwd(p, opt, 256, 256, 256, None, None, None, None, 256, 256, 256, 1 << 30,
+                         None)
+    assert st == B.FM_ERR_INVALID_ARG

@@ -1,0 +1,170 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle.
+
+Sizes are ones the oracle finishes in seconds.  They span several 128-tiles
+and include a ragged tail, every supported (d, dv), every mask family, shared
+and per-head masks, fully masked rows and N = 1.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from sparse_masked_attention_gb300 import attention as fm
+from sparse_masked_attention_gb300 import workloads as W
+
+from gpu_util import (assert_close, assert_lse, check_head_full, cuda_mask, head, mask_slice,
+                      run_fwd_bwd)
+
+pytestmark = pytest.mark.gpu
+
+DIMS = [(64, 64), (128, 128), (192, 128), (256, 256)]
+
+
+def _family(name, N, B, seed):
+    rng = np.random.default_rng(seed)
+    if name == "causal":
+        return W.causal(N, B)
+    if name == "full":
+        return W.full(N, B)
+    if name == "sliding":
+        return W.sliding_window(N, 200, B)
+    if name == "causal_document":
+        return W.causal_document(N, [W.uniform_lengths(rng, 50, 300, N) for _ in range(B)])
+    if name == "prefix_lm":
+        return W.prefix_lm(N, 300, B)
+    if name == "share_question":
+        return W.share_question(
+            N, [W.share_question_groups(rng, N, (100, 300), (2, 4), (50, 200)) for _ in range(B)])
+    if name == "block_sparse":
+        return W.block_sparse(N, rng, B)
+    if name == "global_sliding":
+        return W.global_sliding(N, 64, 300, B)
+    if name == "random":
+        return W.random_vectors(N, rng, B, 1, causal_flag=bool(seed % 2))
+    raise ValueError(name)
+
+
+FAMILIES = ["causal", "full", "sliding", "causal_document", "prefix_lm", "share_question",
+            "block_sparse", "global_sliding", "random"]
+
+
+@pytest.mark.parametrize("family", FAMILIES)
+@pytest.mark.parametrize("N", [1000, 384])
+def test_tile_map_bit_exact(family, N):
+    B = 2
+    mask = _family(family, N, B, seed=N)
+    lts, lte, uts, ute = cuda_mask(mask)
+    got = fm.classify(N, B, 1, lts, lte, uts, ute, mask.causal).cpu().numpy()
+    for b in range(B):
+        want, visible = oracle.tilemap(N, mask.slice(b), mask.causal)
+        np.testing.assert_array_equal(got[b], want)
+    cnt = fm.count_unmasked(N, B, 1, lts, lte, uts, ute, mask.causal).cpu().numpy()
+    for b in range(B):
+        assert int(cnt[b]) == oracle.count_unmasked(N, mask.slice(b), mask.causal)
+
+
+@pytest.mark.parametrize("d,dv", DIMS)
+@pytest.mark.parametrize("family", ["causal", "causal_document", "share_question", "random"])
+def test_fwd_bwd_parity_dims(d, dv, family):
+    B, H, N = 1, 2, 1000
+    q, k, v, do = W.make_inputs(B, N, H, d, dv, seed=1, device="cuda")
+    mask = _family(family, N, B, seed=7)
+    o, lse, grads = run_fwd_bwd(q, k, v, do, mask)
+    for h in range(H):
+        check_head_full(q, k, v, do, mask, o, lse, grads, 0, h)
+
+
+@pytest.mark.parametrize("family", FAMILIES)
+def test_fwd_bwd_parity_families(family):
+    B, H, N, d = 2, 2, 777, 128
+    q, k, v, do = W.make_inputs(B, N, H, d, d, seed=2, device="cuda")
+    mask = _family(family, N, B, seed=3)
+    o, lse, grads = run_fwd_bwd(q, k, v, do, mask)
+    for b in range(B):
+        for h in range(H):
+            check_head_full(q, k, v, do, mask, o, lse, grads, b, h)
+
+
+def test_tiny_causal_document_config():
+    """The 3-document N=256, d=dv=64 workload, every output element."""
+    cfg = W.CONFIGS["tiny_causal_document"]
+    q, k, v, do = W.make_inputs(cfg["B"], cfg["N"], cfg["H"], cfg["d"], cfg["dv"], seed=0,
+                                device="cuda")
+    mask = W.make_mask(cfg, seed=0)
+    o, lse, grads = run_fwd_bwd(q, k, v, do, mask)
+    for h in range(cfg["H"]):
+        check_head_full(q, k, v, do, mask, o, lse, grads, 0, h)
+
+
+def test_per_head_masks():
+    B, H, N, d = 1, 3, 600, 64
+    rng = np.random.default_rng(11)
+    q, k, v, do = W.make_inputs(B, N, H, d, d, seed=4, device="cuda")
+    mask = W.random_vectors(N, rng, B, Hm=H, causal_flag=True, lo=0, hi=N)
+    o, lse, grads = run_fwd_bwd(q, k, v, do, mask)
+    for h in range(H):
+        check_head_full(q, k, v, do, mask, o, lse, grads, 0, h)
+
+
+def test_fully_masked_rows():
+    """Rows [130, 260) see no key: O = 0, LSE = -inf, dQ = 0."""
+    B, H, N, d = 1, 1, 400, 128
+    q, k, v, do = W.make_inputs(B, N, H, d, d, seed=5, device="cuda")
+    lts = np.full((1, 1, N), 130, np.int32)
+    lte = np.full((1, 1, N), 260, np.int32)
+    mask = W.Mask(N, False, lts=lts, lte=lte, family="custom", meta=[{}])
+    o, lse, grads = run_fwd_bwd(q, k, v, do, mask)
+    assert bool((o[0, 130:260] == 0).all())
+    assert bool(torch.isneginf(lse[0, 0, 130:260]).all())
+    assert bool((grads[0][0, 130:260] == 0).all())
+    check_head_full(q, k, v, do, mask, o, lse, grads, 0, 0)
+
+
+@pytest.mark.parametrize("N", [1, 2, 127, 128, 129])
+def test_small_and_edge_lengths(N):
+    B, H, d = 1, 2, 64
+    q, k, v, do = W.make_inputs(B, N, H, d, d, seed=6, device="cuda")
+    for mask in (W.causal(N), W.full(N)):
+        o, lse, grads = run_fwd_bwd(q, k, v, do, mask)
+        for h in range(H):
+            check_head_full(q, k, v, do, mask, o, lse, grads, 0, h)
+
+
+def test_scale_override():
+    B, H, N, d = 1, 1, 300, 128
+    q, k, v, do = W.make_inputs(B, N, H, d, d, seed=8, device="cuda")
+    mask = W.causal(N)
+    o, lse, grads = run_fwd_bwd(q, k, v, do, mask, scale=0.05)
+    check_head_full(q, k, v, do, mask, o, lse, grads, 0, 0, scale=0.05)
+
+
+@pytest.mark.parametrize("d,dv", [(128, 128), (192, 128), (256, 256)])
+def test_deterministic_backward_bit_identical(d, dv):
+    B, H, N = 1, 2, 900
+    q, k, v, do = W.make_inputs(B, N, H, d, dv, seed=9, device="cuda")
+    mask = _family("causal_document", N, B, seed=1)
+    o, lse, g1 = run_fwd_bwd(q, k, v, do, mask, deterministic=True)
+    _, _, g2 = run_fwd_bwd(q, k, v, do, mask, deterministic=True)
+    for a, b in zip(g1, g2):
+        assert torch.equal(a, b)
+
+
+def test_autograd_function():
+    B, H, N, d = 1, 2, 300, 64
+    q, k, v, do = W.make_inputs(B, N, H, d, d, seed=10, device="cuda")
+    mask = W.sliding_window(N, 100)
+    lts, lte, uts, ute = cuda_mask(mask)
+    qq, kk, vv = (x.clone().requires_grad_(True) for x in (q, k, v))
+    o = fm.flashmask_attention(qq, kk, vv, lts, lte, uts, ute, causal=True)
+    o.backward(do)
+    o2, lse2, g = run_fwd_bwd(q, k, v, do, mask)
+    assert torch.equal(o, o2)
+    for a, b in zip((qq.grad, kk.grad, vv.grad), g):
+        assert torch.equal(a, b)
+
+
+def test_timeout_status_is_clean():
+    """No kernel of the suite left a timeout in the device error word."""
+    fm.get_error()
