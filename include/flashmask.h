@@ -154,6 +154,11 @@ fm_status flashmask_get_error(void *stream);
 /* Static text for a status code. */
 const char *flashmask_error_string(fm_status s);
 
+/* Text of the last FM_ERR_CUDA raised on the calling host thread: the failed
+ * step and the CUDA error string.  Empty if none.  Valid until the next call
+ * on the same thread. */
+const char *flashmask_last_error_detail(void);
+
 #ifdef __cplusplus
 }
 #endif

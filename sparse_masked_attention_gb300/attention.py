@@ -22,7 +22,9 @@ class FlashMaskError(RuntimeError):
 
 def _check(status: int, what: str):
     if status != _b.FM_OK:
-        raise FlashMaskError(f"{what}: {_b.flashmask_error_string(status)} (status {status})")
+        detail = _b.flashmask_last_error_detail() if status == _b.FM_ERR_CUDA else ""
+        raise FlashMaskError(f"{what}: {_b.flashmask_error_string(status)} (status {status})"
+                             + (f" [{detail}]" if detail else ""))
 
 
 def _ptr(t: Optional[torch.Tensor]):
@@ -35,6 +37,14 @@ def _stream(stream):
     return stream.cuda_stream
 
 
+def _same_device(a: torch.device, b: torch.device) -> bool:
+    if a.type != b.type:
+        return False
+    ia = a.index if a.index is not None else torch.cuda.current_device()
+    ib = b.index if b.index is not None else torch.cuda.current_device()
+    return ia == ib
+
+
 def _mask_args(masks, B: int, H: int, N: int, device):
     """Validate the four boundary vectors; returns (Hm, [ptr x 4], keep-alive)."""
     Hm = None
@@ -43,7 +53,7 @@ def _mask_args(masks, B: int, H: int, N: int, device):
         if t is None:
             keep.append(None)
             continue
-        if t.dtype != torch.int32 or t.device != device or not t.is_contiguous():
+        if t.dtype != torch.int32 or not _same_device(t.device, device) or not t.is_contiguous():
             raise FlashMaskError(f"{name} must be a contiguous int32 tensor on {device}")
         if t.dim() != 3 or t.shape[0] != B or t.shape[2] != N or t.shape[1] not in (1, H):
             raise FlashMaskError(f"{name} must have shape [B, 1 or H, N], got {tuple(t.shape)}")

@@ -40,7 +40,8 @@ class fm_options(ctypes.Structure):
 
 
 EXPORTS = ("flashmask_workspace_size", "flashmask_fwd", "flashmask_bwd", "flashmask_classify",
-           "flashmask_count_unmasked", "flashmask_get_error", "flashmask_error_string")
+           "flashmask_count_unmasked", "flashmask_get_error", "flashmask_error_string",
+           "flashmask_last_error_detail")
 
 _lock = threading.Lock()
 _lib = None
@@ -76,6 +77,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.flashmask_get_error.restype = ctypes.c_int
         lib.flashmask_error_string.argtypes = [ctypes.c_int]
         lib.flashmask_error_string.restype = ctypes.c_char_p
+        lib.flashmask_last_error_detail.argtypes = []
+        lib.flashmask_last_error_detail.restype = ctypes.c_char_p
         _lib = lib
         return lib
 
@@ -117,3 +120,7 @@ def flashmask_get_error(stream) -> int:
 
 def flashmask_error_string(status: int) -> str:
     return load().flashmask_error_string(status).decode()
+
+
+def flashmask_last_error_detail() -> str:
+    return load().flashmask_last_error_detail().decode()

@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
+#include <stdio.h>
 #include <string.h>
 
 #include <mutex>
@@ -87,7 +88,8 @@ EncodeTiledFn get_encoder() {
 
 // Tensor [B, N, H, dim] bf16 seen by TMA as 4-D (dim, H, N, B), box
 // (64, 1, rows, 1), 128-byte swizzle; rows past N read as zeros.
-bool encode_bnhd(CUtensorMap *map, const void *base, int B, int N, int H, int dim, int rows) {
+bool encode_bnhd(CUtensorMap *map, const void *base, int B, int N, int H, int dim, int rows,
+                 bool fp16 = false) {
     EncodeTiledFn enc = get_encoder();
     if (!enc) return false;
     cuuint64_t gdim[4] = {static_cast<cuuint64_t>(dim), static_cast<cuuint64_t>(H),
@@ -97,7 +99,8 @@ bool encode_bnhd(CUtensorMap *map, const void *base, int B, int N, int H, int di
                              static_cast<cuuint64_t>(N) * H * dim * 2};
     cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(rows), 1};
     cuuint32_t estride[4] = {1, 1, 1, 1};
-    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), gdim,
+    CUresult r = enc(map, fp16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                     4, const_cast<void *>(base), gdim,
                      gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -140,10 +143,15 @@ size_t carve_workspace(const Geometry &g, bool bwd, void *base, Workspace *ws) {
     w.bwd_cnt = static_cast<int *>(take(BM * g.T * sizeof(int)));
     w.lse2 = nullptr;
     w.delta = nullptr;
+    w.v16 = nullptr;
+    w.do16 = nullptr;
     if (bwd) {
         const size_t rows = static_cast<size_t>(g.B) * g.H * g.Npad;
         w.lse2 = static_cast<float *>(take(rows * sizeof(float)));
         w.delta = static_cast<float *>(take(rows * sizeof(float)));
+        const size_t vbytes = static_cast<size_t>(g.B) * g.N * g.H * g.dv * 2;
+        w.v16 = take(vbytes);
+        w.do16 = take(vbytes);
     }
     if (ws) *ws = w;
     return off;
@@ -169,7 +177,15 @@ fm_status prepare(const fm_problem *p, const fm_options *opt, bool bwd, const Ma
     return FM_OK;
 }
 
-fm_status cuda_status(cudaError_t e) { return e == cudaSuccess ? FM_OK : FM_ERR_CUDA; }
+thread_local char g_detail[256] = "";
+
+fm_status fail(cudaError_t e, const char *what) {
+    snprintf(g_detail, sizeof(g_detail), "%s: %s (%d)", what, cudaGetErrorString(e),
+             static_cast<int>(e));
+    return FM_ERR_CUDA;
+}
+
+fm_status cuda_status(cudaError_t e) { return e == cudaSuccess ? FM_OK : fail(e, "launch"); }
 
 Recorder recorder(const fm_options *opt) {
     Recorder r;
@@ -214,7 +230,7 @@ fm_status flashmask_classify(const fm_problem *p, const int32_t *lts, const int3
     if (!tile_class) return FM_ERR_INVALID_ARG;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaError_t e = launch_classify(g, m, ws, st);
-    if (e != cudaSuccess) return FM_ERR_CUDA;
+    if (e != cudaSuccess) return fail(e, "classify launch");
     const size_t bytes = static_cast<size_t>(g.B) * g.Hm * g.T * g.T;
     return cuda_status(
         cudaMemcpyAsync(tile_class, ws.cls, bytes, cudaMemcpyDeviceToDevice, st));
@@ -251,7 +267,7 @@ fm_status flashmask_fwd(const fm_problem *p, const fm_options *opt, const void *
     if (!encode_bnhd(&tq, q, g.B, g.N, g.H, g.d, 128) ||
         !encode_bnhd(&tk, k, g.B, g.N, g.H, g.d, kr) ||
         !encode_bnhd(&tv, v, g.B, g.N, g.H, g.dv, kr))
-        return FM_ERR_CUDA;
+        return fail(cudaErrorInvalidValue, "cuTensorMapEncodeTiled");
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     Recorder rec = recorder(opt);
     cudaError_t e = map_and_lists(g, m, ws, st, rec);
@@ -280,15 +296,17 @@ fm_status flashmask_bwd(const fm_problem *p, const fm_options *opt, const void *
     CUtensorMap tq_q, tk_k, tv_k, tdo_q;  // maps for the dq kernel (query-side)
     CUtensorMap tq_k, tk_kv, tv_kv, tdo_k;  // maps for the dkdv kernel (key-side)
     const int dq_kr = dq_key_rows(g.d), kv_qr = dkdv_query_rows(g.d);
+    // dO and V enter the dP and dV products through their fp16 copies (made by
+    // the preprocess kernel); Q and K stay bf16.
     if (!encode_bnhd(&tq_q, q, g.B, g.N, g.H, g.d, 128) ||
-        !encode_bnhd(&tdo_q, dout, g.B, g.N, g.H, g.dv, 128) ||
+        !encode_bnhd(&tdo_q, ws.do16, g.B, g.N, g.H, g.dv, 128, true) ||
         !encode_bnhd(&tk_k, k, g.B, g.N, g.H, g.d, dq_kr) ||
-        !encode_bnhd(&tv_k, v, g.B, g.N, g.H, g.dv, dq_kr) ||
+        !encode_bnhd(&tv_k, ws.v16, g.B, g.N, g.H, g.dv, dq_kr, true) ||
         !encode_bnhd(&tq_k, q, g.B, g.N, g.H, g.d, kv_qr) ||
-        !encode_bnhd(&tdo_k, dout, g.B, g.N, g.H, g.dv, kv_qr) ||
+        !encode_bnhd(&tdo_k, ws.do16, g.B, g.N, g.H, g.dv, kv_qr, true) ||
         !encode_bnhd(&tk_kv, k, g.B, g.N, g.H, g.d, 128) ||
-        !encode_bnhd(&tv_kv, v, g.B, g.N, g.H, g.dv, 128))
-        return FM_ERR_CUDA;
+        !encode_bnhd(&tv_kv, ws.v16, g.B, g.N, g.H, g.dv, 128, true))
+        return fail(cudaErrorInvalidValue, "cuTensorMapEncodeTiled");
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     Recorder rec = recorder(opt);
     cudaError_t e = map_and_lists(g, m, ws, st, rec);
@@ -303,6 +321,7 @@ fm_status flashmask_bwd(const fm_problem *p, const fm_options *opt, const void *
         a.tm_v_dq = &tv_k;
         a.tm_do_dq = &tdo_q;
         a.o = o;
+        a.v = v;
         a.dout = dout;
         a.lse = lse;
         a.dq = dq;
@@ -315,10 +334,12 @@ fm_status flashmask_bwd(const fm_problem *p, const fm_options *opt, const void *
 
 fm_status flashmask_get_error(void *stream) {
     cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
-    if (e != cudaSuccess) return FM_ERR_CUDA;
+    if (e != cudaSuccess) return fail(e, "cudaStreamSynchronize");
     unsigned err = read_clear_error_classify() | read_clear_error_fwd() | read_clear_error_bwd();
     return err ? FM_ERR_DEVICE_TIMEOUT : FM_OK;
 }
+
+const char *flashmask_last_error_detail(void) { return g_detail; }
 
 const char *flashmask_error_string(fm_status s) {
     switch (s) {

@@ -12,11 +12,13 @@
 //                tiles; padding rows and fully masked rows get LSE = +inf, so
 //                their P is 0.
 //   dq kernel    one CTA per 128-row query tile walks its key tiles:
-//                S = Q K^T, dP = dO V^T (SS MMAs); dS -> shared memory (bf16);
+//                S = Q K^T (bf16), dP = dO V^T (fp16 copies) as SS MMAs;
+//                dS -> shared memory (bf16);
 //                dQ += dS K (SS MMA).  Writes dQ once, in a fixed order.
 //   dkdv kernel  one CTA per 128-key tile walks its query tiles:
-//                S^T = K Q^T, dP^T = V dO^T (SS MMAs); P^T and dS^T -> TMEM
-//                as bf16; dV += P^T dO and dK += dS^T Q (TS MMAs).
+//                S^T = K Q^T (bf16), dP^T = V dO^T (fp16 copies) as SS MMAs;
+//                P^T -> TMEM as fp16, dS^T as bf16; dV += P^T dO (fp16) and
+//                dK += dS^T Q (bf16) as TS MMAs.
 // No atomics are used, so every gradient is bit-reproducible.  For
 // d = dv = 256 the accumulators dK and dV do not fit in TMEM together, so
 // the dkdv kernel runs twice: once for dV, once for dK.
@@ -54,11 +56,27 @@ __device__ __forceinline__ void store_row_bf16(__nv_bfloat16 *dst, const float (
 }
 
 // ---------------------------------------------------------------- preprocess
-// 16 threads per row; each takes 8 consecutive bf16 of dO and O at a time.
+// 16 threads per row; each takes 8 consecutive bf16 of dO, O and V at a time.
+// Besides D and LSE2 it writes fp16 copies of V and dO: the backward's dP and
+// dV products run in fp16 (10 mantissa bits against bf16's 7), which keeps the
+// probabilities' rounding well below the bf16 rounding of the outputs.
+__device__ __forceinline__ uint4 bf16x8_to_fp16x8(uint4 a) {
+    const __nv_bfloat162 *a2 = reinterpret_cast<const __nv_bfloat162 *>(&a);
+    uint4 r;
+    uint32_t *r32 = reinterpret_cast<uint32_t *>(&r);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const float2 f = __bfloat1622float2(a2[e]);
+        r32[e] = pack_fp16(f.x, f.y);
+    }
+    return r;
+}
+
 __global__ void __launch_bounds__(256) preprocess_kernel(
     int N, int H, int dv, int Npad, int rows_total, const __nv_bfloat16 *__restrict__ o,
-    const __nv_bfloat16 *__restrict__ dout, const float *__restrict__ lse,
-    float *__restrict__ lse2, float *__restrict__ delta) {
+    const __nv_bfloat16 *__restrict__ dout, const __nv_bfloat16 *__restrict__ v,
+    const float *__restrict__ lse, float *__restrict__ lse2, float *__restrict__ delta,
+    uint4 *__restrict__ v16, uint4 *__restrict__ do16) {
     const int r0 = blockIdx.x * 16 + (threadIdx.x >> 4);  // over B*H*Npad
     const int t = threadIdx.x & 15;
     const bool valid = r0 < rows_total;
@@ -71,6 +89,9 @@ __global__ void __launch_bounds__(256) preprocess_kernel(
         for (int c = t * 8; c < dv; c += 128) {
             const uint4 a = *reinterpret_cast<const uint4 *>(o + base + c);
             const uint4 g = *reinterpret_cast<const uint4 *>(dout + base + c);
+            const uint4 vv = *reinterpret_cast<const uint4 *>(v + base + c);
+            do16[(base + c) / 8] = bf16x8_to_fp16x8(g);
+            v16[(base + c) / 8] = bf16x8_to_fp16x8(vv);
             const __nv_bfloat162 *a2 = reinterpret_cast<const __nv_bfloat162 *>(&a);
             const __nv_bfloat162 *g2 = reinterpret_cast<const __nv_bfloat162 *>(&g);
 #pragma unroll
@@ -220,6 +241,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     } else if (warp == 1) {
         if (lane == 0 && n > 0) {
             constexpr uint32_t IDESC_S = idesc_bf16(128, C::BN, false, false);
+            constexpr uint32_t IDESC_DP = idesc_fp16(128, C::BN, false, false);
             constexpr uint32_t IDESC_DQ = idesc_bf16(128, C::D, false, true);
             const uint32_t q_addr = smem_u32(sQ), do_addr = smem_u32(sDO);
             const uint32_t ds_addr = smem_u32(sDS);
@@ -242,7 +264,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                         sdesc_sw128(do_addr + (k / 4) * (C::BM * 128) + (k % 4) * 32, 16, 1024);
                     const uint64_t bd = sdesc_sw128(
                         v_addr + s * C::V_BYTES + (k / 4) * (C::BN * 128) + (k % 4) * 32, 16, 1024);
-                    mma_ss(tmem + C::TM_DP, ad, bd, IDESC_S, k > 0 ? 1u : 0u);
+                    mma_ss(tmem + C::TM_DP, ad, bd, IDESC_DP, k > 0 ? 1u : 0u);
                 }
                 mma_commit(s_full);
                 return true;
@@ -476,7 +498,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     } else if (warp == 1) {
         if (lane == 0 && n > 0) {
             constexpr uint32_t IDESC_S = idesc_bf16(128, C::BM, false, false);
-            constexpr uint32_t IDESC_DV = idesc_bf16(128, C::DV, false, true);
+            constexpr uint32_t IDESC_DP = idesc_fp16(128, C::BM, false, false);
+            constexpr uint32_t IDESC_DV = idesc_fp16(128, C::DV, false, true);
             constexpr uint32_t IDESC_DK = idesc_bf16(128, C::D, false, true);
             const uint32_t k_addr = smem_u32(sK), v_addr = smem_u32(sV);
             const uint32_t st_addr = smem_u32(sST);
@@ -503,7 +526,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                             v_addr + (k / 4) * (C::BN * 128) + (k % 4) * 32, 16, 1024);
                         const uint64_t bd = sdesc_sw128(
                             stg + C::ST_DO + (k / 4) * (C::BM * 128) + (k % 4) * 32, 16, 1024);
-                        mma_ss(tmem + C::TM_DP, ad, bd, IDESC_S, k > 0 ? 1u : 0u);
+                        mma_ss(tmem + C::TM_DP, ad, bd, IDESC_DP, k > 0 ? 1u : 0u);
                     }
                 }
                 mma_commit(s_full);
@@ -573,7 +596,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 for (int c = 0; c < C::BM / 64; ++c) {
                     uint32_t r[32];
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) r[i] = pack_bf16(pr[c * 64 + 2 * i], pr[c * 64 + 2 * i + 1]);
+                    for (int i = 0; i < 32; ++i) r[i] = pack_fp16(pr[c * 64 + 2 * i], pr[c * 64 + 2 * i + 1]);
                     tmem_st32(lane_base + C::TM_S + c * 32, r);
                 }
                 tmem_st_wait();
@@ -708,7 +731,8 @@ cudaError_t launch_bwd(const Geometry &g, const Workspace &ws, const BwdArgs &a,
     rec.before(st);
     preprocess_kernel<<<(rows_total + 15) / 16, 256, 0, st>>>(
         g.N, g.H, g.dv, g.Npad, rows_total, static_cast<const __nv_bfloat16 *>(a.o),
-        static_cast<const __nv_bfloat16 *>(a.dout), a.lse, ws.lse2, ws.delta);
+        static_cast<const __nv_bfloat16 *>(a.dout), static_cast<const __nv_bfloat16 *>(a.v),
+        a.lse, ws.lse2, ws.delta, static_cast<uint4 *>(ws.v16), static_cast<uint4 *>(ws.do16));
     rec.after(st);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;

@@ -5,6 +5,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <stdint.h>
 
 namespace fm {
@@ -32,6 +33,11 @@ __device__ __forceinline__ float lg2(float x) {
     float y;
     asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
+}
+
+__device__ __forceinline__ uint32_t pack_fp16(float lo, float hi) {
+    __half2 h = __floats2half2_rn(lo, hi);  // .x (low half) = lo
+    return *reinterpret_cast<uint32_t *>(&h);
 }
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
@@ -144,14 +150,22 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
     return d;
 }
 
-// Instruction descriptor for kind::f16 with bf16 A/B and fp32 accumulation.
-// a_mn / b_mn select MN-major operands.
-__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn, bool b_mn) {
+// Instruction descriptor for kind::f16 with fp32 accumulation; A and B are
+// both bf16 (fp16 = false) or both fp16 (fp16 = true).  a_mn / b_mn select
+// MN-major operands.
+__host__ __device__ constexpr uint32_t idesc_f16kind(int M, int N, bool a_mn, bool b_mn,
+                                                     bool fp16) {
     return (1u << 4)                                  // D: f32
-           | (1u << 7)                                // A: bf16
-           | (1u << 10)                               // B: bf16
+           | ((fp16 ? 0u : 1u) << 7)                  // A: f16 (0) / bf16 (1)
+           | ((fp16 ? 0u : 1u) << 10)                 // B: f16 (0) / bf16 (1)
            | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) |
            (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn, bool b_mn) {
+    return idesc_f16kind(M, N, a_mn, b_mn, false);
+}
+__host__ __device__ constexpr uint32_t idesc_fp16(int M, int N, bool a_mn, bool b_mn) {
+    return idesc_f16kind(M, N, a_mn, b_mn, true);
 }
 
 // ----------------------------------------------------------------- tcgen05

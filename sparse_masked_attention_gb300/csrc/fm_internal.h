@@ -34,6 +34,8 @@ struct Workspace {
     int *bwd_cnt;      // [B*Hm][T]
     float *lse2;       // [B*H][Npad] log2-domain LSE, +inf for empty / padding rows
     float *delta;      // [B*H][Npad] D_i = sum_c dO_ic O_ic
+    void *v16;         // [B,N,H,dv] fp16 copy of V   (backward)
+    void *do16;        // [B,N,H,dv] fp16 copy of dO  (backward)
 };
 
 // Optional per-kernel event recording (fm_options.kernel_events).
@@ -81,7 +83,7 @@ struct BwdArgs {
     const CUtensorMap *tm_q, *tm_k, *tm_v, *tm_do;
     // query-side (dQ) kernel maps: q/dO boxes of 128 rows, k/v of its key sub-tile
     const CUtensorMap *tm_q_dq, *tm_k_dq, *tm_v_dq, *tm_do_dq;
-    const void *o, *dout;
+    const void *o, *v, *dout;
     const float *lse;
     void *dq, *dk, *dv;
 };

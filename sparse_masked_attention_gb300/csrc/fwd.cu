@@ -313,9 +313,12 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         }
 
         // ------------------------------------------------------- epilogue
-        if (n_my > 0) {
-            const int pl = n_my - 1;
-            warp_wait(&pv_done[wg * 2 + (pl & 1)], (pl >> 1) & 1, tmo, abort);
+        // Wait for the last P V of the whole tile: every MMA has then
+        // completed (they run in issue order), so O is final and the K ring is
+        // free for the merge statistics.  A group with no tiles waits too.
+        if (n > 0) {
+            const int ul = n - 1, wl = ul % C::NWG, pl = ul / C::NWG;
+            warp_wait(&pv_done[wl * 2 + (pl & 1)], (pl >> 1) & 1, tmo, abort);
         }
         tc_fence_after();
         __nv_bfloat16 *orow =
