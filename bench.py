@@ -42,6 +42,9 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--fwd-only", action="store_true", help="time the forward pass alone")
+    ap.add_argument("--N", type=int, default=None, help="override the workload's N (profiling)")
+    ap.add_argument("--B", type=int, default=None, help="override the workload's B (profiling)")
+    ap.add_argument("--H", type=int, default=None, help="override the workload's H (profiling)")
     return ap.parse_args()
 
 
@@ -116,6 +119,15 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------- workload
+def workload_cfg(args):
+    from sparse_masked_attention_gb300 import workloads as W
+    cfg = dict(W.CONFIGS[args.workload])
+    for key in ("N", "B", "H"):
+        if getattr(args, key, None):
+            cfg[key] = getattr(args, key)
+    return cfg
+
+
 def flops_per_pair(d, dv):
     return {"fwd": 2 * (d + dv), "bwd": 2 * (3 * d + 2 * dv), "fwd+bwd": 8 * d + 6 * dv}
 
@@ -160,7 +172,7 @@ def run_ours(args, rank, world, local_rank):
 
     torch.cuda.set_device(local_rank)
     device = torch.device("cuda", local_rank)
-    cfg = dict(W.CONFIGS[args.workload])
+    cfg = workload_cfg(args)
     B, H, N, d, dv = cfg["B"], cfg["H"], cfg["N"], cfg["d"], cfg["dv"]
     has_bwd = "bwd" in cfg["passes"] and not args.fwd_only
     det = bool(cfg.get("deterministic", False))
@@ -263,7 +275,9 @@ def run_ours(args, rank, world, local_rank):
         "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": args.workload, "B": B, "H": H, "N": N, "d": d, "dv": dv,
+        "config": {"workload": args.workload + ("" if (B, H, N) == tuple(
+                       W.CONFIGS[args.workload][x] for x in ("B", "H", "N")) else " (resized)"),
+                   "B": B, "H": H, "N": N, "d": d, "dv": dv,
                    "mask": cfg["mask"], "passes": "fwd+bwd" if has_bwd else "fwd",
                    "deterministic": det, "unmasked_pairs": U,
                    "l2": "inputs larger than L2 (q, k, v, dO each "
@@ -372,9 +386,8 @@ def cpu_baseline(cfg, has_bwd, n_rows=8192):
 
 
 def run_reference(args):
-    from sparse_masked_attention_gb300 import workloads as W
     import oracle
-    cfg = dict(W.CONFIGS[args.workload])
+    cfg = workload_cfg(args)
     has_bwd = "bwd" in cfg["passes"] and not args.fwd_only
     n_rows = 4096
     for _ in range(args.warmup):
@@ -422,8 +435,7 @@ def main():
         dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
     result = run_ours(args, rank, world, local_rank)
     if rank == 0 and not args.no_cpu_baseline:
-        from sparse_masked_attention_gb300 import workloads as W
-        cfg = W.CONFIGS[args.workload]
+        cfg = workload_cfg(args)
         result["cpu_baseline"] = cpu_baseline(cfg, "bwd" in cfg["passes"] and not args.fwd_only)
     if rank == 0:
         print(json.dumps(result), flush=True)

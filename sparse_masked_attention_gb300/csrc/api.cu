@@ -88,10 +88,16 @@ EncodeTiledFn get_encoder() {
 
 // Tensor [B, N, H, dim] bf16 seen by TMA as 4-D (dim, H, N, B), box
 // (64, 1, rows, 1), 128-byte swizzle; rows past N read as zeros.
+// Last encoder failure on this thread: which tensor and the driver's code.
+thread_local char g_encode_detail[160] = "";
+
 bool encode_bnhd(CUtensorMap *map, const void *base, int B, int N, int H, int dim, int rows,
                  bool fp16 = false) {
     EncodeTiledFn enc = get_encoder();
-    if (!enc) return false;
+    if (!enc) {
+        snprintf(g_encode_detail, sizeof(g_encode_detail), "driver entry point not found");
+        return false;
+    }
     cuuint64_t gdim[4] = {static_cast<cuuint64_t>(dim), static_cast<cuuint64_t>(H),
                           static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(B)};
     cuuint64_t gstride[3] = {static_cast<cuuint64_t>(dim) * 2,
@@ -104,6 +110,10 @@ bool encode_bnhd(CUtensorMap *map, const void *base, int B, int N, int H, int di
                      gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        snprintf(g_encode_detail, sizeof(g_encode_detail),
+                 "CUresult %d for base %p dims (%d,%d,%d,%d) rows %d", static_cast<int>(r), base,
+                 dim, H, N, B, rows);
     return r == CUDA_SUCCESS;
 }
 
@@ -112,9 +122,20 @@ int fwd_key_rows(int d) { return d == 256 ? 64 : 128; }
 int dq_key_rows(int d) { return d >= 192 ? 64 : 128; }
 int dkdv_query_rows(int d) { return d >= 192 ? 64 : 128; }
 
-bool device_ok() {
+// Makes the device that owns `anchor` (device memory of the caller) current
+// for this library on the calling thread, which also binds its primary
+// context there (the tensor-map encoder is a driver call and needs one), then
+// checks that it is an sm_103 part.  Threads the library has not seen before,
+// such as an autograd worker, have no context bound otherwise.
+bool device_ok(const void *anchor) {
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    cudaPointerAttributes attr;
+    if (anchor && cudaPointerGetAttributes(&attr, anchor) == cudaSuccess &&
+        (attr.type == cudaMemoryTypeDevice || attr.type == cudaMemoryTypeManaged))
+        dev = attr.device;
+    else if (cudaGetDevice(&dev) != cudaSuccess)
+        return false;
+    if (cudaSetDevice(dev) != cudaSuccess) return false;
     int major = 0, minor = 0;
     if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess)
         return false;
@@ -173,7 +194,7 @@ fm_status prepare(const fm_problem *p, const fm_options *opt, bool bwd, const Ma
         return FM_ERR_WORKSPACE;
     if (carve_workspace(*g, bwd, nullptr, nullptr) > ws_bytes) return FM_ERR_WORKSPACE;
     carve_workspace(*g, bwd, workspace, ws);
-    if (!device_ok()) return FM_ERR_UNSUPPORTED;
+    if (!device_ok(workspace)) return FM_ERR_UNSUPPORTED;
     return FM_OK;
 }
 
@@ -211,6 +232,7 @@ cudaError_t map_and_lists(const Geometry &g, const MaskPtrs &m, const Workspace 
 
 }  // namespace
 
+
 extern "C" {
 
 size_t flashmask_workspace_size(const fm_problem *p, const fm_options *opt, int is_bwd) {
@@ -246,7 +268,7 @@ fm_status flashmask_count_unmasked(const fm_problem *p, const int32_t *lts, cons
     s = check_mask(m);
     if (s != FM_OK) return s;
     if (!counts || (reinterpret_cast<uintptr_t>(counts) & 7u)) return FM_ERR_INVALID_ARG;
-    if (!device_ok()) return FM_ERR_UNSUPPORTED;
+    if (!device_ok(counts)) return FM_ERR_UNSUPPORTED;
     return cuda_status(launch_count(g, m, counts, static_cast<cudaStream_t>(stream)));
 }
 
@@ -267,7 +289,7 @@ fm_status flashmask_fwd(const fm_problem *p, const fm_options *opt, const void *
     if (!encode_bnhd(&tq, q, g.B, g.N, g.H, g.d, 128) ||
         !encode_bnhd(&tk, k, g.B, g.N, g.H, g.d, kr) ||
         !encode_bnhd(&tv, v, g.B, g.N, g.H, g.dv, kr))
-        return fail(cudaErrorInvalidValue, "cuTensorMapEncodeTiled");
+        return fail(cudaErrorInvalidValue, g_encode_detail);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     Recorder rec = recorder(opt);
     cudaError_t e = map_and_lists(g, m, ws, st, rec);
@@ -306,7 +328,7 @@ fm_status flashmask_bwd(const fm_problem *p, const fm_options *opt, const void *
         !encode_bnhd(&tdo_k, ws.do16, g.B, g.N, g.H, g.dv, kv_qr, true) ||
         !encode_bnhd(&tk_kv, k, g.B, g.N, g.H, g.d, 128) ||
         !encode_bnhd(&tv_kv, ws.v16, g.B, g.N, g.H, g.dv, 128, true))
-        return fail(cudaErrorInvalidValue, "cuTensorMapEncodeTiled");
+        return fail(cudaErrorInvalidValue, g_encode_detail);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     Recorder rec = recorder(opt);
     cudaError_t e = map_and_lists(g, m, ws, st, rec);
