@@ -151,6 +151,31 @@ fm_status flashmask_count_unmasked(const fm_problem *p,
  */
 fm_status flashmask_get_error(void *stream);
 
+/*
+ * Forward without a workspace, for callers that cannot allocate device memory
+ * (a host that only hands out its own tensors, code where cudaMalloc is not
+ * allowed or would stall, an embedding with no allocator).  It computes
+ * exactly what flashmask_fwd computes; the paper has no counterpart of this
+ * entry point.  Its scratch is a fixed array of FM_NOALLOC_SCRATCH_BYTES
+ * inside the library, held by every GPU that loads it until the process exits.
+ *  - Problems whose forward workspace (flashmask_workspace_size, is_bwd = 0)
+ *    exceeds FM_NOALLOC_SCRATCH_BYTES are rejected with FM_ERR_WORKSPACE, and
+ *    flashmask_last_error_detail says why.
+ *  - The first call on a device looks up the array's device address (a
+ *    one-time cudaGetSymbolAddress with that device current); make that first
+ *    call before any stream capture.
+ *  - All calls on a device share the array.  Calls that overlap on the GPU
+ *    race and give wrong results; order them on one stream.  Nothing in the
+ *    array needs clearing between calls.
+ *  - The device is the one that owns q.  Allocates nothing and frees nothing.
+ */
+#define FM_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
+fm_status flashmask_fwd_noalloc(const fm_problem *p, const fm_options *opt,
+                                const void *q, const void *k, const void *v,
+                                const int32_t *lts, const int32_t *lte,
+                                const int32_t *uts, const int32_t *ute,
+                                void *o, float *lse, void *stream);
+
 /* Static text for a status code. */
 const char *flashmask_error_string(fm_status s);
 

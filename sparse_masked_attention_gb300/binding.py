@@ -41,7 +41,9 @@ class fm_options(ctypes.Structure):
 
 EXPORTS = ("flashmask_workspace_size", "flashmask_fwd", "flashmask_bwd", "flashmask_classify",
            "flashmask_count_unmasked", "flashmask_get_error", "flashmask_error_string",
-           "flashmask_last_error_detail")
+           "flashmask_last_error_detail", "flashmask_fwd_noalloc")
+
+FM_NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024
 
 _lock = threading.Lock()
 _lib = None
@@ -77,6 +79,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.flashmask_get_error.restype = ctypes.c_int
         lib.flashmask_error_string.argtypes = [ctypes.c_int]
         lib.flashmask_error_string.restype = ctypes.c_char_p
+        lib.flashmask_fwd_noalloc.argtypes = [prob, opt, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+        lib.flashmask_fwd_noalloc.restype = ctypes.c_int
         lib.flashmask_last_error_detail.argtypes = []
         lib.flashmask_last_error_detail.restype = ctypes.c_char_p
         _lib = lib
@@ -124,3 +128,8 @@ def flashmask_error_string(status: int) -> str:
 
 def flashmask_last_error_detail() -> str:
     return load().flashmask_last_error_detail().decode()
+
+
+def flashmask_fwd_noalloc(problem, options, q, k, v, lts, lte, uts, ute, o, lse, stream) -> int:
+    return int(load().flashmask_fwd_noalloc(ctypes.byref(problem), _ref(options), q, k, v, lts,
+                                            lte, uts, ute, o, lse, stream))

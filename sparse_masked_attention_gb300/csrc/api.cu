@@ -232,6 +232,10 @@ cudaError_t map_and_lists(const Geometry &g, const MaskPtrs &m, const Workspace 
 
 }  // namespace
 
+namespace fm {
+// Sets the text flashmask_last_error_detail returns on this thread.
+void set_error_detail(const char *msg) { snprintf(g_detail, sizeof(g_detail), "%s", msg); }
+}  // namespace fm
 
 extern "C" {
 

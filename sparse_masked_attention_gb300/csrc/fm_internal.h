@@ -52,6 +52,9 @@ struct Recorder {
     }
 };
 
+// Text returned by flashmask_last_error_detail on this thread (api.cu).
+void set_error_detail(const char *msg);
+
 // Lays the workspace out from `base` (may be nullptr to size it); returns bytes.
 size_t carve_workspace(const Geometry &g, bool bwd, void *base, Workspace *ws);
 
