@@ -48,6 +48,29 @@ def parse():
     return ap.parse_args()
 
 
+def profiled_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary table, or
+    None when there is none or the kernel's source changed since the capture."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "roofline_traffic.txt")
+    try:
+        lines = open(path).read().splitlines()
+    except OSError:
+        return None
+    for line in lines:
+        if line.startswith("#") or not line.strip():
+            continue
+        k, w, nbytes, src, sha = line.split()
+        if k != kernel or w != workload:
+            continue
+        try:
+            cur = hashlib.sha1(open(os.path.join(ROOT, src), "rb").read()).hexdigest()[:12]
+        except OSError:
+            return None
+        return int(nbytes) if cur == sha else None
+    return None
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -258,7 +281,10 @@ def run_ours(args, rank, world, local_rank):
                 "frac": round(achieved / pk["bf16_tflops"], 4),
                 "frac_sustained": round(achieved / pk["bf16_tflops_sustained"], 4),
                 "peak_source": f"{src} burst bf16 (sustained {pk['bf16_tflops_sustained']})",
-                "traffic": None, "avg_ms": round(avg[dominant], 4)}
+                "traffic": profiled_traffic(dom_name, args.workload) if (B, H, N) == tuple(
+                    W.CONFIGS[args.workload][x] for x in ("B", "H", "N")) else None,
+                "traffic_unit": "bytes per launch (ncu, profiles/roofline_traffic.txt)",
+                "avg_ms": round(avg[dominant], 4)}
 
     # forward alone, same inputs (event pairs of the forward calls)
     fwd_ms = sum(avg[f"fwd:{n}"] for n in fwd_names)
