@@ -5,7 +5,8 @@
 // One CTA owns one 128-row query tile of one (batch, head).  It walks only
 // the key tiles the tile map kept for that query tile ("skip unnecessary
 // computation", FlashMask abstract).  Roles, by warp:
-//   warp 0      TMA producer: Q once, then K and V tiles into shared-memory rings
+//   warp 0      TMA producers: lane 0 Q and the K ring, lane 1 the V ring,
+//               lane 2 the ring of each key tile's mask boundaries
 //   warp 1      allocates TMEM; lane 0 issues every tcgen05.mma
 //   warps 2..   NWG softmax warpgroups.  Thread t of a group owns query row t,
 //               which is TMEM lane t.
@@ -45,21 +46,24 @@ struct FwdParams {
     uint64_t timeout_ns;
 };
 
-template <int D_, int DV_, int BN_, int NWG_, int NSB_, int KS_, int VS_>
+template <int D_, int DV_, int BN_, int NWG_, int NSB_, int KS_, int VS_, int ES_>
 struct FwdCfg {
-    static constexpr int D = D_, DV = DV_, BN = BN_, NWG = NWG_, NSB = NSB_, KS = KS_, VS = VS_;
+    static constexpr int D = D_, DV = DV_, BN = BN_, NWG = NWG_, NSB = NSB_, KS = KS_, VS = VS_,
+                         ES = ES_;
     static constexpr int BM = 128;
     static constexpr int SUB = TILE / BN;  // key sub-tiles per list entry
     static constexpr int Q_BYTES = BM * D * 2;
     static constexpr int K_BYTES = BN * D * 2;
     static constexpr int V_BYTES = BN * DV * 2;
+    static constexpr int E_BYTES = BN * 16;  // the tile's normalised mask boundaries
     static constexpr int OFF_Q = 0;
     static constexpr int OFF_K = OFF_Q + Q_BYTES;
     static constexpr int OFF_V = OFF_K + KS * K_BYTES;
-    static constexpr int OFF_BAR = OFF_V + VS * V_BYTES;
-    // q_full, k_full[KS], k_empty[KS], v_full[VS], v_empty[VS],
+    static constexpr int OFF_E = OFF_V + VS * V_BYTES;
+    static constexpr int OFF_BAR = OFF_E + ES * E_BYTES;
+    // q_full, k_full[KS], k_empty[KS], v_full[VS], v_empty[VS], e_full[ES], e_empty[ES],
     // s_full[NWG*NSB], p_full[NWG*NSB], pv_done[NWG*2]
-    static constexpr int NBAR = 1 + 2 * KS + 2 * VS + 2 * NWG * NSB + 2 * NWG;
+    static constexpr int NBAR = 1 + 2 * KS + 2 * VS + 2 * ES + 2 * NWG * NSB + 2 * NWG;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
     static constexpr int TM_O = 0;
@@ -68,7 +72,7 @@ struct FwdCfg {
     static constexpr int THREADS = 64 + NWG * 128;
     static_assert(TM_S + NWG * NSB * BN <= TM_COLS, "TMEM budget");
     static_assert(D % 64 == 0 && DV % 64 == 0 && (BN == 64 || BN == 128), "tile shape");
-    static_assert(DV <= 256 && BN % 32 == 0, "MMA shape");
+    static_assert(DV <= 256 && BN % 64 == 0, "MMA shape");
     static_assert(NWG * 128 * 2 * 4 <= K_BYTES, "merge statistics alias K stage 0");
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 };
@@ -90,13 +94,16 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     uint8_t *sQ = smem + C::OFF_Q;
     uint8_t *sK = smem + C::OFF_K;
     uint8_t *sV = smem + C::OFF_V;
+    uint8_t *sE = smem + C::OFF_E;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
     uint64_t *q_full = bars;
     uint64_t *k_full = q_full + 1;
     uint64_t *k_empty = k_full + C::KS;
     uint64_t *v_full = k_empty + C::KS;
     uint64_t *v_empty = v_full + C::VS;
-    uint64_t *s_full = v_empty + C::VS;
+    uint64_t *e_full = v_empty + C::VS;
+    uint64_t *e_empty = e_full + C::ES;
+    uint64_t *s_full = e_empty + C::ES;
     uint64_t *p_full = s_full + C::NWG * C::NSB;
     uint64_t *pv_done = p_full + C::NWG * C::NSB;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
@@ -123,6 +130,10 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             mbar_init(&v_full[i], 1);
             mbar_init(&v_empty[i], 1);
         }
+        for (int i = 0; i < C::ES; ++i) {
+            mbar_init(&e_full[i], 1);
+            mbar_init(&e_empty[i], 128);
+        }
         for (int i = 0; i < C::NWG * C::NSB; ++i) {
             mbar_init(&s_full[i], 1);
             mbar_init(&p_full[i], 128);
@@ -146,46 +157,52 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     constexpr int L = C::NWG * C::NSB;  // S tiles in flight
 
     if (warp == 0) {
-        // ------------------------------------------------------ TMA producer
+        // ------------------------------------------------------ TMA producers
+        // Three lanes, three independent rings, each filled in the order its
+        // consumer drains it: lane 0 Q and K, lane 1 V, lane 2 the mask
+        // boundaries of each key tile.
         if (lane == 0 && n > 0) {
             prefetch_tmap(&tm_q);
             prefetch_tmap(&tm_k);
-            prefetch_tmap(&tm_v);
             mbar_arrive_expect_tx(q_full, C::Q_BYTES);
 #pragma unroll
             for (int c = 0; c < C::D / 64; ++c)
                 tma_load_4d(sQ + c * C::BM * 128, &tm_q, q_full, c * 64, h, qt * TILE, b);
-            auto load_k = [&](int u) -> bool {
+            for (int u = 0; u < n; ++u) {
                 const int s = u % C::KS;
                 if (u >= C::KS &&
                     !mbar_wait(&k_empty[s], ((u / C::KS) - 1) & 1, tmo, abort, &g_err_fwd))
-                    return false;
+                    break;
                 mbar_arrive_expect_tx(&k_full[s], C::K_BYTES);
                 const int key0 = key0_of(u);
 #pragma unroll
                 for (int c = 0; c < C::D / 64; ++c)
                     tma_load_4d(sK + s * C::K_BYTES + c * C::BN * 128, &tm_k, &k_full[s], c * 64,
                                 h, key0, b);
-                return true;
-            };
-            auto load_v = [&](int u) -> bool {
+            }
+        } else if (lane == 1 && n > 0) {
+            prefetch_tmap(&tm_v);
+            for (int u = 0; u < n; ++u) {
                 const int s = u % C::VS;
                 if (u >= C::VS &&
                     !mbar_wait(&v_empty[s], ((u / C::VS) - 1) & 1, tmo, abort, &g_err_fwd))
-                    return false;
+                    break;
                 mbar_arrive_expect_tx(&v_full[s], C::V_BYTES);
                 const int key0 = key0_of(u);
 #pragma unroll
                 for (int c = 0; c < C::DV / 64; ++c)
                     tma_load_4d(sV + s * C::V_BYTES + c * C::BN * 128, &tm_v, &v_full[s], c * 64,
                                 h, key0, b);
-                return true;
-            };
-            bool ok = true;
-            for (int u = 0; u < L && u < n && ok; ++u) ok = load_k(u);
-            for (int u = 0; u < n && ok; ++u) {
-                ok = load_v(u);
-                if (ok && u + L < n) ok = load_k(u + L);
+            }
+        } else if (lane == 2 && n > 0) {
+            const int4 *vec = p.vec + static_cast<size_t>(bm) * p.Npad;
+            for (int u = 0; u < n; ++u) {
+                const int s = u % C::ES;
+                if (u >= C::ES &&
+                    !mbar_wait(&e_empty[s], ((u / C::ES) - 1) & 1, tmo, abort, &g_err_fwd))
+                    break;
+                mbar_arrive_expect_tx(&e_full[s], C::E_BYTES);
+                bulk_load(sE + s * C::E_BYTES, vec + key0_of(u), C::E_BYTES, &e_full[s]);
             }
         }
     } else if (warp == 1) {
@@ -244,35 +261,64 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         const uint32_t lane_base = tmem + (static_cast<uint32_t>(quad * 32) << 16);
         const int n_my = n > wg ? (n - wg + C::NWG - 1) / C::NWG : 0;
         const float NEG_INF = -INFINITY;
-        const int4 *vec = p.vec + static_cast<size_t>(bm) * p.Npad;
+        const float sl2 = p.sl2;
         float m_ref = NEG_INF, l_sum = 0.f;
+        // The list entry of the group's next tile is read one tile ahead.
+        int entry_next = n_my > 0 ? entries[wg / C::SUB] : 0;
 
         for (int lu = 0; lu < n_my; ++lu) {
             const int u = lu * C::NWG + wg;
             const int sb = wg * C::NSB + lu % C::NSB;
+            const int entry = entry_next;
+            if (u + C::NWG < n) entry_next = entries[(u + C::NWG) / C::SUB];
+            const bool masked_tile = entry & 1;
+            const int key0 = (entry >> 1) * TILE + (u % C::SUB) * C::BN;
+            const int es = u % C::ES;
             if (!warp_wait(&s_full[sb], (lu / C::NSB) & 1, tmo, abort)) break;
             tc_fence_after();
-            float x[C::BN];
             const uint32_t s_addr = lane_base + C::TM_S + sb * C::BN;
+
+            // pass 1: mask (partial tiles only) and row max of raw scores
+            uint32_t mbits[C::BN / 32];
+            float mx8[8];
 #pragma unroll
-            for (int c = 0; c < C::BN / 32; ++c) {
-                uint32_t r[32];
-                tmem_ld32(s_addr + c * 32, r);
+            for (int i = 0; i < 8; ++i) mx8[i] = NEG_INF;
+            if (masked_tile) {
+                if (!warp_wait(&e_full[es], (u / C::ES) & 1, tmo, abort)) break;
+                const int4 *cv = reinterpret_cast<const int4 *>(sE + es * C::E_BYTES);
 #pragma unroll
-                for (int i = 0; i < 32; ++i) x[c * 32 + i] = __uint_as_float(r[i]) * p.sl2;
-            }
-            if (entries[u / C::SUB] & 1) {
-                const int key0 = key0_of(u);
+                for (int c = 0; c < C::BN / 64; ++c) {
+                    float x[64];
+                    tmem_ld64f(s_addr + c * 64, x);
+                    uint32_t w0 = 0, w1 = 0;
 #pragma unroll
-                for (int jj = 0; jj < C::BN; ++jj) {
-                    const int4 cv = __ldg(vec + key0 + jj);
-                    if (masked_at(grow, key0 + jj, cv, p.causal)) x[jj] = NEG_INF;
+                    for (int jj = 0; jj < 64; ++jj) {
+                        const bool mk = masked_at(grow, key0 + c * 64 + jj, cv[c * 64 + jj], p.causal);
+                        if (jj < 32) w0 |= (mk ? 1u : 0u) << jj;
+                        else w1 |= (mk ? 1u : 0u) << (jj - 32);
+                        mx8[jj & 7] = fmaxf(mx8[jj & 7], mk ? NEG_INF : x[jj]);
+                    }
+                    mbits[2 * c] = w0;
+                    mbits[2 * c + 1] = w1;
+                }
+            } else {
+#pragma unroll
+                for (int c = 0; c < C::BN / 64; ++c) {
+                    float x[64];
+                    tmem_ld64f(s_addr + c * 64, x);
+#pragma unroll
+                    for (int jj = 0; jj < 64; ++jj) mx8[jj & 7] = fmaxf(mx8[jj & 7], x[jj]);
                 }
             }
-            float mx = NEG_INF;
-#pragma unroll
-            for (int jj = 0; jj < C::BN; ++jj) mx = fmaxf(mx, x[jj]);
-            const float m_new = fmaxf(m_ref, mx);
+            // The group's producer slot of the boundary ring is free again.
+            // (On unmasked tiles the boundaries were not needed; still wait for
+            // their arrival so the ring's phases stay in step.)
+            if (!masked_tile && !warp_wait(&e_full[es], (u / C::ES) & 1, tmo, abort)) break;
+            mbar_arrive(&e_empty[es]);
+
+            float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+            const float m_new = fmaxf(m_ref, mx * sl2);  // log2 domain (sl2 > 0)
             const bool need = (m_ref != NEG_INF) && (m_new > m_ref + 8.0f);
             if (m_ref == NEG_INF) m_ref = m_new;
             if (__any_sync(0xffffffffu, need)) {
@@ -295,18 +341,33 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 }
             }
             const float m_use = (m_ref == NEG_INF) ? 0.0f : m_ref;
+
+            // pass 2: P = exp2(s*scale*log2e - m), row sum, P -> TMEM (bf16)
+            float l8[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) l8[i] = 0.f;
 #pragma unroll
             for (int c = 0; c < C::BN / 64; ++c) {
+                float x[64];
+                tmem_ld64f(s_addr + c * 64, x);
                 uint32_t r[32];
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
-                    const float p0 = ex2(x[c * 64 + 2 * i] - m_use);
-                    const float p1 = ex2(x[c * 64 + 2 * i + 1] - m_use);
-                    l_sum += p0 + p1;
+                    float p0 = ex2(fmaf(x[2 * i], sl2, -m_use));
+                    float p1 = ex2(fmaf(x[2 * i + 1], sl2, -m_use));
+                    if (masked_tile) {
+                        const uint32_t w = mbits[2 * c + (i >> 4)];
+                        const int bit = (2 * i) & 31;
+                        if ((w >> bit) & 1u) p0 = 0.f;
+                        if ((w >> (bit + 1)) & 1u) p1 = 0.f;
+                    }
+                    l8[(2 * i) & 7] += p0;
+                    l8[(2 * i + 1) & 7] += p1;
                     r[i] = pack_bf16(p0, p1);
                 }
                 tmem_st32(s_addr + c * 32, r);
             }
+            l_sum += ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(&p_full[sb]);
@@ -418,13 +479,15 @@ cudaError_t launch_cfg(const Geometry &g, const Workspace &ws, const FwdArgs &a,
 
 cudaError_t launch_fwd(const Geometry &g, const Workspace &ws, const FwdArgs &a,
                        cudaStream_t st) {
-    if (g.d == 64 && g.dv == 64) return launch_cfg<FwdCfg<64, 64, 128, 2, 1, 3, 3>>(g, ws, a, st);
+    // <d, dv, key tile, softmax groups, S buffers per group, K / V / boundary ring stages>
+    if (g.d == 64 && g.dv == 64)
+        return launch_cfg<FwdCfg<64, 64, 128, 2, 1, 2, 3, 4>>(g, ws, a, st);
     if (g.d == 128 && g.dv == 128)
-        return launch_cfg<FwdCfg<128, 128, 128, 2, 1, 3, 3>>(g, ws, a, st);
+        return launch_cfg<FwdCfg<128, 128, 128, 2, 1, 2, 3, 4>>(g, ws, a, st);
     if (g.d == 192 && g.dv == 128)
-        return launch_cfg<FwdCfg<192, 128, 128, 2, 1, 2, 2>>(g, ws, a, st);
+        return launch_cfg<FwdCfg<192, 128, 128, 2, 1, 2, 2, 4>>(g, ws, a, st);
     if (g.d == 256 && g.dv == 256)
-        return launch_cfg<FwdCfg<256, 256, 64, 1, 2, 2, 2>>(g, ws, a, st);
+        return launch_cfg<FwdCfg<256, 256, 64, 1, 2, 2, 2, 4>>(g, ws, a, st);
     return cudaErrorInvalidValue;
 }
 
