@@ -117,11 +117,6 @@ bool encode_bnhd(CUtensorMap *map, const void *base, int B, int N, int H, int di
     return r == CUDA_SUCCESS;
 }
 
-// Key/query tile heights used by the kernels for each (d, dv).
-int fwd_key_rows(int d) { return d == 256 ? 64 : 128; }
-int dq_key_rows(int d) { return d >= 192 ? 64 : 128; }
-int dkdv_query_rows(int d) { return d >= 192 ? 64 : 128; }
-
 // Makes the device that owns `anchor` (device memory of the caller) current
 // for this library on the calling thread, which also binds its primary
 // context there (the tensor-map encoder is a driver call and needs one), then
@@ -289,7 +284,7 @@ fm_status flashmask_fwd(const fm_problem *p, const fm_options *opt, const void *
     fm_status s = prepare(p, opt, false, m, workspace, ws_bytes, &g, &ws);
     if (s != FM_OK) return s;
     CUtensorMap tq, tk, tv;
-    const int kr = fwd_key_rows(g.d);
+    const int kr = fwd_key_rows(g.d, g.dv);
     if (!encode_bnhd(&tq, q, g.B, g.N, g.H, g.d, 128) ||
         !encode_bnhd(&tk, k, g.B, g.N, g.H, g.d, kr) ||
         !encode_bnhd(&tv, v, g.B, g.N, g.H, g.dv, kr))
@@ -298,7 +293,7 @@ fm_status flashmask_fwd(const fm_problem *p, const fm_options *opt, const void *
     Recorder rec = recorder(opt);
     cudaError_t e = map_and_lists(g, m, ws, st, rec);
     if (e == cudaSuccess) {
-        FwdArgs a{&tq, &tk, &tv, o, lse};
+        FwdArgs a{&tq, &tk, &tv, kr, o, lse};
         rec.before(st);
         e = launch_fwd(g, ws, a, st);
         rec.after(st);
@@ -321,7 +316,7 @@ fm_status flashmask_bwd(const fm_problem *p, const fm_options *opt, const void *
     if (s != FM_OK) return s;
     CUtensorMap tq_q, tk_k, tv_k, tdo_q;  // maps for the dq kernel (query-side)
     CUtensorMap tq_k, tk_kv, tv_kv, tdo_k;  // maps for the dkdv kernel (key-side)
-    const int dq_kr = dq_key_rows(g.d), kv_qr = dkdv_query_rows(g.d);
+    const int dq_kr = dq_key_rows(g.d, g.dv), kv_qr = dkdv_query_rows(g.d, g.dv);
     // dO and V enter the dP and dV products through their fp16 copies (made by
     // the preprocess kernel); Q and K stay bf16.
     if (!encode_bnhd(&tq_q, q, g.B, g.N, g.H, g.d, 128) ||
@@ -338,6 +333,8 @@ fm_status flashmask_bwd(const fm_problem *p, const fm_options *opt, const void *
     cudaError_t e = map_and_lists(g, m, ws, st, rec);
     if (e == cudaSuccess) {
         BwdArgs a;
+        a.dq_k_rows = dq_kr;
+        a.kv_q_rows = kv_qr;
         a.tm_q = &tq_k;
         a.tm_k = &tk_kv;
         a.tm_v = &tv_kv;

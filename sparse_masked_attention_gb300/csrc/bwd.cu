@@ -130,9 +130,12 @@ struct BwdParams {
 };
 
 // ------------------------------------------------------------------ dq kernel
-template <int D_, int DV_, int BN_, int ST_>
+// One CTA per 128-row query tile.  NWG compute warpgroups take alternate key
+// sub-tiles of BN keys; each has its own S/dP region in TMEM and its own dS
+// buffer in shared memory, and all of them feed one dQ accumulator.
+template <int D_, int DV_, int BN_, int ST_, int NWG_, int ES_>
 struct DqCfg {
-    static constexpr int D = D_, DV = DV_, BN = BN_, ST = ST_;
+    static constexpr int D = D_, DV = DV_, BN = BN_, ST = ST_, NWG = NWG_, ES = ES_;
     static constexpr int BM = 128;
     static constexpr int SUB = TILE / BN;
     static constexpr int Q_BYTES = BM * D * 2;
@@ -140,21 +143,28 @@ struct DqCfg {
     static constexpr int K_BYTES = BN * D * 2;
     static constexpr int V_BYTES = BN * DV * 2;
     static constexpr int DS_BYTES = BM * BN * 2;
+    static constexpr int E_BYTES = BN * 16;
     static constexpr int OFF_Q = 0;
     static constexpr int OFF_DO = OFF_Q + Q_BYTES;
     static constexpr int OFF_DS = OFF_DO + DO_BYTES;
-    static constexpr int OFF_K = OFF_DS + DS_BYTES;
+    static constexpr int OFF_K = OFF_DS + NWG * DS_BYTES;
     static constexpr int OFF_V = OFF_K + ST * K_BYTES;
-    static constexpr int OFF_BAR = OFF_V + ST * V_BYTES;
-    // q_full, kv_full[ST], kv_empty[ST], s_full, ds_full, dq_done
-    static constexpr int NBAR = 1 + 2 * ST + 3;
+    static constexpr int OFF_E = OFF_V + ST * V_BYTES;
+    static constexpr int OFF_BAR = OFF_E + ES * E_BYTES;
+    // q_full, kv_full[ST], kv_empty[ST], e_full[ES], e_empty[ES], s_full[NWG],
+    // ds_full[NWG], dq_done
+    static constexpr int NBAR = 1 + 2 * ST + 2 * ES + 2 * NWG + 1;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
-    static constexpr int TM_S = 0, TM_DP = BN, TM_DQ = 2 * BN;
+    static constexpr int TM_SDP = 2 * BN;  // per group: S then dP
+    static constexpr int TM_DQ = NWG * TM_SDP;
     static constexpr int TM_COLS = 512;
-    static constexpr int THREADS = 192;
+    static constexpr int THREADS = 64 + NWG * 128;
     static_assert(TM_DQ + D <= TM_COLS, "TMEM budget");
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+    static_assert(BN == 64 || BN == 128, "key sub-tile");
+    static_assert(ST >= NWG && ES % NWG == 0, "ring depths");
+    static_assert((D / 32) % NWG == 0, "epilogue column split");
 };
 
 template <class C>
@@ -166,10 +176,11 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint8_t *sQ = smem + C::OFF_Q, *sDO = smem + C::OFF_DO, *sDS = smem + C::OFF_DS;
-    uint8_t *sK = smem + C::OFF_K, *sV = smem + C::OFF_V;
+    uint8_t *sK = smem + C::OFF_K, *sV = smem + C::OFF_V, *sE = smem + C::OFF_E;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
     uint64_t *q_full = bars, *kv_full = bars + 1, *kv_empty = kv_full + C::ST;
-    uint64_t *s_full = kv_empty + C::ST, *ds_full = s_full + 1, *dq_done = ds_full + 1;
+    uint64_t *e_full = kv_empty + C::ST, *e_empty = e_full + C::ES;
+    uint64_t *s_full = e_empty + C::ES, *ds_full = s_full + C::NWG, *dq_done = ds_full + C::NWG;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
     volatile int *abort = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
 
@@ -190,8 +201,14 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             mbar_init(&kv_full[i], 1);
             mbar_init(&kv_empty[i], 1);
         }
-        mbar_init(s_full, 1);
-        mbar_init(ds_full, 128);
+        for (int i = 0; i < C::ES; ++i) {
+            mbar_init(&e_full[i], 1);
+            mbar_init(&e_empty[i], 128);
+        }
+        for (int i = 0; i < C::NWG; ++i) {
+            mbar_init(&s_full[i], 1);
+            mbar_init(&ds_full[i], 128);
+        }
         mbar_init(dq_done, 1);
         *abort = 0;
         fence_barrier_init();
@@ -237,6 +254,16 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     tma_load_4d(sV + s * C::V_BYTES + c * C::BN * 128, &tm_v, &kv_full[s],
                                 c * 64, h, key0, b);
             }
+        } else if (lane == 1 && n > 0) {
+            const int4 *vec = p.vec + static_cast<size_t>(bm) * p.Npad;
+            for (int u = 0; u < n; ++u) {
+                const int s = u % C::ES;
+                if (u >= C::ES &&
+                    !mbar_wait(&e_empty[s], ((u / C::ES) - 1) & 1, tmo, abort, &g_err_bwd))
+                    break;
+                mbar_arrive_expect_tx(&e_full[s], C::E_BYTES);
+                bulk_load(sE + s * C::E_BYTES, vec + key0_of(u), C::E_BYTES, &e_full[s]);
+            }
         }
     } else if (warp == 1) {
         if (lane == 0 && n > 0) {
@@ -247,16 +274,17 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             const uint32_t ds_addr = smem_u32(sDS);
             const uint32_t k_addr = smem_u32(sK), v_addr = smem_u32(sV);
             auto issue_s_dp = [&](int u) -> bool {
-                const int s = u % C::ST;
+                const int s = u % C::ST, w = u % C::NWG;
                 if (!mbar_wait(&kv_full[s], (u / C::ST) & 1, tmo, abort, &g_err_bwd)) return false;
                 tc_fence_after();
+                const uint32_t t_s = tmem + w * C::TM_SDP, t_dp = t_s + C::BN;
 #pragma unroll
                 for (int k = 0; k < C::D / 16; ++k) {
                     const uint64_t ad =
                         sdesc_sw128(q_addr + (k / 4) * (C::BM * 128) + (k % 4) * 32, 16, 1024);
                     const uint64_t bd = sdesc_sw128(
                         k_addr + s * C::K_BYTES + (k / 4) * (C::BN * 128) + (k % 4) * 32, 16, 1024);
-                    mma_ss(tmem + C::TM_S, ad, bd, IDESC_S, k > 0 ? 1u : 0u);
+                    mma_ss(t_s, ad, bd, IDESC_S, k > 0 ? 1u : 0u);
                 }
 #pragma unroll
                 for (int k = 0; k < C::DV / 16; ++k) {
@@ -264,33 +292,35 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                         sdesc_sw128(do_addr + (k / 4) * (C::BM * 128) + (k % 4) * 32, 16, 1024);
                     const uint64_t bd = sdesc_sw128(
                         v_addr + s * C::V_BYTES + (k / 4) * (C::BN * 128) + (k % 4) * 32, 16, 1024);
-                    mma_ss(tmem + C::TM_DP, ad, bd, IDESC_DP, k > 0 ? 1u : 0u);
+                    mma_ss(t_dp, ad, bd, IDESC_DP, k > 0 ? 1u : 0u);
                 }
-                mma_commit(s_full);
+                mma_commit(&s_full[w]);
                 return true;
             };
             bool ok = mbar_wait(q_full, 0, tmo, abort, &g_err_bwd);
-            if (ok) ok = issue_s_dp(0);
+            for (int u = 0; u < C::NWG && u < n && ok; ++u) ok = issue_s_dp(u);
             for (int u = 0; u < n && ok; ++u) {
-                if (!mbar_wait(ds_full, u & 1, tmo, abort, &g_err_bwd)) break;
+                const int w = u % C::NWG, lu = u / C::NWG, s = u % C::ST;
+                if (!mbar_wait(&ds_full[w], lu & 1, tmo, abort, &g_err_bwd)) break;
                 tc_fence_after();
-                const int s = u % C::ST;
-                // dQ += dS K_u: A = dS (K-major, BN keys), B = K_u (MN-major over d).
+                // dQ += dS K_u: A = dS (K-major over BN keys), B = K_u (MN-major over d).
+                const uint32_t dsw = ds_addr + w * C::DS_BYTES;
 #pragma unroll
                 for (int k = 0; k < C::BN / 16; ++k) {
                     const uint64_t ad =
-                        sdesc_sw128(ds_addr + (k / 4) * (C::BM * 128) + (k % 4) * 32, 16, 1024);
+                        sdesc_sw128(dsw + (k / 4) * (C::BM * 128) + (k % 4) * 32, 16, 1024);
                     const uint64_t bd =
                         sdesc_sw128(k_addr + s * C::K_BYTES + k * 2048, C::BN * 128, 1024);
                     mma_ss(tmem + C::TM_DQ, ad, bd, IDESC_DQ, (u > 0 || k > 0) ? 1u : 0u);
                 }
                 mma_commit(&kv_empty[s]);
-                if (u + 1 < n) ok = issue_s_dp(u + 1);
+                if (u + C::NWG < n) ok = issue_s_dp(u + C::NWG);
             }
             mma_commit(dq_done);
         }
     } else {
-        // compute warpgroup: thread = query row
+        // compute warpgroups: thread = query row
+        const int wg = (warp - 2) >> 2;
         const int quad = warp & 3;
         const int row = quad * 32 + lane;
         const int grow = qt * TILE + row;
@@ -298,63 +328,65 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         const size_t bh = static_cast<size_t>(b) * p.H + h;
         const float lse2 = p.lse2[bh * p.Npad + grow];
         const float Drow = p.delta[bh * p.Npad + grow];
-        const int4 *vec = p.vec + static_cast<size_t>(bm) * p.Npad;
-        // dS row r of the K-major swizzled tile: 16-byte chunk c of 64-column
-        // box kb lives at kb*BM*128 + r*128 + ((c ^ (r & 7)) * 16).
-        uint8_t *ds_row = sDS + row * 128;
-        for (int u = 0; u < n; ++u) {
-            if (!warp_wait(s_full, u & 1, tmo, abort)) break;
+        const float sl2 = p.sl2;
+        const int n_my = n > wg ? (n - wg + C::NWG - 1) / C::NWG : 0;
+        // dS row of the K-major swizzled tile: 16-byte chunk c of 64-column box
+        // kb lives at kb*BM*128 + r*128 + ((c ^ (r & 7)) * 16).
+        uint8_t *ds_row = sDS + wg * C::DS_BYTES + row * 128;
+        int entry_next = n_my > 0 ? entries[wg / C::SUB] : 0;
+        for (int lu = 0; lu < n_my; ++lu) {
+            const int u = lu * C::NWG + wg;
+            const int entry = entry_next;
+            if (u + C::NWG < n) entry_next = entries[(u + C::NWG) / C::SUB];
+            const bool masked_tile = entry & 1;
+            const int key0 = (entry >> 1) * TILE + (u % C::SUB) * C::BN;
+            const int es = u % C::ES;
+            if (!warp_wait(&s_full[wg], lu & 1, tmo, abort)) break;
+            if (!warp_wait(&e_full[es], (u / C::ES) & 1, tmo, abort)) break;
             tc_fence_after();
-            float pr[C::BN];
+            const uint32_t t_s = lane_base + wg * C::TM_SDP, t_dp = t_s + C::BN;
+            const int4 *cv = reinterpret_cast<const int4 *>(sE + es * C::E_BYTES);
 #pragma unroll
-            for (int c = 0; c < C::BN / 32; ++c) {
-                uint32_t r[32];
-                tmem_ld32(lane_base + C::TM_S + c * 32, r);
+            for (int c = 0; c < C::BN / 64; ++c) {
+                float pr[64];
+                tmem_ld64f(t_s + c * 64, pr);
 #pragma unroll
-                for (int i = 0; i < 32; ++i)
-                    pr[c * 32 + i] = ex2(__uint_as_float(r[i]) * p.sl2 - lse2);
-            }
-            if (entries[u / C::SUB] & 1) {
-                const int key0 = key0_of(u);
+                for (int jj = 0; jj < 64; ++jj) pr[jj] = ex2(fmaf(pr[jj], sl2, -lse2));
+                if (masked_tile) {
 #pragma unroll
-                for (int jj = 0; jj < C::BN; ++jj) {
-                    const int4 cv = __ldg(vec + key0 + jj);
-                    if (masked_at(grow, key0 + jj, cv, p.causal)) pr[jj] = 0.f;
+                    for (int jj = 0; jj < 64; ++jj)
+                        if (masked_at(grow, key0 + c * 64 + jj, cv[c * 64 + jj], p.causal))
+                            pr[jj] = 0.f;
+                }
+                float dp[64];
+                tmem_ld64f(t_dp + c * 64, dp);
+                uint8_t *box = ds_row + c * C::BM * 128;
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    uint4 w4;
+                    w4.x = pack_bf16(pr[q * 8 + 0] * (dp[q * 8 + 0] - Drow),
+                                     pr[q * 8 + 1] * (dp[q * 8 + 1] - Drow));
+                    w4.y = pack_bf16(pr[q * 8 + 2] * (dp[q * 8 + 2] - Drow),
+                                     pr[q * 8 + 3] * (dp[q * 8 + 3] - Drow));
+                    w4.z = pack_bf16(pr[q * 8 + 4] * (dp[q * 8 + 4] - Drow),
+                                     pr[q * 8 + 5] * (dp[q * 8 + 5] - Drow));
+                    w4.w = pack_bf16(pr[q * 8 + 6] * (dp[q * 8 + 6] - Drow),
+                                     pr[q * 8 + 7] * (dp[q * 8 + 7] - Drow));
+                    *reinterpret_cast<uint4 *>(box + ((q ^ (row & 7)) * 16)) = w4;
                 }
             }
-#pragma unroll
-            for (int c = 0; c < C::BN / 32; ++c) {
-                uint32_t r[32];
-                tmem_ld32(lane_base + C::TM_DP + c * 32, r);
-                // 32 columns = 4 chunks of 8 bf16 in box (c*32)/64
-                const int box = (c * 32) / 64;
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const int col = c * 32 + q * 8;
-                    uint4 w;
-                    float d8[8];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e)
-                        d8[e] = pr[col + e] * (__uint_as_float(r[q * 8 + e]) - Drow);
-                    w.x = pack_bf16(d8[0], d8[1]);
-                    w.y = pack_bf16(d8[2], d8[3]);
-                    w.z = pack_bf16(d8[4], d8[5]);
-                    w.w = pack_bf16(d8[6], d8[7]);
-                    const int chunk = (col % 64) / 8;
-                    *reinterpret_cast<uint4 *>(ds_row + box * C::BM * 128 +
-                                               ((chunk ^ (row & 7)) * 16)) = w;
-                }
-            }
+            mbar_arrive(&e_empty[es]);
             fence_proxy_async_smem();
             tc_fence_before();
-            mbar_arrive(ds_full);
+            mbar_arrive(&ds_full[wg]);
         }
         if (n > 0) warp_wait(dq_done, 0, tmo, abort);
         tc_fence_after();
         __nv_bfloat16 *dst =
             p.dq + ((static_cast<size_t>(b) * p.N + grow) * p.H + h) * static_cast<size_t>(C::D);
+        constexpr int CPW = (C::D / 32) / C::NWG;  // 32-column chunks per group
 #pragma unroll 1
-        for (int c = 0; c < C::D / 32; ++c) {
+        for (int c = wg * CPW; c < (wg + 1) * CPW; ++c) {
             uint32_t r[32];
             tmem_ld32(lane_base + C::TM_DQ + c * 32, r);
             float v[32];
@@ -374,9 +406,12 @@ __global__ void __launch_bounds__(C::THREADS, 1)
 }
 
 // ---------------------------------------------------------------- dkdv kernel
-template <int D_, int DV_, int BM_, int ST_, bool DK_, bool DV_ON_>
+// One CTA per 128-key tile.  NWG compute warpgroups take alternate query
+// sub-tiles of BM rows; each has its own S^T/dP^T region in TMEM, and all of
+// them feed the one dK and the one dV accumulator.
+template <int D_, int DV_, int BM_, int ST_, bool DK_, bool DV_ON_, int NWG_>
 struct DkdvCfg {
-    static constexpr int D = D_, DV = DV_, BM = BM_, ST = ST_;
+    static constexpr int D = D_, DV = DV_, BM = BM_, ST = ST_, NWG = NWG_;
     static constexpr bool DO_DK = DK_, DO_DV = DV_ON_;
     static constexpr int BN = 128;            // keys per CTA (TMEM lanes)
     static constexpr int SUB = TILE / BM;     // query sub-tiles per list entry
@@ -393,20 +428,22 @@ struct DkdvCfg {
                          ST_D = ST_LSE + BM * 4;
     static constexpr int STAGE_STRIDE = (STAGE_BYTES + 1023) / 1024 * 1024;
     static constexpr int OFF_BAR = OFF_ST + ST * STAGE_STRIDE;
-    // kv_full, q_full[ST], q_empty[ST], s_full, p_full, ds_full, done
-    static constexpr int NBAR = 1 + 2 * ST + 4;
+    // kv_full, q_full[ST], q_empty[ST], s_full[NWG], p_full[NWG], ds_full[NWG], done
+    static constexpr int NBAR = 1 + 2 * ST + 3 * NWG + 1;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
     static constexpr int TM_DK = 0;
     static constexpr int TM_DV = DO_DK ? D : 0;
-    static constexpr int TM_S = TM_DV + (DO_DV ? DV : 0);
-    static constexpr int TM_DP = TM_S + BM;
-    static constexpr int TM_END = TM_DP + (DO_DK ? BM : 0);
+    static constexpr int TM_W0 = TM_DV + (DO_DV ? DV : 0);
+    static constexpr int TM_SDP = BM + (DO_DK ? BM : 0);  // per group: S^T then dP^T
+    static constexpr int TM_END = TM_W0 + NWG * TM_SDP;
     static constexpr int TM_COLS = 512;
-    static constexpr int THREADS = 192;
+    static constexpr int THREADS = 64 + NWG * 128;
     static_assert(TM_END <= TM_COLS, "TMEM budget");
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
-    static_assert(D <= 256 && DV <= 256 && BM % 32 == 0, "MMA shape");
+    static_assert(D <= 256 && DV <= 256 && BM % 64 == 0, "MMA shape");
+    static_assert(ST >= NWG, "ring depth");
+    static_assert((D / 32) % NWG == 0 && (DV / 32) % NWG == 0, "epilogue column split");
 };
 
 template <class C>
@@ -420,8 +457,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     uint8_t *sK = smem + C::OFF_K, *sV = smem + C::OFF_V, *sST = smem + C::OFF_ST;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
     uint64_t *kv_full = bars, *q_full = bars + 1, *q_empty = q_full + C::ST;
-    uint64_t *s_full = q_empty + C::ST, *p_full = s_full + 1, *ds_full = p_full + 1,
-             *done = ds_full + 1;
+    uint64_t *s_full = q_empty + C::ST, *p_full = s_full + C::NWG, *ds_full = p_full + C::NWG,
+             *done = ds_full + C::NWG;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
     volatile int *abort = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
 
@@ -443,9 +480,11 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             mbar_init(&q_full[i], 1);
             mbar_init(&q_empty[i], 1);
         }
-        mbar_init(s_full, 1);
-        mbar_init(p_full, 128);
-        mbar_init(ds_full, 128);
+        for (int i = 0; i < C::NWG; ++i) {
+            mbar_init(&s_full[i], 1);
+            mbar_init(&p_full[i], 128);
+            mbar_init(&ds_full[i], 128);
+        }
         mbar_init(done, 1);
         *abort = 0;
         fence_barrier_init();
@@ -503,12 +542,12 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             constexpr uint32_t IDESC_DK = idesc_bf16(128, C::D, false, true);
             const uint32_t k_addr = smem_u32(sK), v_addr = smem_u32(sV);
             const uint32_t st_addr = smem_u32(sST);
-            bool ok = mbar_wait(kv_full, 0, tmo, abort, &g_err_bwd);
-            for (int u = 0; u < n && ok; ++u) {
-                const int s = u % C::ST;
+            auto issue_s = [&](int u) -> bool {
+                const int s = u % C::ST, w = u % C::NWG;
                 const uint32_t stg = st_addr + s * C::STAGE_STRIDE;
-                if (!mbar_wait(&q_full[s], (u / C::ST) & 1, tmo, abort, &g_err_bwd)) break;
+                if (!mbar_wait(&q_full[s], (u / C::ST) & 1, tmo, abort, &g_err_bwd)) return false;
                 tc_fence_after();
+                const uint32_t t_s = tmem + C::TM_W0 + w * C::TM_SDP, t_dp = t_s + C::BM;
                 // S^T = K Q^T
 #pragma unroll
                 for (int k = 0; k < C::D / 16; ++k) {
@@ -516,7 +555,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                         sdesc_sw128(k_addr + (k / 4) * (C::BN * 128) + (k % 4) * 32, 16, 1024);
                     const uint64_t bd = sdesc_sw128(
                         stg + C::ST_Q + (k / 4) * (C::BM * 128) + (k % 4) * 32, 16, 1024);
-                    mma_ss(tmem + C::TM_S, ad, bd, IDESC_S, k > 0 ? 1u : 0u);
+                    mma_ss(t_s, ad, bd, IDESC_S, k > 0 ? 1u : 0u);
                 }
                 if constexpr (C::DO_DK) {
                     // dP^T = V dO^T
@@ -526,113 +565,115 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                             v_addr + (k / 4) * (C::BN * 128) + (k % 4) * 32, 16, 1024);
                         const uint64_t bd = sdesc_sw128(
                             stg + C::ST_DO + (k / 4) * (C::BM * 128) + (k % 4) * 32, 16, 1024);
-                        mma_ss(tmem + C::TM_DP, ad, bd, IDESC_DP, k > 0 ? 1u : 0u);
+                        mma_ss(t_dp, ad, bd, IDESC_DP, k > 0 ? 1u : 0u);
                     }
                 }
-                mma_commit(s_full);
+                mma_commit(&s_full[w]);
+                return true;
+            };
+            bool ok = mbar_wait(kv_full, 0, tmo, abort, &g_err_bwd);
+            for (int u = 0; u < C::NWG && u < n && ok; ++u) ok = issue_s(u);
+            for (int u = 0; u < n && ok; ++u) {
+                const int s = u % C::ST, w = u % C::NWG, lu = u / C::NWG;
+                const uint32_t stg = st_addr + s * C::STAGE_STRIDE;
+                const uint32_t t_s = tmem + C::TM_W0 + w * C::TM_SDP, t_dp = t_s + C::BM;
                 if constexpr (C::DO_DV) {
-                    if (!mbar_wait(p_full, u & 1, tmo, abort, &g_err_bwd)) break;
+                    if (!mbar_wait(&p_full[w], lu & 1, tmo, abort, &g_err_bwd)) break;
                     tc_fence_after();
-                    // dV += P^T dO: A = P^T (TMEM, bf16), B = dO (MN-major over dv)
+                    // dV += P^T dO: A = P^T (TMEM, fp16), B = dO (MN-major over dv)
 #pragma unroll
                     for (int k = 0; k < C::BM / 16; ++k) {
                         const uint64_t bd =
                             sdesc_sw128(stg + C::ST_DO + k * 2048, C::BM * 128, 1024);
-                        mma_ts(tmem + C::TM_DV, tmem + C::TM_S + k * 8, bd, IDESC_DV,
+                        mma_ts(tmem + C::TM_DV, t_s + k * 8, bd, IDESC_DV,
                                (u > 0 || k > 0) ? 1u : 0u);
                     }
                 }
+                // The group is done with this sub-tile's S^T / dP^T reads.
+                if (!mbar_wait(&ds_full[w], lu & 1, tmo, abort, &g_err_bwd)) break;
+                tc_fence_after();
                 if constexpr (C::DO_DK) {
-                    if (!mbar_wait(ds_full, u & 1, tmo, abort, &g_err_bwd)) break;
-                    tc_fence_after();
                     // dK += dS^T Q: A = dS^T (TMEM, bf16), B = Q (MN-major over d)
 #pragma unroll
                     for (int k = 0; k < C::BM / 16; ++k) {
                         const uint64_t bd =
                             sdesc_sw128(stg + C::ST_Q + k * 2048, C::BM * 128, 1024);
-                        mma_ts(tmem + C::TM_DK, tmem + C::TM_DP + k * 8, bd, IDESC_DK,
+                        mma_ts(tmem + C::TM_DK, t_dp + k * 8, bd, IDESC_DK,
                                (u > 0 || k > 0) ? 1u : 0u);
                     }
-                } else {
-                    // S^T is read back before P^T is written; keep the order
-                    // "compute done with S^T" -> next S^T explicit.
-                    if (!mbar_wait(ds_full, u & 1, tmo, abort, &g_err_bwd)) break;
                 }
                 mma_commit(&q_empty[s]);
+                if (u + C::NWG < n) ok = issue_s(u + C::NWG);
             }
             mma_commit(done);
         }
     } else {
-        // compute warpgroup: thread = key column (TMEM lane)
+        // compute warpgroups: thread = key column (TMEM lane)
+        const int wg = (warp - 2) >> 2;
         const int quad = warp & 3;
         const int row = quad * 32 + lane;
         const int gkey = kt * TILE + row;
         const uint32_t lane_base = tmem + (static_cast<uint32_t>(quad * 32) << 16);
         const int4 cv = p.vec[static_cast<size_t>(bm) * p.Npad + gkey];
-        for (int u = 0; u < n; ++u) {
+        const float sl2 = p.sl2;
+        const int n_my = n > wg ? (n - wg + C::NWG - 1) / C::NWG : 0;
+        int entry_next = n_my > 0 ? entries[wg / C::SUB] : 0;
+        for (int lu = 0; lu < n_my; ++lu) {
+            const int u = lu * C::NWG + wg;
             const int s = u % C::ST;
+            const int entry = entry_next;
+            if (u + C::NWG < n) entry_next = entries[(u + C::NWG) / C::SUB];
+            const bool need_mask = entry & 1;
+            const int q0 = (entry >> 1) * TILE + (u % C::SUB) * C::BM;
             const uint8_t *stg = sST + s * C::STAGE_STRIDE;
             const float *slse = reinterpret_cast<const float *>(stg + C::ST_LSE);
             const float *sd = reinterpret_cast<const float *>(stg + C::ST_D);
-            if (!warp_wait(s_full, u & 1, tmo, abort)) break;
+            if (!warp_wait(&s_full[wg], lu & 1, tmo, abort)) break;
             tc_fence_after();
-            const int q0 = q0_of(u);
-            const bool need_mask = entries[u / C::SUB] & 1;
-            float pr[C::BM];
+            const uint32_t t_s = lane_base + C::TM_W0 + wg * C::TM_SDP, t_dp = t_s + C::BM;
 #pragma unroll
-            for (int c = 0; c < C::BM / 32; ++c) {
-                uint32_t r[32];
-                tmem_ld32(lane_base + C::TM_S + c * 32, r);
+            for (int c = 0; c < C::BM / 64; ++c) {
+                float pr[64];
+                tmem_ld64f(t_s + c * 64, pr);
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const int qi = c * 32 + i;
-                    float v = ex2(__uint_as_float(r[i]) * p.sl2 - slse[qi]);
+                for (int i = 0; i < 64; ++i) {
+                    const int qi = c * 64 + i;
+                    float v = ex2(fmaf(pr[i], sl2, -slse[qi]));
                     if (need_mask && masked_at(q0 + qi, gkey, cv, p.causal)) v = 0.f;
-                    pr[qi] = v;
+                    pr[i] = v;
                 }
-            }
-            if constexpr (C::DO_DV) {
-#pragma unroll
-                for (int c = 0; c < C::BM / 64; ++c) {
+                if constexpr (C::DO_DV) {
                     uint32_t r[32];
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) r[i] = pack_fp16(pr[c * 64 + 2 * i], pr[c * 64 + 2 * i + 1]);
-                    tmem_st32(lane_base + C::TM_S + c * 32, r);
+                    for (int i = 0; i < 32; ++i) r[i] = pack_fp16(pr[2 * i], pr[2 * i + 1]);
+                    tmem_st32(t_s + c * 32, r);
                 }
-                tmem_st_wait();
-                tc_fence_before();
-                mbar_arrive(p_full);
-            }
-            if constexpr (C::DO_DK) {
-#pragma unroll
-                for (int c = 0; c < C::BM / 32; ++c) {
+                if constexpr (C::DO_DK) {
+                    float dp[64];
+                    tmem_ld64f(t_dp + c * 64, dp);
                     uint32_t r[32];
-                    tmem_ld32(lane_base + C::TM_DP + c * 32, r);
 #pragma unroll
                     for (int i = 0; i < 32; ++i) {
-                        const int qi = c * 32 + i;
-                        pr[qi] = pr[qi] * (__uint_as_float(r[i]) - sd[qi]);
+                        const int qi = c * 64 + 2 * i;
+                        r[i] = pack_bf16(pr[2 * i] * (dp[2 * i] - sd[qi]),
+                                         pr[2 * i + 1] * (dp[2 * i + 1] - sd[qi + 1]));
                     }
+                    tmem_st32(t_dp + c * 32, r);
                 }
-#pragma unroll
-                for (int c = 0; c < C::BM / 64; ++c) {
-                    uint32_t r[32];
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) r[i] = pack_bf16(pr[c * 64 + 2 * i], pr[c * 64 + 2 * i + 1]);
-                    tmem_st32(lane_base + C::TM_DP + c * 32, r);
-                }
-                tmem_st_wait();
             }
+            tmem_st_wait();
             tc_fence_before();
-            mbar_arrive(ds_full);
+            if constexpr (C::DO_DV) mbar_arrive(&p_full[wg]);
+            mbar_arrive(&ds_full[wg]);
         }
         if (n > 0) warp_wait(done, 0, tmo, abort);
         tc_fence_after();
         const bool store = gkey < p.N;
         const size_t rowoff = (static_cast<size_t>(b) * p.N + gkey) * p.H + h;
         if constexpr (C::DO_DK) {
+            constexpr int CPW = (C::D / 32) / C::NWG;
 #pragma unroll 1
-            for (int c = 0; c < C::D / 32; ++c) {
+            for (int c = wg * CPW; c < (wg + 1) * CPW; ++c) {
                 uint32_t r[32];
                 tmem_ld32(lane_base + C::TM_DK + c * 32, r);
                 float v[32];
@@ -642,8 +683,9 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             }
         }
         if constexpr (C::DO_DV) {
+            constexpr int CPW = (C::DV / 32) / C::NWG;
 #pragma unroll 1
-            for (int c = 0; c < C::DV / 32; ++c) {
+            for (int c = wg * CPW; c < (wg + 1) * CPW; ++c) {
                 uint32_t r[32];
                 tmem_ld32(lane_base + C::TM_DV + c * 32, r);
                 float v[32];
@@ -687,6 +729,7 @@ BwdParams make_params(const Geometry &g, const Workspace &ws, const BwdArgs &a, 
 
 template <class C>
 cudaError_t launch_dq(const Geometry &g, const Workspace &ws, const BwdArgs &a, cudaStream_t st) {
+    if (a.dq_k_rows != C::BN) return cudaErrorInvalidValue;  // map boxes must match the tile
     auto kern = dq_kernel<C>;
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
@@ -700,6 +743,7 @@ cudaError_t launch_dq(const Geometry &g, const Workspace &ws, const BwdArgs &a, 
 template <class C>
 cudaError_t launch_dkdv(const Geometry &g, const Workspace &ws, const BwdArgs &a,
                         cudaStream_t st) {
+    if (a.kv_q_rows != C::BM) return cudaErrorInvalidValue;  // map boxes must match the tile
     auto kern = dkdv_kernel<C>;
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
@@ -725,6 +769,10 @@ cudaError_t launch_pair(const Geometry &g, const Workspace &ws, const BwdArgs &a
 
 }  // namespace
 
+// Every DqCfg below uses 64-key sub-tiles and every DkdvCfg 64-query sub-tiles.
+int dq_key_rows(int, int) { return 64; }
+int dkdv_query_rows(int, int) { return 64; }
+
 cudaError_t launch_bwd(const Geometry &g, const Workspace &ws, const BwdArgs &a,
                        cudaStream_t st, Recorder &rec) {
     const int rows_total = g.B * g.H * g.Npad;
@@ -736,21 +784,23 @@ cudaError_t launch_bwd(const Geometry &g, const Workspace &ws, const BwdArgs &a,
     rec.after(st);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
+    // DkdvCfg<d, dv, query sub-tile, stages, dK, dV, groups>;
+    // DqCfg<d, dv, key sub-tile, stages, groups, boundary stages>
     if (g.d == 64 && g.dv == 64)
-        return launch_pair<DkdvCfg<64, 64, 128, 3, true, true>, DqCfg<64, 64, 128, 3>>(g, ws, a,
-                                                                                     st, rec);
+        return launch_pair<DkdvCfg<64, 64, 64, 4, true, true, 2>, DqCfg<64, 64, 64, 4, 2, 4>>(
+            g, ws, a, st, rec);
     if (g.d == 128 && g.dv == 128)
-        return launch_pair<DkdvCfg<128, 128, 128, 2, true, true>, DqCfg<128, 128, 128, 2>>(
+        return launch_pair<DkdvCfg<128, 128, 64, 4, true, true, 2>, DqCfg<128, 128, 64, 3, 2, 4>>(
             g, ws, a, st, rec);
     if (g.d == 192 && g.dv == 128)
-        return launch_pair<DkdvCfg<192, 128, 64, 2, true, true>, DqCfg<192, 128, 64, 2>>(
+        return launch_pair<DkdvCfg<192, 128, 64, 2, true, true, 1>, DqCfg<192, 128, 64, 2, 2, 4>>(
             g, ws, a, st, rec);
     if (g.d == 256 && g.dv == 256) {
         rec.before(st);
-        e = launch_dkdv<DkdvCfg<256, 256, 64, 2, false, true>>(g, ws, a, st);
+        e = launch_dkdv<DkdvCfg<256, 256, 64, 2, false, true, 2>>(g, ws, a, st);
         rec.after(st);
         if (e != cudaSuccess) return e;
-        return launch_pair<DkdvCfg<256, 256, 64, 1, true, false>, DqCfg<256, 256, 64, 1>>(
+        return launch_pair<DkdvCfg<256, 256, 64, 1, true, false, 1>, DqCfg<256, 256, 64, 1, 1, 2>>(
             g, ws, a, st, rec);
     }
     return cudaErrorInvalidValue;

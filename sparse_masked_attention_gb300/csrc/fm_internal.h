@@ -71,8 +71,12 @@ cudaError_t launch_count(const Geometry &g, const MaskPtrs &m, unsigned long lon
 unsigned read_clear_error_classify();
 
 // fwd.cu
+// Box heights (rows) of the K/V tensor maps the forward kernel expects.
+int fwd_key_rows(int d, int dv);
+
 struct FwdArgs {
     const CUtensorMap *tm_q, *tm_k, *tm_v;
+    int k_rows;  // box height of tm_k / tm_v; must equal the kernel's key tile
     void *o;
     float *lse;
 };
@@ -81,7 +85,14 @@ cudaError_t launch_fwd(const Geometry &g, const Workspace &ws, const FwdArgs &a,
 unsigned read_clear_error_fwd();
 
 // bwd.cu
+// Box heights the backward kernels expect: key sub-tile of the query-side
+// kernel (its K/V maps) and query sub-tile of the key-side kernel (its Q/dO maps).
+int dq_key_rows(int d, int dv);
+int dkdv_query_rows(int d, int dv);
+
 struct BwdArgs {
+    int dq_k_rows;   // box height of tm_k_dq / tm_v_dq
+    int kv_q_rows;   // box height of tm_q / tm_do
     // key-side (dK/dV) kernel maps: q/dO boxes of its query sub-tile, k/v of 128 rows
     const CUtensorMap *tm_q, *tm_k, *tm_v, *tm_do;
     // query-side (dQ) kernel maps: q/dO boxes of 128 rows, k/v of its key sub-tile

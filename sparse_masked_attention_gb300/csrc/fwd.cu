@@ -466,6 +466,7 @@ cudaError_t launch_cfg(const Geometry &g, const Workspace &ws, const FwdArgs &a,
     p.causal = g.causal;
     p.sl2 = g.scale * 1.4426950408889634f;
     p.timeout_ns = g.timeout_ns;
+    if (a.k_rows != C::BN) return cudaErrorInvalidValue;  // map boxes must match the tile
     auto kern = fwd_kernel<C>;
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
@@ -476,6 +477,8 @@ cudaError_t launch_cfg(const Geometry &g, const Workspace &ws, const FwdArgs &a,
 }
 
 }  // namespace
+
+int fwd_key_rows(int d, int dv) { return (d == 256 && dv == 256) ? 64 : 128; }
 
 cudaError_t launch_fwd(const Geometry &g, const Workspace &ws, const FwdArgs &a,
                        cudaStream_t st) {
