@@ -348,8 +348,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             const int4 *cv = reinterpret_cast<const int4 *>(sE + es * C::E_BYTES);
 #pragma unroll
             for (int c = 0; c < C::BN / 64; ++c) {
-                float pr[64];
-                tmem_ld64f(t_s + c * 64, pr);
+                float pr[64], dp[64];
+                tmem_ld64f_x2(t_s + c * 64, pr, t_dp + c * 64, dp);
 #pragma unroll
                 for (int jj = 0; jj < 64; ++jj) pr[jj] = ex2(fmaf(pr[jj], sl2, -lse2));
                 if (masked_tile) {
@@ -358,8 +358,6 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                         if (masked_at(grow, key0 + c * 64 + jj, cv[c * 64 + jj], p.causal))
                             pr[jj] = 0.f;
                 }
-                float dp[64];
-                tmem_ld64f(t_dp + c * 64, dp);
                 uint8_t *box = ds_row + c * C::BM * 128;
 #pragma unroll
                 for (int q = 0; q < 8; ++q) {

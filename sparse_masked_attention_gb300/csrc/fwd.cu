@@ -278,96 +278,102 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             tc_fence_after();
             const uint32_t s_addr = lane_base + C::TM_S + sb * C::BN;
 
-            // pass 1: mask (partial tiles only) and row max of raw scores
-            uint32_t mbits[C::BN / 32];
-            float mx8[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) mx8[i] = NEG_INF;
-            if (masked_tile) {
-                if (!warp_wait(&e_full[es], (u / C::ES) & 1, tmo, abort)) break;
-                const int4 *cv = reinterpret_cast<const int4 *>(sE + es * C::E_BYTES);
-#pragma unroll
-                for (int c = 0; c < C::BN / 64; ++c) {
-                    float x[64];
-                    tmem_ld64f(s_addr + c * 64, x);
-                    uint32_t w0 = 0, w1 = 0;
-#pragma unroll
-                    for (int jj = 0; jj < 64; ++jj) {
-                        const bool mk = masked_at(grow, key0 + c * 64 + jj, cv[c * 64 + jj], p.causal);
-                        if (jj < 32) w0 |= (mk ? 1u : 0u) << jj;
-                        else w1 |= (mk ? 1u : 0u) << (jj - 32);
-                        mx8[jj & 7] = fmaxf(mx8[jj & 7], mk ? NEG_INF : x[jj]);
-                    }
-                    mbits[2 * c] = w0;
-                    mbits[2 * c + 1] = w1;
-                }
-            } else {
-#pragma unroll
-                for (int c = 0; c < C::BN / 64; ++c) {
-                    float x[64];
-                    tmem_ld64f(s_addr + c * 64, x);
-#pragma unroll
-                    for (int jj = 0; jj < 64; ++jj) mx8[jj & 7] = fmaxf(mx8[jj & 7], x[jj]);
-                }
-            }
-            // The group's producer slot of the boundary ring is free again.
-            // (On unmasked tiles the boundaries were not needed; still wait for
-            // their arrival so the ring's phases stay in step.)
-            if (!masked_tile && !warp_wait(&e_full[es], (u / C::ES) & 1, tmo, abort)) break;
-            mbar_arrive(&e_empty[es]);
-
-            float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
-            const float m_new = fmaxf(m_ref, mx * sl2);  // log2 domain (sl2 > 0)
-            const bool need = (m_ref != NEG_INF) && (m_new > m_ref + 8.0f);
-            if (m_ref == NEG_INF) m_ref = m_new;
-            if (__any_sync(0xffffffffu, need)) {
-                // O_w holds the sum over this group's earlier tiles; rescale it.
-                const float alpha = need ? ex2(m_ref - m_new) : 1.0f;
-                if (need) m_ref = m_new;
-                l_sum *= alpha;
-                const int pl = lu - 1;
-                if (!warp_wait(&pv_done[wg * 2 + (pl & 1)], (pl >> 1) & 1, tmo, abort)) break;
-                tc_fence_after();
-                const uint32_t o_addr = lane_base + C::TM_O + wg * C::DV;
-#pragma unroll
-                for (int c = 0; c < C::DV / 32; ++c) {
-                    uint32_t r[32];
-                    tmem_ld32(o_addr + c * 32, r);
-#pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-                    tmem_st32(o_addr + c * 32, r);
-                }
-            }
-            const float m_use = (m_ref == NEG_INF) ? 0.0f : m_ref;
-
-            // pass 2: P = exp2(s*scale*log2e - m), row sum, P -> TMEM (bf16)
-            float l8[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) l8[i] = 0.f;
+            // One pass over the tile in 64-column chunks.  Each chunk is masked
+            // (partial tiles only), its row max taken, and its P written back.
+            // The reference max m_ref moves only when a chunk exceeds it by more
+            // than 2^8; then O, the row sum and the P chunks of this tile that
+            // are already written are rescaled (rare after the first chunk).
+            if (masked_tile && !warp_wait(&e_full[es], (u / C::ES) & 1, tmo, abort)) break;
+            const int4 *cv = reinterpret_cast<const int4 *>(sE + es * C::E_BYTES);
+            bool o_synced = false;  // PV of the group's previous tile observed
+            bool failed = false;
 #pragma unroll
             for (int c = 0; c < C::BN / 64; ++c) {
                 float x[64];
                 tmem_ld64f(s_addr + c * 64, x);
+                if (masked_tile) {
+#pragma unroll
+                    for (int jj = 0; jj < 64; ++jj)
+                        if (masked_at(grow, key0 + c * 64 + jj, cv[c * 64 + jj], p.causal))
+                            x[jj] = NEG_INF;
+                }
+                float mx8[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) mx8[i] = x[i];
+#pragma unroll
+                for (int jj = 8; jj < 64; ++jj) mx8[jj & 7] = fmaxf(mx8[jj & 7], x[jj]);
+                const float mc = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                                       fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) *
+                                 sl2;  // log2 domain (sl2 > 0)
+                const bool need = (m_ref == NEG_INF) ? (mc != NEG_INF) : (mc > m_ref + 8.0f);
+                if (__any_sync(0xffffffffu, need)) {
+                    const float m_new = need ? mc : m_ref;
+                    // alpha = 0 when the row had no visible key yet (O, l, P all 0)
+                    const float alpha =
+                        need ? (m_ref == NEG_INF ? 0.f : ex2(m_ref - m_new)) : 1.0f;
+                    const bool fix = need && m_ref != NEG_INF;
+                    m_ref = m_new;
+                    l_sum *= alpha;
+                    if (__any_sync(0xffffffffu, fix)) {
+                        if (lu > 0) {
+                            if (!o_synced) {
+                                const int pl = lu - 1;
+                                if (!warp_wait(&pv_done[wg * 2 + (pl & 1)], (pl >> 1) & 1, tmo,
+                                               abort)) {
+                                    failed = true;
+                                    break;
+                                }
+                                tc_fence_after();
+                                o_synced = true;
+                            }
+                            const uint32_t o_addr = lane_base + C::TM_O + wg * C::DV;
+#pragma unroll 1
+                            for (int oc = 0; oc < C::DV / 32; ++oc) {
+                                uint32_t r[32];
+                                tmem_ld32(o_addr + oc * 32, r);
+#pragma unroll
+                                for (int i = 0; i < 32; ++i)
+                                    r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+                                tmem_st32(o_addr + oc * 32, r);
+                            }
+                        }
+                        if (c > 0) tmem_st_wait();  // earlier chunks' P stores landed
+#pragma unroll 1
+                        for (int pc = 0; pc < c; ++pc) {  // this tile's P already written
+                            uint32_t r[32];
+                            tmem_ld32(s_addr + pc * 32, r);
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) {
+                                __nv_bfloat162 h2 = *reinterpret_cast<__nv_bfloat162 *>(&r[i]);
+                                const float2 f2 = __bfloat1622float2(h2);
+                                r[i] = pack_bf16(f2.x * alpha, f2.y * alpha);
+                            }
+                            tmem_st32(s_addr + pc * 32, r);
+                        }
+                    }
+                }
+                const float m_use = (m_ref == NEG_INF) ? 0.0f : m_ref;
+                float l8[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) l8[i] = 0.f;
                 uint32_t r[32];
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
-                    float p0 = ex2(fmaf(x[2 * i], sl2, -m_use));
-                    float p1 = ex2(fmaf(x[2 * i + 1], sl2, -m_use));
-                    if (masked_tile) {
-                        const uint32_t w = mbits[2 * c + (i >> 4)];
-                        const int bit = (2 * i) & 31;
-                        if ((w >> bit) & 1u) p0 = 0.f;
-                        if ((w >> (bit + 1)) & 1u) p1 = 0.f;
-                    }
+                    const float p0 = ex2(fmaf(x[2 * i], sl2, -m_use));
+                    const float p1 = ex2(fmaf(x[2 * i + 1], sl2, -m_use));
                     l8[(2 * i) & 7] += p0;
                     l8[(2 * i + 1) & 7] += p1;
                     r[i] = pack_bf16(p0, p1);
                 }
                 tmem_st32(s_addr + c * 32, r);
+                l_sum += ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));
             }
-            l_sum += ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));
+            if (failed) break;
+            // The boundary ring slot is free again.  (On unmasked tiles the
+            // boundaries were not needed; still wait for their arrival so the
+            // ring's phases stay in step.)
+            if (!masked_tile && !warp_wait(&e_full[es], (u / C::ES) & 1, tmo, abort)) break;
+            mbar_arrive(&e_empty[es]);
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(&p_full[sb]);
