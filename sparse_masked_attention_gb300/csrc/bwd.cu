@@ -270,29 +270,32 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             constexpr uint32_t IDESC_S = idesc_bf16(128, C::BN, false, false);
             constexpr uint32_t IDESC_DP = idesc_fp16(128, C::BN, false, false);
             constexpr uint32_t IDESC_DQ = idesc_bf16(128, C::D, false, true);
-            const uint32_t q_addr = smem_u32(sQ), do_addr = smem_u32(sDO);
-            const uint32_t ds_addr = smem_u32(sDS);
-            const uint32_t k_addr = smem_u32(sK), v_addr = smem_u32(sV);
+            // Descriptors are built once; an MMA step only adds its byte offset
+            // (in 16-byte units) to the start-address field.
+            const uint64_t q_desc = sdesc_sw128(smem_u32(sQ), 16, 1024);
+            const uint64_t do_desc = sdesc_sw128(smem_u32(sDO), 16, 1024);
+            const uint64_t ds_desc = sdesc_sw128(smem_u32(sDS), 16, 1024);
+            const uint64_t k_desc = sdesc_sw128(smem_u32(sK), 16, 1024);
+            const uint64_t k_desc_mn = sdesc_sw128(smem_u32(sK), C::BN * 128, 1024);
+            const uint64_t v_desc = sdesc_sw128(smem_u32(sV), 16, 1024);
             auto issue_s_dp = [&](int u) -> bool {
                 const int s = u % C::ST, w = u % C::NWG;
                 if (!mbar_wait(&kv_full[s], (u / C::ST) & 1, tmo, abort, &g_err_bwd)) return false;
                 tc_fence_after();
                 const uint32_t t_s = tmem + w * C::TM_SDP, t_dp = t_s + C::BN;
+                const uint64_t ks = k_desc + static_cast<uint64_t>((s * C::K_BYTES) >> 4);
+                const uint64_t vsd = v_desc + static_cast<uint64_t>((s * C::V_BYTES) >> 4);
 #pragma unroll
                 for (int k = 0; k < C::D / 16; ++k) {
-                    const uint64_t ad =
-                        sdesc_sw128(q_addr + (k / 4) * (C::BM * 128) + (k % 4) * 32, 16, 1024);
-                    const uint64_t bd = sdesc_sw128(
-                        k_addr + s * C::K_BYTES + (k / 4) * (C::BN * 128) + (k % 4) * 32, 16, 1024);
-                    mma_ss(t_s, ad, bd, IDESC_S, k > 0 ? 1u : 0u);
+                    const uint32_t a_off = ((k / 4) * (C::BM * 128) + (k % 4) * 32) >> 4;
+                    const uint32_t b_off = ((k / 4) * (C::BN * 128) + (k % 4) * 32) >> 4;
+                    mma_ss(t_s, q_desc + a_off, ks + b_off, IDESC_S, k > 0 ? 1u : 0u);
                 }
 #pragma unroll
                 for (int k = 0; k < C::DV / 16; ++k) {
-                    const uint64_t ad =
-                        sdesc_sw128(do_addr + (k / 4) * (C::BM * 128) + (k % 4) * 32, 16, 1024);
-                    const uint64_t bd = sdesc_sw128(
-                        v_addr + s * C::V_BYTES + (k / 4) * (C::BN * 128) + (k % 4) * 32, 16, 1024);
-                    mma_ss(t_dp, ad, bd, IDESC_DP, k > 0 ? 1u : 0u);
+                    const uint32_t a_off = ((k / 4) * (C::BM * 128) + (k % 4) * 32) >> 4;
+                    const uint32_t b_off = ((k / 4) * (C::BN * 128) + (k % 4) * 32) >> 4;
+                    mma_ss(t_dp, do_desc + a_off, vsd + b_off, IDESC_DP, k > 0 ? 1u : 0u);
                 }
                 mma_commit(&s_full[w]);
                 return true;
@@ -304,14 +307,13 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 if (!mbar_wait(&ds_full[w], lu & 1, tmo, abort, &g_err_bwd)) break;
                 tc_fence_after();
                 // dQ += dS K_u: A = dS (K-major over BN keys), B = K_u (MN-major over d).
-                const uint32_t dsw = ds_addr + w * C::DS_BYTES;
+                const uint64_t dsw = ds_desc + static_cast<uint64_t>((w * C::DS_BYTES) >> 4);
+                const uint64_t kmn = k_desc_mn + static_cast<uint64_t>((s * C::K_BYTES) >> 4);
 #pragma unroll
                 for (int k = 0; k < C::BN / 16; ++k) {
-                    const uint64_t ad =
-                        sdesc_sw128(dsw + (k / 4) * (C::BM * 128) + (k % 4) * 32, 16, 1024);
-                    const uint64_t bd =
-                        sdesc_sw128(k_addr + s * C::K_BYTES + k * 2048, C::BN * 128, 1024);
-                    mma_ss(tmem + C::TM_DQ, ad, bd, IDESC_DQ, (u > 0 || k > 0) ? 1u : 0u);
+                    const uint32_t a_off = ((k / 4) * (C::BM * 128) + (k % 4) * 32) >> 4;
+                    mma_ss(tmem + C::TM_DQ, dsw + a_off, kmn + ((k * 2048) >> 4), IDESC_DQ,
+                           (u > 0 || k > 0) ? 1u : 0u);
                 }
                 mma_commit(&kv_empty[s]);
                 if (u + C::NWG < n) ok = issue_s_dp(u + C::NWG);
@@ -353,10 +355,19 @@ __global__ void __launch_bounds__(C::THREADS, 1)
 #pragma unroll
                 for (int jj = 0; jj < 64; ++jj) pr[jj] = ex2(fmaf(pr[jj], sl2, -lse2));
                 if (masked_tile) {
+                    // Row bits of key columns lane, lane + 32 over the warp's rows,
+                    // transposed so each lane holds its row's column bits.
+                    const int R = grow - lane;
+                    const int ja = key0 + c * 64 + lane;
+                    const uint32_t wa = warp_transpose32(
+                        column_row_bits(R, ja, cv[c * 64 + lane], p.causal), lane);
+                    const uint32_t wb = warp_transpose32(
+                        column_row_bits(R, ja + 32, cv[c * 64 + 32 + lane], p.causal), lane);
 #pragma unroll
-                    for (int jj = 0; jj < 64; ++jj)
-                        if (masked_at(grow, key0 + c * 64 + jj, cv[c * 64 + jj], p.causal))
-                            pr[jj] = 0.f;
+                    for (int jj = 0; jj < 32; ++jj) {
+                        if ((wa >> jj) & 1u) pr[jj] = 0.f;
+                        if ((wb >> jj) & 1u) pr[32 + jj] = 0.f;
+                    }
                 }
                 uint8_t *box = ds_row + c * C::BM * 128;
 #pragma unroll
@@ -538,32 +549,33 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             constexpr uint32_t IDESC_DP = idesc_fp16(128, C::BM, false, false);
             constexpr uint32_t IDESC_DV = idesc_fp16(128, C::DV, false, true);
             constexpr uint32_t IDESC_DK = idesc_bf16(128, C::D, false, true);
-            const uint32_t k_addr = smem_u32(sK), v_addr = smem_u32(sV);
-            const uint32_t st_addr = smem_u32(sST);
+            // Descriptors are built once; an MMA step only adds its byte offset
+            // (in 16-byte units) to the start-address field.
+            const uint64_t k_desc = sdesc_sw128(smem_u32(sK), 16, 1024);
+            const uint64_t v_desc = sdesc_sw128(smem_u32(sV), 16, 1024);
+            const uint64_t st_desc = sdesc_sw128(smem_u32(sST), 16, 1024);
+            const uint64_t st_desc_mn = sdesc_sw128(smem_u32(sST), C::BM * 128, 1024);
             auto issue_s = [&](int u) -> bool {
                 const int s = u % C::ST, w = u % C::NWG;
-                const uint32_t stg = st_addr + s * C::STAGE_STRIDE;
+                const uint64_t stg = st_desc + static_cast<uint64_t>((s * C::STAGE_STRIDE) >> 4);
                 if (!mbar_wait(&q_full[s], (u / C::ST) & 1, tmo, abort, &g_err_bwd)) return false;
                 tc_fence_after();
                 const uint32_t t_s = tmem + C::TM_W0 + w * C::TM_SDP, t_dp = t_s + C::BM;
                 // S^T = K Q^T
 #pragma unroll
                 for (int k = 0; k < C::D / 16; ++k) {
-                    const uint64_t ad =
-                        sdesc_sw128(k_addr + (k / 4) * (C::BN * 128) + (k % 4) * 32, 16, 1024);
-                    const uint64_t bd = sdesc_sw128(
-                        stg + C::ST_Q + (k / 4) * (C::BM * 128) + (k % 4) * 32, 16, 1024);
-                    mma_ss(t_s, ad, bd, IDESC_S, k > 0 ? 1u : 0u);
+                    const uint32_t a_off = ((k / 4) * (C::BN * 128) + (k % 4) * 32) >> 4;
+                    const uint32_t b_off = (C::ST_Q + (k / 4) * (C::BM * 128) + (k % 4) * 32) >> 4;
+                    mma_ss(t_s, k_desc + a_off, stg + b_off, IDESC_S, k > 0 ? 1u : 0u);
                 }
                 if constexpr (C::DO_DK) {
                     // dP^T = V dO^T
 #pragma unroll
                     for (int k = 0; k < C::DV / 16; ++k) {
-                        const uint64_t ad = sdesc_sw128(
-                            v_addr + (k / 4) * (C::BN * 128) + (k % 4) * 32, 16, 1024);
-                        const uint64_t bd = sdesc_sw128(
-                            stg + C::ST_DO + (k / 4) * (C::BM * 128) + (k % 4) * 32, 16, 1024);
-                        mma_ss(t_dp, ad, bd, IDESC_DP, k > 0 ? 1u : 0u);
+                        const uint32_t a_off = ((k / 4) * (C::BN * 128) + (k % 4) * 32) >> 4;
+                        const uint32_t b_off =
+                            (C::ST_DO + (k / 4) * (C::BM * 128) + (k % 4) * 32) >> 4;
+                        mma_ss(t_dp, v_desc + a_off, stg + b_off, IDESC_DP, k > 0 ? 1u : 0u);
                     }
                 }
                 mma_commit(&s_full[w]);
@@ -573,19 +585,17 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             for (int u = 0; u < C::NWG && u < n && ok; ++u) ok = issue_s(u);
             for (int u = 0; u < n && ok; ++u) {
                 const int s = u % C::ST, w = u % C::NWG, lu = u / C::NWG;
-                const uint32_t stg = st_addr + s * C::STAGE_STRIDE;
+                const uint64_t stg_mn =
+                    st_desc_mn + static_cast<uint64_t>((s * C::STAGE_STRIDE) >> 4);
                 const uint32_t t_s = tmem + C::TM_W0 + w * C::TM_SDP, t_dp = t_s + C::BM;
                 if constexpr (C::DO_DV) {
                     if (!mbar_wait(&p_full[w], lu & 1, tmo, abort, &g_err_bwd)) break;
                     tc_fence_after();
                     // dV += P^T dO: A = P^T (TMEM, fp16), B = dO (MN-major over dv)
 #pragma unroll
-                    for (int k = 0; k < C::BM / 16; ++k) {
-                        const uint64_t bd =
-                            sdesc_sw128(stg + C::ST_DO + k * 2048, C::BM * 128, 1024);
-                        mma_ts(tmem + C::TM_DV, t_s + k * 8, bd, IDESC_DV,
-                               (u > 0 || k > 0) ? 1u : 0u);
-                    }
+                    for (int k = 0; k < C::BM / 16; ++k)
+                        mma_ts(tmem + C::TM_DV, t_s + k * 8, stg_mn + ((C::ST_DO + k * 2048) >> 4),
+                               IDESC_DV, (u > 0 || k > 0) ? 1u : 0u);
                 }
                 // The group is done with this sub-tile's S^T / dP^T reads.
                 if (!mbar_wait(&ds_full[w], lu & 1, tmo, abort, &g_err_bwd)) break;
@@ -593,12 +603,9 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 if constexpr (C::DO_DK) {
                     // dK += dS^T Q: A = dS^T (TMEM, bf16), B = Q (MN-major over d)
 #pragma unroll
-                    for (int k = 0; k < C::BM / 16; ++k) {
-                        const uint64_t bd =
-                            sdesc_sw128(stg + C::ST_Q + k * 2048, C::BM * 128, 1024);
-                        mma_ts(tmem + C::TM_DK, t_dp + k * 8, bd, IDESC_DK,
-                               (u > 0 || k > 0) ? 1u : 0u);
-                    }
+                    for (int k = 0; k < C::BM / 16; ++k)
+                        mma_ts(tmem + C::TM_DK, t_dp + k * 8, stg_mn + ((C::ST_Q + k * 2048) >> 4),
+                               IDESC_DK, (u > 0 || k > 0) ? 1u : 0u);
                 }
                 mma_commit(&q_empty[s]);
                 if (u + C::NWG < n) ok = issue_s(u + C::NWG);
@@ -633,11 +640,15 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             for (int c = 0; c < C::BM / 64; ++c) {
                 float pr[64];
                 tmem_ld64f(t_s + c * 64, pr);
+                // This thread's key column: masked query rows of the sub-tile as bits.
+                const uint32_t mw0 = need_mask ? column_row_bits(q0 + c * 64, gkey, cv, p.causal) : 0u;
+                const uint32_t mw1 =
+                    need_mask ? column_row_bits(q0 + c * 64 + 32, gkey, cv, p.causal) : 0u;
 #pragma unroll
                 for (int i = 0; i < 64; ++i) {
                     const int qi = c * 64 + i;
                     float v = ex2(fmaf(pr[i], sl2, -slse[qi]));
-                    if (need_mask && masked_at(q0 + qi, gkey, cv, p.causal)) v = 0.f;
+                    if ((((i < 32) ? mw0 : mw1) >> (i & 31)) & 1u) v = 0.f;
                     pr[i] = v;
                 }
                 if constexpr (C::DO_DV) {

@@ -287,6 +287,40 @@ __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
 }
 
 // ------------------------------------------------------------- mask helper
+// Bits [lo, hi) of a 32-bit word, lo and hi clamped to [0, 32].
+__device__ __forceinline__ uint32_t bit_range(int lo, int hi) {
+    lo = max(lo, 0);
+    hi = min(hi, 32);
+    if (hi <= lo) return 0u;
+    const uint32_t below_hi = hi >= 32 ? 0xffffffffu : ((1u << hi) - 1u);
+    return below_hi & ~((1u << lo) - 1u);
+}
+
+// Rows R .. R+31 of key column j: bit r set <=> row R + r is masked.  The
+// masked rows of one column are the union of at most three intervals: [0, j)
+// under the causal flag, [LTS, LTE) and [UTS, UTE).
+__device__ __forceinline__ uint32_t column_row_bits(int R, int j, int4 c, int causal) {
+    uint32_t m = causal ? bit_range(-R, j - R) : 0u;
+    m |= bit_range(c.x - R, c.y - R);
+    m |= bit_range(c.z - R, c.w - R);
+    return m;
+}
+
+// 32x32 bit transpose across a warp: on entry lane l holds row l of a bit
+// matrix (bit b = element [l][b]); on exit lane l holds column l (bit b =
+// element [b][l]).  Five exchange steps of halving block size.
+__device__ __forceinline__ uint32_t warp_transpose32(uint32_t x, int lane) {
+    const uint32_t keep[5] = {0x0000FFFFu, 0x00FF00FFu, 0x0F0F0F0Fu, 0x33333333u, 0x55555555u};
+#pragma unroll
+    for (int k = 0; k < 5; ++k) {
+        const int s = 16 >> k;
+        const uint32_t m = keep[k];
+        const uint32_t y = __shfl_xor_sync(0xffffffffu, x, s);
+        x = (lane & s) ? ((x & ~m) | ((y & ~m) >> s)) : ((x & m) | ((y & m) << s));
+    }
+    return x;
+}
+
 // Column-wise mask predicate on normalised boundaries c = (LTS, LTE, UTS, UTE).
 __device__ __forceinline__ bool masked_at(int i, int j, int4 c, int causal) {
     return (causal && i < j) | (c.x <= i && i < c.y) | (c.z <= i && i < c.w);

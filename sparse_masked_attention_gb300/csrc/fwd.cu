@@ -210,21 +210,22 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         if (lane == 0 && n > 0) {
             constexpr uint32_t IDESC_S = idesc_bf16(128, C::BN, false, false);
             constexpr uint32_t IDESC_PV = idesc_bf16(128, C::DV, false, true);
-            const uint32_t q_addr = smem_u32(sQ);
-            const uint32_t k_addr = smem_u32(sK);
-            const uint32_t v_addr = smem_u32(sV);
+            // Descriptors are built once; an MMA step only adds its byte offset
+            // (in 16-byte units) to the start-address field.
+            const uint64_t q_desc = sdesc_sw128(smem_u32(sQ), 16, 1024);
+            const uint64_t k_desc = sdesc_sw128(smem_u32(sK), 16, 1024);
+            const uint64_t v_desc = sdesc_sw128(smem_u32(sV), C::BN * 128, 1024);
             auto issue_s = [&](int u) -> bool {
                 const int w = u % C::NWG, lu = u / C::NWG, sb = w * C::NSB + lu % C::NSB;
                 const int s = u % C::KS;
                 if (!mbar_wait(&k_full[s], (u / C::KS) & 1, tmo, abort, &g_err_fwd)) return false;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem + C::TM_S + sb * C::BN;
+                const uint64_t ks = k_desc + static_cast<uint64_t>((s * C::K_BYTES) >> 4);
 #pragma unroll
                 for (int k = 0; k < C::D / 16; ++k) {
-                    const uint64_t ad =
-                        sdesc_sw128(q_addr + (k / 4) * (C::BM * 128) + (k % 4) * 32, 16, 1024);
-                    const uint64_t bd = sdesc_sw128(
-                        k_addr + s * C::K_BYTES + (k / 4) * (C::BN * 128) + (k % 4) * 32, 16, 1024);
+                    const uint64_t ad = q_desc + (((k / 4) * (C::BM * 128) + (k % 4) * 32) >> 4);
+                    const uint64_t bd = ks + (((k / 4) * (C::BN * 128) + (k % 4) * 32) >> 4);
                     mma_ss(d_tmem, ad, bd, IDESC_S, k > 0 ? 1u : 0u);
                 }
                 mma_commit(&k_empty[s]);
@@ -241,12 +242,11 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 tc_fence_after();
                 const uint32_t o_tmem = tmem + C::TM_O + w * C::DV;
                 const uint32_t p_tmem = tmem + C::TM_S + sb * C::BN;
+                const uint64_t vsd = v_desc + static_cast<uint64_t>((vs * C::V_BYTES) >> 4);
 #pragma unroll
-                for (int k = 0; k < C::BN / 16; ++k) {
-                    const uint64_t bd =
-                        sdesc_sw128(v_addr + vs * C::V_BYTES + k * 2048, C::BN * 128, 1024);
-                    mma_ts(o_tmem, p_tmem + k * 8, bd, IDESC_PV, (lu > 0 || k > 0) ? 1u : 0u);
-                }
+                for (int k = 0; k < C::BN / 16; ++k)
+                    mma_ts(o_tmem, p_tmem + k * 8, vsd + ((k * 2048) >> 4), IDESC_PV,
+                           (lu > 0 || k > 0) ? 1u : 0u);
                 mma_commit(&v_empty[vs]);
                 mma_commit(&pv_done[w * 2 + (lu & 1)]);
                 if (u + L < n) ok = issue_s(u + L);
@@ -292,10 +292,20 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 float x[64];
                 tmem_ld64f(s_addr + c * 64, x);
                 if (masked_tile) {
+                    // Lane l builds the row bits of key columns l and l + 32 of
+                    // the chunk over this warp's 32 rows; a bit transpose hands
+                    // every lane the column bits of its own row.
+                    const int R = grow - lane;
+                    const int ja = key0 + c * 64 + lane;
+                    const uint32_t wa = warp_transpose32(
+                        column_row_bits(R, ja, cv[c * 64 + lane], p.causal), lane);
+                    const uint32_t wb = warp_transpose32(
+                        column_row_bits(R, ja + 32, cv[c * 64 + 32 + lane], p.causal), lane);
 #pragma unroll
-                    for (int jj = 0; jj < 64; ++jj)
-                        if (masked_at(grow, key0 + c * 64 + jj, cv[c * 64 + jj], p.causal))
-                            x[jj] = NEG_INF;
+                    for (int jj = 0; jj < 32; ++jj) {
+                        if ((wa >> jj) & 1u) x[jj] = NEG_INF;
+                        if ((wb >> jj) & 1u) x[32 + jj] = NEG_INF;
+                    }
                 }
                 float mx8[8];
 #pragma unroll
