@@ -13,8 +13,9 @@
 //                their P is 0.
 //   dq kernel    one CTA per 128-row query tile walks its key tiles:
 //                S = Q K^T (bf16), dP = dO V^T (fp16 copies) as SS MMAs;
-//                dS -> shared memory (bf16);
-//                dQ += dS K (SS MMA).  Writes dQ once, in a fixed order.
+//                dS -> TMEM (bf16);
+//                dQ += dS K (TS MMA, dS read from TMEM).  Writes dQ once, in a
+//                fixed order.
 //   dkdv kernel  one CTA per 128-key tile walks its query tiles:
 //                S^T = K Q^T (bf16), dP^T = V dO^T (fp16 copies) as SS MMAs;
 //                P^T -> TMEM as fp16, dS^T as bf16; dV += P^T dO (fp16) and
@@ -130,40 +131,40 @@ struct BwdParams {
 };
 
 // ------------------------------------------------------------------ dq kernel
-// One CTA per 128-row query tile.  NWG compute warpgroups take alternate key
-// sub-tiles of BN keys; each has its own S/dP region in TMEM and its own dS
-// buffer in shared memory, and all of them feed one dQ accumulator.
-template <int D_, int DV_, int BN_, int ST_, int NWG_, int ES_>
+// One CTA per 128-row query tile; NWG compute warpgroups take alternate key
+// sub-tiles of BN keys.  Each group owns one BN-column TMEM region that holds,
+// in turn, S (fp32), then dP (fp32), then dS (bf16, packed); all groups feed
+// one dQ accumulator, and dQ += dS K reads dS straight from TMEM.
+// Rings: K in KS stages shared in tile order (S and dQ read it), V in one
+// stage per group (dP reads it).  The MMA thread serves whichever group is
+// ready, so one group's late operand never stalls the other group's work;
+// only the dQ accumulation keeps tile order (bit-reproducible sums).
+template <int D_, int DV_, int BN_, int KS_, int NWG_>
 struct DqCfg {
-    static constexpr int D = D_, DV = DV_, BN = BN_, ST = ST_, NWG = NWG_, ES = ES_;
+    static constexpr int D = D_, DV = DV_, BN = BN_, KS = KS_, NWG = NWG_;
     static constexpr int BM = 128;
     static constexpr int SUB = TILE / BN;
     static constexpr int Q_BYTES = BM * D * 2;
     static constexpr int DO_BYTES = BM * DV * 2;
     static constexpr int K_BYTES = BN * D * 2;
     static constexpr int V_BYTES = BN * DV * 2;
-    static constexpr int DS_BYTES = BM * BN * 2;
-    static constexpr int E_BYTES = BN * 16;
     static constexpr int OFF_Q = 0;
     static constexpr int OFF_DO = OFF_Q + Q_BYTES;
-    static constexpr int OFF_DS = OFF_DO + DO_BYTES;
-    static constexpr int OFF_K = OFF_DS + NWG * DS_BYTES;
-    static constexpr int OFF_V = OFF_K + ST * K_BYTES;
-    static constexpr int OFF_E = OFF_V + ST * V_BYTES;
-    static constexpr int OFF_BAR = OFF_E + ES * E_BYTES;
-    // q_full, kv_full[ST], kv_empty[ST], e_full[ES], e_empty[ES], s_full[NWG],
-    // ds_full[NWG], dq_done
-    static constexpr int NBAR = 1 + 2 * ST + 2 * ES + 2 * NWG + 1;
+    static constexpr int OFF_K = OFF_DO + DO_BYTES;
+    static constexpr int OFF_V = OFF_K + KS * K_BYTES;
+    static constexpr int OFF_BAR = OFF_V + NWG * V_BYTES;
+    // q_full, k_full[KS], k_empty[KS], v_full[NWG], v_empty[NWG],
+    // s_full[NWG], p_full[NWG], dp_full[NWG], ds_full[NWG], dq_done
+    static constexpr int NBAR = 1 + 2 * KS + 6 * NWG + 1;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
-    static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
-    static constexpr int TM_SDP = 2 * BN;  // per group: S then dP
-    static constexpr int TM_DQ = NWG * TM_SDP;
+    static constexpr int SMEM_BYTES = OFF_MISC + 16;
+    static constexpr int TM_DQ = NWG * BN;  // group w's region: columns [w*BN, (w+1)*BN)
     static constexpr int TM_COLS = 512;
     static constexpr int THREADS = 64 + NWG * 128;
     static_assert(TM_DQ + D <= TM_COLS, "TMEM budget");
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
     static_assert(BN == 64 || BN == 128, "key sub-tile");
-    static_assert(ST >= NWG && ES % NWG == 0, "ring depths");
+    static_assert(KS >= NWG, "ring depth");
     static_assert((D / 32) % NWG == 0, "epilogue column split");
 };
 
@@ -172,15 +173,18 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
               const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
               const BwdParams p) {
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    uint8_t *sQ = smem + C::OFF_Q, *sDO = smem + C::OFF_DO, *sDS = smem + C::OFF_DS;
-    uint8_t *sK = smem + C::OFF_K, *sV = smem + C::OFF_V, *sE = smem + C::OFF_E;
+    extern __shared__ __align__(1024) uint8_t smem[];
+    if (smem_u32(smem) & 1023u) {  // swizzled tiles need 1024-byte alignment
+        if (threadIdx.x == 0) atomicExch(&g_err_bwd, ERR_SMEM_ALIGN);
+        return;
+    }
+    uint8_t *sQ = smem + C::OFF_Q, *sDO = smem + C::OFF_DO;
+    uint8_t *sK = smem + C::OFF_K, *sV = smem + C::OFF_V;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
-    uint64_t *q_full = bars, *kv_full = bars + 1, *kv_empty = kv_full + C::ST;
-    uint64_t *e_full = kv_empty + C::ST, *e_empty = e_full + C::ES;
-    uint64_t *s_full = e_empty + C::ES, *ds_full = s_full + C::NWG, *dq_done = ds_full + C::NWG;
+    uint64_t *q_full = bars, *k_full = bars + 1, *k_empty = k_full + C::KS;
+    uint64_t *v_full = k_empty + C::KS, *v_empty = v_full + C::NWG;
+    uint64_t *s_full = v_empty + C::NWG, *p_full = s_full + C::NWG, *dp_full = p_full + C::NWG;
+    uint64_t *ds_full = dp_full + C::NWG, *dq_done = ds_full + C::NWG;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
     volatile int *abort = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
 
@@ -194,19 +198,20 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     const int n = (*reinterpret_cast<volatile unsigned *>(&g_err_bwd) != 0) ? 0
                                                                             : n_entries * C::SUB;
     const uint64_t tmo = p.timeout_ns;
+    auto n_of = [&](int w) { return n > w ? (n - w + C::NWG - 1) / C::NWG : 0; };
 
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
-        for (int i = 0; i < C::ST; ++i) {
-            mbar_init(&kv_full[i], 1);
-            mbar_init(&kv_empty[i], 1);
-        }
-        for (int i = 0; i < C::ES; ++i) {
-            mbar_init(&e_full[i], 1);
-            mbar_init(&e_empty[i], 128);
+        for (int i = 0; i < C::KS; ++i) {
+            mbar_init(&k_full[i], 1);
+            mbar_init(&k_empty[i], 1);
         }
         for (int i = 0; i < C::NWG; ++i) {
+            mbar_init(&v_full[i], 1);
+            mbar_init(&v_empty[i], 1);
             mbar_init(&s_full[i], 1);
+            mbar_init(&p_full[i], 128);
+            mbar_init(&dp_full[i], 1);
             mbar_init(&ds_full[i], 128);
         }
         mbar_init(dq_done, 1);
@@ -229,7 +234,6 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         if (lane == 0 && n > 0) {
             prefetch_tmap(&tm_q);
             prefetch_tmap(&tm_k);
-            prefetch_tmap(&tm_v);
             prefetch_tmap(&tm_do);
             mbar_arrive_expect_tx(q_full, C::Q_BYTES + C::DO_BYTES);
 #pragma unroll
@@ -239,30 +243,29 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             for (int c = 0; c < C::DV / 64; ++c)
                 tma_load_4d(sDO + c * C::BM * 128, &tm_do, q_full, c * 64, h, qt * TILE, b);
             for (int u = 0; u < n; ++u) {
-                const int s = u % C::ST;
-                if (u >= C::ST &&
-                    !mbar_wait(&kv_empty[s], ((u / C::ST) - 1) & 1, tmo, abort, &g_err_bwd))
+                const int s = u % C::KS;
+                if (u >= C::KS &&
+                    !mbar_wait(&k_empty[s], ((u / C::KS) - 1) & 1, tmo, abort, &g_err_bwd))
                     break;
-                mbar_arrive_expect_tx(&kv_full[s], C::K_BYTES + C::V_BYTES);
+                mbar_arrive_expect_tx(&k_full[s], C::K_BYTES);
                 const int key0 = key0_of(u);
 #pragma unroll
                 for (int c = 0; c < C::D / 64; ++c)
-                    tma_load_4d(sK + s * C::K_BYTES + c * C::BN * 128, &tm_k, &kv_full[s],
-                                c * 64, h, key0, b);
-#pragma unroll
-                for (int c = 0; c < C::DV / 64; ++c)
-                    tma_load_4d(sV + s * C::V_BYTES + c * C::BN * 128, &tm_v, &kv_full[s],
-                                c * 64, h, key0, b);
+                    tma_load_4d(sK + s * C::K_BYTES + c * C::BN * 128, &tm_k, &k_full[s], c * 64,
+                                h, key0, b);
             }
         } else if (lane == 1 && n > 0) {
-            const int4 *vec = p.vec + static_cast<size_t>(bm) * p.Npad;
+            prefetch_tmap(&tm_v);
             for (int u = 0; u < n; ++u) {
-                const int s = u % C::ES;
-                if (u >= C::ES &&
-                    !mbar_wait(&e_empty[s], ((u / C::ES) - 1) & 1, tmo, abort, &g_err_bwd))
+                const int w = u % C::NWG, lw = u / C::NWG;
+                if (lw >= 1 && !mbar_wait(&v_empty[w], (lw - 1) & 1, tmo, abort, &g_err_bwd))
                     break;
-                mbar_arrive_expect_tx(&e_full[s], C::E_BYTES);
-                bulk_load(sE + s * C::E_BYTES, vec + key0_of(u), C::E_BYTES, &e_full[s]);
+                mbar_arrive_expect_tx(&v_full[w], C::V_BYTES);
+                const int key0 = key0_of(u);
+#pragma unroll
+                for (int c = 0; c < C::DV / 64; ++c)
+                    tma_load_4d(sV + w * C::V_BYTES + c * C::BN * 128, &tm_v, &v_full[w], c * 64,
+                                h, key0, b);
             }
         }
     } else if (warp == 1) {
@@ -274,49 +277,86 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             // (in 16-byte units) to the start-address field.
             const uint64_t q_desc = sdesc_sw128(smem_u32(sQ), 16, 1024);
             const uint64_t do_desc = sdesc_sw128(smem_u32(sDO), 16, 1024);
-            const uint64_t ds_desc = sdesc_sw128(smem_u32(sDS), 16, 1024);
             const uint64_t k_desc = sdesc_sw128(smem_u32(sK), 16, 1024);
             const uint64_t k_desc_mn = sdesc_sw128(smem_u32(sK), C::BN * 128, 1024);
             const uint64_t v_desc = sdesc_sw128(smem_u32(sV), 16, 1024);
-            auto issue_s_dp = [&](int u) -> bool {
-                const int s = u % C::ST, w = u % C::NWG;
-                if (!mbar_wait(&kv_full[s], (u / C::ST) & 1, tmo, abort, &g_err_bwd)) return false;
-                tc_fence_after();
-                const uint32_t t_s = tmem + w * C::TM_SDP, t_dp = t_s + C::BN;
-                const uint64_t ks = k_desc + static_cast<uint64_t>((s * C::K_BYTES) >> 4);
-                const uint64_t vsd = v_desc + static_cast<uint64_t>((s * C::V_BYTES) >> 4);
+            int lu_[C::NWG], st_[C::NWG];
+            int remaining = 0;
 #pragma unroll
-                for (int k = 0; k < C::D / 16; ++k) {
-                    const uint32_t a_off = ((k / 4) * (C::BM * 128) + (k % 4) * 32) >> 4;
-                    const uint32_t b_off = ((k / 4) * (C::BN * 128) + (k % 4) * 32) >> 4;
-                    mma_ss(t_s, q_desc + a_off, ks + b_off, IDESC_S, k > 0 ? 1u : 0u);
-                }
-#pragma unroll
-                for (int k = 0; k < C::DV / 16; ++k) {
-                    const uint32_t a_off = ((k / 4) * (C::BM * 128) + (k % 4) * 32) >> 4;
-                    const uint32_t b_off = ((k / 4) * (C::BN * 128) + (k % 4) * 32) >> 4;
-                    mma_ss(t_dp, do_desc + a_off, vsd + b_off, IDESC_DP, k > 0 ? 1u : 0u);
-                }
-                mma_commit(&s_full[w]);
-                return true;
-            };
+            for (int w = 0; w < C::NWG; ++w) {
+                lu_[w] = 0;
+                st_[w] = 0;
+                remaining += n_of(w) > 0;
+            }
+            // S tiles are issued in tile order (K ring phases); the dQ
+            // accumulation too, so its fp32 sums are the same on every run.
+            int next_s = 0, next_q = 0;
             bool ok = mbar_wait(q_full, 0, tmo, abort, &g_err_bwd);
-            for (int u = 0; u < C::NWG && u < n && ok; ++u) ok = issue_s_dp(u);
-            for (int u = 0; u < n && ok; ++u) {
-                const int w = u % C::NWG, lu = u / C::NWG, s = u % C::ST;
-                if (!mbar_wait(&ds_full[w], lu & 1, tmo, abort, &g_err_bwd)) break;
-                tc_fence_after();
-                // dQ += dS K_u: A = dS (K-major over BN keys), B = K_u (MN-major over d).
-                const uint64_t dsw = ds_desc + static_cast<uint64_t>((w * C::DS_BYTES) >> 4);
-                const uint64_t kmn = k_desc_mn + static_cast<uint64_t>((s * C::K_BYTES) >> 4);
+            uint64_t last = globaltimer();
+            while (ok && remaining > 0) {
+                bool prog = false;
 #pragma unroll
-                for (int k = 0; k < C::BN / 16; ++k) {
-                    const uint32_t a_off = ((k / 4) * (C::BM * 128) + (k % 4) * 32) >> 4;
-                    mma_ss(tmem + C::TM_DQ, dsw + a_off, kmn + ((k * 2048) >> 4), IDESC_DQ,
-                           (u > 0 || k > 0) ? 1u : 0u);
+                for (int w = 0; w < C::NWG; ++w) {
+                    const int lu = lu_[w];
+                    if (lu >= n_of(w)) continue;
+                    const int u = lu * C::NWG + w;
+                    const int s = u % C::KS;
+                    const uint32_t t_r = tmem + w * C::BN;
+                    if (st_[w] == 0) {  // S = Q K^T
+                        if (u != next_s || !mbar_test(&k_full[s], (u / C::KS) & 1)) continue;
+                        tc_fence_after();
+                        const uint64_t ks = k_desc + static_cast<uint64_t>((s * C::K_BYTES) >> 4);
+#pragma unroll
+                        for (int k = 0; k < C::D / 16; ++k) {
+                            const uint32_t a_off = ((k / 4) * (C::BM * 128) + (k % 4) * 32) >> 4;
+                            const uint32_t b_off = ((k / 4) * (C::BN * 128) + (k % 4) * 32) >> 4;
+                            mma_ss(t_r, q_desc + a_off, ks + b_off, IDESC_S, k > 0 ? 1u : 0u);
+                        }
+                        mma_commit(&s_full[w]);
+                        st_[w] = 1;
+                        ++next_s;
+                        prog = true;
+                    } else if (st_[w] == 1) {  // dP = dO V^T, once the group has read S
+                        if (!mbar_test(&p_full[w], lu & 1) || !mbar_test(&v_full[w], lu & 1))
+                            continue;
+                        tc_fence_after();
+                        const uint64_t vsd = v_desc + static_cast<uint64_t>((w * C::V_BYTES) >> 4);
+#pragma unroll
+                        for (int k = 0; k < C::DV / 16; ++k) {
+                            const uint32_t a_off = ((k / 4) * (C::BM * 128) + (k % 4) * 32) >> 4;
+                            const uint32_t b_off = ((k / 4) * (C::BN * 128) + (k % 4) * 32) >> 4;
+                            mma_ss(t_r, do_desc + a_off, vsd + b_off, IDESC_DP, k > 0 ? 1u : 0u);
+                        }
+                        mma_commit(&v_empty[w]);
+                        mma_commit(&dp_full[w]);
+                        st_[w] = 2;
+                        prog = true;
+                    } else {  // dQ += dS K (dS from TMEM, K MN-major over d)
+                        if (u != next_q || !mbar_test(&ds_full[w], lu & 1)) continue;
+                        tc_fence_after();
+                        const uint64_t kmn =
+                            k_desc_mn + static_cast<uint64_t>((s * C::K_BYTES) >> 4);
+#pragma unroll
+                        for (int k = 0; k < C::BN / 16; ++k)
+                            mma_ts(tmem + C::TM_DQ, t_r + k * 8, kmn + ((k * 2048) >> 4), IDESC_DQ,
+                                   (u > 0 || k > 0) ? 1u : 0u);
+                        ++next_q;
+                        mma_commit(&k_empty[s]);
+                        st_[w] = 0;
+                        lu_[w] = lu + 1;
+                        if (lu + 1 >= n_of(w)) --remaining;
+                        prog = true;
+                    }
                 }
-                mma_commit(&kv_empty[s]);
-                if (u + C::NWG < n) ok = issue_s_dp(u + C::NWG);
+                if (prog) {
+                    last = globaltimer();
+                } else if (*abort) {
+                    ok = false;
+                } else if (globaltimer() - last > tmo) {
+                    *abort = 1;
+                    atomicExch(&g_err_bwd, ERR_TIMEOUT);
+                    ok = false;
+                }
             }
             mma_commit(dq_done);
         }
@@ -327,65 +367,86 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         const int row = quad * 32 + lane;
         const int grow = qt * TILE + row;
         const uint32_t lane_base = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+        const uint32_t t_r = lane_base + wg * C::BN;
         const size_t bh = static_cast<size_t>(b) * p.H + h;
         const float lse2 = p.lse2[bh * p.Npad + grow];
         const float Drow = p.delta[bh * p.Npad + grow];
         const float sl2 = p.sl2;
-        const int n_my = n > wg ? (n - wg + C::NWG - 1) / C::NWG : 0;
-        // dS row of the K-major swizzled tile: 16-byte chunk c of 64-column box
-        // kb lives at kb*BM*128 + r*128 + ((c ^ (r & 7)) * 16).
-        uint8_t *ds_row = sDS + wg * C::DS_BYTES + row * 128;
+        const int n_my = n_of(wg);
+        const int4 *vec = p.vec + static_cast<size_t>(bm) * p.Npad;
+        // The next tile's list entry and mask boundaries are read one tile ahead.
+        int4 cv_next[C::BN / 64][2];
+        auto load_bounds = [&](int u, int entry) {
+            if (!(entry & 1)) return;
+            const int key0 = (entry >> 1) * TILE + (u % C::SUB) * C::BN;
+#pragma unroll
+            for (int c = 0; c < C::BN / 64; ++c) {
+                cv_next[c][0] = __ldg(vec + key0 + c * 64 + lane);
+                cv_next[c][1] = __ldg(vec + key0 + c * 64 + 32 + lane);
+            }
+        };
         int entry_next = n_my > 0 ? entries[wg / C::SUB] : 0;
+        if (n_my > 0) load_bounds(wg, entry_next);
         for (int lu = 0; lu < n_my; ++lu) {
             const int u = lu * C::NWG + wg;
             const int entry = entry_next;
-            if (u + C::NWG < n) entry_next = entries[(u + C::NWG) / C::SUB];
             const bool masked_tile = entry & 1;
             const int key0 = (entry >> 1) * TILE + (u % C::SUB) * C::BN;
-            const int es = u % C::ES;
-            if (!warp_wait(&s_full[wg], lu & 1, tmo, abort)) break;
-            if (!warp_wait(&e_full[es], (u / C::ES) & 1, tmo, abort)) break;
-            tc_fence_after();
-            const uint32_t t_s = lane_base + wg * C::TM_SDP, t_dp = t_s + C::BN;
-            const int4 *cv = reinterpret_cast<const int4 *>(sE + es * C::E_BYTES);
+            int4 cv[C::BN / 64][2];
 #pragma unroll
             for (int c = 0; c < C::BN / 64; ++c) {
-                float pr[64], dp[64];
-                tmem_ld64f_x2(t_s + c * 64, pr, t_dp + c * 64, dp);
+                cv[c][0] = cv_next[c][0];
+                cv[c][1] = cv_next[c][1];
+            }
+            if (u + C::NWG < n) entry_next = entries[(u + C::NWG) / C::SUB];
+            if (!warp_wait(&s_full[wg], lu & 1, tmo, abort)) break;
+            tc_fence_after();
+            // phase 1: P = exp2(S * scale * log2e - LSE2), masked, kept as fp16 pairs
+            uint32_t pk[C::BN / 2];
 #pragma unroll
-                for (int jj = 0; jj < 64; ++jj) pr[jj] = ex2(fmaf(pr[jj], sl2, -lse2));
+            for (int c = 0; c < C::BN / 64; ++c) {
+                float x[64];
+                tmem_ld64f(t_r + c * 64, x);
+#pragma unroll
+                for (int jj = 0; jj < 64; ++jj) x[jj] = ex2(fmaf(x[jj], sl2, -lse2));
                 if (masked_tile) {
                     // Row bits of key columns lane, lane + 32 over the warp's rows,
                     // transposed so each lane holds its row's column bits.
                     const int R = grow - lane;
                     const int ja = key0 + c * 64 + lane;
-                    const uint32_t wa = warp_transpose32(
-                        column_row_bits(R, ja, cv[c * 64 + lane], p.causal), lane);
-                    const uint32_t wb = warp_transpose32(
-                        column_row_bits(R, ja + 32, cv[c * 64 + 32 + lane], p.causal), lane);
+                    const uint32_t wa =
+                        warp_transpose32(column_row_bits(R, ja, cv[c][0], p.causal), lane);
+                    const uint32_t wb =
+                        warp_transpose32(column_row_bits(R, ja + 32, cv[c][1], p.causal), lane);
 #pragma unroll
                     for (int jj = 0; jj < 32; ++jj) {
-                        if ((wa >> jj) & 1u) pr[jj] = 0.f;
-                        if ((wb >> jj) & 1u) pr[32 + jj] = 0.f;
+                        if ((wa >> jj) & 1u) x[jj] = 0.f;
+                        if ((wb >> jj) & 1u) x[32 + jj] = 0.f;
                     }
                 }
-                uint8_t *box = ds_row + c * C::BM * 128;
 #pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    uint4 w4;
-                    w4.x = pack_bf16(pr[q * 8 + 0] * (dp[q * 8 + 0] - Drow),
-                                     pr[q * 8 + 1] * (dp[q * 8 + 1] - Drow));
-                    w4.y = pack_bf16(pr[q * 8 + 2] * (dp[q * 8 + 2] - Drow),
-                                     pr[q * 8 + 3] * (dp[q * 8 + 3] - Drow));
-                    w4.z = pack_bf16(pr[q * 8 + 4] * (dp[q * 8 + 4] - Drow),
-                                     pr[q * 8 + 5] * (dp[q * 8 + 5] - Drow));
-                    w4.w = pack_bf16(pr[q * 8 + 6] * (dp[q * 8 + 6] - Drow),
-                                     pr[q * 8 + 7] * (dp[q * 8 + 7] - Drow));
-                    *reinterpret_cast<uint4 *>(box + ((q ^ (row & 7)) * 16)) = w4;
-                }
+                for (int i = 0; i < 32; ++i) pk[c * 32 + i] = pack_fp16(x[2 * i], x[2 * i + 1]);
             }
-            mbar_arrive(&e_empty[es]);
-            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(&p_full[wg]);  // S read: the region may take dP
+            if (u + C::NWG < n) load_bounds(u + C::NWG, entry_next);
+            // phase 2: dS = P * (dP - D) -> the region, bf16
+            if (!warp_wait(&dp_full[wg], lu & 1, tmo, abort)) break;
+            tc_fence_after();
+#pragma unroll
+            for (int c = 0; c < C::BN / 64; ++c) {
+                float dp[64];
+                tmem_ld64f(t_r + c * 64, dp);
+                uint32_t r[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    __half2 h2 = *reinterpret_cast<__half2 *>(&pk[c * 32 + i]);
+                    const float2 pf = __half22float2(h2);
+                    r[i] = pack_bf16(pf.x * (dp[2 * i] - Drow), pf.y * (dp[2 * i + 1] - Drow));
+                }
+                tmem_st32(t_r + c * 32, r);  // columns already read
+            }
+            tmem_st_wait();
             tc_fence_before();
             mbar_arrive(&ds_full[wg]);
         }
@@ -415,12 +476,17 @@ __global__ void __launch_bounds__(C::THREADS, 1)
 }
 
 // ---------------------------------------------------------------- dkdv kernel
-// One CTA per 128-key tile.  NWG compute warpgroups take alternate query
-// sub-tiles of BM rows; each has its own S^T/dP^T region in TMEM, and all of
-// them feed the one dK and the one dV accumulator.
-template <int D_, int DV_, int BM_, int ST_, bool DK_, bool DV_ON_, int NWG_>
+// One CTA per 128-key tile; NWG compute warpgroups take alternate query
+// sub-tiles of BM rows.  Each group owns one BM-column TMEM region that holds,
+// in turn, S^T (fp32) then P^T (fp16, packed), then dP^T (fp32) then dS^T
+// (bf16, packed); all groups feed the one dK and the one dV accumulator.
+// Rings: Q in QS stages shared in tile order (S^T and dK read it); dO with
+// the tile's LSE2 and D in one stage per group (dV, dP^T and the compute read
+// them).  The MMA thread serves whichever group is ready; the dV and dK
+// accumulations keep tile order (bit-reproducible sums).
+template <int D_, int DV_, int BM_, int QS_, bool DK_, bool DV_ON_, int NWG_>
 struct DkdvCfg {
-    static constexpr int D = D_, DV = DV_, BM = BM_, ST = ST_, NWG = NWG_;
+    static constexpr int D = D_, DV = DV_, BM = BM_, QS = QS_, NWG = NWG_;
     static constexpr bool DO_DK = DK_, DO_DV = DV_ON_;
     static constexpr int BN = 128;            // keys per CTA (TMEM lanes)
     static constexpr int SUB = TILE / BM;     // query sub-tiles per list entry
@@ -429,29 +495,28 @@ struct DkdvCfg {
     static constexpr int V_BYTES = NEED_V ? BN * DV * 2 : 0;
     static constexpr int Q_BYTES = BM * D * 2;
     static constexpr int DO_BYTES = BM * DV * 2;
-    static constexpr int STAGE_BYTES = Q_BYTES + DO_BYTES + 2 * BM * 4;
+    static constexpr int LD_BYTES = 2 * BM * 4;  // LSE2 then D of the sub-tile's rows
     static constexpr int OFF_K = 0;
     static constexpr int OFF_V = OFF_K + K_BYTES;
-    static constexpr int OFF_ST = OFF_V + V_BYTES;
-    static constexpr int ST_Q = 0, ST_DO = Q_BYTES, ST_LSE = Q_BYTES + DO_BYTES,
-                         ST_D = ST_LSE + BM * 4;
-    static constexpr int STAGE_STRIDE = (STAGE_BYTES + 1023) / 1024 * 1024;
-    static constexpr int OFF_BAR = OFF_ST + ST * STAGE_STRIDE;
-    // kv_full, q_full[ST], q_empty[ST], s_full[NWG], p_full[NWG], ds_full[NWG], done
-    static constexpr int NBAR = 1 + 2 * ST + 3 * NWG + 1;
+    static constexpr int OFF_Q = OFF_V + V_BYTES;
+    static constexpr int OFF_DO = OFF_Q + QS * Q_BYTES;
+    static constexpr int OFF_LD = OFF_DO + NWG * DO_BYTES;
+    static constexpr int OFF_BAR = OFF_LD + NWG * LD_BYTES;
+    // kv_full, q_full[QS], q_empty[QS], o_full[NWG], o_empty[NWG],
+    // s_full[NWG], p_full[NWG], dp_full[NWG], ds_full[NWG], done
+    static constexpr int NBAR = 1 + 2 * QS + 6 * NWG + 1;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
-    static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
+    static constexpr int SMEM_BYTES = OFF_MISC + 16;
     static constexpr int TM_DK = 0;
     static constexpr int TM_DV = DO_DK ? D : 0;
-    static constexpr int TM_W0 = TM_DV + (DO_DV ? DV : 0);
-    static constexpr int TM_SDP = BM + (DO_DK ? BM : 0);  // per group: S^T then dP^T
-    static constexpr int TM_END = TM_W0 + NWG * TM_SDP;
+    static constexpr int TM_W0 = TM_DV + (DO_DV ? DV : 0);  // group w: [TM_W0 + w*BM, +BM)
+    static constexpr int TM_END = TM_W0 + NWG * BM;
     static constexpr int TM_COLS = 512;
     static constexpr int THREADS = 64 + NWG * 128;
     static_assert(TM_END <= TM_COLS, "TMEM budget");
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
-    static_assert(D <= 256 && DV <= 256 && BM % 64 == 0, "MMA shape");
-    static_assert(ST >= NWG, "ring depth");
+    static_assert(D <= 256 && DV <= 256 && (BM == 64 || BM == 128), "MMA shape");
+    static_assert(QS >= NWG, "ring depth");
     static_assert((D / 32) % NWG == 0 && (DV / 32) % NWG == 0, "epilogue column split");
 };
 
@@ -460,14 +525,18 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v,
                 const __grid_constant__ CUtensorMap tm_do, const BwdParams p) {
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    uint8_t *sK = smem + C::OFF_K, *sV = smem + C::OFF_V, *sST = smem + C::OFF_ST;
+    extern __shared__ __align__(1024) uint8_t smem[];
+    if (smem_u32(smem) & 1023u) {  // swizzled tiles need 1024-byte alignment
+        if (threadIdx.x == 0) atomicExch(&g_err_bwd, ERR_SMEM_ALIGN);
+        return;
+    }
+    uint8_t *sK = smem + C::OFF_K, *sV = smem + C::OFF_V, *sQ = smem + C::OFF_Q;
+    uint8_t *sDO = smem + C::OFF_DO, *sLD = smem + C::OFF_LD;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
-    uint64_t *kv_full = bars, *q_full = bars + 1, *q_empty = q_full + C::ST;
-    uint64_t *s_full = q_empty + C::ST, *p_full = s_full + C::NWG, *ds_full = p_full + C::NWG,
-             *done = ds_full + C::NWG;
+    uint64_t *kv_full = bars, *q_full = bars + 1, *q_empty = q_full + C::QS;
+    uint64_t *o_full = q_empty + C::QS, *o_empty = o_full + C::NWG;
+    uint64_t *s_full = o_empty + C::NWG, *p_full = s_full + C::NWG, *dp_full = p_full + C::NWG,
+             *ds_full = dp_full + C::NWG, *done = ds_full + C::NWG;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
     volatile int *abort = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
 
@@ -482,16 +551,20 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                                                                             : n_entries * C::SUB;
     const uint64_t tmo = p.timeout_ns;
     const size_t bh = static_cast<size_t>(b) * p.H + h;
+    auto n_of = [&](int w) { return n > w ? (n - w + C::NWG - 1) / C::NWG : 0; };
 
     if (threadIdx.x == 0) {
         mbar_init(kv_full, 1);
-        for (int i = 0; i < C::ST; ++i) {
+        for (int i = 0; i < C::QS; ++i) {
             mbar_init(&q_full[i], 1);
             mbar_init(&q_empty[i], 1);
         }
         for (int i = 0; i < C::NWG; ++i) {
+            mbar_init(&o_full[i], 1);
+            mbar_init(&o_empty[i], 1);
             mbar_init(&s_full[i], 1);
             mbar_init(&p_full[i], 128);
+            mbar_init(&dp_full[i], 1);
             mbar_init(&ds_full[i], 128);
         }
         mbar_init(done, 1);
@@ -512,7 +585,6 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         if (lane == 0 && n > 0) {
             prefetch_tmap(&tm_q);
             prefetch_tmap(&tm_k);
-            prefetch_tmap(&tm_do);
             mbar_arrive_expect_tx(kv_full, C::K_BYTES + C::V_BYTES);
 #pragma unroll
             for (int c = 0; c < C::D / 64; ++c)
@@ -524,23 +596,32 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     tma_load_4d(sV + c * C::BN * 128, &tm_v, kv_full, c * 64, h, kt * TILE, b);
             }
             for (int u = 0; u < n; ++u) {
-                const int s = u % C::ST;
-                if (u >= C::ST &&
-                    !mbar_wait(&q_empty[s], ((u / C::ST) - 1) & 1, tmo, abort, &g_err_bwd))
+                const int s = u % C::QS;
+                if (u >= C::QS &&
+                    !mbar_wait(&q_empty[s], ((u / C::QS) - 1) & 1, tmo, abort, &g_err_bwd))
                     break;
-                uint8_t *stg = sST + s * C::STAGE_STRIDE;
-                mbar_arrive_expect_tx(&q_full[s], C::STAGE_BYTES);
+                mbar_arrive_expect_tx(&q_full[s], C::Q_BYTES);
                 const int q0 = q0_of(u);
 #pragma unroll
                 for (int c = 0; c < C::D / 64; ++c)
-                    tma_load_4d(stg + C::ST_Q + c * C::BM * 128, &tm_q, &q_full[s], c * 64, h, q0,
-                                b);
+                    tma_load_4d(sQ + s * C::Q_BYTES + c * C::BM * 128, &tm_q, &q_full[s], c * 64,
+                                h, q0, b);
+            }
+        } else if (lane == 1 && n > 0) {
+            prefetch_tmap(&tm_do);
+            for (int u = 0; u < n; ++u) {
+                const int w = u % C::NWG, lw = u / C::NWG;
+                if (lw >= 1 && !mbar_wait(&o_empty[w], (lw - 1) & 1, tmo, abort, &g_err_bwd))
+                    break;
+                mbar_arrive_expect_tx(&o_full[w], C::DO_BYTES + C::LD_BYTES);
+                const int q0 = q0_of(u);
 #pragma unroll
                 for (int c = 0; c < C::DV / 64; ++c)
-                    tma_load_4d(stg + C::ST_DO + c * C::BM * 128, &tm_do, &q_full[s], c * 64, h,
-                                q0, b);
-                bulk_load(stg + C::ST_LSE, p.lse2 + bh * p.Npad + q0, C::BM * 4, &q_full[s]);
-                bulk_load(stg + C::ST_D, p.delta + bh * p.Npad + q0, C::BM * 4, &q_full[s]);
+                    tma_load_4d(sDO + w * C::DO_BYTES + c * C::BM * 128, &tm_do, &o_full[w],
+                                c * 64, h, q0, b);
+                uint8_t *ld = sLD + w * C::LD_BYTES;
+                bulk_load(ld, p.lse2 + bh * p.Npad + q0, C::BM * 4, &o_full[w]);
+                bulk_load(ld + C::BM * 4, p.delta + bh * p.Npad + q0, C::BM * 4, &o_full[w]);
             }
         }
     } else if (warp == 1) {
@@ -553,62 +634,108 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             // (in 16-byte units) to the start-address field.
             const uint64_t k_desc = sdesc_sw128(smem_u32(sK), 16, 1024);
             const uint64_t v_desc = sdesc_sw128(smem_u32(sV), 16, 1024);
-            const uint64_t st_desc = sdesc_sw128(smem_u32(sST), 16, 1024);
-            const uint64_t st_desc_mn = sdesc_sw128(smem_u32(sST), C::BM * 128, 1024);
-            auto issue_s = [&](int u) -> bool {
-                const int s = u % C::ST, w = u % C::NWG;
-                const uint64_t stg = st_desc + static_cast<uint64_t>((s * C::STAGE_STRIDE) >> 4);
-                if (!mbar_wait(&q_full[s], (u / C::ST) & 1, tmo, abort, &g_err_bwd)) return false;
-                tc_fence_after();
-                const uint32_t t_s = tmem + C::TM_W0 + w * C::TM_SDP, t_dp = t_s + C::BM;
-                // S^T = K Q^T
+            const uint64_t q_desc = sdesc_sw128(smem_u32(sQ), 16, 1024);
+            const uint64_t q_desc_mn = sdesc_sw128(smem_u32(sQ), C::BM * 128, 1024);
+            const uint64_t do_desc = sdesc_sw128(smem_u32(sDO), 16, 1024);
+            const uint64_t do_desc_mn = sdesc_sw128(smem_u32(sDO), C::BM * 128, 1024);
+            int lu_[C::NWG], st_[C::NWG];
+            int remaining = 0;
 #pragma unroll
-                for (int k = 0; k < C::D / 16; ++k) {
-                    const uint32_t a_off = ((k / 4) * (C::BN * 128) + (k % 4) * 32) >> 4;
-                    const uint32_t b_off = (C::ST_Q + (k / 4) * (C::BM * 128) + (k % 4) * 32) >> 4;
-                    mma_ss(t_s, k_desc + a_off, stg + b_off, IDESC_S, k > 0 ? 1u : 0u);
-                }
-                if constexpr (C::DO_DK) {
-                    // dP^T = V dO^T
+            for (int w = 0; w < C::NWG; ++w) {
+                lu_[w] = 0;
+                st_[w] = 0;
+                remaining += n_of(w) > 0;
+            }
+            // S^T tiles are issued in tile order (Q ring phases); the dV and dK
+            // accumulations too, so their fp32 sums are the same on every run.
+            int next_s = 0, next_v = 0, next_k = 0;
+            bool ok = mbar_wait(kv_full, 0, tmo, abort, &g_err_bwd);
+            uint64_t last = globaltimer();
+            while (ok && remaining > 0) {
+                bool prog = false;
 #pragma unroll
-                    for (int k = 0; k < C::DV / 16; ++k) {
-                        const uint32_t a_off = ((k / 4) * (C::BN * 128) + (k % 4) * 32) >> 4;
-                        const uint32_t b_off =
-                            (C::ST_DO + (k / 4) * (C::BM * 128) + (k % 4) * 32) >> 4;
-                        mma_ss(t_dp, v_desc + a_off, stg + b_off, IDESC_DP, k > 0 ? 1u : 0u);
+                for (int w = 0; w < C::NWG; ++w) {
+                    const int lu = lu_[w];
+                    if (lu >= n_of(w)) continue;
+                    const int u = lu * C::NWG + w;
+                    const int s = u % C::QS;
+                    const uint32_t t_r = tmem + C::TM_W0 + w * C::BM;
+                    if (st_[w] == 0) {  // S^T = K Q^T
+                        if (u != next_s || !mbar_test(&q_full[s], (u / C::QS) & 1)) continue;
+                        tc_fence_after();
+                        const uint64_t qs = q_desc + static_cast<uint64_t>((s * C::Q_BYTES) >> 4);
+#pragma unroll
+                        for (int k = 0; k < C::D / 16; ++k) {
+                            const uint32_t a_off = ((k / 4) * (C::BN * 128) + (k % 4) * 32) >> 4;
+                            const uint32_t b_off = ((k / 4) * (C::BM * 128) + (k % 4) * 32) >> 4;
+                            mma_ss(t_r, k_desc + a_off, qs + b_off, IDESC_S, k > 0 ? 1u : 0u);
+                        }
+                        mma_commit(&s_full[w]);
+                        st_[w] = 1;
+                        ++next_s;
+                        prog = true;
+                    } else if (st_[w] == 1) {
+                        // The group has read S^T (and written P^T): dV += P^T dO,
+                        // then dP^T = V dO^T into the same region.
+                        if (u != next_v || !mbar_test(&p_full[w], lu & 1) ||
+                            !mbar_test(&o_full[w], lu & 1))
+                            continue;
+                        tc_fence_after();
+                        ++next_v;
+                        if constexpr (C::DO_DV) {
+                            const uint64_t dmn =
+                                do_desc_mn + static_cast<uint64_t>((w * C::DO_BYTES) >> 4);
+#pragma unroll
+                            for (int k = 0; k < C::BM / 16; ++k)
+                                mma_ts(tmem + C::TM_DV, t_r + k * 8, dmn + ((k * 2048) >> 4),
+                                       IDESC_DV, (u > 0 || k > 0) ? 1u : 0u);
+                        }
+                        if constexpr (C::DO_DK) {
+                            const uint64_t dd =
+                                do_desc + static_cast<uint64_t>((w * C::DO_BYTES) >> 4);
+#pragma unroll
+                            for (int k = 0; k < C::DV / 16; ++k) {
+                                const uint32_t a_off =
+                                    ((k / 4) * (C::BN * 128) + (k % 4) * 32) >> 4;
+                                const uint32_t b_off =
+                                    ((k / 4) * (C::BM * 128) + (k % 4) * 32) >> 4;
+                                mma_ss(t_r, v_desc + a_off, dd + b_off, IDESC_DP, k > 0 ? 1u : 0u);
+                            }
+                            mma_commit(&dp_full[w]);
+                        }
+                        st_[w] = 2;
+                        prog = true;
+                    } else {
+                        // The group has written dS^T: dK += dS^T Q; then the
+                        // tile's Q, dO, LSE2 and D stages are free.
+                        if (u != next_k || !mbar_test(&ds_full[w], lu & 1)) continue;
+                        tc_fence_after();
+                        ++next_k;
+                        if constexpr (C::DO_DK) {
+                            const uint64_t qmn =
+                                q_desc_mn + static_cast<uint64_t>((s * C::Q_BYTES) >> 4);
+#pragma unroll
+                            for (int k = 0; k < C::BM / 16; ++k)
+                                mma_ts(tmem + C::TM_DK, t_r + k * 8, qmn + ((k * 2048) >> 4),
+                                       IDESC_DK, (u > 0 || k > 0) ? 1u : 0u);
+                        }
+                        mma_commit(&q_empty[s]);
+                        mma_commit(&o_empty[w]);
+                        st_[w] = 0;
+                        lu_[w] = lu + 1;
+                        if (lu + 1 >= n_of(w)) --remaining;
+                        prog = true;
                     }
                 }
-                mma_commit(&s_full[w]);
-                return true;
-            };
-            bool ok = mbar_wait(kv_full, 0, tmo, abort, &g_err_bwd);
-            for (int u = 0; u < C::NWG && u < n && ok; ++u) ok = issue_s(u);
-            for (int u = 0; u < n && ok; ++u) {
-                const int s = u % C::ST, w = u % C::NWG, lu = u / C::NWG;
-                const uint64_t stg_mn =
-                    st_desc_mn + static_cast<uint64_t>((s * C::STAGE_STRIDE) >> 4);
-                const uint32_t t_s = tmem + C::TM_W0 + w * C::TM_SDP, t_dp = t_s + C::BM;
-                if constexpr (C::DO_DV) {
-                    if (!mbar_wait(&p_full[w], lu & 1, tmo, abort, &g_err_bwd)) break;
-                    tc_fence_after();
-                    // dV += P^T dO: A = P^T (TMEM, fp16), B = dO (MN-major over dv)
-#pragma unroll
-                    for (int k = 0; k < C::BM / 16; ++k)
-                        mma_ts(tmem + C::TM_DV, t_s + k * 8, stg_mn + ((C::ST_DO + k * 2048) >> 4),
-                               IDESC_DV, (u > 0 || k > 0) ? 1u : 0u);
+                if (prog) {
+                    last = globaltimer();
+                } else if (*abort) {
+                    ok = false;
+                } else if (globaltimer() - last > tmo) {
+                    *abort = 1;
+                    atomicExch(&g_err_bwd, ERR_TIMEOUT);
+                    ok = false;
                 }
-                // The group is done with this sub-tile's S^T / dP^T reads.
-                if (!mbar_wait(&ds_full[w], lu & 1, tmo, abort, &g_err_bwd)) break;
-                tc_fence_after();
-                if constexpr (C::DO_DK) {
-                    // dK += dS^T Q: A = dS^T (TMEM, bf16), B = Q (MN-major over d)
-#pragma unroll
-                    for (int k = 0; k < C::BM / 16; ++k)
-                        mma_ts(tmem + C::TM_DK, t_dp + k * 8, stg_mn + ((C::ST_Q + k * 2048) >> 4),
-                               IDESC_DK, (u > 0 || k > 0) ? 1u : 0u);
-                }
-                mma_commit(&q_empty[s]);
-                if (u + C::NWG < n) ok = issue_s(u + C::NWG);
             }
             mma_commit(done);
         }
@@ -619,60 +746,75 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         const int row = quad * 32 + lane;
         const int gkey = kt * TILE + row;
         const uint32_t lane_base = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+        const uint32_t t_r = lane_base + C::TM_W0 + wg * C::BM;
         const int4 cv = p.vec[static_cast<size_t>(bm) * p.Npad + gkey];
         const float sl2 = p.sl2;
-        const int n_my = n > wg ? (n - wg + C::NWG - 1) / C::NWG : 0;
+        const int n_my = n_of(wg);
+        const float *slse = reinterpret_cast<const float *>(sLD + wg * C::LD_BYTES);
+        const float *sd = slse + C::BM;
         int entry_next = n_my > 0 ? entries[wg / C::SUB] : 0;
         for (int lu = 0; lu < n_my; ++lu) {
             const int u = lu * C::NWG + wg;
-            const int s = u % C::ST;
             const int entry = entry_next;
             if (u + C::NWG < n) entry_next = entries[(u + C::NWG) / C::SUB];
             const bool need_mask = entry & 1;
             const int q0 = (entry >> 1) * TILE + (u % C::SUB) * C::BM;
-            const uint8_t *stg = sST + s * C::STAGE_STRIDE;
-            const float *slse = reinterpret_cast<const float *>(stg + C::ST_LSE);
-            const float *sd = reinterpret_cast<const float *>(stg + C::ST_D);
             if (!warp_wait(&s_full[wg], lu & 1, tmo, abort)) break;
+            if (!warp_wait(&o_full[wg], lu & 1, tmo, abort)) break;
             tc_fence_after();
-            const uint32_t t_s = lane_base + C::TM_W0 + wg * C::TM_SDP, t_dp = t_s + C::BM;
+            // phase 1: P^T = exp2(S^T * scale * log2e - LSE2), masked; fp16 pairs
+            uint32_t pk[C::BM / 2];
 #pragma unroll
             for (int c = 0; c < C::BM / 64; ++c) {
-                float pr[64];
-                tmem_ld64f(t_s + c * 64, pr);
-                // This thread's key column: masked query rows of the sub-tile as bits.
-                const uint32_t mw0 = need_mask ? column_row_bits(q0 + c * 64, gkey, cv, p.causal) : 0u;
+                float x[64];
+                tmem_ld64f(t_r + c * 64, x);
+                // This thread's key column: masked query rows of the chunk as bits.
+                const uint32_t mw0 =
+                    need_mask ? column_row_bits(q0 + c * 64, gkey, cv, p.causal) : 0u;
                 const uint32_t mw1 =
                     need_mask ? column_row_bits(q0 + c * 64 + 32, gkey, cv, p.causal) : 0u;
 #pragma unroll
-                for (int i = 0; i < 64; ++i) {
-                    const int qi = c * 64 + i;
-                    float v = ex2(fmaf(pr[i], sl2, -slse[qi]));
-                    if ((((i < 32) ? mw0 : mw1) >> (i & 31)) & 1u) v = 0.f;
-                    pr[i] = v;
+                for (int i = 0; i < 32; ++i) {
+                    const int q = c * 64 + 2 * i;
+                    float p0 = ex2(fmaf(x[2 * i], sl2, -slse[q]));
+                    float p1 = ex2(fmaf(x[2 * i + 1], sl2, -slse[q + 1]));
+                    const uint32_t w = (2 * i < 32) ? mw0 : mw1;
+                    if ((w >> ((2 * i) & 31)) & 1u) p0 = 0.f;
+                    if ((w >> ((2 * i + 1) & 31)) & 1u) p1 = 0.f;
+                    pk[c * 32 + i] = pack_fp16(p0, p1);
                 }
                 if constexpr (C::DO_DV) {
                     uint32_t r[32];
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) r[i] = pack_fp16(pr[2 * i], pr[2 * i + 1]);
-                    tmem_st32(t_s + c * 32, r);
+                    for (int i = 0; i < 32; ++i) r[i] = pk[c * 32 + i];
+                    tmem_st32(t_r + c * 32, r);  // columns already read
                 }
-                if constexpr (C::DO_DK) {
+            }
+            if constexpr (C::DO_DV) tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(&p_full[wg]);  // S^T read (and P^T written)
+            if constexpr (C::DO_DK) {
+                // phase 2: dS^T = P^T * (dP^T - D) -> the region, bf16
+                if (!warp_wait(&dp_full[wg], lu & 1, tmo, abort)) break;
+                tc_fence_after();
+#pragma unroll
+                for (int c = 0; c < C::BM / 64; ++c) {
                     float dp[64];
-                    tmem_ld64f(t_dp + c * 64, dp);
+                    tmem_ld64f(t_r + c * 64, dp);
                     uint32_t r[32];
 #pragma unroll
                     for (int i = 0; i < 32; ++i) {
-                        const int qi = c * 64 + 2 * i;
-                        r[i] = pack_bf16(pr[2 * i] * (dp[2 * i] - sd[qi]),
-                                         pr[2 * i + 1] * (dp[2 * i + 1] - sd[qi + 1]));
+                        const int q = c * 64 + 2 * i;
+                        __half2 h2 = *reinterpret_cast<__half2 *>(&pk[c * 32 + i]);
+                        const float2 pf = __half22float2(h2);
+                        r[i] = pack_bf16(pf.x * (dp[2 * i] - sd[q]),
+                                         pf.y * (dp[2 * i + 1] - sd[q + 1]));
                     }
-                    tmem_st32(t_dp + c * 32, r);
+                    tmem_st32(t_r + c * 32, r);  // columns already read
                 }
+                tmem_st_wait();
+                tc_fence_before();
             }
-            tmem_st_wait();
-            tc_fence_before();
-            if constexpr (C::DO_DV) mbar_arrive(&p_full[wg]);
             mbar_arrive(&ds_full[wg]);
         }
         if (n > 0) warp_wait(done, 0, tmo, abort);
@@ -778,9 +920,10 @@ cudaError_t launch_pair(const Geometry &g, const Workspace &ws, const BwdArgs &a
 
 }  // namespace
 
-// Every DqCfg below uses 64-key sub-tiles and every DkdvCfg 64-query sub-tiles.
-int dq_key_rows(int, int) { return 64; }
-int dkdv_query_rows(int, int) { return 64; }
+// Key sub-tile of the query-side kernel and query sub-tile of the key-side
+// kernel: 128 (full-rate N = 128 MMAs) up to d = 128, 64 above (shared memory).
+int dq_key_rows(int d, int) { return d <= 128 ? 128 : 64; }
+int dkdv_query_rows(int d, int) { return d <= 128 ? 128 : 64; }
 
 cudaError_t launch_bwd(const Geometry &g, const Workspace &ws, const BwdArgs &a,
                        cudaStream_t st, Recorder &rec) {
@@ -793,23 +936,23 @@ cudaError_t launch_bwd(const Geometry &g, const Workspace &ws, const BwdArgs &a,
     rec.after(st);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    // DkdvCfg<d, dv, query sub-tile, stages, dK, dV, groups>;
-    // DqCfg<d, dv, key sub-tile, stages, groups, boundary stages>
+    // DkdvCfg<d, dv, query sub-tile, Q stages, dK, dV, groups>;
+    // DqCfg<d, dv, key sub-tile, K stages, groups>
     if (g.d == 64 && g.dv == 64)
-        return launch_pair<DkdvCfg<64, 64, 64, 4, true, true, 2>, DqCfg<64, 64, 64, 4, 2, 4>>(
+        return launch_pair<DkdvCfg<64, 64, 128, 3, true, true, 2>, DqCfg<64, 64, 128, 3, 2>>(
             g, ws, a, st, rec);
     if (g.d == 128 && g.dv == 128)
-        return launch_pair<DkdvCfg<128, 128, 64, 4, true, true, 2>, DqCfg<128, 128, 64, 3, 2, 4>>(
+        return launch_pair<DkdvCfg<128, 128, 128, 3, true, true, 2>, DqCfg<128, 128, 128, 3, 2>>(
             g, ws, a, st, rec);
     if (g.d == 192 && g.dv == 128)
-        return launch_pair<DkdvCfg<192, 128, 64, 2, true, true, 1>, DqCfg<192, 128, 64, 2, 2, 4>>(
+        return launch_pair<DkdvCfg<192, 128, 64, 3, true, true, 2>, DqCfg<192, 128, 64, 3, 2>>(
             g, ws, a, st, rec);
     if (g.d == 256 && g.dv == 256) {
         rec.before(st);
-        e = launch_dkdv<DkdvCfg<256, 256, 64, 2, false, true, 2>>(g, ws, a, st);
+        e = launch_dkdv<DkdvCfg<256, 256, 64, 3, false, true, 2>>(g, ws, a, st);
         rec.after(st);
         if (e != cudaSuccess) return e;
-        return launch_pair<DkdvCfg<256, 256, 64, 1, true, false, 1>, DqCfg<256, 256, 64, 1, 1, 2>>(
+        return launch_pair<DkdvCfg<256, 256, 64, 1, true, false, 1>, DqCfg<256, 256, 64, 2, 1>>(
             g, ws, a, st, rec);
     }
     return cudaErrorInvalidValue;

@@ -79,8 +79,21 @@ __device__ __forceinline__ uint32_t mbar_try_wait(uint64_t *bar, uint32_t parity
     return ok;
 }
 
+// Non-blocking probe: has the phase of `bar` with this parity completed?
+__device__ __forceinline__ uint32_t mbar_test(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok;
+}
+
 // Error codes a kernel may leave in its device error word.
-enum : unsigned { ERR_NONE = 0, ERR_TIMEOUT = 1 };
+enum : unsigned { ERR_NONE = 0, ERR_TIMEOUT = 1, ERR_SMEM_ALIGN = 2 };
 
 // Bounded wait for the phase of `bar` with the given parity to complete.
 // Returns false when `timeout_ns` elapsed or another role of the CTA already
