@@ -356,6 +356,10 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     *abort = 1;
                     atomicExch(&g_err_bwd, ERR_TIMEOUT);
                     ok = false;
+                } else {
+                    // Nothing ready: yield the issue slots to the compute warps
+                    // that share this warp's sub-partition.
+                    __nanosleep(40);
                 }
             }
             mma_commit(dq_done);
@@ -735,6 +739,10 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     *abort = 1;
                     atomicExch(&g_err_bwd, ERR_TIMEOUT);
                     ok = false;
+                } else {
+                    // Nothing ready: yield the issue slots to the compute warps
+                    // that share this warp's sub-partition.
+                    __nanosleep(40);
                 }
             }
             mma_commit(done);

@@ -5,8 +5,7 @@
 // One CTA owns one 128-row query tile of one (batch, head).  It walks only
 // the key tiles the tile map kept for that query tile ("skip unnecessary
 // computation", FlashMask abstract).  Roles, by warp:
-//   warp 0      TMA producers: lane 0 Q and the K ring, lane 1 the V ring,
-//               lane 2 the ring of each key tile's mask boundaries
+//   warp 0      TMA producers: lane 0 Q and the K ring, lane 1 the V ring
 //   warp 1      allocates TMEM; lane 0 issues every tcgen05.mma
 //   warps 2..   NWG softmax warpgroups.  Thread t of a group owns query row t,
 //               which is TMEM lane t.
@@ -46,26 +45,23 @@ struct FwdParams {
     uint64_t timeout_ns;
 };
 
-template <int D_, int DV_, int BN_, int NWG_, int NSB_, int KS_, int VS_, int ES_>
+template <int D_, int DV_, int BN_, int NWG_, int NSB_, int KS_, int VS_>
 struct FwdCfg {
-    static constexpr int D = D_, DV = DV_, BN = BN_, NWG = NWG_, NSB = NSB_, KS = KS_, VS = VS_,
-                         ES = ES_;
+    static constexpr int D = D_, DV = DV_, BN = BN_, NWG = NWG_, NSB = NSB_, KS = KS_, VS = VS_;
     static constexpr int BM = 128;
     static constexpr int SUB = TILE / BN;  // key sub-tiles per list entry
     static constexpr int Q_BYTES = BM * D * 2;
     static constexpr int K_BYTES = BN * D * 2;
     static constexpr int V_BYTES = BN * DV * 2;
-    static constexpr int E_BYTES = BN * 16;  // the tile's normalised mask boundaries
     static constexpr int OFF_Q = 0;
     static constexpr int OFF_K = OFF_Q + Q_BYTES;
     static constexpr int OFF_V = OFF_K + KS * K_BYTES;
-    static constexpr int OFF_E = OFF_V + VS * V_BYTES;
-    static constexpr int OFF_BAR = OFF_E + ES * E_BYTES;
-    // q_full, k_full[KS], k_empty[KS], v_full[VS], v_empty[VS], e_full[ES], e_empty[ES],
-    // s_full[NWG*NSB], p_full[NWG*NSB], pv_done[NWG*2]
-    static constexpr int NBAR = 1 + 2 * KS + 2 * VS + 2 * ES + 2 * NWG * NSB + 2 * NWG;
+    static constexpr int OFF_BAR = OFF_V + VS * V_BYTES;
+    // q_full, k_full[KS], k_empty[KS], v_full[VS], v_empty[VS],
+    // s_full[NWG*NSB], p_full[NWG*NSB], pv_done[NWG*2], mma_done
+    static constexpr int NBAR = 1 + 2 * KS + 2 * VS + 2 * NWG * NSB + 2 * NWG + 1;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
-    static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
+    static constexpr int SMEM_BYTES = OFF_MISC + 16;
     static constexpr int TM_O = 0;
     static constexpr int TM_S = NWG * DV;
     static constexpr int TM_COLS = 512;
@@ -75,6 +71,7 @@ struct FwdCfg {
     static_assert(DV <= 256 && BN % 64 == 0, "MMA shape");
     static_assert(NWG * 128 * 2 * 4 <= K_BYTES, "merge statistics alias K stage 0");
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+    static_assert(KS % NWG == 0 && VS % NWG == 0, "per-group ring stages");
 };
 
 // Warp-uniform bounded wait: every lane polls, the warp agrees on the result.
@@ -88,24 +85,24 @@ template <class C>
 __global__ void __launch_bounds__(C::THREADS, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    extern __shared__ __align__(1024) uint8_t smem[];
+    if (smem_u32(smem) & 1023u) {  // swizzled tiles need 1024-byte alignment
+        if (threadIdx.x == 0) atomicExch(&g_err_fwd, ERR_SMEM_ALIGN);
+        return;
+    }
     uint8_t *sQ = smem + C::OFF_Q;
     uint8_t *sK = smem + C::OFF_K;
     uint8_t *sV = smem + C::OFF_V;
-    uint8_t *sE = smem + C::OFF_E;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
     uint64_t *q_full = bars;
     uint64_t *k_full = q_full + 1;
     uint64_t *k_empty = k_full + C::KS;
     uint64_t *v_full = k_empty + C::KS;
     uint64_t *v_empty = v_full + C::VS;
-    uint64_t *e_full = v_empty + C::VS;
-    uint64_t *e_empty = e_full + C::ES;
-    uint64_t *s_full = e_empty + C::ES;
+    uint64_t *s_full = v_empty + C::VS;
     uint64_t *p_full = s_full + C::NWG * C::NSB;
     uint64_t *pv_done = p_full + C::NWG * C::NSB;
+    uint64_t *mma_done = pv_done + C::NWG * 2;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
     volatile int *abort = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
 
@@ -119,6 +116,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     const int n = (*reinterpret_cast<volatile unsigned *>(&g_err_fwd) != 0) ? 0
                                                                             : n_entries * C::SUB;
     const uint64_t tmo = p.timeout_ns;
+    auto n_of = [&](int w) { return n > w ? (n - w + C::NWG - 1) / C::NWG : 0; };
 
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
@@ -130,15 +128,12 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             mbar_init(&v_full[i], 1);
             mbar_init(&v_empty[i], 1);
         }
-        for (int i = 0; i < C::ES; ++i) {
-            mbar_init(&e_full[i], 1);
-            mbar_init(&e_empty[i], 128);
-        }
         for (int i = 0; i < C::NWG * C::NSB; ++i) {
             mbar_init(&s_full[i], 1);
             mbar_init(&p_full[i], 128);
         }
         for (int i = 0; i < C::NWG * 2; ++i) mbar_init(&pv_done[i], 1);
+        mbar_init(mma_done, 1);
         *abort = 0;
         fence_barrier_init();
     }
@@ -154,13 +149,11 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     auto key0_of = [&](int u) {
         return (entries[u / C::SUB] >> 1) * TILE + (u % C::SUB) * C::BN;
     };
-    constexpr int L = C::NWG * C::NSB;  // S tiles in flight
 
     if (warp == 0) {
         // ------------------------------------------------------ TMA producers
-        // Three lanes, three independent rings, each filled in the order its
-        // consumer drains it: lane 0 Q and K, lane 1 V, lane 2 the mask
-        // boundaries of each key tile.
+        // Two lanes, two independent rings, each filled in the order its
+        // consumer drains it: lane 0 Q and K, lane 1 V.
         if (lane == 0 && n > 0) {
             prefetch_tmap(&tm_q);
             prefetch_tmap(&tm_k);
@@ -194,16 +187,6 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     tma_load_4d(sV + s * C::V_BYTES + c * C::BN * 128, &tm_v, &v_full[s], c * 64,
                                 h, key0, b);
             }
-        } else if (lane == 2 && n > 0) {
-            const int4 *vec = p.vec + static_cast<size_t>(bm) * p.Npad;
-            for (int u = 0; u < n; ++u) {
-                const int s = u % C::ES;
-                if (u >= C::ES &&
-                    !mbar_wait(&e_empty[s], ((u / C::ES) - 1) & 1, tmo, abort, &g_err_fwd))
-                    break;
-                mbar_arrive_expect_tx(&e_full[s], C::E_BYTES);
-                bulk_load(sE + s * C::E_BYTES, vec + key0_of(u), C::E_BYTES, &e_full[s]);
-            }
         }
     } else if (warp == 1) {
         // --------------------------------------------------- tcgen05 issuer
@@ -215,42 +198,85 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             const uint64_t q_desc = sdesc_sw128(smem_u32(sQ), 16, 1024);
             const uint64_t k_desc = sdesc_sw128(smem_u32(sK), 16, 1024);
             const uint64_t v_desc = sdesc_sw128(smem_u32(sV), C::BN * 128, 1024);
-            auto issue_s = [&](int u) -> bool {
-                const int w = u % C::NWG, lu = u / C::NWG, sb = w * C::NSB + lu % C::NSB;
-                const int s = u % C::KS;
-                if (!mbar_wait(&k_full[s], (u / C::KS) & 1, tmo, abort, &g_err_fwd)) return false;
-                tc_fence_after();
-                const uint32_t d_tmem = tmem + C::TM_S + sb * C::BN;
-                const uint64_t ks = k_desc + static_cast<uint64_t>((s * C::K_BYTES) >> 4);
+            // Event-driven issue: each pass serves whichever group has its next
+            // S (K tile landed, S buffer free) or its next P V (P written, V
+            // landed) ready.  Both rings hold KS/NWG, VS/NWG stages per group,
+            // so every stage is consumed by one group in its own tile order.
+            int s_cnt[C::NWG], pv_cnt[C::NWG];
+            int remaining = 0;
 #pragma unroll
-                for (int k = 0; k < C::D / 16; ++k) {
-                    const uint64_t ad = q_desc + (((k / 4) * (C::BM * 128) + (k % 4) * 32) >> 4);
-                    const uint64_t bd = ks + (((k / 4) * (C::BN * 128) + (k % 4) * 32) >> 4);
-                    mma_ss(d_tmem, ad, bd, IDESC_S, k > 0 ? 1u : 0u);
-                }
-                mma_commit(&k_empty[s]);
-                mma_commit(&s_full[sb]);
-                return true;
-            };
-            bool ok = mbar_wait(q_full, 0, tmo, abort, &g_err_fwd);
-            for (int u = 0; u < L && u < n && ok; ++u) ok = issue_s(u);
-            for (int u = 0; u < n && ok; ++u) {
-                const int w = u % C::NWG, lu = u / C::NWG, sb = w * C::NSB + lu % C::NSB;
-                if (!mbar_wait(&p_full[sb], (lu / C::NSB) & 1, tmo, abort, &g_err_fwd)) break;
-                const int vs = u % C::VS;
-                if (!mbar_wait(&v_full[vs], (u / C::VS) & 1, tmo, abort, &g_err_fwd)) break;
-                tc_fence_after();
-                const uint32_t o_tmem = tmem + C::TM_O + w * C::DV;
-                const uint32_t p_tmem = tmem + C::TM_S + sb * C::BN;
-                const uint64_t vsd = v_desc + static_cast<uint64_t>((vs * C::V_BYTES) >> 4);
-#pragma unroll
-                for (int k = 0; k < C::BN / 16; ++k)
-                    mma_ts(o_tmem, p_tmem + k * 8, vsd + ((k * 2048) >> 4), IDESC_PV,
-                           (lu > 0 || k > 0) ? 1u : 0u);
-                mma_commit(&v_empty[vs]);
-                mma_commit(&pv_done[w * 2 + (lu & 1)]);
-                if (u + L < n) ok = issue_s(u + L);
+            for (int w = 0; w < C::NWG; ++w) {
+                s_cnt[w] = 0;
+                pv_cnt[w] = 0;
+                remaining += n_of(w) > 0;
             }
+            bool ok = mbar_wait(q_full, 0, tmo, abort, &g_err_fwd);
+            uint64_t last = globaltimer();
+            while (ok && remaining > 0) {
+                bool prog = false;
+#pragma unroll
+                for (int w = 0; w < C::NWG; ++w) {
+                    const int nm = n_of(w);
+                    const int lp = pv_cnt[w];
+                    if (lp < s_cnt[w]) {  // O_w += P V
+                        const int u = lp * C::NWG + w, vs = u % C::VS;
+                        const int sb = w * C::NSB + lp % C::NSB;
+                        if (mbar_test(&p_full[sb], (lp / C::NSB) & 1) &&
+                            mbar_test(&v_full[vs], (u / C::VS) & 1)) {
+                            tc_fence_after();
+                            const uint32_t o_tmem = tmem + C::TM_O + w * C::DV;
+                            const uint32_t p_tmem = tmem + C::TM_S + sb * C::BN;
+                            const uint64_t vsd =
+                                v_desc + static_cast<uint64_t>((vs * C::V_BYTES) >> 4);
+#pragma unroll
+                            for (int k = 0; k < C::BN / 16; ++k)
+                                mma_ts(o_tmem, p_tmem + k * 8, vsd + ((k * 2048) >> 4), IDESC_PV,
+                                       (lp > 0 || k > 0) ? 1u : 0u);
+                            mma_commit(&v_empty[vs]);
+                            mma_commit(&pv_done[w * 2 + (lp & 1)]);
+                            pv_cnt[w] = lp + 1;
+                            if (lp + 1 >= nm) --remaining;
+                            prog = true;
+                        }
+                    }
+                    const int ls = s_cnt[w];
+                    if (ls < nm && ls < pv_cnt[w] + C::NSB) {  // S = Q K^T
+                        const int u = ls * C::NWG + w, s = u % C::KS;
+                        if (mbar_test(&k_full[s], (u / C::KS) & 1)) {
+                            tc_fence_after();
+                            const int sb = w * C::NSB + ls % C::NSB;
+                            const uint32_t d_tmem = tmem + C::TM_S + sb * C::BN;
+                            const uint64_t ks = k_desc + static_cast<uint64_t>((s * C::K_BYTES) >> 4);
+#pragma unroll
+                            for (int k = 0; k < C::D / 16; ++k) {
+                                const uint64_t ad =
+                                    q_desc + (((k / 4) * (C::BM * 128) + (k % 4) * 32) >> 4);
+                                const uint64_t bd =
+                                    ks + (((k / 4) * (C::BN * 128) + (k % 4) * 32) >> 4);
+                                mma_ss(d_tmem, ad, bd, IDESC_S, k > 0 ? 1u : 0u);
+                            }
+                            mma_commit(&k_empty[s]);
+                            mma_commit(&s_full[sb]);
+                            s_cnt[w] = ls + 1;
+                            prog = true;
+                        }
+                    }
+                }
+                if (prog) {
+                    last = globaltimer();
+                } else if (*abort) {
+                    ok = false;
+                } else if (globaltimer() - last > tmo) {
+                    *abort = 1;
+                    atomicExch(&g_err_fwd, ERR_TIMEOUT);
+                    ok = false;
+                } else {
+                    // Nothing ready: yield the issue slots to the compute warps
+                    // that share this warp's sub-partition.
+                    __nanosleep(40);
+                }
+            }
+            mma_commit(mma_done);  // every MMA of the CTA has completed
         }
     } else {
         // ------------------------------------------------ softmax warpgroups
@@ -262,6 +288,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         const int n_my = n > wg ? (n - wg + C::NWG - 1) / C::NWG : 0;
         const float NEG_INF = -INFINITY;
         const float sl2 = p.sl2;
+        const int4 *vec = p.vec + static_cast<size_t>(bm) * p.Npad;
         float m_ref = NEG_INF, l_sum = 0.f;
         // The list entry of the group's next tile is read one tile ahead.
         int entry_next = n_my > 0 ? entries[wg / C::SUB] : 0;
@@ -273,7 +300,17 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             if (u + C::NWG < n) entry_next = entries[(u + C::NWG) / C::SUB];
             const bool masked_tile = entry & 1;
             const int key0 = (entry >> 1) * TILE + (u % C::SUB) * C::BN;
-            const int es = u % C::ES;
+
+            // Partial tiles: this lane's key columns' boundaries, loaded before the
+            // wait for S so that the wait hides their latency.
+            int4 cv[C::BN / 64][2];
+            if (masked_tile) {
+#pragma unroll
+                for (int c = 0; c < C::BN / 64; ++c) {
+                    cv[c][0] = __ldg(vec + key0 + c * 64 + lane);
+                    cv[c][1] = __ldg(vec + key0 + c * 64 + 32 + lane);
+                }
+            }
             if (!warp_wait(&s_full[sb], (lu / C::NSB) & 1, tmo, abort)) break;
             tc_fence_after();
             const uint32_t s_addr = lane_base + C::TM_S + sb * C::BN;
@@ -283,8 +320,6 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             // The reference max m_ref moves only when a chunk exceeds it by more
             // than 2^8; then O, the row sum and the P chunks of this tile that
             // are already written are rescaled (rare after the first chunk).
-            if (masked_tile && !warp_wait(&e_full[es], (u / C::ES) & 1, tmo, abort)) break;
-            const int4 *cv = reinterpret_cast<const int4 *>(sE + es * C::E_BYTES);
             bool o_synced = false;  // PV of the group's previous tile observed
             bool failed = false;
 #pragma unroll
@@ -298,9 +333,9 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     const int R = grow - lane;
                     const int ja = key0 + c * 64 + lane;
                     const uint32_t wa = warp_transpose32(
-                        column_row_bits(R, ja, cv[c * 64 + lane], p.causal), lane);
+                        column_row_bits(R, ja, cv[c][0], p.causal), lane);
                     const uint32_t wb = warp_transpose32(
-                        column_row_bits(R, ja + 32, cv[c * 64 + 32 + lane], p.causal), lane);
+                        column_row_bits(R, ja + 32, cv[c][1], p.causal), lane);
 #pragma unroll
                     for (int jj = 0; jj < 32; ++jj) {
                         if ((wa >> jj) & 1u) x[jj] = NEG_INF;
@@ -379,24 +414,16 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 l_sum += ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));
             }
             if (failed) break;
-            // The boundary ring slot is free again.  (On unmasked tiles the
-            // boundaries were not needed; still wait for their arrival so the
-            // ring's phases stay in step.)
-            if (!masked_tile && !warp_wait(&e_full[es], (u / C::ES) & 1, tmo, abort)) break;
-            mbar_arrive(&e_empty[es]);
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(&p_full[sb]);
         }
 
         // ------------------------------------------------------- epilogue
-        // Wait for the last P V of the whole tile: every MMA has then
-        // completed (they run in issue order), so O is final and the K ring is
-        // free for the merge statistics.  A group with no tiles waits too.
-        if (n > 0) {
-            const int ul = n - 1, wl = ul % C::NWG, pl = ul / C::NWG;
-            warp_wait(&pv_done[wl * 2 + (pl & 1)], (pl >> 1) & 1, tmo, abort);
-        }
+        // Wait until every MMA of the CTA has completed: O is then final and
+        // the K ring is free for the merge statistics.  A group with no tiles
+        // waits too.
+        if (n > 0) warp_wait(mma_done, 0, tmo, abort);
         tc_fence_after();
         __nv_bfloat16 *orow =
             p.o + ((static_cast<size_t>(b) * p.N + grow) * p.H + h) * static_cast<size_t>(C::DV);
@@ -498,15 +525,15 @@ int fwd_key_rows(int d, int dv) { return (d == 256 && dv == 256) ? 64 : 128; }
 
 cudaError_t launch_fwd(const Geometry &g, const Workspace &ws, const FwdArgs &a,
                        cudaStream_t st) {
-    // <d, dv, key tile, softmax groups, S buffers per group, K / V / boundary ring stages>
+    // <d, dv, key tile, softmax groups, S buffers per group, K / V ring stages>
     if (g.d == 64 && g.dv == 64)
-        return launch_cfg<FwdCfg<64, 64, 128, 2, 1, 2, 3, 4>>(g, ws, a, st);
+        return launch_cfg<FwdCfg<64, 64, 128, 2, 1, 4, 2>>(g, ws, a, st);
     if (g.d == 128 && g.dv == 128)
-        return launch_cfg<FwdCfg<128, 128, 128, 2, 1, 2, 3, 4>>(g, ws, a, st);
+        return launch_cfg<FwdCfg<128, 128, 128, 2, 1, 4, 2>>(g, ws, a, st);
     if (g.d == 192 && g.dv == 128)
-        return launch_cfg<FwdCfg<192, 128, 128, 2, 1, 2, 2, 4>>(g, ws, a, st);
+        return launch_cfg<FwdCfg<192, 128, 128, 2, 1, 2, 2>>(g, ws, a, st);
     if (g.d == 256 && g.dv == 256)
-        return launch_cfg<FwdCfg<256, 256, 64, 1, 2, 2, 2, 4>>(g, ws, a, st);
+        return launch_cfg<FwdCfg<256, 256, 64, 1, 2, 3, 2>>(g, ws, a, st);
     return cudaErrorInvalidValue;
 }
 
