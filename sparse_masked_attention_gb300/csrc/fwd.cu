@@ -310,6 +310,14 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     cv[c][0] = __ldg(vec + key0 + c * 64 + lane);
                     cv[c][1] = __ldg(vec + key0 + c * 64 + 32 + lane);
                 }
+                // Pin the loads here: left to itself the compiler sinks them
+                // past the wait, to their first use, and exposes their latency.
+#pragma unroll
+                for (int c = 0; c < C::BN / 64; ++c)
+#pragma unroll
+                    for (int e = 0; e < 2; ++e)
+                        asm volatile("" ::"r"(cv[c][e].x), "r"(cv[c][e].y), "r"(cv[c][e].z),
+                                     "r"(cv[c][e].w));
             }
             if (!warp_wait(&s_full[sb], (lu / C::NSB) & 1, tmo, abort)) break;
             tc_fence_after();
@@ -398,20 +406,24 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     }
                 }
                 const float m_use = (m_ref == NEG_INF) ? 0.0f : m_ref;
-                float l8[8];
+                // Exponent arguments and partial row sums two columns at a time
+                // (paired fp32 FMA and add).
+                const float2 sl2x2 = make_float2(sl2, sl2);
+                const float2 negm = make_float2(-m_use, -m_use);
+                float2 l4[4];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) l8[i] = 0.f;
+                for (int i = 0; i < 4; ++i) l4[i] = make_float2(0.f, 0.f);
                 uint32_t r[32];
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
-                    const float p0 = ex2(fmaf(x[2 * i], sl2, -m_use));
-                    const float p1 = ex2(fmaf(x[2 * i + 1], sl2, -m_use));
-                    l8[(2 * i) & 7] += p0;
-                    l8[(2 * i + 1) & 7] += p1;
-                    r[i] = pack_bf16(p0, p1);
+                    const float2 t = __ffma2_rn(make_float2(x[2 * i], x[2 * i + 1]), sl2x2, negm);
+                    const float2 pp = make_float2(ex2(t.x), ex2(t.y));
+                    l4[i & 3] = __fadd2_rn(l4[i & 3], pp);
+                    r[i] = pack_bf16(pp.x, pp.y);
                 }
                 tmem_st32(s_addr + c * 32, r);
-                l_sum += ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));
+                const float2 la = __fadd2_rn(__fadd2_rn(l4[0], l4[1]), __fadd2_rn(l4[2], l4[3]));
+                l_sum += la.x + la.y;
             }
             if (failed) break;
             tmem_st_wait();
