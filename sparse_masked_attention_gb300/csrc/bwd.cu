@@ -615,7 +615,12 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             prefetch_tmap(&tm_do);
             for (int u = 0; u < n; ++u) {
                 const int w = u % C::NWG, lw = u / C::NWG;
-                if (lw >= 1 && !mbar_wait(&o_empty[w], (lw - 1) & 1, tmo, abort, &g_err_bwd))
+                // The stage is free once the group's previous tile no longer
+                // needs it: with dK, when its compute has written dS^T (the dV
+                // and dP^T MMAs, the last readers of dO, completed before dP^T
+                // was handed over); without dK, when the dV MMA has completed.
+                uint64_t *free_bar = C::DO_DK ? &ds_full[w] : &o_empty[w];
+                if (lw >= 1 && !mbar_wait(free_bar, (lw - 1) & 1, tmo, abort, &g_err_bwd))
                     break;
                 mbar_arrive_expect_tx(&o_full[w], C::DO_BYTES + C::LD_BYTES);
                 const int q0 = q0_of(u);
@@ -706,12 +711,14 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                                 mma_ss(t_r, v_desc + a_off, dd + b_off, IDESC_DP, k > 0 ? 1u : 0u);
                             }
                             mma_commit(&dp_full[w]);
+                        } else {
+                            mma_commit(&o_empty[w]);  // dO and LSE2 read
                         }
                         st_[w] = 2;
                         prog = true;
                     } else {
                         // The group has written dS^T: dK += dS^T Q; then the
-                        // tile's Q, dO, LSE2 and D stages are free.
+                        // tile's Q stage is free.
                         if (u != next_k || !mbar_test(&ds_full[w], lu & 1)) continue;
                         tc_fence_after();
                         ++next_k;
@@ -724,7 +731,6 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                                        IDESC_DK, (u > 0 || k > 0) ? 1u : 0u);
                         }
                         mma_commit(&q_empty[s]);
-                        mma_commit(&o_empty[w]);
                         st_[w] = 0;
                         lu_[w] = lu + 1;
                         if (lu + 1 >= n_of(w)) --remaining;
