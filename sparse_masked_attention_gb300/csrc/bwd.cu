@@ -396,11 +396,24 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             const int entry = entry_next;
             const bool masked_tile = entry & 1;
             const int key0 = (entry >> 1) * TILE + (u % C::SUB) * C::BN;
-            int4 cv[C::BN / 64][2];
+            // Partial tiles: the mask bits of this lane's row, built before the
+            // wait for S.  Lane l holds the boundaries of key columns l and
+            // l + 32 of each 64-column chunk; their row bits over this warp's
+            // rows are transposed so that each lane gets its row's column bits.
+            uint32_t mbits[C::BN / 64][2];
+            if (masked_tile) {
+                const int R = grow - lane;
 #pragma unroll
-            for (int c = 0; c < C::BN / 64; ++c) {
-                cv[c][0] = cv_next[c][0];
-                cv[c][1] = cv_next[c][1];
+                for (int c = 0; c < C::BN / 64; ++c)
+#pragma unroll
+                    for (int e = 0; e < 2; ++e)
+                        mbits[c][e] = warp_transpose32(
+                            column_row_bits(R, key0 + c * 64 + e * 32 + lane, cv_next[c][e],
+                                            p.causal),
+                            lane);
+#pragma unroll
+                for (int c = 0; c < C::BN / 64; ++c)
+                    asm volatile("" ::"r"(mbits[c][0]), "r"(mbits[c][1]));
             }
             if (u + C::NWG < n) entry_next = entries[(u + C::NWG) / C::SUB];
             if (!warp_wait(&s_full[wg], lu & 1, tmo, abort)) break;
@@ -414,14 +427,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
 #pragma unroll
                 for (int jj = 0; jj < 64; ++jj) x[jj] = ex2(fmaf(x[jj], sl2, -lse2));
                 if (masked_tile) {
-                    // Row bits of key columns lane, lane + 32 over the warp's rows,
-                    // transposed so each lane holds its row's column bits.
-                    const int R = grow - lane;
-                    const int ja = key0 + c * 64 + lane;
-                    const uint32_t wa =
-                        warp_transpose32(column_row_bits(R, ja, cv[c][0], p.causal), lane);
-                    const uint32_t wb =
-                        warp_transpose32(column_row_bits(R, ja + 32, cv[c][1], p.causal), lane);
+                    const uint32_t wa = mbits[c][0], wb = mbits[c][1];
 #pragma unroll
                     for (int jj = 0; jj < 32; ++jj) {
                         if ((wa >> jj) & 1u) x[jj] = 0.f;

@@ -301,23 +301,36 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             const bool masked_tile = entry & 1;
             const int key0 = (entry >> 1) * TILE + (u % C::SUB) * C::BN;
 
-            // Partial tiles: this lane's key columns' boundaries, loaded before the
-            // wait for S so that the wait hides their latency.
-            int4 cv[C::BN / 64][2];
+            // Partial tiles: the mask bits of this lane's row over the tile's key
+            // columns, built before the wait for S (they do not depend on S), so
+            // that the wait hides the boundary loads and the bit transposes.
+            // Lane l loads the boundaries of key columns l and l + 32 of each
+            // 64-column chunk and builds their row bits over this warp's 32
+            // rows; a bit transpose hands every lane the column bits of its row.
+            uint32_t mbits[C::BN / 64][2];
             if (masked_tile) {
+                int4 cv[C::BN / 64][2];
 #pragma unroll
                 for (int c = 0; c < C::BN / 64; ++c) {
                     cv[c][0] = __ldg(vec + key0 + c * 64 + lane);
                     cv[c][1] = __ldg(vec + key0 + c * 64 + 32 + lane);
                 }
-                // Pin the loads here: left to itself the compiler sinks them
-                // past the wait, to their first use, and exposes their latency.
+                const int R = grow - lane;
 #pragma unroll
                 for (int c = 0; c < C::BN / 64; ++c)
 #pragma unroll
                     for (int e = 0; e < 2; ++e)
-                        asm volatile("" ::"r"(cv[c][e].x), "r"(cv[c][e].y), "r"(cv[c][e].z),
-                                     "r"(cv[c][e].w));
+                        mbits[c][e] = column_row_bits(R, key0 + c * 64 + e * 32 + lane, cv[c][e],
+                                                      p.causal);
+#pragma unroll
+                for (int c = 0; c < C::BN / 64; ++c)
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) mbits[c][e] = warp_transpose32(mbits[c][e], lane);
+                // Keep the bits ahead of the wait: left to itself the compiler
+                // sinks this work past the wait, to its first use.
+#pragma unroll
+                for (int c = 0; c < C::BN / 64; ++c)
+                    asm volatile("" ::"r"(mbits[c][0]), "r"(mbits[c][1]));
             }
             if (!warp_wait(&s_full[sb], (lu / C::NSB) & 1, tmo, abort)) break;
             tc_fence_after();
@@ -335,15 +348,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 float x[64];
                 tmem_ld64f(s_addr + c * 64, x);
                 if (masked_tile) {
-                    // Lane l builds the row bits of key columns l and l + 32 of
-                    // the chunk over this warp's 32 rows; a bit transpose hands
-                    // every lane the column bits of its own row.
-                    const int R = grow - lane;
-                    const int ja = key0 + c * 64 + lane;
-                    const uint32_t wa = warp_transpose32(
-                        column_row_bits(R, ja, cv[c][0], p.causal), lane);
-                    const uint32_t wb = warp_transpose32(
-                        column_row_bits(R, ja + 32, cv[c][1], p.causal), lane);
+                    const uint32_t wa = mbits[c][0], wb = mbits[c][1];
 #pragma unroll
                     for (int jj = 0; jj < 32; ++jj) {
                         if ((wa >> jj) & 1u) x[jj] = NEG_INF;
