@@ -128,6 +128,7 @@ struct BwdParams {
     float sl2;    // scale * log2(e)
     float scale;
     uint64_t timeout_ns;
+    int ordered;  // deterministic mode: accumulate the tiles in tile order
 };
 
 // ------------------------------------------------------------------ dq kernel
@@ -288,8 +289,12 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 st_[w] = 0;
                 remaining += n_of(w) > 0;
             }
-            // S tiles are issued in tile order (K ring phases); the dQ
-            // accumulation too, so its fp32 sums are the same on every run.
+            // Deterministic mode issues the S tiles and the dQ accumulations in
+            // tile order, so the fp32 sums are the same on every run.  Otherwise
+            // whichever group is ready goes first: the sums' order, and their
+            // last bits, vary, but neither group waits for the other.  The K
+            // ring is filled in tile order; a group gets at most one ring length
+            // ahead, since a stage is refilled only after its older tile's dQ.
             int next_s = 0, next_q = 0;
             bool ok = mbar_wait(q_full, 0, tmo, abort, &g_err_bwd);
             uint64_t last = globaltimer();
@@ -303,7 +308,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     const int s = u % C::KS;
                     const uint32_t t_r = tmem + w * C::BN;
                     if (st_[w] == 0) {  // S = Q K^T
-                        if (u != next_s || !mbar_test(&k_full[s], (u / C::KS) & 1)) continue;
+                        if ((p.ordered && u != next_s) || !mbar_test(&k_full[s], (u / C::KS) & 1))
+                            continue;
                         tc_fence_after();
                         const uint64_t ks = k_desc + static_cast<uint64_t>((s * C::K_BYTES) >> 4);
 #pragma unroll
@@ -332,14 +338,14 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                         st_[w] = 2;
                         prog = true;
                     } else {  // dQ += dS K (dS from TMEM, K MN-major over d)
-                        if (u != next_q || !mbar_test(&ds_full[w], lu & 1)) continue;
+                        if ((p.ordered && u != next_q) || !mbar_test(&ds_full[w], lu & 1)) continue;
                         tc_fence_after();
                         const uint64_t kmn =
                             k_desc_mn + static_cast<uint64_t>((s * C::K_BYTES) >> 4);
 #pragma unroll
                         for (int k = 0; k < C::BN / 16; ++k)
                             mma_ts(tmem + C::TM_DQ, t_r + k * 8, kmn + ((k * 2048) >> 4), IDESC_DQ,
-                                   (u > 0 || k > 0) ? 1u : 0u);
+                                   (next_q > 0 || k > 0) ? 1u : 0u);
                         ++next_q;
                         mma_commit(&k_empty[s]);
                         st_[w] = 0;
@@ -661,8 +667,12 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 st_[w] = 0;
                 remaining += n_of(w) > 0;
             }
-            // S^T tiles are issued in tile order (Q ring phases); the dV and dK
-            // accumulations too, so their fp32 sums are the same on every run.
+            // Deterministic mode issues the S^T tiles and the dV and dK
+            // accumulations in tile order, so the fp32 sums are the same on
+            // every run.  Otherwise whichever group is ready goes first: the
+            // sums' order, and their last bits, vary, but neither group waits
+            // for the other.  The Q ring is filled in tile order; a stage is
+            // refilled only after its older tile's dK.
             int next_s = 0, next_v = 0, next_k = 0;
             bool ok = mbar_wait(kv_full, 0, tmo, abort, &g_err_bwd);
             uint64_t last = globaltimer();
@@ -676,7 +686,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     const int s = u % C::QS;
                     const uint32_t t_r = tmem + C::TM_W0 + w * C::BM;
                     if (st_[w] == 0) {  // S^T = K Q^T
-                        if (u != next_s || !mbar_test(&q_full[s], (u / C::QS) & 1)) continue;
+                        if ((p.ordered && u != next_s) || !mbar_test(&q_full[s], (u / C::QS) & 1))
+                            continue;
                         tc_fence_after();
                         const uint64_t qs = q_desc + static_cast<uint64_t>((s * C::Q_BYTES) >> 4);
 #pragma unroll
@@ -692,10 +703,11 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     } else if (st_[w] == 1) {
                         // The group has read S^T (and written P^T): dV += P^T dO,
                         // then dP^T = V dO^T into the same region.
-                        if (u != next_v || !mbar_test(&p_full[w], lu & 1) ||
+                        if ((p.ordered && u != next_v) || !mbar_test(&p_full[w], lu & 1) ||
                             !mbar_test(&o_full[w], lu & 1))
                             continue;
                         tc_fence_after();
+                        const bool acc_v = next_v > 0;  // the first dV product initialises
                         ++next_v;
                         if constexpr (C::DO_DV) {
                             const uint64_t dmn =
@@ -703,7 +715,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
 #pragma unroll
                             for (int k = 0; k < C::BM / 16; ++k)
                                 mma_ts(tmem + C::TM_DV, t_r + k * 8, dmn + ((k * 2048) >> 4),
-                                       IDESC_DV, (u > 0 || k > 0) ? 1u : 0u);
+                                       IDESC_DV, (acc_v || k > 0) ? 1u : 0u);
                         }
                         if constexpr (C::DO_DK) {
                             const uint64_t dd =
@@ -725,8 +737,9 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     } else {
                         // The group has written dS^T: dK += dS^T Q; then the
                         // tile's Q stage is free.
-                        if (u != next_k || !mbar_test(&ds_full[w], lu & 1)) continue;
+                        if ((p.ordered && u != next_k) || !mbar_test(&ds_full[w], lu & 1)) continue;
                         tc_fence_after();
+                        const bool acc_k = next_k > 0;  // the first dK product initialises
                         ++next_k;
                         if constexpr (C::DO_DK) {
                             const uint64_t qmn =
@@ -734,7 +747,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
 #pragma unroll
                             for (int k = 0; k < C::BM / 16; ++k)
                                 mma_ts(tmem + C::TM_DK, t_r + k * 8, qmn + ((k * 2048) >> 4),
-                                       IDESC_DK, (u > 0 || k > 0) ? 1u : 0u);
+                                       IDESC_DK, (acc_k || k > 0) ? 1u : 0u);
                         }
                         mma_commit(&q_empty[s]);
                         st_[w] = 0;
@@ -895,6 +908,7 @@ BwdParams make_params(const Geometry &g, const Workspace &ws, const BwdArgs &a, 
     p.sl2 = g.scale * 1.4426950408889634f;
     p.scale = g.scale;
     p.timeout_ns = g.timeout_ns;
+    p.ordered = g.deterministic != 0;
     return p;
 }
 
