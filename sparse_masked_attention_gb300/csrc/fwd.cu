@@ -198,82 +198,110 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             const uint64_t q_desc = sdesc_sw128(smem_u32(sQ), 16, 1024);
             const uint64_t k_desc = sdesc_sw128(smem_u32(sK), 16, 1024);
             const uint64_t v_desc = sdesc_sw128(smem_u32(sV), C::BN * 128, 1024);
-            // Event-driven issue: each pass serves whichever group has its next
-            // S (K tile landed, S buffer free) or its next P V (P written, V
-            // landed) ready.  Both rings hold KS/NWG, VS/NWG stages per group,
-            // so every stage is consumed by one group in its own tile order.
-            int s_cnt[C::NWG], pv_cnt[C::NWG];
+            // S = Q K^T of group w's tile ls (K stage landed, S buffer free)
+            auto issue_s = [&](int w, int ls) {
+                const int u = ls * C::NWG + w, s = u % C::KS;
+                const uint32_t d_tmem = tmem + C::TM_S + (w * C::NSB + ls % C::NSB) * C::BN;
+                const uint64_t ks = k_desc + static_cast<uint64_t>((s * C::K_BYTES) >> 4);
+#pragma unroll
+                for (int k = 0; k < C::D / 16; ++k) {
+                    const uint64_t ad = q_desc + (((k / 4) * (C::BM * 128) + (k % 4) * 32) >> 4);
+                    const uint64_t bd = ks + (((k / 4) * (C::BN * 128) + (k % 4) * 32) >> 4);
+                    mma_ss(d_tmem, ad, bd, IDESC_S, k > 0 ? 1u : 0u);
+                }
+            };
+            // Each commit costs the issuing thread about as long as an MMA, time
+            // in which the tensor pipe runs dry, so a step commits once: S done.
+            // The softmax group frees the K stage when it sees S, and the V
+            // stage of its tile lp - NSB, since the pipe ran that P V before S.
+            auto commit_s = [&](int w, int ls) { mma_commit(&s_full[w * C::NSB + ls % C::NSB]); };
+            auto k_ready = [&](int w, int ls) {
+                const int u = ls * C::NWG + w;
+                return mbar_test(&k_full[u % C::KS], (u / C::KS) & 1) != 0;
+            };
+            // O_w += P V of group w's tile lp (P written, V stage landed)
+            auto issue_pv = [&](int w, int lp) {
+                const int u = lp * C::NWG + w, vs = u % C::VS;
+                const uint32_t o_tmem = tmem + C::TM_O + w * C::DV;
+                const uint32_t p_tmem = tmem + C::TM_S + (w * C::NSB + lp % C::NSB) * C::BN;
+                const uint64_t vsd = v_desc + static_cast<uint64_t>((vs * C::V_BYTES) >> 4);
+#pragma unroll
+                for (int k = 0; k < C::BN / 16; ++k)
+                    mma_ts(o_tmem, p_tmem + k * 8, vsd + ((k * 2048) >> 4), IDESC_PV,
+                           (lp > 0 || k > 0) ? 1u : 0u);
+            };
+            // With one S buffer per group the group's next S implies its P V is
+            // done; with two, the rescale of O waits for this commit.
+            auto commit_pv = [&](int w, int lp) {
+                if constexpr (C::NSB > 1) mma_commit(&pv_done[w * 2 + (lp & 1)]);
+            };
+            auto pv_ready = [&](int w, int lp) {
+                const int u = lp * C::NWG + w;
+                return mbar_test(&p_full[w * C::NSB + lp % C::NSB], (lp / C::NSB) & 1) &&
+                       mbar_test(&v_full[u % C::VS], (u / C::VS) & 1);
+            };
+            bool ok = mbar_wait(q_full, 0, tmo, abort, &g_err_fwd);
+            // Prologue: S of every group's first NSB tiles, in tile order.
+            for (int ls = 0; ok && ls < C::NSB; ++ls)
+                for (int w = 0; ok && w < C::NWG; ++w) {
+                    if (ls >= n_of(w)) continue;
+                    const int u = ls * C::NWG + w;
+                    ok = mbar_wait(&k_full[u % C::KS], (u / C::KS) & 1, tmo, abort, &g_err_fwd);
+                    if (!ok) break;
+                    tc_fence_after();
+                    issue_s(w, ls);
+                    commit_s(w, ls);
+                }
+            // Steady state: a step of group w is its P V for tile lp and the S of
+            // tile lp + NSB (the buffer P V frees; the tensor pipe runs them in
+            // order), issued as one run once P, V and K are all ready, with the
+            // commits after the run.  The thread serves the groups in turn and
+            // reads the clock only while idle, so consecutive runs follow each
+            // other without a gap that would drain the MMA queue.  Both rings
+            // hold a multiple of NWG stages: a group waits only on its own
+            // older tiles.
+            int pv_cnt[C::NWG];
             int remaining = 0;
 #pragma unroll
             for (int w = 0; w < C::NWG; ++w) {
-                s_cnt[w] = 0;
                 pv_cnt[w] = 0;
                 remaining += n_of(w) > 0;
             }
-            bool ok = mbar_wait(q_full, 0, tmo, abort, &g_err_fwd);
-            uint64_t last = globaltimer();
+            int w = 0;
+            bool idle = false;
+            uint64_t idle_t0 = 0;
             while (ok && remaining > 0) {
                 bool prog = false;
 #pragma unroll
-                for (int w = 0; w < C::NWG; ++w) {
-                    const int nm = n_of(w);
-                    const int lp = pv_cnt[w];
-                    if (lp < s_cnt[w]) {  // O_w += P V
-                        const int u = lp * C::NWG + w, vs = u % C::VS;
-                        const int sb = w * C::NSB + lp % C::NSB;
-                        if (mbar_test(&p_full[sb], (lp / C::NSB) & 1) &&
-                            mbar_test(&v_full[vs], (u / C::VS) & 1)) {
-                            tc_fence_after();
-                            const uint32_t o_tmem = tmem + C::TM_O + w * C::DV;
-                            const uint32_t p_tmem = tmem + C::TM_S + sb * C::BN;
-                            const uint64_t vsd =
-                                v_desc + static_cast<uint64_t>((vs * C::V_BYTES) >> 4);
-#pragma unroll
-                            for (int k = 0; k < C::BN / 16; ++k)
-                                mma_ts(o_tmem, p_tmem + k * 8, vsd + ((k * 2048) >> 4), IDESC_PV,
-                                       (lp > 0 || k > 0) ? 1u : 0u);
-                            mma_commit(&v_empty[vs]);
-                            mma_commit(&pv_done[w * 2 + (lp & 1)]);
-                            pv_cnt[w] = lp + 1;
-                            if (lp + 1 >= nm) --remaining;
-                            prog = true;
-                        }
+                for (int i = 0; i < C::NWG; ++i) {
+                    const int nm = n_of(w), lp = pv_cnt[w];
+                    const int ls = lp + C::NSB;
+                    if (lp < nm && pv_ready(w, lp) && (ls >= nm || k_ready(w, ls))) {
+                        tc_fence_after();
+                        issue_pv(w, lp);
+                        if (ls < nm) issue_s(w, ls);
+                        commit_pv(w, lp);
+                        if (ls < nm) commit_s(w, ls);
+                        pv_cnt[w] = lp + 1;
+                        if (lp + 1 >= nm) --remaining;
+                        prog = true;
                     }
-                    const int ls = s_cnt[w];
-                    if (ls < nm && ls < pv_cnt[w] + C::NSB) {  // S = Q K^T
-                        const int u = ls * C::NWG + w, s = u % C::KS;
-                        if (mbar_test(&k_full[s], (u / C::KS) & 1)) {
-                            tc_fence_after();
-                            const int sb = w * C::NSB + ls % C::NSB;
-                            const uint32_t d_tmem = tmem + C::TM_S + sb * C::BN;
-                            const uint64_t ks = k_desc + static_cast<uint64_t>((s * C::K_BYTES) >> 4);
-#pragma unroll
-                            for (int k = 0; k < C::D / 16; ++k) {
-                                const uint64_t ad =
-                                    q_desc + (((k / 4) * (C::BM * 128) + (k % 4) * 32) >> 4);
-                                const uint64_t bd =
-                                    ks + (((k / 4) * (C::BN * 128) + (k % 4) * 32) >> 4);
-                                mma_ss(d_tmem, ad, bd, IDESC_S, k > 0 ? 1u : 0u);
-                            }
-                            mma_commit(&k_empty[s]);
-                            mma_commit(&s_full[sb]);
-                            s_cnt[w] = ls + 1;
-                            prog = true;
-                        }
-                    }
+                    w = (w + 1 == C::NWG) ? 0 : w + 1;
                 }
                 if (prog) {
-                    last = globaltimer();
+                    idle = false;
                 } else if (*abort) {
                     ok = false;
-                } else if (globaltimer() - last > tmo) {
-                    *abort = 1;
-                    atomicExch(&g_err_fwd, ERR_TIMEOUT);
-                    ok = false;
                 } else {
-                    // Nothing ready: yield the issue slots to the compute warps
-                    // that share this warp's sub-partition.
-                    __nanosleep(40);
+                    const uint64_t now = globaltimer();
+                    if (!idle) {
+                        idle = true;
+                        idle_t0 = now;
+                    } else if (now - idle_t0 > tmo) {
+                        *abort = 1;
+                        atomicExch(&g_err_fwd, ERR_TIMEOUT);
+                        ok = false;
+                    }
                 }
             }
             mma_commit(mma_done);  // every MMA of the CTA has completed
@@ -334,6 +362,12 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             }
             if (!warp_wait(&s_full[sb], (lu / C::NSB) & 1, tmo, abort)) break;
             tc_fence_after();
+            if (((warp - 2) & 3) == 0 && lane == 0) {
+                // S of this tile is done, and so is the group's P V of tile
+                // lu - NSB (issued before it): their K and V stages are free.
+                mbar_arrive(&k_empty[u % C::KS]);
+                if (lu >= C::NSB) mbar_arrive(&v_empty[((lu - C::NSB) * C::NWG + wg) % C::VS]);
+            }
             const uint32_t s_addr = lane_base + C::TM_S + sb * C::BN;
 
             // One pass over the tile in 64-column chunks.  Each chunk is masked
@@ -374,7 +408,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     l_sum *= alpha;
                     if (__any_sync(0xffffffffu, fix)) {
                         if (lu > 0) {
-                            if (!o_synced) {
+                            if (C::NSB > 1 && !o_synced) {  // NSB = 1: S implies the P V
                                 const int pl = lu - 1;
                                 if (!warp_wait(&pv_done[wg * 2 + (pl & 1)], (pl >> 1) & 1, tmo,
                                                abort)) {
