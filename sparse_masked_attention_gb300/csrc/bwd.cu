@@ -166,6 +166,9 @@ struct DqCfg {
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
     static_assert(BN == 64 || BN == 128, "key sub-tile");
     static_assert(KS >= NWG, "ring depth");
+    // The compute frees a K stage when it sees the group's next S; that S must
+    // not need the stage itself.
+    static constexpr bool RELAY_K = KS > NWG;
     static_assert((D / 32) % NWG == 0, "epilogue column split");
 };
 
@@ -296,8 +299,33 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             // ring is filled in tile order; a group gets at most one ring length
             // ahead, since a stage is refilled only after its older tile's dQ.
             int next_s = 0, next_q = 0;
+            // A tcgen05.commit costs this thread about as long as an MMA, time in
+            // which the tensor pipe runs dry, so commits are kept to the two the
+            // compute waits for (S, dP).  The compute frees the V stage when it
+            // sees dP, and the K stage of its tile lu - 1 when it sees S of tile
+            // lu (the pipe ran that dQ first); the MMA thread commits the K
+            // stage only after a group's last dQ.  A dQ and the group's next S
+            // go out as one run.
+            auto issue_s = [&](int w, int u) {  // S = Q K^T into group w's region
+                const uint64_t ks =
+                    k_desc + static_cast<uint64_t>(((u % C::KS) * C::K_BYTES) >> 4);
+#pragma unroll
+                for (int k = 0; k < C::D / 16; ++k) {
+                    const uint32_t a_off = ((k / 4) * (C::BM * 128) + (k % 4) * 32) >> 4;
+                    const uint32_t b_off = ((k / 4) * (C::BN * 128) + (k % 4) * 32) >> 4;
+                    mma_ss(tmem + w * C::BN, q_desc + a_off, ks + b_off, IDESC_S,
+                           k > 0 ? 1u : 0u);
+                }
+                mma_commit(&s_full[w]);
+                ++next_s;
+            };
+            auto s_ready = [&](int u) {
+                return (!p.ordered || u == next_s) &&
+                       mbar_test(&k_full[u % C::KS], (u / C::KS) & 1) != 0;
+            };
             bool ok = mbar_wait(q_full, 0, tmo, abort, &g_err_bwd);
-            uint64_t last = globaltimer();
+            bool idle = false;
+            uint64_t idle_t0 = 0;
             while (ok && remaining > 0) {
                 bool prog = false;
 #pragma unroll
@@ -308,19 +336,10 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     const int s = u % C::KS;
                     const uint32_t t_r = tmem + w * C::BN;
                     if (st_[w] == 0) {  // S = Q K^T
-                        if ((p.ordered && u != next_s) || !mbar_test(&k_full[s], (u / C::KS) & 1))
-                            continue;
+                        if (!s_ready(u)) continue;
                         tc_fence_after();
-                        const uint64_t ks = k_desc + static_cast<uint64_t>((s * C::K_BYTES) >> 4);
-#pragma unroll
-                        for (int k = 0; k < C::D / 16; ++k) {
-                            const uint32_t a_off = ((k / 4) * (C::BM * 128) + (k % 4) * 32) >> 4;
-                            const uint32_t b_off = ((k / 4) * (C::BN * 128) + (k % 4) * 32) >> 4;
-                            mma_ss(t_r, q_desc + a_off, ks + b_off, IDESC_S, k > 0 ? 1u : 0u);
-                        }
-                        mma_commit(&s_full[w]);
+                        issue_s(w, u);
                         st_[w] = 1;
-                        ++next_s;
                         prog = true;
                     } else if (st_[w] == 1) {  // dP = dO V^T, once the group has read S
                         if (!mbar_test(&p_full[w], lu & 1) || !mbar_test(&v_full[w], lu & 1))
@@ -333,11 +352,10 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                             const uint32_t b_off = ((k / 4) * (C::BN * 128) + (k % 4) * 32) >> 4;
                             mma_ss(t_r, do_desc + a_off, vsd + b_off, IDESC_DP, k > 0 ? 1u : 0u);
                         }
-                        mma_commit(&v_empty[w]);
                         mma_commit(&dp_full[w]);
                         st_[w] = 2;
                         prog = true;
-                    } else {  // dQ += dS K (dS from TMEM, K MN-major over d)
+                    } else {  // dQ += dS K (dS from TMEM, K MN-major over d), then next S
                         if ((p.ordered && u != next_q) || !mbar_test(&ds_full[w], lu & 1)) continue;
                         tc_fence_after();
                         const uint64_t kmn =
@@ -347,25 +365,34 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                             mma_ts(tmem + C::TM_DQ, t_r + k * 8, kmn + ((k * 2048) >> 4), IDESC_DQ,
                                    (next_q > 0 || k > 0) ? 1u : 0u);
                         ++next_q;
-                        mma_commit(&k_empty[s]);
-                        st_[w] = 0;
                         lu_[w] = lu + 1;
-                        if (lu + 1 >= n_of(w)) --remaining;
+                        st_[w] = 0;
+                        // no later S of this group frees the stage (or, with no
+                        // more stages than groups, that S would need it first)
+                        if (!C::RELAY_K || lu + 1 >= n_of(w)) mma_commit(&k_empty[s]);
+                        if (lu + 1 >= n_of(w)) {
+                            --remaining;
+                        } else if (s_ready(u + C::NWG)) {
+                            issue_s(w, u + C::NWG);
+                            st_[w] = 1;
+                        }
                         prog = true;
                     }
                 }
                 if (prog) {
-                    last = globaltimer();
+                    idle = false;
                 } else if (*abort) {
                     ok = false;
-                } else if (globaltimer() - last > tmo) {
-                    *abort = 1;
-                    atomicExch(&g_err_bwd, ERR_TIMEOUT);
-                    ok = false;
                 } else {
-                    // Nothing ready: yield the issue slots to the compute warps
-                    // that share this warp's sub-partition.
-                    __nanosleep(40);
+                    const uint64_t now = globaltimer();
+                    if (!idle) {
+                        idle = true;
+                        idle_t0 = now;
+                    } else if (now - idle_t0 > tmo) {
+                        *abort = 1;
+                        atomicExch(&g_err_bwd, ERR_TIMEOUT);
+                        ok = false;
+                    }
                 }
             }
             mma_commit(dq_done);
@@ -424,6 +451,9 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             if (u + C::NWG < n) entry_next = entries[(u + C::NWG) / C::SUB];
             if (!warp_wait(&s_full[wg], lu & 1, tmo, abort)) break;
             tc_fence_after();
+            // S of this tile ran after the group's previous dQ: that K stage is free.
+            if (C::RELAY_K && ((warp - 2) & 3) == 0 && lane == 0 && lu > 0)
+                mbar_arrive(&k_empty[(u - C::NWG) % C::KS]);
             // phase 1: P = exp2(S * scale * log2e - LSE2), masked, kept as fp16 pairs
             uint32_t pk[C::BN / 2];
 #pragma unroll
@@ -449,6 +479,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             // phase 2: dS = P * (dP - D) -> the region, bf16
             if (!warp_wait(&dp_full[wg], lu & 1, tmo, abort)) break;
             tc_fence_after();
+            if (((warp - 2) & 3) == 0 && lane == 0) mbar_arrive(&v_empty[wg]);  // dP read V
 #pragma unroll
             for (int c = 0; c < C::BN / 64; ++c) {
                 float dp[64];
@@ -533,6 +564,9 @@ struct DkdvCfg {
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
     static_assert(D <= 256 && DV <= 256 && (BM == 64 || BM == 128), "MMA shape");
     static_assert(QS >= NWG, "ring depth");
+    // The compute frees a Q stage when it sees the group's next S^T; that S^T
+    // must not need the stage itself.
+    static constexpr bool RELAY_Q = QS > NWG;
     static_assert((D / 32) % NWG == 0 && (DV / 32) % NWG == 0, "epilogue column split");
 };
 
@@ -674,8 +708,32 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             // for the other.  The Q ring is filled in tile order; a stage is
             // refilled only after its older tile's dK.
             int next_s = 0, next_v = 0, next_k = 0;
+            // A tcgen05.commit costs this thread about as long as an MMA, time in
+            // which the tensor pipe runs dry, so commits are kept to the two the
+            // compute waits for (S^T, dP^T).  The compute frees the Q stage of
+            // its tile lu - 1 when it sees S^T of tile lu (the pipe ran that dK
+            // first); the MMA thread commits the Q stage only after a group's
+            // last dK.  A dK and the group's next S^T go out as one run.
+            auto issue_s = [&](int w, int u) {  // S^T = K Q^T into group w's region
+                const uint64_t qs =
+                    q_desc + static_cast<uint64_t>(((u % C::QS) * C::Q_BYTES) >> 4);
+#pragma unroll
+                for (int k = 0; k < C::D / 16; ++k) {
+                    const uint32_t a_off = ((k / 4) * (C::BN * 128) + (k % 4) * 32) >> 4;
+                    const uint32_t b_off = ((k / 4) * (C::BM * 128) + (k % 4) * 32) >> 4;
+                    mma_ss(tmem + C::TM_W0 + w * C::BM, k_desc + a_off, qs + b_off, IDESC_S,
+                           k > 0 ? 1u : 0u);
+                }
+                mma_commit(&s_full[w]);
+                ++next_s;
+            };
+            auto s_ready = [&](int u) {
+                return (!p.ordered || u == next_s) &&
+                       mbar_test(&q_full[u % C::QS], (u / C::QS) & 1) != 0;
+            };
             bool ok = mbar_wait(kv_full, 0, tmo, abort, &g_err_bwd);
-            uint64_t last = globaltimer();
+            bool idle = false;
+            uint64_t idle_t0 = 0;
             while (ok && remaining > 0) {
                 bool prog = false;
 #pragma unroll
@@ -686,19 +744,10 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     const int s = u % C::QS;
                     const uint32_t t_r = tmem + C::TM_W0 + w * C::BM;
                     if (st_[w] == 0) {  // S^T = K Q^T
-                        if ((p.ordered && u != next_s) || !mbar_test(&q_full[s], (u / C::QS) & 1))
-                            continue;
+                        if (!s_ready(u)) continue;
                         tc_fence_after();
-                        const uint64_t qs = q_desc + static_cast<uint64_t>((s * C::Q_BYTES) >> 4);
-#pragma unroll
-                        for (int k = 0; k < C::D / 16; ++k) {
-                            const uint32_t a_off = ((k / 4) * (C::BN * 128) + (k % 4) * 32) >> 4;
-                            const uint32_t b_off = ((k / 4) * (C::BM * 128) + (k % 4) * 32) >> 4;
-                            mma_ss(t_r, k_desc + a_off, qs + b_off, IDESC_S, k > 0 ? 1u : 0u);
-                        }
-                        mma_commit(&s_full[w]);
+                        issue_s(w, u);
                         st_[w] = 1;
-                        ++next_s;
                         prog = true;
                     } else if (st_[w] == 1) {
                         // The group has read S^T (and written P^T): dV += P^T dO,
@@ -735,8 +784,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                         st_[w] = 2;
                         prog = true;
                     } else {
-                        // The group has written dS^T: dK += dS^T Q; then the
-                        // tile's Q stage is free.
+                        // The group has written dS^T: dK += dS^T Q, then the
+                        // group's next S^T.
                         if ((p.ordered && u != next_k) || !mbar_test(&ds_full[w], lu & 1)) continue;
                         tc_fence_after();
                         const bool acc_k = next_k > 0;  // the first dK product initialises
@@ -749,25 +798,34 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                                 mma_ts(tmem + C::TM_DK, t_r + k * 8, qmn + ((k * 2048) >> 4),
                                        IDESC_DK, (acc_k || k > 0) ? 1u : 0u);
                         }
-                        mma_commit(&q_empty[s]);
-                        st_[w] = 0;
                         lu_[w] = lu + 1;
-                        if (lu + 1 >= n_of(w)) --remaining;
+                        st_[w] = 0;
+                        // no later S^T of this group frees the stage (or, with no
+                        // more stages than groups, that S^T would need it first)
+                        if (!C::RELAY_Q || lu + 1 >= n_of(w)) mma_commit(&q_empty[s]);
+                        if (lu + 1 >= n_of(w)) {
+                            --remaining;
+                        } else if (s_ready(u + C::NWG)) {
+                            issue_s(w, u + C::NWG);
+                            st_[w] = 1;
+                        }
                         prog = true;
                     }
                 }
                 if (prog) {
-                    last = globaltimer();
+                    idle = false;
                 } else if (*abort) {
                     ok = false;
-                } else if (globaltimer() - last > tmo) {
-                    *abort = 1;
-                    atomicExch(&g_err_bwd, ERR_TIMEOUT);
-                    ok = false;
                 } else {
-                    // Nothing ready: yield the issue slots to the compute warps
-                    // that share this warp's sub-partition.
-                    __nanosleep(40);
+                    const uint64_t now = globaltimer();
+                    if (!idle) {
+                        idle = true;
+                        idle_t0 = now;
+                    } else if (now - idle_t0 > tmo) {
+                        *abort = 1;
+                        atomicExch(&g_err_bwd, ERR_TIMEOUT);
+                        ok = false;
+                    }
                 }
             }
             mma_commit(done);
@@ -795,6 +853,9 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             if (!warp_wait(&s_full[wg], lu & 1, tmo, abort)) break;
             if (!warp_wait(&o_full[wg], lu & 1, tmo, abort)) break;
             tc_fence_after();
+            // S^T of this tile ran after the group's previous dK: that Q stage is free.
+            if (C::RELAY_Q && ((warp - 2) & 3) == 0 && lane == 0 && lu > 0)
+                mbar_arrive(&q_empty[(u - C::NWG) % C::QS]);
             // phase 1: P^T = exp2(S^T * scale * log2e - LSE2), masked; fp16 pairs
             uint32_t pk[C::BM / 2];
 #pragma unroll
