@@ -461,7 +461,12 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 float x[64];
                 tmem_ld64f(t_r + c * 64, x);
 #pragma unroll
-                for (int jj = 0; jj < 64; ++jj) x[jj] = ex2(fmaf(x[jj], sl2, -lse2));
+                for (int i = 0; i < 32; ++i) {  // paired fp32 FMA for the exponents
+                    const float2 t = __ffma2_rn(make_float2(x[2 * i], x[2 * i + 1]),
+                                                make_float2(sl2, sl2), make_float2(-lse2, -lse2));
+                    x[2 * i] = ex2(t.x);
+                    x[2 * i + 1] = ex2(t.y);
+                }
                 if (masked_tile) {
                     const uint32_t wa = mbits[c][0], wb = mbits[c][1];
 #pragma unroll
@@ -486,10 +491,12 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 tmem_ld64f(t_r + c * 64, dp);
                 uint32_t r[32];
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
+                for (int i = 0; i < 32; ++i) {  // paired fp32 add and multiply
                     __half2 h2 = *reinterpret_cast<__half2 *>(&pk[c * 32 + i]);
-                    const float2 pf = __half22float2(h2);
-                    r[i] = pack_bf16(pf.x * (dp[2 * i] - Drow), pf.y * (dp[2 * i + 1] - Drow));
+                    const float2 ds = __fmul2_rn(
+                        __half22float2(h2),
+                        __fadd2_rn(make_float2(dp[2 * i], dp[2 * i + 1]), make_float2(-Drow, -Drow)));
+                    r[i] = pack_bf16(ds.x, ds.y);
                 }
                 tmem_st32(t_r + c * 32, r);  // columns already read
             }
@@ -869,9 +876,11 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     need_mask ? column_row_bits(q0 + c * 64 + 32, gkey, cv, p.causal) : 0u;
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
-                    const int q = c * 64 + 2 * i;
-                    float p0 = ex2(fmaf(x[2 * i], sl2, -slse[q]));
-                    float p1 = ex2(fmaf(x[2 * i + 1], sl2, -slse[q + 1]));
+                    const float2 l2 = *reinterpret_cast<const float2 *>(slse + c * 64 + 2 * i);
+                    const float2 t = __ffma2_rn(make_float2(x[2 * i], x[2 * i + 1]),
+                                                make_float2(sl2, sl2), make_float2(-l2.x, -l2.y));
+                    float p0 = ex2(t.x);
+                    float p1 = ex2(t.y);
                     const uint32_t w = (2 * i < 32) ? mw0 : mw1;
                     if ((w >> ((2 * i) & 31)) & 1u) p0 = 0.f;
                     if ((w >> ((2 * i + 1) & 31)) & 1u) p1 = 0.f;
@@ -897,12 +906,14 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     tmem_ld64f(t_r + c * 64, dp);
                     uint32_t r[32];
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const int q = c * 64 + 2 * i;
+                    for (int i = 0; i < 32; ++i) {  // paired fp32 add and multiply
+                        const float2 dd = *reinterpret_cast<const float2 *>(sd + c * 64 + 2 * i);
                         __half2 h2 = *reinterpret_cast<__half2 *>(&pk[c * 32 + i]);
-                        const float2 pf = __half22float2(h2);
-                        r[i] = pack_bf16(pf.x * (dp[2 * i] - sd[q]),
-                                         pf.y * (dp[2 * i + 1] - sd[q + 1]));
+                        const float2 ds = __fmul2_rn(
+                            __half22float2(h2),
+                            __fadd2_rn(make_float2(dp[2 * i], dp[2 * i + 1]),
+                                       make_float2(-dd.x, -dd.y)));
+                        r[i] = pack_bf16(ds.x, ds.y);
                     }
                     tmem_st32(t_r + c * 32, r);  // columns already read
                 }
