@@ -876,7 +876,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     need_mask ? column_row_bits(q0 + c * 64 + 32, gkey, cv, p.causal) : 0u;
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
-                    const float2 l2 = *reinterpret_cast<const float2 *>(slse + c * 64 + 2 * i);
+                    const float4 l4 = *reinterpret_cast<const float4 *>(slse + c * 64 + 4 * (i / 2));
+                    const float2 l2 = (i & 1) ? make_float2(l4.z, l4.w) : make_float2(l4.x, l4.y);
                     const float2 t = __ffma2_rn(make_float2(x[2 * i], x[2 * i + 1]),
                                                 make_float2(sl2, sl2), make_float2(-l2.x, -l2.y));
                     float p0 = ex2(t.x);
@@ -907,7 +908,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     uint32_t r[32];
 #pragma unroll
                     for (int i = 0; i < 32; ++i) {  // paired fp32 add and multiply
-                        const float2 dd = *reinterpret_cast<const float2 *>(sd + c * 64 + 2 * i);
+                        const float4 d4 = *reinterpret_cast<const float4 *>(sd + c * 64 + 4 * (i / 2));
+                        const float2 dd = (i & 1) ? make_float2(d4.z, d4.w) : make_float2(d4.x, d4.y);
                         __half2 h2 = *reinterpret_cast<__half2 *>(&pk[c * 32 + i]);
                         const float2 ds = __fmul2_rn(
                             __half22float2(h2),

@@ -389,11 +389,14 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                         if ((wb >> jj) & 1u) x[32 + jj] = NEG_INF;
                     }
                 }
+                // max(m, max(a, b)) steps: one three-input max instruction each
                 float mx8[8];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) mx8[i] = x[i];
+                for (int i = 0; i < 8; ++i) mx8[i] = fmaxf(x[i], x[8 + i]);
 #pragma unroll
-                for (int jj = 8; jj < 64; ++jj) mx8[jj & 7] = fmaxf(mx8[jj & 7], x[jj]);
+                for (int jj = 16; jj < 64; jj += 16)
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) mx8[i] = fmaxf(mx8[i], fmaxf(x[jj + i], x[jj + 8 + i]));
                 const float mc = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
                                        fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) *
                                  sl2;  // log2 domain (sl2 > 0)
