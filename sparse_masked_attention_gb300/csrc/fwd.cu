@@ -371,101 +371,126 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             const uint32_t s_addr = lane_base + C::TM_S + sb * C::BN;
 
             // One pass over the tile in 64-column chunks.  Each chunk is masked
-            // (partial tiles only), its row max taken, and its P written back.
-            // The reference max m_ref moves only when a chunk exceeds it by more
-            // than 2^8; then O, the row sum and the P chunks of this tile that
-            // are already written are rescaled (rare after the first chunk).
+            // (partial tiles only) and its P written back over S.
+            // Fast path: the exponents are taken against the current reference
+            // m_ref without a row max.  It is valid when every row of the warp
+            // has a reference and no row's chunk sum exceeds 2^32: then no P,
+            // no row sum and no product with V can overflow.  Otherwise the
+            // chunk takes the reference path: its row max, and when the max
+            // grew by more than 2^8 a new reference, with O, the row sum and
+            // the P chunks of this tile already written rescaled (rare after
+            // the first chunk of a row).
             bool o_synced = false;  // PV of the group's previous tile observed
             bool failed = false;
+            const float2 sl2x2 = make_float2(sl2, sl2);
 #pragma unroll
             for (int c = 0; c < C::BN / 64; ++c) {
-                float x[64];
-                tmem_ld64f(s_addr + c * 64, x);
-                if (masked_tile) {
-                    const uint32_t wa = mbits[c][0], wb = mbits[c][1];
+                auto load_masked = [&](float (&x)[64]) {
+                    tmem_ld64f(s_addr + c * 64, x);
+                    if (masked_tile) {
+                        const uint32_t wa = mbits[c][0], wb = mbits[c][1];
 #pragma unroll
-                    for (int jj = 0; jj < 32; ++jj) {
-                        if ((wa >> jj) & 1u) x[jj] = NEG_INF;
-                        if ((wb >> jj) & 1u) x[32 + jj] = NEG_INF;
-                    }
-                }
-                // max(m, max(a, b)) steps: one three-input max instruction each
-                float mx8[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) mx8[i] = fmaxf(x[i], x[8 + i]);
-#pragma unroll
-                for (int jj = 16; jj < 64; jj += 16)
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) mx8[i] = fmaxf(mx8[i], fmaxf(x[jj + i], x[jj + 8 + i]));
-                const float mc = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                                       fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) *
-                                 sl2;  // log2 domain (sl2 > 0)
-                const bool need = (m_ref == NEG_INF) ? (mc != NEG_INF) : (mc > m_ref + 8.0f);
-                if (__any_sync(0xffffffffu, need)) {
-                    const float m_new = need ? mc : m_ref;
-                    // alpha = 0 when the row had no visible key yet (O, l, P all 0)
-                    const float alpha =
-                        need ? (m_ref == NEG_INF ? 0.f : ex2(m_ref - m_new)) : 1.0f;
-                    const bool fix = need && m_ref != NEG_INF;
-                    m_ref = m_new;
-                    l_sum *= alpha;
-                    if (__any_sync(0xffffffffu, fix)) {
-                        if (lu > 0) {
-                            if (C::NSB > 1 && !o_synced) {  // NSB = 1: S implies the P V
-                                const int pl = lu - 1;
-                                if (!warp_wait(&pv_done[wg * 2 + (pl & 1)], (pl >> 1) & 1, tmo,
-                                               abort)) {
-                                    failed = true;
-                                    break;
-                                }
-                                tc_fence_after();
-                                o_synced = true;
-                            }
-                            const uint32_t o_addr = lane_base + C::TM_O + wg * C::DV;
-#pragma unroll 1
-                            for (int oc = 0; oc < C::DV / 32; ++oc) {
-                                uint32_t r[32];
-                                tmem_ld32(o_addr + oc * 32, r);
-#pragma unroll
-                                for (int i = 0; i < 32; ++i)
-                                    r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-                                tmem_st32(o_addr + oc * 32, r);
-                            }
-                        }
-                        if (c > 0) tmem_st_wait();  // earlier chunks' P stores landed
-#pragma unroll 1
-                        for (int pc = 0; pc < c; ++pc) {  // this tile's P already written
-                            uint32_t r[32];
-                            tmem_ld32(s_addr + pc * 32, r);
-#pragma unroll
-                            for (int i = 0; i < 32; ++i) {
-                                __nv_bfloat162 h2 = *reinterpret_cast<__nv_bfloat162 *>(&r[i]);
-                                const float2 f2 = __bfloat1622float2(h2);
-                                r[i] = pack_bf16(f2.x * alpha, f2.y * alpha);
-                            }
-                            tmem_st32(s_addr + pc * 32, r);
+                        for (int jj = 0; jj < 32; ++jj) {
+                            if ((wa >> jj) & 1u) x[jj] = NEG_INF;
+                            if ((wb >> jj) & 1u) x[32 + jj] = NEG_INF;
                         }
                     }
-                }
-                const float m_use = (m_ref == NEG_INF) ? 0.0f : m_ref;
-                // Exponent arguments and partial row sums two columns at a time
-                // (paired fp32 FMA and add).
-                const float2 sl2x2 = make_float2(sl2, sl2);
-                const float2 negm = make_float2(-m_use, -m_use);
-                float2 l4[4];
+                };
+                // P = exp2(x * sl2 - m) as bf16 pairs, and the row sum of P
+                auto exp_pack = [&](const float (&x)[64], float m, uint32_t (&r)[32]) {
+                    const float2 negm = make_float2(-m, -m);
+                    float2 l4[4];
 #pragma unroll
-                for (int i = 0; i < 4; ++i) l4[i] = make_float2(0.f, 0.f);
+                    for (int i = 0; i < 4; ++i) l4[i] = make_float2(0.f, 0.f);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const float2 t =
+                            __ffma2_rn(make_float2(x[2 * i], x[2 * i + 1]), sl2x2, negm);
+                        const float2 pp = make_float2(ex2(t.x), ex2(t.y));
+                        l4[i & 3] = __fadd2_rn(l4[i & 3], pp);
+                        r[i] = pack_bf16(pp.x, pp.y);
+                    }
+                    const float2 la =
+                        __fadd2_rn(__fadd2_rn(l4[0], l4[1]), __fadd2_rn(l4[2], l4[3]));
+                    return la.x + la.y;
+                };
                 uint32_t r[32];
+                float lc = 0.f;
+                bool fast = __all_sync(0xffffffffu, m_ref != NEG_INF);
+                if (fast) {
+                    float x[64];
+                    load_masked(x);
+                    lc = exp_pack(x, m_ref, r);
+                    fast = __all_sync(0xffffffffu, lc <= 4294967296.0f);  // false for NaN
+                }
+                if (!fast) {
+                    float x[64];
+                    load_masked(x);  // S is still in TMEM: P not stored yet
+                    // max(m, max(a, b)) steps: one three-input max instruction each
+                    float mx8[8];
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const float2 t = __ffma2_rn(make_float2(x[2 * i], x[2 * i + 1]), sl2x2, negm);
-                    const float2 pp = make_float2(ex2(t.x), ex2(t.y));
-                    l4[i & 3] = __fadd2_rn(l4[i & 3], pp);
-                    r[i] = pack_bf16(pp.x, pp.y);
+                    for (int i = 0; i < 8; ++i) mx8[i] = fmaxf(x[i], x[8 + i]);
+#pragma unroll
+                    for (int jj = 16; jj < 64; jj += 16)
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            mx8[i] = fmaxf(mx8[i], fmaxf(x[jj + i], x[jj + 8 + i]));
+                    const float mc = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                                           fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) *
+                                     sl2;  // log2 domain (sl2 > 0)
+                    const bool need =
+                        (m_ref == NEG_INF) ? (mc != NEG_INF) : (mc > m_ref + 8.0f);
+                    if (__any_sync(0xffffffffu, need)) {
+                        const float m_new = need ? mc : m_ref;
+                        // alpha = 0 when the row had no visible key yet (O, l, P all 0)
+                        const float alpha =
+                            need ? (m_ref == NEG_INF ? 0.f : ex2(m_ref - m_new)) : 1.0f;
+                        const bool fix = need && m_ref != NEG_INF;
+                        m_ref = m_new;
+                        l_sum *= alpha;
+                        if (__any_sync(0xffffffffu, fix)) {
+                            if (lu > 0) {
+                                if (C::NSB > 1 && !o_synced) {  // NSB = 1: S implies the P V
+                                    const int pl = lu - 1;
+                                    if (!warp_wait(&pv_done[wg * 2 + (pl & 1)], (pl >> 1) & 1,
+                                                   tmo, abort)) {
+                                        failed = true;
+                                        break;
+                                    }
+                                    tc_fence_after();
+                                    o_synced = true;
+                                }
+                                const uint32_t o_addr = lane_base + C::TM_O + wg * C::DV;
+#pragma unroll 1
+                                for (int oc = 0; oc < C::DV / 32; ++oc) {
+                                    uint32_t ro[32];
+                                    tmem_ld32(o_addr + oc * 32, ro);
+#pragma unroll
+                                    for (int i = 0; i < 32; ++i)
+                                        ro[i] = __float_as_uint(__uint_as_float(ro[i]) * alpha);
+                                    tmem_st32(o_addr + oc * 32, ro);
+                                }
+                            }
+                            if (c > 0) tmem_st_wait();  // earlier chunks' P stores landed
+#pragma unroll 1
+                            for (int pc = 0; pc < c; ++pc) {  // this tile's P already written
+                                uint32_t rp[32];
+                                tmem_ld32(s_addr + pc * 32, rp);
+#pragma unroll
+                                for (int i = 0; i < 32; ++i) {
+                                    __nv_bfloat162 h2 =
+                                        *reinterpret_cast<__nv_bfloat162 *>(&rp[i]);
+                                    const float2 f2 = __bfloat1622float2(h2);
+                                    rp[i] = pack_bf16(f2.x * alpha, f2.y * alpha);
+                                }
+                                tmem_st32(s_addr + pc * 32, rp);
+                            }
+                        }
+                    }
+                    lc = exp_pack(x, (m_ref == NEG_INF) ? 0.0f : m_ref, r);
                 }
                 tmem_st32(s_addr + c * 32, r);
-                const float2 la = __fadd2_rn(__fadd2_rn(l4[0], l4[1]), __fadd2_rn(l4[2], l4[3]));
-                l_sum += la.x + la.y;
+                l_sum += lc;
             }
             if (failed) break;
             tmem_st_wait();
