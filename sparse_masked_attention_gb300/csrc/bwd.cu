@@ -27,6 +27,8 @@
 #include <math.h>
 #include <stdint.h>
 
+#include <type_traits>
+
 #include "fm_device.cuh"
 #include "fm_internal.h"
 
@@ -869,24 +871,34 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             for (int c = 0; c < C::BM / 64; ++c) {
                 float x[64];
                 tmem_ld64f(t_r + c * 64, x);
-                // This thread's key column: masked query rows of the chunk as bits.
-                const uint32_t mw0 =
-                    need_mask ? column_row_bits(q0 + c * 64, gkey, cv, p.causal) : 0u;
-                const uint32_t mw1 =
-                    need_mask ? column_row_bits(q0 + c * 64 + 32, gkey, cv, p.causal) : 0u;
+                // Partial tiles: this thread's key column's masked query rows of
+                // the chunk as bits, applied after the exponent (two loop copies,
+                // so that full tiles carry no selects).
+                auto exp_pack = [&](auto masked, uint32_t mw0, uint32_t mw1) {
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const float4 l4 = *reinterpret_cast<const float4 *>(slse + c * 64 + 4 * (i / 2));
-                    const float2 l2 = (i & 1) ? make_float2(l4.z, l4.w) : make_float2(l4.x, l4.y);
-                    const float2 t = __ffma2_rn(make_float2(x[2 * i], x[2 * i + 1]),
-                                                make_float2(sl2, sl2), make_float2(-l2.x, -l2.y));
-                    float p0 = ex2(t.x);
-                    float p1 = ex2(t.y);
-                    const uint32_t w = (2 * i < 32) ? mw0 : mw1;
-                    if ((w >> ((2 * i) & 31)) & 1u) p0 = 0.f;
-                    if ((w >> ((2 * i + 1) & 31)) & 1u) p1 = 0.f;
-                    pk[c * 32 + i] = pack_fp16(p0, p1);
-                }
+                    for (int i = 0; i < 32; ++i) {
+                        const float4 l4 =
+                            *reinterpret_cast<const float4 *>(slse + c * 64 + 4 * (i / 2));
+                        const float2 l2 =
+                            (i & 1) ? make_float2(l4.z, l4.w) : make_float2(l4.x, l4.y);
+                        const float2 t =
+                            __ffma2_rn(make_float2(x[2 * i], x[2 * i + 1]), make_float2(sl2, sl2),
+                                       make_float2(-l2.x, -l2.y));
+                        float p0 = ex2(t.x);
+                        float p1 = ex2(t.y);
+                        if constexpr (decltype(masked)::value) {
+                            const uint32_t w = (2 * i < 32) ? mw0 : mw1;
+                            if ((w >> ((2 * i) & 31)) & 1u) p0 = 0.f;
+                            if ((w >> ((2 * i + 1) & 31)) & 1u) p1 = 0.f;
+                        }
+                        pk[c * 32 + i] = pack_fp16(p0, p1);
+                    }
+                };
+                if (need_mask)
+                    exp_pack(std::true_type{}, column_row_bits(q0 + c * 64, gkey, cv, p.causal),
+                             column_row_bits(q0 + c * 64 + 32, gkey, cv, p.causal));
+                else
+                    exp_pack(std::false_type{}, 0u, 0u);
                 if constexpr (C::DO_DV) {
                     uint32_t r[32];
 #pragma unroll
