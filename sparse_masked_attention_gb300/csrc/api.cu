@@ -283,17 +283,18 @@ fm_status flashmask_fwd(const fm_problem *p, const fm_options *opt, const void *
         if (!x || !aligned16(x)) return FM_ERR_INVALID_ARG;
     fm_status s = prepare(p, opt, false, m, workspace, ws_bytes, &g, &ws);
     if (s != FM_OK) return s;
-    CUtensorMap tq, tk, tv;
+    CUtensorMap tq, tk, tv, to;
     const int kr = fwd_key_rows(g.d, g.dv);
     if (!encode_bnhd(&tq, q, g.B, g.N, g.H, g.d, 128) ||
         !encode_bnhd(&tk, k, g.B, g.N, g.H, g.d, kr) ||
-        !encode_bnhd(&tv, v, g.B, g.N, g.H, g.dv, kr))
+        !encode_bnhd(&tv, v, g.B, g.N, g.H, g.dv, kr) ||
+        !encode_bnhd(&to, o, g.B, g.N, g.H, g.dv, 128))
         return fail(cudaErrorInvalidValue, g_encode_detail);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     Recorder rec = recorder(opt);
     cudaError_t e = map_and_lists(g, m, ws, st, rec);
     if (e == cudaSuccess) {
-        FwdArgs a{&tq, &tk, &tv, kr, o, lse};
+        FwdArgs a{&tq, &tk, &tv, kr, &to, o, lse};
         rec.before(st);
         e = launch_fwd(g, ws, a, st);
         rec.after(st);

@@ -77,6 +77,7 @@ int fwd_key_rows(int d, int dv);
 struct FwdArgs {
     const CUtensorMap *tm_q, *tm_k, *tm_v;
     int k_rows;  // box height of tm_k / tm_v; must equal the kernel's key tile
+    const CUtensorMap *tm_o;  // O, 64-column x 128-row boxes (the output is stored by TMA)
     void *o;
     float *lse;
 };

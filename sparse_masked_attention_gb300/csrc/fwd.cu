@@ -38,7 +38,6 @@ struct FwdParams {
     const int4 *vec;
     const int *list;
     const int *cnt;
-    __nv_bfloat16 *o;
     float *lse;
     int N, H, Hm, T, Npad, causal;
     float sl2;  // scale * log2(e)
@@ -70,6 +69,7 @@ struct FwdCfg {
     static_assert(D % 64 == 0 && DV % 64 == 0 && (BN == 64 || BN == 128), "tile shape");
     static_assert(DV <= 256 && BN % 64 == 0, "MMA shape");
     static_assert(NWG * 128 * 2 * 4 <= K_BYTES, "merge statistics alias K stage 0");
+    static_assert((KS - 1) * K_BYTES >= BM * DV * 2, "output tile staging aliases K stages 1..");
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
     static_assert(KS % NWG == 0 && VS % NWG == 0, "per-group ring stages");
 };
@@ -84,7 +84,8 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, uint64
 template <class C>
 __global__ void __launch_bounds__(C::THREADS, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-               const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
+               const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+               const FwdParams p) {
     extern __shared__ __align__(1024) uint8_t smem[];
     if (smem_u32(smem) & 1023u) {  // swizzled tiles need 1024-byte alignment
         if (threadIdx.x == 0) atomicExch(&g_err_fwd, ERR_SMEM_ALIGN);
@@ -504,8 +505,6 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         // waits too.
         if (n > 0) warp_wait(mma_done, 0, tmo, abort);
         tc_fence_after();
-        __nv_bfloat16 *orow =
-            p.o + ((static_cast<size_t>(b) * p.N + grow) * p.H + h) * static_cast<size_t>(C::DV);
         const bool store = grow < p.N;
         float m_all = m_ref, l_all = l_sum, a0 = 1.f, a1 = 0.f;
         float l0 = l_sum, l1 = 0.f;
@@ -529,6 +528,11 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             c_end = c_begin + C::DV / 64;
         }
         const float inv = l_all > 0.f ? 1.0f / l_all : 0.f;
+        // The normalised bf16 row goes to shared memory in the 128B-swizzled
+        // layout of the output tensor map (64-column boxes of 128 rows; K
+        // stages 1.. are idle by now); TMA then stores whole boxes, clipping
+        // rows past N.
+        uint8_t *stage = sK + C::K_BYTES;
         for (int c = c_begin; c < c_end; ++c) {
             uint32_t r0[32];
             tmem_ld32(lane_base + C::TM_O + c * 32, r0);
@@ -542,18 +546,24 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 for (int i = 0; i < 32; ++i)
                     o[i] += l1 > 0.f ? a1 * __uint_as_float(r1[i]) : 0.f;
             }
-            if (store) {
-                uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
+            uint8_t *box_row = stage + (c / 2) * (C::BM * 128) + row * 128;
 #pragma unroll
-                for (int v = 0; v < 4; ++v) {
-                    uint4 w;
-                    w.x = pack_bf16(o[v * 8 + 0] * inv, o[v * 8 + 1] * inv);
-                    w.y = pack_bf16(o[v * 8 + 2] * inv, o[v * 8 + 3] * inv);
-                    w.z = pack_bf16(o[v * 8 + 4] * inv, o[v * 8 + 5] * inv);
-                    w.w = pack_bf16(o[v * 8 + 6] * inv, o[v * 8 + 7] * inv);
-                    dst[v] = w;
-                }
+            for (int v = 0; v < 4; ++v) {
+                uint4 w;
+                w.x = pack_bf16(o[v * 8 + 0] * inv, o[v * 8 + 1] * inv);
+                w.y = pack_bf16(o[v * 8 + 2] * inv, o[v * 8 + 3] * inv);
+                w.z = pack_bf16(o[v * 8 + 4] * inv, o[v * 8 + 5] * inv);
+                w.w = pack_bf16(o[v * 8 + 6] * inv, o[v * 8 + 7] * inv);
+                const int unit = (c % 2) * 4 + v;  // 16-byte unit of the 128-byte row
+                *reinterpret_cast<uint4 *>(box_row + ((unit ^ (row & 7)) * 16)) = w;
             }
+        }
+        fence_proxy_async_smem();              // generic stores -> visible to TMA
+        named_bar_sync(2, C::NWG * 128);       // every row of every box is staged
+        if (threadIdx.x == 64) {
+            for (int box = 0; box < C::DV / 64; ++box)
+                tma_store_4d(&tm_o, stage + box * (C::BM * 128), box * 64, h, qt * TILE, b);
+            bulk_commit_wait_read();           // shared memory read before the CTA exits
         }
         if (wg == 0 && store) {
             const float ln2 = 0.69314718055994530942f;
@@ -578,7 +588,6 @@ cudaError_t launch_cfg(const Geometry &g, const Workspace &ws, const FwdArgs &a,
     p.vec = ws.vec;
     p.list = ws.fwd_list;
     p.cnt = ws.fwd_cnt;
-    p.o = static_cast<__nv_bfloat16 *>(a.o);
     p.lse = a.lse;
     p.N = g.N;
     p.H = g.H;
@@ -594,7 +603,7 @@ cudaError_t launch_cfg(const Geometry &g, const Workspace &ws, const FwdArgs &a,
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     dim3 grid(g.T, g.H, g.B);
-    kern<<<grid, C::THREADS, C::SMEM_BYTES, st>>>(*a.tm_q, *a.tm_k, *a.tm_v, p);
+    kern<<<grid, C::THREADS, C::SMEM_BYTES, st>>>(*a.tm_q, *a.tm_k, *a.tm_v, *a.tm_o, p);
     return cudaGetLastError();
 }
 
