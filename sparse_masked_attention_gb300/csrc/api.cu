@@ -317,6 +317,7 @@ fm_status flashmask_bwd(const fm_problem *p, const fm_options *opt, const void *
     if (s != FM_OK) return s;
     CUtensorMap tq_q, tk_k, tv_k, tdo_q;  // maps for the dq kernel (query-side)
     CUtensorMap tq_k, tk_kv, tv_kv, tdo_k;  // maps for the dkdv kernel (key-side)
+    CUtensorMap tdq_o, tdk_o, tdv_o;        // the gradients, stored by TMA
     const int dq_kr = dq_key_rows(g.d, g.dv), kv_qr = dkdv_query_rows(g.d, g.dv);
     // dO and V enter the dP and dV products through their fp16 copies (made by
     // the preprocess kernel); Q and K stay bf16.
@@ -327,7 +328,10 @@ fm_status flashmask_bwd(const fm_problem *p, const fm_options *opt, const void *
         !encode_bnhd(&tq_k, q, g.B, g.N, g.H, g.d, kv_qr) ||
         !encode_bnhd(&tdo_k, ws.do16, g.B, g.N, g.H, g.dv, kv_qr, true) ||
         !encode_bnhd(&tk_kv, k, g.B, g.N, g.H, g.d, 128) ||
-        !encode_bnhd(&tv_kv, ws.v16, g.B, g.N, g.H, g.dv, 128, true))
+        !encode_bnhd(&tv_kv, ws.v16, g.B, g.N, g.H, g.dv, 128, true) ||
+        !encode_bnhd(&tdq_o, dq, g.B, g.N, g.H, g.d, 128) ||
+        !encode_bnhd(&tdk_o, dk, g.B, g.N, g.H, g.d, 128) ||
+        !encode_bnhd(&tdv_o, dv, g.B, g.N, g.H, g.dv, 128))
         return fail(cudaErrorInvalidValue, g_encode_detail);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     Recorder rec = recorder(opt);
@@ -344,6 +348,9 @@ fm_status flashmask_bwd(const fm_problem *p, const fm_options *opt, const void *
         a.tm_k_dq = &tk_k;
         a.tm_v_dq = &tv_k;
         a.tm_do_dq = &tdo_q;
+        a.tm_dq_out = &tdq_o;
+        a.tm_dk_out = &tdk_o;
+        a.tm_dv_out = &tdv_o;
         a.o = o;
         a.v = v;
         a.dout = dout;

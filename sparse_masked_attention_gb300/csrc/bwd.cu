@@ -44,9 +44,12 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, uint64
     return __all_sync(0xffffffffu, ok);
 }
 
-__device__ __forceinline__ void store_row_bf16(__nv_bfloat16 *dst, const float (&v)[32],
-                                               float mul) {
-    uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+// 32 values of a 128-row output tile (columns 32c .. 32c + 31 of row `row`),
+// times `mul`, as bf16 into the 128B-swizzled shared-memory layout of a
+// 64-column x 128-row TMA box: box c / 2, 16-byte units 4 (c % 2) .. + 3.
+__device__ __forceinline__ void stage_row_bf16(uint8_t *stage, int c, int row,
+                                               const float (&v)[32], float mul) {
+    uint8_t *box_row = stage + (c / 2) * (128 * 128) + row * 128;
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
         uint4 w;
@@ -54,7 +57,8 @@ __device__ __forceinline__ void store_row_bf16(__nv_bfloat16 *dst, const float (
         w.y = pack_bf16(v[q * 8 + 2] * mul, v[q * 8 + 3] * mul);
         w.z = pack_bf16(v[q * 8 + 4] * mul, v[q * 8 + 5] * mul);
         w.w = pack_bf16(v[q * 8 + 6] * mul, v[q * 8 + 7] * mul);
-        d4[q] = w;
+        const int unit = (c % 2) * 4 + q;
+        *reinterpret_cast<uint4 *>(box_row + ((unit ^ (row & 7)) * 16)) = w;
     }
 }
 
@@ -168,6 +172,7 @@ struct DqCfg {
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
     static_assert(BN == 64 || BN == 128, "key sub-tile");
     static_assert(KS >= NWG, "ring depth");
+    static_assert(KS * K_BYTES >= BM * D * 2, "dQ staging aliases the K ring");
     // The compute frees a K stage when it sees the group's next S; that S must
     // not need the stage itself.
     static constexpr bool RELAY_K = KS > NWG;
@@ -178,7 +183,7 @@ template <class C>
 __global__ void __launch_bounds__(C::THREADS, 1)
     dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
               const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-              const BwdParams p) {
+              const __grid_constant__ CUtensorMap tm_dq, const BwdParams p) {
     extern __shared__ __align__(1024) uint8_t smem[];
     if (smem_u32(smem) & 1023u) {  // swizzled tiles need 1024-byte alignment
         if (threadIdx.x == 0) atomicExch(&g_err_bwd, ERR_SMEM_ALIGN);
@@ -508,8 +513,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         }
         if (n > 0) warp_wait(dq_done, 0, tmo, abort);
         tc_fence_after();
-        __nv_bfloat16 *dst =
-            p.dq + ((static_cast<size_t>(b) * p.N + grow) * p.H + h) * static_cast<size_t>(C::D);
+        // dQ (scaled) to the 128B-swizzled layout of the output map in the idle
+        // K ring, then TMA stores of its 64-column boxes (rows past N clipped).
         constexpr int CPW = (C::D / 32) / C::NWG;  // 32-column chunks per group
 #pragma unroll 1
         for (int c = wg * CPW; c < (wg + 1) * CPW; ++c) {
@@ -518,7 +523,14 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             float v[32];
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] = n > 0 ? __uint_as_float(r[i]) : 0.f;
-            if (grow < p.N) store_row_bf16(dst + c * 32, v, p.scale);
+            stage_row_bf16(sK, c, row, v, p.scale);
+        }
+        fence_proxy_async_smem();
+        named_bar_sync(1, C::NWG * 128);
+        if (threadIdx.x == 64) {
+            for (int box = 0; box < C::D / 64; ++box)
+                tma_store_4d(&tm_dq, sK + box * (128 * 128), box * 64, h, qt * TILE, b);
+            bulk_commit_wait_read();
         }
     }
 
@@ -573,6 +585,9 @@ struct DkdvCfg {
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
     static_assert(D <= 256 && DV <= 256 && (BM == 64 || BM == 128), "MMA shape");
     static_assert(QS >= NWG, "ring depth");
+    static_assert(QS * Q_BYTES + NWG * DO_BYTES >=
+                      (DO_DK ? BN * D * 2 : 0) + (DO_DV ? BN * DV * 2 : 0),
+                  "dK / dV staging aliases the Q ring and the dO stages");
     // The compute frees a Q stage when it sees the group's next S^T; that S^T
     // must not need the stage itself.
     static constexpr bool RELAY_Q = QS > NWG;
@@ -582,8 +597,9 @@ struct DkdvCfg {
 template <class C>
 __global__ void __launch_bounds__(C::THREADS, 1)
     dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                const __grid_constant__ CUtensorMap tm_v,
-                const __grid_constant__ CUtensorMap tm_do, const BwdParams p) {
+                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_dv,
+                const BwdParams p) {
     extern __shared__ __align__(1024) uint8_t smem[];
     if (smem_u32(smem) & 1023u) {  // swizzled tiles need 1024-byte alignment
         if (threadIdx.x == 0) atomicExch(&g_err_bwd, ERR_SMEM_ALIGN);
@@ -938,8 +954,11 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         }
         if (n > 0) warp_wait(done, 0, tmo, abort);
         tc_fence_after();
-        const bool store = gkey < p.N;
-        const size_t rowoff = (static_cast<size_t>(b) * p.N + gkey) * p.H + h;
+        // dK (scaled) and dV to the 128B-swizzled layouts of the output maps in
+        // the idle Q ring and dO stages, then TMA stores of their 64-column
+        // boxes (rows past N clipped).
+        uint8_t *stage_dk = sQ;
+        uint8_t *stage_dv = sQ + (C::DO_DK ? C::D / 64 : 0) * (128 * 128);
         if constexpr (C::DO_DK) {
             constexpr int CPW = (C::D / 32) / C::NWG;
 #pragma unroll 1
@@ -949,7 +968,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 float v[32];
 #pragma unroll
                 for (int i = 0; i < 32; ++i) v[i] = n > 0 ? __uint_as_float(r[i]) : 0.f;
-                if (store) store_row_bf16(p.dk + rowoff * C::D + c * 32, v, p.scale);
+                stage_row_bf16(stage_dk, c, row, v, p.scale);
             }
         }
         if constexpr (C::DO_DV) {
@@ -961,8 +980,19 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 float v[32];
 #pragma unroll
                 for (int i = 0; i < 32; ++i) v[i] = n > 0 ? __uint_as_float(r[i]) : 0.f;
-                if (store) store_row_bf16(p.dv + rowoff * C::DV + c * 32, v, 1.0f);
+                stage_row_bf16(stage_dv, c, row, v, 1.0f);
             }
+        }
+        fence_proxy_async_smem();
+        named_bar_sync(1, C::NWG * 128);
+        if (threadIdx.x == 64) {
+            if constexpr (C::DO_DK)
+                for (int box = 0; box < C::D / 64; ++box)
+                    tma_store_4d(&tm_dk, stage_dk + box * (128 * 128), box * 64, h, kt * TILE, b);
+            if constexpr (C::DO_DV)
+                for (int box = 0; box < C::DV / 64; ++box)
+                    tma_store_4d(&tm_dv, stage_dv + box * (128 * 128), box * 64, h, kt * TILE, b);
+            bulk_commit_wait_read();
         }
     }
 
@@ -1007,7 +1037,8 @@ cudaError_t launch_dq(const Geometry &g, const Workspace &ws, const BwdArgs &a, 
     if (e != cudaSuccess) return e;
     dim3 grid(g.T, g.H, g.B);
     kern<<<grid, C::THREADS, C::SMEM_BYTES, st>>>(*a.tm_q_dq, *a.tm_k_dq, *a.tm_v_dq,
-                                                  *a.tm_do_dq, make_params(g, ws, a, true));
+                                                  *a.tm_do_dq, *a.tm_dq_out,
+                                                  make_params(g, ws, a, true));
     return cudaGetLastError();
 }
 
@@ -1021,6 +1052,7 @@ cudaError_t launch_dkdv(const Geometry &g, const Workspace &ws, const BwdArgs &a
     if (e != cudaSuccess) return e;
     dim3 grid(g.T, g.H, g.B);
     kern<<<grid, C::THREADS, C::SMEM_BYTES, st>>>(*a.tm_q, *a.tm_k, *a.tm_v, *a.tm_do,
+                                                  *a.tm_dk_out, *a.tm_dv_out,
                                                   make_params(g, ws, a, false));
     return cudaGetLastError();
 }

@@ -98,6 +98,8 @@ struct BwdArgs {
     const CUtensorMap *tm_q, *tm_k, *tm_v, *tm_do;
     // query-side (dQ) kernel maps: q/dO boxes of 128 rows, k/v of its key sub-tile
     const CUtensorMap *tm_q_dq, *tm_k_dq, *tm_v_dq, *tm_do_dq;
+    // outputs, 64-column x 128-row boxes (stored by TMA)
+    const CUtensorMap *tm_dq_out, *tm_dk_out, *tm_dv_out;
     const void *o, *v, *dout;
     const float *lse;
     void *dq, *dk, *dv;
