@@ -228,6 +228,15 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         mbar_init(dq_done, 1);
         *abort = 0;
         fence_barrier_init();
+        if (n > 0) {  // Q and dO before the CTA-wide barrier: latency overlaps the setup
+            mbar_arrive_expect_tx(q_full, C::Q_BYTES + C::DO_BYTES);
+#pragma unroll
+            for (int c = 0; c < C::D / 64; ++c)
+                tma_load_4d(sQ + c * C::BM * 128, &tm_q, q_full, c * 64, h, qt * TILE, b);
+#pragma unroll
+            for (int c = 0; c < C::DV / 64; ++c)
+                tma_load_4d(sDO + c * C::BM * 128, &tm_do, q_full, c * 64, h, qt * TILE, b);
+        }
     }
     if (warp == 1) {
         tmem_alloc(tmem_slot, C::TM_COLS);
@@ -243,16 +252,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
 
     if (warp == 0) {
         if (lane == 0 && n > 0) {
-            prefetch_tmap(&tm_q);
             prefetch_tmap(&tm_k);
-            prefetch_tmap(&tm_do);
-            mbar_arrive_expect_tx(q_full, C::Q_BYTES + C::DO_BYTES);
-#pragma unroll
-            for (int c = 0; c < C::D / 64; ++c)
-                tma_load_4d(sQ + c * C::BM * 128, &tm_q, q_full, c * 64, h, qt * TILE, b);
-#pragma unroll
-            for (int c = 0; c < C::DV / 64; ++c)
-                tma_load_4d(sDO + c * C::BM * 128, &tm_do, q_full, c * 64, h, qt * TILE, b);
             for (int u = 0; u < n; ++u) {
                 const int s = u % C::KS;
                 if (u >= C::KS &&
@@ -645,6 +645,17 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         mbar_init(done, 1);
         *abort = 0;
         fence_barrier_init();
+        if (n > 0) {  // K and V before the CTA-wide barrier: latency overlaps the setup
+            mbar_arrive_expect_tx(kv_full, C::K_BYTES + C::V_BYTES);
+#pragma unroll
+            for (int c = 0; c < C::D / 64; ++c)
+                tma_load_4d(sK + c * C::BN * 128, &tm_k, kv_full, c * 64, h, kt * TILE, b);
+            if constexpr (C::NEED_V) {
+#pragma unroll
+                for (int c = 0; c < C::DV / 64; ++c)
+                    tma_load_4d(sV + c * C::BN * 128, &tm_v, kv_full, c * 64, h, kt * TILE, b);
+            }
+        }
     }
     if (warp == 1) {
         tmem_alloc(tmem_slot, C::TM_COLS);
@@ -659,17 +670,6 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     if (warp == 0) {
         if (lane == 0 && n > 0) {
             prefetch_tmap(&tm_q);
-            prefetch_tmap(&tm_k);
-            mbar_arrive_expect_tx(kv_full, C::K_BYTES + C::V_BYTES);
-#pragma unroll
-            for (int c = 0; c < C::D / 64; ++c)
-                tma_load_4d(sK + c * C::BN * 128, &tm_k, kv_full, c * 64, h, kt * TILE, b);
-            if constexpr (C::NEED_V) {
-                prefetch_tmap(&tm_v);
-#pragma unroll
-                for (int c = 0; c < C::DV / 64; ++c)
-                    tma_load_4d(sV + c * C::BN * 128, &tm_v, kv_full, c * 64, h, kt * TILE, b);
-            }
             for (int u = 0; u < n; ++u) {
                 const int s = u % C::QS;
                 if (u >= C::QS &&

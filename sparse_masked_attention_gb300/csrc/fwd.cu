@@ -137,6 +137,12 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         mbar_init(mma_done, 1);
         *abort = 0;
         fence_barrier_init();
+        if (n > 0) {  // Q before the CTA-wide barrier: its latency overlaps the setup
+            mbar_arrive_expect_tx(q_full, C::Q_BYTES);
+#pragma unroll
+            for (int c = 0; c < C::D / 64; ++c)
+                tma_load_4d(sQ + c * C::BM * 128, &tm_q, q_full, c * 64, h, qt * TILE, b);
+        }
     }
     if (warp == 1) {
         tmem_alloc(tmem_slot, C::TM_COLS);
@@ -156,12 +162,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         // Two lanes, two independent rings, each filled in the order its
         // consumer drains it: lane 0 Q and K, lane 1 V.
         if (lane == 0 && n > 0) {
-            prefetch_tmap(&tm_q);
             prefetch_tmap(&tm_k);
-            mbar_arrive_expect_tx(q_full, C::Q_BYTES);
-#pragma unroll
-            for (int c = 0; c < C::D / 64; ++c)
-                tma_load_4d(sQ + c * C::BM * 128, &tm_q, q_full, c * 64, h, qt * TILE, b);
             for (int u = 0; u < n; ++u) {
                 const int s = u % C::KS;
                 if (u >= C::KS &&
