@@ -42,27 +42,30 @@ __device__ __forceinline__ bool covers(int cj, int4 c, int r0, int r1) {
     return reach >= r1;
 }
 
-__device__ __forceinline__ int block_min(int v, int *red) {
+__device__ __forceinline__ int warp_min(int v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v = min(v, __shfl_xor_sync(0xffffffffu, v, o));
-    __syncthreads();
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
-    __syncthreads();
-    return min(min(red[0], red[1]), min(red[2], red[3]));
+    return v;
 }
 
-__device__ __forceinline__ int block_max(int v, int *red) {
-    return -block_min(-v, red);
-}
-
+// Per query tile qt, one word of `state` collects the CTA's verdict:
+//   bits 0..3  column test "every column of warp w covers the tile"
+//   bits 4..7  column test "some column of warp w reaches into the tile"
+//   bit  8     the column test ran (the tile map's min/max left the tile open)
+//   bits 9..10 the class + 1, when the min/max settled the tile
+// The loop over query tiles needs no CTA barrier: warps vote on their own and
+// OR their bits in; warp 0 then reads every verdict in tile order, writes the
+// classes and compacts the ordered list of kept query tiles.
 __global__ void __launch_bounds__(128) classify_kernel(
     int N, int T, int Npad, int Hm, int causal, const int32_t *__restrict__ lts,
     const int32_t *__restrict__ lte, const int32_t *__restrict__ uts,
     const int32_t *__restrict__ ute, int4 *__restrict__ vec, uint8_t *__restrict__ cls,
     int *__restrict__ bwd_list, int *__restrict__ bwd_cnt) {
-    __shared__ int red[4];
+    extern __shared__ unsigned state[];  // [T]
+    __shared__ int red[4][8];
     const int kt = blockIdx.x;
     const int bm = blockIdx.y;  // b * Hm + hm
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int j = kt * TILE + threadIdx.x;
     const bool in_range = j < N;
     const size_t row = static_cast<size_t>(bm) * N;
@@ -77,52 +80,76 @@ __global__ void __launch_bounds__(128) classify_kernel(
         c = make_int4(0, N, 0, 0);  // padding column: masked for every row
     }
     vec[static_cast<size_t>(bm) * Npad + j] = c;
+    for (int q = threadIdx.x; q < T; q += 128) state[q] = 0u;
 
-    // Per-tile min/max over in-range columns (padding columns are neutral).
+    // Per-tile min/max over in-range columns (padding columns are neutral):
+    // warp reductions, then one exchange through shared memory.
     const int BIG = 0x7fffffff;
-    const int mn_lts = block_min(in_range ? c.x : BIG, red);
-    const int mx_lts = block_max(in_range ? c.x : -BIG, red);
-    const int mn_lte = block_min(in_range ? c.y : BIG, red);
-    const int mx_lte = block_max(in_range ? c.y : -BIG, red);
-    const int mn_uts = block_min(in_range ? c.z : BIG, red);
-    const int mx_uts = block_max(in_range ? c.z : -BIG, red);
-    const int mn_ute = block_min(in_range ? c.w : BIG, red);
-    const int mx_ute = block_max(in_range ? c.w : -BIG, red);
+    int mm[8] = {in_range ? c.x : BIG, in_range ? -c.x : BIG, in_range ? c.y : BIG,
+                 in_range ? -c.y : BIG, in_range ? c.z : BIG, in_range ? -c.z : BIG,
+                 in_range ? c.w : BIG, in_range ? -c.w : BIG};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) mm[i] = warp_min(mm[i]);
+    if (lane == 0)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) red[warp][i] = mm[i];
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < 8; ++i) mm[i] = min(min(red[0][i], red[1][i]), min(red[2][i], red[3][i]));
+    const int mn_lts = mm[0], mx_lts = -mm[1], mn_lte = mm[2], mx_lte = -mm[3];
+    const int mn_uts = mm[4], mx_uts = -mm[5], mn_ute = mm[6], mx_ute = -mm[7];
     const int j_first = kt * TILE;
     const int j_last = min(kt * TILE + TILE, N) - 1;
     const bool tail_kt = (N % TILE) != 0 && kt == T - 1;
     const int cj = causal ? j : 0;
 
-    int count = 0;
-    int *my_list = bwd_list + (static_cast<size_t>(bm) * T + kt) * T;
     for (int qt = 0; qt < T; ++qt) {
         const int r0 = qt * TILE;
         const int r1 = min(r0 + TILE, N);
-        int klass = -1;
         // All columns covered by one mechanism alone.
         if ((causal && j_first >= r1) || (mx_lts <= r0 && mn_lte >= r1) ||
             (mx_uts <= r0 && mn_ute >= r1)) {
-            klass = FM_TILE_SKIP;
+            if (threadIdx.x == 0) atomicOr(&state[qt], (FM_TILE_SKIP + 1u) << 9);
         } else if ((!causal || j_last <= r0) && (mn_lts >= r1 || mx_lte <= r0) &&
                    (mn_uts >= r1 || mx_ute <= r0)) {
             // No mechanism reaches into the tile.
-            klass = FM_TILE_UNMASKED;
+            if (threadIdx.x == 0) atomicOr(&state[qt], (FM_TILE_UNMASKED + 1u) << 9);
         } else {
             const bool col_cov = !in_range || covers(cj, c, r0, r1);
-            const bool col_touch =
-                in_range && ((causal && j > r0) || meets(c.x, c.y, r0, r1) || meets(c.z, c.w, r0, r1));
-            const int all_cov = __syncthreads_and(col_cov);
-            const int any_touch = __syncthreads_or(col_touch);
-            klass = all_cov ? FM_TILE_SKIP : (any_touch ? FM_TILE_PARTIAL : FM_TILE_UNMASKED);
+            const bool col_touch = in_range && ((causal && j > r0) || meets(c.x, c.y, r0, r1) ||
+                                                meets(c.z, c.w, r0, r1));
+            const bool all_cov = __all_sync(0xffffffffu, col_cov);
+            const bool any_touch = __any_sync(0xffffffffu, col_touch);
+            if (lane == 0)
+                atomicOr(&state[qt], (all_cov ? 1u << warp : 0u) | (any_touch ? 16u << warp : 0u) |
+                                         0x100u);
         }
-        if (threadIdx.x == 0) {
-            cls[(static_cast<size_t>(bm) * T + qt) * T + kt] = static_cast<uint8_t>(klass);
-            if (klass != FM_TILE_SKIP)
-                my_list[count] = (qt << 1) | ((klass == FM_TILE_PARTIAL || tail_kt) ? 1 : 0);
-        }
-        count += (klass != FM_TILE_SKIP);
     }
-    if (threadIdx.x == 0) bwd_cnt[static_cast<size_t>(bm) * T + kt] = count;
+    __syncthreads();
+    if (warp == 0) {
+        int *my_list = bwd_list + (static_cast<size_t>(bm) * T + kt) * T;
+        int count = 0;
+        for (int q0 = 0; q0 < T; q0 += 32) {
+            const int qt = q0 + lane;
+            int klass = FM_TILE_SKIP;
+            if (qt < T) {
+                const unsigned v = state[qt];
+                if (v & 0x100u)
+                    klass = (v & 0xfu) == 0xfu ? FM_TILE_SKIP
+                                               : ((v & 0xf0u) ? FM_TILE_PARTIAL : FM_TILE_UNMASKED);
+                else
+                    klass = static_cast<int>((v >> 9) & 3u) - 1;
+                cls[(static_cast<size_t>(bm) * T + qt) * T + kt] = static_cast<uint8_t>(klass);
+            }
+            const bool keep = qt < T && klass != FM_TILE_SKIP;
+            const unsigned ballot = __ballot_sync(0xffffffffu, keep);
+            if (keep)
+                my_list[count + __popc(ballot & ((1u << lane) - 1u))] =
+                    (qt << 1) | ((klass == FM_TILE_PARTIAL || tail_kt) ? 1 : 0);
+            count += __popc(ballot);
+        }
+        if (lane == 0) bwd_cnt[static_cast<size_t>(bm) * T + kt] = count;
+    }
 }
 
 // One warp per (mask head, q-tile): ordered list of its non-skipped k-tiles.
@@ -193,8 +220,16 @@ __global__ void __launch_bounds__(1024) count_kernel(int N, int causal,
 cudaError_t launch_classify(const Geometry &g, const MaskPtrs &m, const Workspace &ws,
                             cudaStream_t st) {
     dim3 grid(g.T, g.B * g.Hm);
-    classify_kernel<<<grid, 128, 0, st>>>(g.N, g.T, g.Npad, g.Hm, g.causal, m.lts, m.lte, m.uts,
-                                          m.ute, ws.vec, ws.cls, ws.bwd_list, ws.bwd_cnt);
+    const size_t smem = static_cast<size_t>(g.T) * sizeof(unsigned);
+    if (smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(classify_kernel,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+    }
+    classify_kernel<<<grid, 128, smem, st>>>(g.N, g.T, g.Npad, g.Hm, g.causal, m.lts, m.lte,
+                                             m.uts, m.ute, ws.vec, ws.cls, ws.bwd_list,
+                                             ws.bwd_cnt);
     return cudaGetLastError();
 }
 
