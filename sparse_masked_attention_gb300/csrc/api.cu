@@ -157,6 +157,9 @@ size_t carve_workspace(const Geometry &g, bool bwd, void *base, Workspace *ws) {
     w.fwd_cnt = static_cast<int *>(take(BM * g.T * sizeof(int)));
     w.bwd_list = static_cast<int *>(take(BM * TT * sizeof(int)));
     w.bwd_cnt = static_cast<int *>(take(BM * g.T * sizeof(int)));
+    const size_t TP = (static_cast<size_t>(g.T) + 1) / 2;
+    w.pair_list = static_cast<int *>(take(BM * TP * g.T * sizeof(int)));
+    w.pair_cnt = static_cast<int *>(take(BM * TP * sizeof(int)));
     w.lse2 = nullptr;
     w.delta = nullptr;
     w.v16 = nullptr;

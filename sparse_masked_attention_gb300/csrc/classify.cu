@@ -152,31 +152,62 @@ __global__ void __launch_bounds__(128) classify_kernel(
     }
 }
 
-// One warp per (mask head, q-tile): ordered list of its non-skipped k-tiles.
-__global__ void __launch_bounds__(128) fwd_lists_kernel(int N, int T, int rows,
+// One warp per (mask head, q-tile): ordered list of its non-skipped k-tiles;
+// then one warp per (mask head, q-tile pair): the ordered union of the pair's
+// lists, with a needs-mask bit per q-tile (a tile the q-tile skips needs it too).
+__global__ void __launch_bounds__(128) fwd_lists_kernel(int N, int T, int rows, int pair_rows,
                                                         const uint8_t *__restrict__ cls,
                                                         int *__restrict__ fwd_list,
-                                                        int *__restrict__ fwd_cnt) {
-    const int r = blockIdx.x * 4 + (threadIdx.x >> 5);  // (bm * T + qt)
+                                                        int *__restrict__ fwd_cnt,
+                                                        int *__restrict__ pair_list,
+                                                        int *__restrict__ pair_cnt) {
+    const int r = blockIdx.x * 4 + (threadIdx.x >> 5);  // (bm * T + qt), then pairs
     const int lane = threadIdx.x & 31;
-    if (r >= rows) return;
-    const uint8_t *src = cls + static_cast<size_t>(r) * T;
-    int *dst = fwd_list + static_cast<size_t>(r) * T;
     const bool has_tail = (N % TILE) != 0;
+    if (r < rows) {
+        const uint8_t *src = cls + static_cast<size_t>(r) * T;
+        int *dst = fwd_list + static_cast<size_t>(r) * T;
+        int count = 0;
+        for (int k0 = 0; k0 < T; k0 += 32) {
+            const int kt = k0 + lane;
+            const int c = kt < T ? src[kt] : FM_TILE_SKIP;
+            const bool keep = c != FM_TILE_SKIP;
+            const unsigned ballot = __ballot_sync(0xffffffffu, keep);
+            if (keep) {
+                const int pos = count + __popc(ballot & ((1u << lane) - 1u));
+                const bool need = c == FM_TILE_PARTIAL || (has_tail && kt == T - 1);
+                dst[pos] = (kt << 1) | (need ? 1 : 0);
+            }
+            count += __popc(ballot);
+        }
+        if (lane == 0) fwd_cnt[r] = count;
+        return;
+    }
+    const int pr = r - rows;  // (bm * TP + p)
+    if (pr >= pair_rows) return;
+    const int TP = (T + 1) / 2;
+    const int bm = pr / TP, pp = pr % TP;
+    const uint8_t *src_a = cls + (static_cast<size_t>(bm) * T + 2 * pp) * T;
+    const bool has_b = 2 * pp + 1 < T;
+    const uint8_t *src_b = src_a + T;
+    int *dst = pair_list + static_cast<size_t>(pr) * T;
     int count = 0;
     for (int k0 = 0; k0 < T; k0 += 32) {
         const int kt = k0 + lane;
-        const int c = kt < T ? src[kt] : FM_TILE_SKIP;
-        const bool keep = c != FM_TILE_SKIP;
+        const int ca = kt < T ? src_a[kt] : FM_TILE_SKIP;
+        const int cb = (kt < T && has_b) ? src_b[kt] : FM_TILE_SKIP;
+        const bool keep = ca != FM_TILE_SKIP || cb != FM_TILE_SKIP;
         const unsigned ballot = __ballot_sync(0xffffffffu, keep);
         if (keep) {
-            const int pos = count + __popc(ballot & ((1u << lane) - 1u));
-            const bool need = c == FM_TILE_PARTIAL || (has_tail && kt == T - 1);
-            dst[pos] = (kt << 1) | (need ? 1 : 0);
+            const bool tail = has_tail && kt == T - 1;
+            const bool need_a = ca != FM_TILE_UNMASKED || tail;
+            const bool need_b = cb != FM_TILE_UNMASKED || tail;
+            dst[count + __popc(ballot & ((1u << lane) - 1u))] =
+                (kt << 2) | (need_a ? 2 : 0) | (need_b ? 1 : 0);
         }
         count += __popc(ballot);
     }
-    if (lane == 0) fwd_cnt[r] = count;
+    if (lane == 0) pair_cnt[pr] = count;
 }
 
 // Unmasked pairs per mask head: sum over columns of N - |masked rows of j|.
@@ -235,8 +266,9 @@ cudaError_t launch_classify(const Geometry &g, const MaskPtrs &m, const Workspac
 
 cudaError_t launch_fwd_lists(const Geometry &g, const Workspace &ws, cudaStream_t st) {
     const int rows = g.B * g.Hm * g.T;
-    fwd_lists_kernel<<<(rows + 3) / 4, 128, 0, st>>>(g.N, g.T, rows, ws.cls, ws.fwd_list,
-                                                     ws.fwd_cnt);
+    const int pair_rows = g.B * g.Hm * ((g.T + 1) / 2);
+    fwd_lists_kernel<<<(rows + pair_rows + 3) / 4, 128, 0, st>>>(
+        g.N, g.T, rows, pair_rows, ws.cls, ws.fwd_list, ws.fwd_cnt, ws.pair_list, ws.pair_cnt);
     return cudaGetLastError();
 }
 

@@ -32,6 +32,11 @@ struct Workspace {
     int *fwd_cnt;      // [B*Hm][T]
     int *bwd_list;     // [B*Hm][T][T] per k-tile: (qt << 1) | needs_mask
     int *bwd_cnt;      // [B*Hm][T]
+    int *pair_list;    // [B*Hm][TP][T] per pair of q-tiles (2p, 2p+1), TP = ceil(T/2):
+                       // (kt << 2) | (needs_mask of 2p) << 1 | needs_mask of 2p+1,
+                       // every k-tile either q-tile keeps; a tile one of them skips
+                       // counts as needing the mask for it
+    int *pair_cnt;     // [B*Hm][TP]
     float *lse2;       // [B*H][Npad] log2-domain LSE, +inf for empty / padding rows
     float *delta;      // [B*H][Npad] D_i = sum_c dO_ic O_ic
     void *v16;         // [B,N,H,dv] fp16 copy of V   (backward)
