@@ -160,6 +160,7 @@ size_t carve_workspace(const Geometry &g, bool bwd, void *base, Workspace *ws) {
     const size_t TP = (static_cast<size_t>(g.T) + 1) / 2;
     w.pair_list = static_cast<int *>(take(BM * TP * g.T * sizeof(int)));
     w.pair_cnt = static_cast<int *>(take(BM * TP * sizeof(int)));
+    w.pair_order = static_cast<int *>(take(BM * TP * sizeof(int)));
     w.lse2 = nullptr;
     w.delta = nullptr;
     w.v16 = nullptr;

@@ -152,6 +152,27 @@ __global__ void __launch_bounds__(128) classify_kernel(
     }
 }
 
+// Pairs of q-tiles of one mask head by decreasing key-tile count (the union
+// of the pair's lists, from the lists kernel), ties by index: the forward
+// hands them out heaviest first.  One block per mask head.
+__global__ void __launch_bounds__(1024) pair_order_kernel(int TP, const int *__restrict__ pair_cnt,
+                                                          int *__restrict__ order) {
+    extern __shared__ int pcnt[];  // [TP]
+    const int bm = blockIdx.x;
+    for (int pp = threadIdx.x; pp < TP; pp += blockDim.x)
+        pcnt[pp] = pair_cnt[static_cast<size_t>(bm) * TP + pp];
+    __syncthreads();
+    for (int pp = threadIdx.x; pp < TP; pp += blockDim.x) {
+        const int c = pcnt[pp];
+        int rank = 0;
+        for (int k = 0; k < TP; ++k) {
+            const int ck = pcnt[k];
+            rank += (ck > c || (ck == c && k < pp)) ? 1 : 0;
+        }
+        order[static_cast<size_t>(bm) * TP + rank] = pp;
+    }
+}
+
 // One warp per (mask head, q-tile): ordered list of its non-skipped k-tiles;
 // then one warp per (mask head, q-tile pair): the ordered union of the pair's
 // lists, with a needs-mask bit per q-tile (a tile the q-tile skips needs it too).
@@ -269,6 +290,16 @@ cudaError_t launch_fwd_lists(const Geometry &g, const Workspace &ws, cudaStream_
     const int pair_rows = g.B * g.Hm * ((g.T + 1) / 2);
     fwd_lists_kernel<<<(rows + pair_rows + 3) / 4, 128, 0, st>>>(
         g.N, g.T, rows, pair_rows, ws.cls, ws.fwd_list, ws.fwd_cnt, ws.pair_list, ws.pair_cnt);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const int TP = (g.T + 1) / 2;
+    const size_t smem = static_cast<size_t>(TP) * sizeof(int);
+    if (smem > 48 * 1024) {
+        e = cudaFuncSetAttribute(pair_order_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+    }
+    pair_order_kernel<<<g.B * g.Hm, 1024, smem, st>>>(TP, ws.pair_cnt, ws.pair_order);
     return cudaGetLastError();
 }
 

@@ -37,6 +37,7 @@ struct Workspace {
                        // every k-tile either q-tile keeps; a tile one of them skips
                        // counts as needing the mask for it
     int *pair_cnt;     // [B*Hm][TP]
+    int *pair_order;   // [B*Hm][TP] pair indices by decreasing key-tile count
     float *lse2;       // [B*H][Npad] log2-domain LSE, +inf for empty / padding rows
     float *delta;      // [B*H][Npad] D_i = sum_c dO_ic O_ic
     void *v16;         // [B,N,H,dv] fp16 copy of V   (backward)

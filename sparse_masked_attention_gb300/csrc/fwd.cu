@@ -38,8 +38,9 @@ struct FwdParams {
     const int4 *vec;
     const int *list;  // per query tile, or per query-tile pair (pair kernel)
     const int *cnt;
+    const int *order;  // pair kernel: pairs by decreasing key-tile count
     float *lse;
-    int N, H, Hm, T, Npad, causal;
+    int N, H, Hm, T, B, Npad, causal;
     float sl2;  // scale * log2(e)
     uint64_t timeout_ns;
 };
@@ -607,6 +608,8 @@ cudaError_t launch_cfg(const Geometry &g, const Workspace &ws, const FwdArgs &a,
     p.vec = ws.vec;
     p.list = ws.fwd_list;
     p.cnt = ws.fwd_cnt;
+    p.order = nullptr;
+    p.B = g.B;
     p.lse = a.lse;
     p.N = g.N;
     p.H = g.H;
@@ -693,9 +696,12 @@ __global__ void __launch_bounds__(C::THREADS, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int TP = (p.T + 1) / 2;
-    const int pp = TP - 1 - static_cast<int>(blockIdx.x);  // heaviest pairs first
-    const int h = blockIdx.y, b = blockIdx.z;
+    // CTA c takes the pair of rank c / (H B) (heaviest first) of head-batch
+    // c % (H B): every head's heaviest pairs start in the first waves.
+    const int hb = static_cast<int>(blockIdx.x) % (p.H * p.B);
+    const int h = hb % p.H, b = hb / p.H;
     const int bm = b * p.Hm + (p.Hm == 1 ? 0 : h);
+    const int pp = p.order[static_cast<size_t>(bm) * TP + static_cast<int>(blockIdx.x) / (p.H * p.B)];
     const int *entries = p.list + (static_cast<size_t>(bm) * TP + pp) * p.T;
     // key tiles; none after a bounded wait gave up anywhere
     const int n = (*reinterpret_cast<volatile unsigned *>(&g_err_fwd) != 0)
@@ -968,6 +974,8 @@ cudaError_t launch_pair(const Geometry &g, const Workspace &ws, const FwdArgs &a
     p.vec = ws.vec;
     p.list = ws.pair_list;
     p.cnt = ws.pair_cnt;
+    p.order = ws.pair_order;
+    p.B = g.B;
     p.lse = a.lse;
     p.N = g.N;
     p.H = g.H;
@@ -982,8 +990,10 @@ cudaError_t launch_pair(const Geometry &g, const Workspace &ws, const FwdArgs &a
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    dim3 grid((g.T + 1) / 2, g.H, g.B);
-    kern<<<grid, C::THREADS, C::SMEM_BYTES, st>>>(*a.tm_q, *a.tm_k, *a.tm_v, *a.tm_o, p);
+    const long long ctas = static_cast<long long>((g.T + 1) / 2) * g.H * g.B;
+    if (ctas > 0x7fffffffLL) return cudaErrorInvalidValue;
+    kern<<<static_cast<unsigned>(ctas), C::THREADS, C::SMEM_BYTES, st>>>(*a.tm_q, *a.tm_k,
+                                                                        *a.tm_v, *a.tm_o, p);
     return cudaGetLastError();
 }
 
