@@ -289,8 +289,7 @@ def run_ours(args, rank, world, local_rank):
     # forward alone, same inputs (event pairs of the forward calls)
     fwd_ms = sum(avg[f"fwd:{n}"] for n in fwd_names)
     value = step_flops / (ms_step * 1e-3) / 1e12 * world
-    # one kernel per event step, except "lists": the tile lists and the pair order
-    launches = K * (len(fwd_names) + 1 + ((len(bwd_names) + 1) if has_bwd else 0))
+    launches = K * (len(fwd_names) + (len(bwd_names) if has_bwd else 0))
 
     e2e = None
     if not args.no_e2e:

@@ -69,13 +69,11 @@ typedef struct {
  * 0 selects 1 s.
  * kernel_events (optional, may be NULL): an array of n_kernel_events
  * cudaEvent_t handles owned by the caller.  The call records
- * kernel_events[2i] on `stream` just before its i-th launch step and
+ * kernel_events[2i] on `stream` just before its i-th kernel launch and
  * kernel_events[2i+1] just after it.  Events beyond the array are skipped.
- * Step order: fwd = classify, lists, attention; bwd = classify, lists,
+ * Kernel order: fwd = classify, lists, attention; bwd = classify, lists,
  * preprocess, key-side gradient (twice when d = dv = 256), query-side gradient.
- * Every step is one kernel launch except lists, which is two (the tile lists,
- * then the order of the query-tile pairs).  A NULL options pointer selects all
- * defaults. */
+ * A NULL options pointer selects all defaults. */
 typedef struct {
     int deterministic;
     int debug_bounds;

@@ -152,38 +152,52 @@ __global__ void __launch_bounds__(128) classify_kernel(
     }
 }
 
-// Pairs of q-tiles of one mask head by decreasing key-tile count (the union
-// of the pair's lists, from the lists kernel), ties by index: the forward
-// hands them out heaviest first.  One block per mask head.
-__global__ void __launch_bounds__(1024) pair_order_kernel(int TP, const int *__restrict__ pair_cnt,
-                                                          int *__restrict__ order) {
-    extern __shared__ int pcnt[];  // [TP]
-    const int bm = blockIdx.x;
-    for (int pp = threadIdx.x; pp < TP; pp += blockDim.x)
-        pcnt[pp] = pair_cnt[static_cast<size_t>(bm) * TP + pp];
-    __syncthreads();
-    for (int pp = threadIdx.x; pp < TP; pp += blockDim.x) {
-        const int c = pcnt[pp];
-        int rank = 0;
-        for (int k = 0; k < TP; ++k) {
-            const int ck = pcnt[k];
-            rank += (ck > c || (ck == c && k < pp)) ? 1 : 0;
+// One launch, 1024-thread blocks, three jobs:
+// - one warp per (mask head, q-tile): the ordered list of its non-skipped
+//   k-tiles;
+// - one warp per (mask head, q-tile pair): the ordered union of the pair's
+//   lists, with a needs-mask bit per q-tile (a tile the q-tile skips needs it
+//   too);
+// - one block per mask head, after the list blocks: the pairs by decreasing
+//   length of that union, ties by index (the forward hands them out heaviest
+//   first).  Its warps count the union lengths from the tile map themselves,
+//   so the job needs no other block's output.
+__global__ void __launch_bounds__(1024) fwd_lists_kernel(int N, int T, int rows, int pair_rows,
+                                                         int list_blocks,
+                                                         const uint8_t *__restrict__ cls,
+                                                         int *__restrict__ fwd_list,
+                                                         int *__restrict__ fwd_cnt,
+                                                         int *__restrict__ pair_list,
+                                                         int *__restrict__ pair_cnt,
+                                                         int *__restrict__ pair_order) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int TP = (T + 1) / 2;
+    if (static_cast<int>(blockIdx.x) >= list_blocks) {
+        extern __shared__ int pcnt[];  // [TP]
+        const int bm = blockIdx.x - list_blocks;
+        for (int pp = warp; pp < TP; pp += 32) {  // a warp per pair, lanes over kt
+            const uint8_t *a = cls + (static_cast<size_t>(bm) * T + 2 * pp) * T;
+            const bool has_b = 2 * pp + 1 < T;
+            int c = 0;
+            for (int kt = lane; kt < T; kt += 32)
+                c += (a[kt] != FM_TILE_SKIP || (has_b && a[T + kt] != FM_TILE_SKIP)) ? 1 : 0;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
+            if (lane == 0) pcnt[pp] = c;
         }
-        order[static_cast<size_t>(bm) * TP + rank] = pp;
+        __syncthreads();
+        for (int pp = threadIdx.x; pp < TP; pp += blockDim.x) {
+            const int c = pcnt[pp];
+            int rank = 0;
+            for (int k = 0; k < TP; ++k) {
+                const int ck = pcnt[k];
+                rank += (ck > c || (ck == c && k < pp)) ? 1 : 0;
+            }
+            pair_order[static_cast<size_t>(bm) * TP + rank] = pp;
+        }
+        return;
     }
-}
-
-// One warp per (mask head, q-tile): ordered list of its non-skipped k-tiles;
-// then one warp per (mask head, q-tile pair): the ordered union of the pair's
-// lists, with a needs-mask bit per q-tile (a tile the q-tile skips needs it too).
-__global__ void __launch_bounds__(128) fwd_lists_kernel(int N, int T, int rows, int pair_rows,
-                                                        const uint8_t *__restrict__ cls,
-                                                        int *__restrict__ fwd_list,
-                                                        int *__restrict__ fwd_cnt,
-                                                        int *__restrict__ pair_list,
-                                                        int *__restrict__ pair_cnt) {
-    const int r = blockIdx.x * 4 + (threadIdx.x >> 5);  // (bm * T + qt), then pairs
-    const int lane = threadIdx.x & 31;
+    const int r = blockIdx.x * 32 + warp;  // (bm * T + qt), then pairs
     const bool has_tail = (N % TILE) != 0;
     if (r < rows) {
         const uint8_t *src = cls + static_cast<size_t>(r) * T;
@@ -206,7 +220,6 @@ __global__ void __launch_bounds__(128) fwd_lists_kernel(int N, int T, int rows, 
     }
     const int pr = r - rows;  // (bm * TP + p)
     if (pr >= pair_rows) return;
-    const int TP = (T + 1) / 2;
     const int bm = pr / TP, pp = pr % TP;
     const uint8_t *src_a = cls + (static_cast<size_t>(bm) * T + 2 * pp) * T;
     const bool has_b = 2 * pp + 1 < T;
@@ -288,18 +301,17 @@ cudaError_t launch_classify(const Geometry &g, const MaskPtrs &m, const Workspac
 cudaError_t launch_fwd_lists(const Geometry &g, const Workspace &ws, cudaStream_t st) {
     const int rows = g.B * g.Hm * g.T;
     const int pair_rows = g.B * g.Hm * ((g.T + 1) / 2);
-    fwd_lists_kernel<<<(rows + pair_rows + 3) / 4, 128, 0, st>>>(
-        g.N, g.T, rows, pair_rows, ws.cls, ws.fwd_list, ws.fwd_cnt, ws.pair_list, ws.pair_cnt);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    const int TP = (g.T + 1) / 2;
-    const size_t smem = static_cast<size_t>(TP) * sizeof(int);
+    const int list_blocks = (rows + pair_rows + 31) / 32;
+    const size_t smem = static_cast<size_t>((g.T + 1) / 2) * sizeof(int);
     if (smem > 48 * 1024) {
-        e = cudaFuncSetAttribute(pair_order_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(smem));
+        cudaError_t e = cudaFuncSetAttribute(fwd_lists_kernel,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(smem));
         if (e != cudaSuccess) return e;
     }
-    pair_order_kernel<<<g.B * g.Hm, 1024, smem, st>>>(TP, ws.pair_cnt, ws.pair_order);
+    fwd_lists_kernel<<<list_blocks + g.B * g.Hm, 1024, smem, st>>>(
+        g.N, g.T, rows, pair_rows, list_blocks, ws.cls, ws.fwd_list, ws.fwd_cnt, ws.pair_list,
+        ws.pair_cnt, ws.pair_order);
     return cudaGetLastError();
 }
 
