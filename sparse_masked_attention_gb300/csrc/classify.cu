@@ -42,29 +42,32 @@ __device__ __forceinline__ bool covers(int cj, int4 c, int r0, int r1) {
     return reach >= r1;
 }
 
+constexpr int kClassifyChunk = 32;  // query tiles per classify CTA
+
 __device__ __forceinline__ int warp_min(int v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v = min(v, __shfl_xor_sync(0xffffffffu, v, o));
     return v;
 }
 
+// One CTA per (key tile, chunk of kClassifyChunk query tiles, mask head).
 // Per query tile qt, one word of `state` collects the CTA's verdict:
 //   bits 0..3  column test "every column of warp w covers the tile"
 //   bits 4..7  column test "some column of warp w reaches into the tile"
 //   bit  8     the column test ran (the tile map's min/max left the tile open)
 //   bits 9..10 the class + 1, when the min/max settled the tile
 // The loop over query tiles needs no CTA barrier: warps vote on their own and
-// OR their bits in; warp 0 then reads every verdict in tile order, writes the
-// classes and compacts the ordered list of kept query tiles.
+// OR their bits in; after one barrier the classes are written.
 __global__ void __launch_bounds__(128) classify_kernel(
     int N, int T, int Npad, int Hm, int causal, const int32_t *__restrict__ lts,
     const int32_t *__restrict__ lte, const int32_t *__restrict__ uts,
-    const int32_t *__restrict__ ute, int4 *__restrict__ vec, uint8_t *__restrict__ cls,
-    int *__restrict__ bwd_list, int *__restrict__ bwd_cnt) {
-    extern __shared__ unsigned state[];  // [T]
+    const int32_t *__restrict__ ute, int4 *__restrict__ vec, uint8_t *__restrict__ cls) {
+    __shared__ unsigned state[kClassifyChunk];
     __shared__ int red[4][8];
     const int kt = blockIdx.x;
-    const int bm = blockIdx.y;  // b * Hm + hm
+    const int q_begin = blockIdx.y * kClassifyChunk;
+    const int q_end = min(T, q_begin + kClassifyChunk);
+    const int bm = blockIdx.z;  // b * Hm + hm
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int j = kt * TILE + threadIdx.x;
     const bool in_range = j < N;
@@ -79,8 +82,8 @@ __global__ void __launch_bounds__(128) classify_kernel(
     } else {
         c = make_int4(0, N, 0, 0);  // padding column: masked for every row
     }
-    vec[static_cast<size_t>(bm) * Npad + j] = c;
-    for (int q = threadIdx.x; q < T; q += 128) state[q] = 0u;
+    if (blockIdx.y == 0) vec[static_cast<size_t>(bm) * Npad + j] = c;
+    for (int q = threadIdx.x; q < kClassifyChunk; q += 128) state[q] = 0u;
 
     // Per-tile min/max over in-range columns (padding columns are neutral):
     // warp reductions, then one exchange through shared memory.
@@ -100,20 +103,19 @@ __global__ void __launch_bounds__(128) classify_kernel(
     const int mn_uts = mm[4], mx_uts = -mm[5], mn_ute = mm[6], mx_ute = -mm[7];
     const int j_first = kt * TILE;
     const int j_last = min(kt * TILE + TILE, N) - 1;
-    const bool tail_kt = (N % TILE) != 0 && kt == T - 1;
     const int cj = causal ? j : 0;
 
-    for (int qt = 0; qt < T; ++qt) {
+    for (int qt = q_begin; qt < q_end; ++qt) {
         const int r0 = qt * TILE;
         const int r1 = min(r0 + TILE, N);
         // All columns covered by one mechanism alone.
         if ((causal && j_first >= r1) || (mx_lts <= r0 && mn_lte >= r1) ||
             (mx_uts <= r0 && mn_ute >= r1)) {
-            if (threadIdx.x == 0) atomicOr(&state[qt], (FM_TILE_SKIP + 1u) << 9);
+            if (threadIdx.x == 0) atomicOr(&state[qt - q_begin], (FM_TILE_SKIP + 1u) << 9);
         } else if ((!causal || j_last <= r0) && (mn_lts >= r1 || mx_lte <= r0) &&
                    (mn_uts >= r1 || mx_ute <= r0)) {
             // No mechanism reaches into the tile.
-            if (threadIdx.x == 0) atomicOr(&state[qt], (FM_TILE_UNMASKED + 1u) << 9);
+            if (threadIdx.x == 0) atomicOr(&state[qt - q_begin], (FM_TILE_UNMASKED + 1u) << 9);
         } else {
             const bool col_cov = !in_range || covers(cj, c, r0, r1);
             const bool col_touch = in_range && ((causal && j > r0) || meets(c.x, c.y, r0, r1) ||
@@ -121,40 +123,28 @@ __global__ void __launch_bounds__(128) classify_kernel(
             const bool all_cov = __all_sync(0xffffffffu, col_cov);
             const bool any_touch = __any_sync(0xffffffffu, col_touch);
             if (lane == 0)
-                atomicOr(&state[qt], (all_cov ? 1u << warp : 0u) | (any_touch ? 16u << warp : 0u) |
-                                         0x100u);
+                atomicOr(&state[qt - q_begin], (all_cov ? 1u << warp : 0u) |
+                                                   (any_touch ? 16u << warp : 0u) | 0x100u);
         }
     }
     __syncthreads();
-    if (warp == 0) {
-        int *my_list = bwd_list + (static_cast<size_t>(bm) * T + kt) * T;
-        int count = 0;
-        for (int q0 = 0; q0 < T; q0 += 32) {
-            const int qt = q0 + lane;
-            int klass = FM_TILE_SKIP;
-            if (qt < T) {
-                const unsigned v = state[qt];
-                if (v & 0x100u)
-                    klass = (v & 0xfu) == 0xfu ? FM_TILE_SKIP
-                                               : ((v & 0xf0u) ? FM_TILE_PARTIAL : FM_TILE_UNMASKED);
-                else
-                    klass = static_cast<int>((v >> 9) & 3u) - 1;
-                cls[(static_cast<size_t>(bm) * T + qt) * T + kt] = static_cast<uint8_t>(klass);
-            }
-            const bool keep = qt < T && klass != FM_TILE_SKIP;
-            const unsigned ballot = __ballot_sync(0xffffffffu, keep);
-            if (keep)
-                my_list[count + __popc(ballot & ((1u << lane) - 1u))] =
-                    (qt << 1) | ((klass == FM_TILE_PARTIAL || tail_kt) ? 1 : 0);
-            count += __popc(ballot);
-        }
-        if (lane == 0) bwd_cnt[static_cast<size_t>(bm) * T + kt] = count;
+    for (int qt = q_begin + threadIdx.x; qt < q_end; qt += 128) {
+        const unsigned v = state[qt - q_begin];
+        int klass;
+        if (v & 0x100u)
+            klass = (v & 0xfu) == 0xfu ? FM_TILE_SKIP
+                                       : ((v & 0xf0u) ? FM_TILE_PARTIAL : FM_TILE_UNMASKED);
+        else
+            klass = static_cast<int>((v >> 9) & 3u) - 1;
+        cls[(static_cast<size_t>(bm) * T + qt) * T + kt] = static_cast<uint8_t>(klass);
     }
 }
 
-// One launch, 1024-thread blocks, three jobs:
+// One launch, 1024-thread blocks, four jobs:
 // - one warp per (mask head, q-tile): the ordered list of its non-skipped
 //   k-tiles;
+// - one warp per (mask head, k-tile): the ordered list of its non-skipped
+//   q-tiles (the key-side backward);
 // - one warp per (mask head, q-tile pair): the ordered union of the pair's
 //   lists, with a needs-mask bit per q-tile (a tile the q-tile skips needs it
 //   too);
@@ -167,6 +157,8 @@ __global__ void __launch_bounds__(1024) fwd_lists_kernel(int N, int T, int rows,
                                                          const uint8_t *__restrict__ cls,
                                                          int *__restrict__ fwd_list,
                                                          int *__restrict__ fwd_cnt,
+                                                         int *__restrict__ bwd_list,
+                                                         int *__restrict__ bwd_cnt,
                                                          int *__restrict__ pair_list,
                                                          int *__restrict__ pair_cnt,
                                                          int *__restrict__ pair_order) {
@@ -218,7 +210,27 @@ __global__ void __launch_bounds__(1024) fwd_lists_kernel(int N, int T, int rows,
         if (lane == 0) fwd_cnt[r] = count;
         return;
     }
-    const int pr = r - rows;  // (bm * TP + p)
+    if (r < 2 * rows) {  // (bm * T + kt): the column kt of the map, over qt
+        const int kr = r - rows;
+        const int bm = kr / T, kt = kr % T;
+        const uint8_t *src = cls + static_cast<size_t>(bm) * T * T + kt;
+        int *dst = bwd_list + static_cast<size_t>(kr) * T;
+        const bool tail_kt = has_tail && kt == T - 1;
+        int count = 0;
+        for (int q0 = 0; q0 < T; q0 += 32) {
+            const int qt = q0 + lane;
+            const int c = qt < T ? src[static_cast<size_t>(qt) * T] : FM_TILE_SKIP;
+            const bool keep = c != FM_TILE_SKIP;
+            const unsigned ballot = __ballot_sync(0xffffffffu, keep);
+            if (keep)
+                dst[count + __popc(ballot & ((1u << lane) - 1u))] =
+                    (qt << 1) | ((c == FM_TILE_PARTIAL || tail_kt) ? 1 : 0);
+            count += __popc(ballot);
+        }
+        if (lane == 0) bwd_cnt[kr] = count;
+        return;
+    }
+    const int pr = r - 2 * rows;  // (bm * TP + p)
     if (pr >= pair_rows) return;
     const int bm = pr / TP, pp = pr % TP;
     const uint8_t *src_a = cls + (static_cast<size_t>(bm) * T + 2 * pp) * T;
@@ -284,24 +296,16 @@ __global__ void __launch_bounds__(1024) count_kernel(int N, int causal,
 
 cudaError_t launch_classify(const Geometry &g, const MaskPtrs &m, const Workspace &ws,
                             cudaStream_t st) {
-    dim3 grid(g.T, g.B * g.Hm);
-    const size_t smem = static_cast<size_t>(g.T) * sizeof(unsigned);
-    if (smem > 48 * 1024) {
-        cudaError_t e = cudaFuncSetAttribute(classify_kernel,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(smem));
-        if (e != cudaSuccess) return e;
-    }
-    classify_kernel<<<grid, 128, smem, st>>>(g.N, g.T, g.Npad, g.Hm, g.causal, m.lts, m.lte,
-                                             m.uts, m.ute, ws.vec, ws.cls, ws.bwd_list,
-                                             ws.bwd_cnt);
+    dim3 grid(g.T, (g.T + kClassifyChunk - 1) / kClassifyChunk, g.B * g.Hm);
+    classify_kernel<<<grid, 128, 0, st>>>(g.N, g.T, g.Npad, g.Hm, g.causal, m.lts, m.lte, m.uts,
+                                          m.ute, ws.vec, ws.cls);
     return cudaGetLastError();
 }
 
 cudaError_t launch_fwd_lists(const Geometry &g, const Workspace &ws, cudaStream_t st) {
     const int rows = g.B * g.Hm * g.T;
     const int pair_rows = g.B * g.Hm * ((g.T + 1) / 2);
-    const int list_blocks = (rows + pair_rows + 31) / 32;
+    const int list_blocks = (2 * rows + pair_rows + 31) / 32;
     const size_t smem = static_cast<size_t>((g.T + 1) / 2) * sizeof(int);
     if (smem > 48 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(fwd_lists_kernel,
@@ -310,8 +314,8 @@ cudaError_t launch_fwd_lists(const Geometry &g, const Workspace &ws, cudaStream_
         if (e != cudaSuccess) return e;
     }
     fwd_lists_kernel<<<list_blocks + g.B * g.Hm, 1024, smem, st>>>(
-        g.N, g.T, rows, pair_rows, list_blocks, ws.cls, ws.fwd_list, ws.fwd_cnt, ws.pair_list,
-        ws.pair_cnt, ws.pair_order);
+        g.N, g.T, rows, pair_rows, list_blocks, ws.cls, ws.fwd_list, ws.fwd_cnt, ws.bwd_list,
+        ws.bwd_cnt, ws.pair_list, ws.pair_cnt, ws.pair_order);
     return cudaGetLastError();
 }
 
