@@ -2,25 +2,26 @@
 //
 //   O = softmax(Q K^T * scale + M) V        (FlashMask README, "Formulation")
 //
-// One CTA owns one 128-row query tile of one (batch, head).  It walks only
-// the key tiles the tile map kept for that query tile ("skip unnecessary
-// computation", FlashMask abstract).  Roles, by warp:
+// Only the key tiles the tile map kept are walked ("skip unnecessary
+// computation", FlashMask abstract).  Two kernels:
+// - fwd_pair_kernel (d <= 128): one CTA per pair of 128-row query tiles of
+//   one (batch, head); softmax group g owns query tile 2p + g, and both groups
+//   walk the union of the two tiles' key-tile lists, so K / V are loaded once.
+// - fwd_kernel (larger heads): one CTA per query tile; with two groups they
+//   take alternate key tiles of that tile and merge their halves at the end.
+// Roles, by warp:
 //   warp 0      TMA producers: lane 0 Q and the K ring, lane 1 the V ring
 //   warp 1      allocates TMEM; lane 0 issues every tcgen05.mma
-//   warps 2..   NWG softmax warpgroups.  Thread t of a group owns query row t,
+//   warps 2..   softmax warpgroups.  Thread t of a group owns query row t,
 //               which is TMEM lane t.
-// With NWG = 2, the two groups take alternate key tiles of the same query
-// tile.  Each group keeps its own running max, running sum and O accumulator
-// in TMEM.  The two halves are merged in the epilogue.  While one group runs
-// exp2 on its S tile, the tensor core works on the other group's tiles.
+// While one group runs its softmax, the tensor core works on the other's tiles.
 //
-// Per key tile u, owned by group w:
-//   S_w  = Q K_u^T                (SS MMA, fp32 in TMEM)
+// Per key tile, group g:
+//   S_g  = Q K^T                  (SS MMA, fp32 in TMEM)
 //   softmax thread: S -> registers; apply the mask elementwise on partial
 //   tiles only; online max/sum in the log2 domain with exp2; P -> TMEM as
-//   bf16, in place of S; the O_w rescale is deferred until the max has grown
-//   by more than 2^8
-//   O_w += P V_u                  (TS MMA: P read from TMEM, V from smem)
+//   bf16, in place of S (softmax_tile)
+//   O_g += P V                    (TS MMA: P read from TMEM, V from smem)
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
