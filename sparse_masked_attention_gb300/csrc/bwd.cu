@@ -84,6 +84,8 @@ __global__ void __launch_bounds__(256) preprocess_kernel(
     const __nv_bfloat16 *__restrict__ dout, const __nv_bfloat16 *__restrict__ v,
     const float *__restrict__ lse, float *__restrict__ lse2, float *__restrict__ delta,
     uint4 *__restrict__ v16, uint4 *__restrict__ do16) {
+    pdl_wait();  // orders it after the kernels before (it rewrites their inputs' copies)
+    pdl_trigger();
     const int r0 = blockIdx.x * 16 + (threadIdx.x >> 4);  // over B*H*Npad
     const int t = threadIdx.x & 15;
     const bool valid = r0 < rows_total;
@@ -185,8 +187,14 @@ __global__ void __launch_bounds__(C::THREADS, 1)
               const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
               const __grid_constant__ CUtensorMap tm_dq, const BwdParams p) {
     extern __shared__ __align__(1024) uint8_t smem[];
+    // Launched behind the key-side kernel, which it does not depend on: it can
+    // start only once every key-side CTA has passed its own pdl_wait(), so the
+    // lists, LSE2, D and the fp16 copies are complete.  It waits for the
+    // key-side grid before it exits, so that its completion implies both.
+    pdl_trigger();
     if (smem_u32(smem) & 1023u) {  // swizzled tiles need 1024-byte alignment
         if (threadIdx.x == 0) atomicExch(&g_err_bwd, ERR_SMEM_ALIGN);
+        pdl_wait();
         return;
     }
     uint8_t *sQ = smem + C::OFF_Q, *sDO = smem + C::OFF_DO;
@@ -541,6 +549,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         tc_fence_after();
         tmem_dealloc(tmem, C::TM_COLS);
     }
+    pdl_wait();
 }
 
 // ---------------------------------------------------------------- dkdv kernel
@@ -601,6 +610,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_dv,
                 const BwdParams p) {
     extern __shared__ __align__(1024) uint8_t smem[];
+    pdl_wait();  // lists, LSE2, D and the fp16 copies of the kernels before
+    pdl_trigger();
     if (smem_u32(smem) & 1023u) {  // swizzled tiles need 1024-byte alignment
         if (threadIdx.x == 0) atomicExch(&g_err_bwd, ERR_SMEM_ALIGN);
         return;
@@ -1035,11 +1046,9 @@ cudaError_t launch_dq(const Geometry &g, const Workspace &ws, const BwdArgs &a, 
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    dim3 grid(g.T, g.H, g.B);
-    kern<<<grid, C::THREADS, C::SMEM_BYTES, st>>>(*a.tm_q_dq, *a.tm_k_dq, *a.tm_v_dq,
-                                                  *a.tm_do_dq, *a.tm_dq_out,
-                                                  make_params(g, ws, a, true));
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(g.T, g.H, g.B), dim3(C::THREADS), C::SMEM_BYTES, st,
+                      *a.tm_q_dq, *a.tm_k_dq, *a.tm_v_dq, *a.tm_do_dq, *a.tm_dq_out,
+                      make_params(g, ws, a, true));
 }
 
 template <class C>
@@ -1050,11 +1059,9 @@ cudaError_t launch_dkdv(const Geometry &g, const Workspace &ws, const BwdArgs &a
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    dim3 grid(g.T, g.H, g.B);
-    kern<<<grid, C::THREADS, C::SMEM_BYTES, st>>>(*a.tm_q, *a.tm_k, *a.tm_v, *a.tm_do,
-                                                  *a.tm_dk_out, *a.tm_dv_out,
-                                                  make_params(g, ws, a, false));
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(g.T, g.H, g.B), dim3(C::THREADS), C::SMEM_BYTES, st, *a.tm_q,
+                      *a.tm_k, *a.tm_v, *a.tm_do, *a.tm_dk_out, *a.tm_dv_out,
+                      make_params(g, ws, a, false));
 }
 
 template <class KV, class DQ>
@@ -1081,12 +1088,13 @@ cudaError_t launch_bwd(const Geometry &g, const Workspace &ws, const BwdArgs &a,
                        cudaStream_t st, Recorder &rec) {
     const int rows_total = g.B * g.H * g.Npad;
     rec.before(st);
-    preprocess_kernel<<<(rows_total + 15) / 16, 256, 0, st>>>(
-        g.N, g.H, g.dv, g.Npad, rows_total, static_cast<const __nv_bfloat16 *>(a.o),
+    cudaError_t e = launch_pdl(
+        preprocess_kernel, dim3((rows_total + 15) / 16), dim3(256), 0, st, g.N, g.H, g.dv, g.Npad,
+        rows_total, static_cast<const __nv_bfloat16 *>(a.o),
         static_cast<const __nv_bfloat16 *>(a.dout), static_cast<const __nv_bfloat16 *>(a.v),
-        a.lse, ws.lse2, ws.delta, static_cast<uint4 *>(ws.v16), static_cast<uint4 *>(ws.do16));
+        static_cast<const float *>(a.lse), ws.lse2, ws.delta, static_cast<uint4 *>(ws.v16),
+        static_cast<uint4 *>(ws.do16));
     rec.after(st);
-    cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     // DkdvCfg<d, dv, query sub-tile, Q stages, dK, dV, groups>;
     // DqCfg<d, dv, key sub-tile, K stages, groups>

@@ -64,6 +64,8 @@ __global__ void __launch_bounds__(128) classify_kernel(
     const int32_t *__restrict__ ute, int4 *__restrict__ vec, uint8_t *__restrict__ cls) {
     __shared__ unsigned state[kClassifyChunk];
     __shared__ int red[4][8];
+    pdl_wait();  // the vectors and the workspace belong to earlier stream work
+    pdl_trigger();
     const int kt = blockIdx.x;
     const int q_begin = blockIdx.y * kClassifyChunk;
     const int q_end = min(T, q_begin + kClassifyChunk);
@@ -162,6 +164,8 @@ __global__ void __launch_bounds__(1024) fwd_lists_kernel(int N, int T, int rows,
                                                          int *__restrict__ pair_list,
                                                          int *__restrict__ pair_cnt,
                                                          int *__restrict__ pair_order) {
+    pdl_wait();  // the tile map of the kernel before
+    pdl_trigger();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int TP = (T + 1) / 2;
     if (static_cast<int>(blockIdx.x) >= list_blocks) {
@@ -297,9 +301,8 @@ __global__ void __launch_bounds__(1024) count_kernel(int N, int causal,
 cudaError_t launch_classify(const Geometry &g, const MaskPtrs &m, const Workspace &ws,
                             cudaStream_t st) {
     dim3 grid(g.T, (g.T + kClassifyChunk - 1) / kClassifyChunk, g.B * g.Hm);
-    classify_kernel<<<grid, 128, 0, st>>>(g.N, g.T, g.Npad, g.Hm, g.causal, m.lts, m.lte, m.uts,
-                                          m.ute, ws.vec, ws.cls);
-    return cudaGetLastError();
+    return launch_pdl(classify_kernel, grid, dim3(128), 0, st, g.N, g.T, g.Npad, g.Hm, g.causal,
+                      m.lts, m.lte, m.uts, m.ute, ws.vec, ws.cls);
 }
 
 cudaError_t launch_fwd_lists(const Geometry &g, const Workspace &ws, cudaStream_t st) {
@@ -313,10 +316,10 @@ cudaError_t launch_fwd_lists(const Geometry &g, const Workspace &ws, cudaStream_
                                              static_cast<int>(smem));
         if (e != cudaSuccess) return e;
     }
-    fwd_lists_kernel<<<list_blocks + g.B * g.Hm, 1024, smem, st>>>(
-        g.N, g.T, rows, pair_rows, list_blocks, ws.cls, ws.fwd_list, ws.fwd_cnt, ws.bwd_list,
-        ws.bwd_cnt, ws.pair_list, ws.pair_cnt, ws.pair_order);
-    return cudaGetLastError();
+    return launch_pdl(fwd_lists_kernel, dim3(list_blocks + g.B * g.Hm), dim3(1024), smem, st,
+                      g.N, g.T, rows, pair_rows, list_blocks,
+                      static_cast<const uint8_t *>(ws.cls), ws.fwd_list, ws.fwd_cnt, ws.bwd_list,
+                      ws.bwd_cnt, ws.pair_list, ws.pair_cnt, ws.pair_order);
 }
 
 cudaError_t launch_count(const Geometry &g, const MaskPtrs &m, unsigned long long *counts,

@@ -234,6 +234,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                const FwdParams p) {
     extern __shared__ __align__(1024) uint8_t smem[];
+    pdl_wait();  // tile lists of the kernel before
+    pdl_trigger();
     if (smem_u32(smem) & 1023u) {  // swizzled tiles need 1024-byte alignment
         if (threadIdx.x == 0) atomicExch(&g_err_fwd, ERR_SMEM_ALIGN);
         return;
@@ -625,9 +627,8 @@ cudaError_t launch_cfg(const Geometry &g, const Workspace &ws, const FwdArgs &a,
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    dim3 grid(g.T, g.H, g.B);
-    kern<<<grid, C::THREADS, C::SMEM_BYTES, st>>>(*a.tm_q, *a.tm_k, *a.tm_v, *a.tm_o, p);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(g.T, g.H, g.B), dim3(C::THREADS), C::SMEM_BYTES, st, *a.tm_q,
+                      *a.tm_k, *a.tm_v, *a.tm_o, p);
 }
 
 
@@ -676,6 +677,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     const __grid_constant__ CUtensorMap tm_v,
                     const __grid_constant__ CUtensorMap tm_o, const FwdParams p) {
     extern __shared__ __align__(1024) uint8_t smem[];
+    pdl_wait();  // tile lists of the kernel before
+    pdl_trigger();
     if (smem_u32(smem) & 1023u) {  // swizzled tiles need 1024-byte alignment
         if (threadIdx.x == 0) atomicExch(&g_err_fwd, ERR_SMEM_ALIGN);
         return;
@@ -993,9 +996,8 @@ cudaError_t launch_pair(const Geometry &g, const Workspace &ws, const FwdArgs &a
     if (e != cudaSuccess) return e;
     const long long ctas = static_cast<long long>((g.T + 1) / 2) * g.H * g.B;
     if (ctas > 0x7fffffffLL) return cudaErrorInvalidValue;
-    kern<<<static_cast<unsigned>(ctas), C::THREADS, C::SMEM_BYTES, st>>>(*a.tm_q, *a.tm_k,
-                                                                        *a.tm_v, *a.tm_o, p);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(static_cast<unsigned>(ctas)), dim3(C::THREADS), C::SMEM_BYTES,
+                      st, *a.tm_q, *a.tm_k, *a.tm_v, *a.tm_o, p);
 }
 
 }  // namespace
