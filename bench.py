@@ -331,51 +331,88 @@ def run_ours(args, rank, world, local_rank):
 
 
 def run_e2e(q, k, v, do, vec, mask, cfg, has_bwd, det, args, step_flops, world, device):
-    """Same step through the public API with pinned host buffers; the H2D copies
-    of q, k, v, dO and the mask vectors and the D2H read of the results are
-    inside the timed region."""
+    """Same step through the public API with pinned host buffers.  Every step
+    copies its own q, k, v, dO and mask vectors host -> device and reads its
+    results (O, and dQ, dK, dV) device -> host, all inside the timed region.
+    The copies run on their own streams into double-buffered device tensors,
+    so step i + 1's inputs and step i - 1's results move while step i computes
+    (a pipelined input feed, as a training or serving loop runs it).  The
+    region opens before the first input copy and closes after the last
+    result copy."""
     import torch
     from sparse_masked_attention_gb300 import attention as fm
-    host_in = [t.cpu().pin_memory() for t in (q, k, v, do)]
+    n_in = 4 if has_bwd else 3
+    host_in = [t.cpu().pin_memory() for t in (q, k, v, do)[:n_in]]
     host_vec = [None if t is None else t.cpu().pin_memory() for t in vec]
-    dev_in = [torch.empty_like(t) for t in (q, k, v, do)]
-    dev_vec = [None if t is None else torch.empty_like(t) for t in vec]
-    outs_dev = None
-    h2d = sum(t.numel() * t.element_size() for t in host_in[: (4 if has_bwd else 3)])
+    dev_in = [[torch.empty_like(t, device=device) for t in host_in] for _ in range(2)]
+    dev_vec = [[None if t is None else torch.empty_like(t, device=device) for t in host_vec]
+               for _ in range(2)]
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
     h2d += sum(t.numel() * t.element_size() for t in host_vec if t is not None)
     B, H, N, d, dv = cfg["B"], cfg["H"], cfg["N"], cfg["d"], cfg["dv"]
     out_shapes = [(B, N, H, dv)] + ([(B, N, H, d), (B, N, H, d), (B, N, H, dv)] if has_bwd else [])
-    host_out = [torch.empty(s, dtype=torch.bfloat16).pin_memory() for s in out_shapes]
+    dev_out = [[torch.empty(s_, dtype=torch.bfloat16, device=device) for s_ in out_shapes]
+               for _ in range(2)]
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=device)
+    host_out = [torch.empty(s_, dtype=torch.bfloat16).pin_memory() for s_ in out_shapes]
     d2h = sum(t.numel() * t.element_size() for t in host_out)
+    ws_f = torch.empty(fm.workspace_size(B, H, 1, N, d, dv, False), dtype=torch.uint8,
+                       device=device)
+    ws_b = torch.empty(fm.workspace_size(B, H, 1, N, d, dv, True, det), dtype=torch.uint8,
+                       device=device) if has_bwd else None
+    s_comp = torch.cuda.current_stream(device)
+    s_in, s_out = torch.cuda.Stream(device), torch.cuda.Stream(device)
+    ev = lambda: torch.cuda.Event()
+    in_ready, comp_done, out_done = ([ev(), ev()] for _ in range(3))
+    used = [False, False]
 
-    def step():
-        for hsrc, ddst in zip(host_in, dev_in):
-            ddst.copy_(hsrc, non_blocking=True)
-        for hsrc, ddst in zip(host_vec, dev_vec):
-            if hsrc is not None:
+    def step(i):
+        sl = i % 2
+        with torch.cuda.stream(s_in):
+            if used[sl]:
+                s_in.wait_event(comp_done[sl])  # the step two back has read this slot
+            for hsrc, ddst in zip(host_in, dev_in[sl]):
                 ddst.copy_(hsrc, non_blocking=True)
-        o, lse = fm.fwd(dev_in[0], dev_in[1], dev_in[2], *dev_vec, causal=mask.causal)
-        outs = [o]
+            for hsrc, ddst in zip(host_vec, dev_vec[sl]):
+                if hsrc is not None:
+                    ddst.copy_(hsrc, non_blocking=True)
+            in_ready[sl].record(s_in)
+        s_comp.wait_event(in_ready[sl])
+        if used[sl]:
+            s_comp.wait_event(out_done[sl])  # its results have left the slot
+        x = dev_in[sl]
+        o = dev_out[sl]
+        fm.fwd(x[0], x[1], x[2], *dev_vec[sl], causal=mask.causal, out=o[0], lse=lse,
+               workspace=ws_f)
         if has_bwd:
-            outs += list(fm.bwd(dev_in[0], dev_in[1], dev_in[2], o, lse, dev_in[3], *dev_vec,
-                                causal=mask.causal, deterministic=det))
-        for hdst, dsrc in zip(host_out, outs):
-            hdst.copy_(dsrc, non_blocking=True)
+            fm.bwd(x[0], x[1], x[2], o[0], lse, x[3], *dev_vec[sl], causal=mask.causal,
+                   deterministic=det, dq=o[1], dk=o[2], dv=o[3], workspace=ws_b)
+        comp_done[sl].record(s_comp)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(comp_done[sl])
+            for hdst, dsrc in zip(host_out, o):
+                hdst.copy_(dsrc, non_blocking=True)
+            out_done[sl].record(s_out)
+        used[sl] = True
 
-    for _ in range(2):
-        step()
+    for i in range(3):
+        step(i)
     torch.cuda.synchronize()
-    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    K = max(1, min(args.steps, 5))
-    s.record()
-    for _ in range(K):
-        step()
-    e.record()
+    used[0] = used[1] = False
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    K = max(1, args.steps)
+    start.record(s_in)
+    for i in range(K):
+        step(i)
+    s_out.wait_stream(s_in)
+    s_out.wait_stream(s_comp)
+    end.record(s_out)
     torch.cuda.synchronize()
-    ms = s.elapsed_time(e) / K
+    ms = start.elapsed_time(end) / K
     return {"value": round(step_flops / (ms * 1e-3) / 1e12 * world, 3), "unit": "TFLOP/s",
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-            "ms_per_step": round(ms, 3)}
+            "ms_per_step": round(ms, 3), "steps": K,
+            "copies": "own streams, double-buffered: step i+1 in and step i-1 out overlap step i"}
 
 
 # ----------------------------------------------------------- CPU (oracle) side
