@@ -42,7 +42,7 @@ __device__ __forceinline__ bool covers(int cj, int4 c, int r0, int r1) {
     return reach >= r1;
 }
 
-constexpr int kClassifyChunk = 32;  // query tiles per classify CTA
+constexpr int kClassifyChunk = 32;  // most query tiles per classify CTA
 
 __device__ __forceinline__ int warp_min(int v) {
 #pragma unroll
@@ -50,7 +50,7 @@ __device__ __forceinline__ int warp_min(int v) {
     return v;
 }
 
-// One CTA per (key tile, chunk of kClassifyChunk query tiles, mask head).
+// One CTA per (key tile, chunk of at most kClassifyChunk query tiles, mask head).
 // Per query tile qt, one word of `state` collects the CTA's verdict:
 //   bits 0..3  column test "every column of warp w covers the tile"
 //   bits 4..7  column test "some column of warp w reaches into the tile"
@@ -59,7 +59,7 @@ __device__ __forceinline__ int warp_min(int v) {
 // The loop over query tiles needs no CTA barrier: warps vote on their own and
 // OR their bits in; after one barrier the classes are written.
 __global__ void __launch_bounds__(128) classify_kernel(
-    int N, int T, int Npad, int Hm, int causal, const int32_t *__restrict__ lts,
+    int N, int T, int Npad, int Hm, int causal, int chunk, const int32_t *__restrict__ lts,
     const int32_t *__restrict__ lte, const int32_t *__restrict__ uts,
     const int32_t *__restrict__ ute, int4 *__restrict__ vec, uint8_t *__restrict__ cls) {
     __shared__ unsigned state[kClassifyChunk];
@@ -67,8 +67,8 @@ __global__ void __launch_bounds__(128) classify_kernel(
     pdl_wait();  // the vectors and the workspace belong to earlier stream work
     pdl_trigger();
     const int kt = blockIdx.x;
-    const int q_begin = blockIdx.y * kClassifyChunk;
-    const int q_end = min(T, q_begin + kClassifyChunk);
+    const int q_begin = blockIdx.y * chunk;
+    const int q_end = min(T, q_begin + chunk);
     const int bm = blockIdx.z;  // b * Hm + hm
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int j = kt * TILE + threadIdx.x;
@@ -300,9 +300,14 @@ __global__ void __launch_bounds__(1024) count_kernel(int N, int causal,
 
 cudaError_t launch_classify(const Geometry &g, const MaskPtrs &m, const Workspace &ws,
                             cudaStream_t st) {
-    dim3 grid(g.T, (g.T + kClassifyChunk - 1) / kClassifyChunk, g.B * g.Hm);
+    // Chunks of 32 query tiles share each CTA's per-tile reduction; a small
+    // map takes shorter chunks so that the grid still fills the GPU.
+    int chunk = kClassifyChunk;
+    const long long heads = static_cast<long long>(g.B) * g.Hm;
+    while (chunk > 8 && heads * g.T * ((g.T + chunk - 1) / chunk) < 512) chunk /= 2;
+    dim3 grid(g.T, (g.T + chunk - 1) / chunk, g.B * g.Hm);
     return launch_pdl(classify_kernel, grid, dim3(128), 0, st, g.N, g.T, g.Npad, g.Hm, g.causal,
-                      m.lts, m.lte, m.uts, m.ute, ws.vec, ws.cls);
+                      chunk, m.lts, m.lte, m.uts, m.ute, ws.vec, ws.cls);
 }
 
 cudaError_t launch_fwd_lists(const Geometry &g, const Workspace &ws, cudaStream_t st) {

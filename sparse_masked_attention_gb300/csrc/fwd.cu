@@ -136,11 +136,16 @@ __device__ __forceinline__ bool softmax_tile(uint32_t s_addr, uint32_t o_addr, b
         };
         uint32_t r[32];
         float lc = 0.f;
-        bool fast = __all_sync(0xffffffffu, m_ref != NEG_INF);
+        // A row with no reference yet takes the fast path too when every
+        // column of this chunk is masked for it: its P is 0 whatever the
+        // reference (as for the rows of a document that starts inside the
+        // query tile, over the key tiles of the document before).
+        const bool row_empty = masked_tile && (mbits[c][0] & mbits[c][1]) == 0xffffffffu;
+        bool fast = __all_sync(0xffffffffu, m_ref != NEG_INF || row_empty);
         if (fast) {
             float x[64];
             load_masked(x);
-            lc = exp_pack(x, m_ref, r);
+            lc = exp_pack(x, m_ref == NEG_INF ? 0.0f : m_ref, r);
             fast = __all_sync(0xffffffffu, lc <= 4294967296.0f);  // false for NaN
         }
         if (!fast) {
