@@ -107,9 +107,24 @@ __device__ __forceinline__ bool softmax_tile(uint32_t s_addr, uint32_t o_addr, b
     const float2 sl2x2 = make_float2(sl2, sl2);
 #pragma unroll
     for (int c = 0; c < C::BN / 64; ++c) {
+        // Partial tiles: a chunk every column of which is masked for every row
+        // of the warp has P = 0 (nothing to load, exponentiate or add); one in
+        // which no row of the warp masks anything needs no masking.
+        bool chunk_masked = masked_tile;
+        if (masked_tile) {
+            const uint32_t wa = mbits[c][0], wb = mbits[c][1];
+            if (__all_sync(0xffffffffu, (wa & wb) == 0xffffffffu)) {
+                uint32_t z[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) z[i] = 0u;
+                tmem_st32(s_addr + c * 32, z);
+                continue;
+            }
+            chunk_masked = __any_sync(0xffffffffu, (wa | wb) != 0u);
+        }
         auto load_masked = [&](float (&x)[64]) {
             tmem_ld64f(s_addr + c * 64, x);
-            if (masked_tile) {
+            if (chunk_masked) {
                 const uint32_t wa = mbits[c][0], wb = mbits[c][1];
 #pragma unroll
                 for (int jj = 0; jj < 32; ++jj) {
