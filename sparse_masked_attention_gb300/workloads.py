@@ -5,7 +5,10 @@ arithmetic, and it serves the CUDA path and the CPU oracle alike.
 
 Mask families are those named in the FlashMask-3 abstract: document,
 prefix-LM, share-question, sliding-window and block-sparse, plus causal and
-global+sliding.  Each family is first drawn as a structure, such as document
+global+sliding.  Further structured variants of the same kind widen the set:
+bidirectional documents, documents with a bidirectional prefix each, a
+symmetric (bidirectional) sliding window, and causal attention with random
+key eviction.  Each family is first drawn as a structure, such as document
 lengths or a window width.  That structure is then encoded in the column-wise
 form of the FlashMask README "Overview".  Key column ``j`` gets query-row
 intervals ``[LTS_j, LTE_j)`` and ``[UTS_j, UTE_j)``.  Row ``i`` is masked
@@ -126,6 +129,91 @@ def prefix_lm(N: int, prefix: int, B: int = 1) -> Mask:
     rep = lambda x: np.repeat(x[None, None], B, axis=0)
     return Mask(N, False, uts=rep(uts), ute=rep(ute), family="prefix_lm",
                 meta=[{"prefix": prefix} for _ in range(B)])
+
+
+def _doc_bounds(N, lengths):
+    ends = np.cumsum(lengths)
+    starts = ends - np.asarray(lengths)
+    return (np.repeat(starts, lengths).astype(np.int32),
+            np.repeat(ends, lengths).astype(np.int32))
+
+
+def document(N: int, lengths_per_sample: list) -> Mask:
+    """Bidirectional within a document, nothing across documents (no causal
+    flag): column j is masked above its document's start and from its end."""
+    B = len(lengths_per_sample)
+    lts = np.zeros((B, 1, N), np.int32)
+    lte = np.full((B, 1, N), N, np.int32)
+    uts = np.zeros((B, 1, N), np.int32)
+    ute = np.zeros((B, 1, N), np.int32)
+    for b, lengths in enumerate(lengths_per_sample):
+        assert sum(lengths) == N
+        start, end = _doc_bounds(N, lengths)
+        lts[b, 0], ute[b, 0] = end, start
+    return Mask(N, False, lts=lts, lte=lte, uts=uts, ute=ute, family="document",
+                meta=[{"lengths": list(map(int, x))} for x in lengths_per_sample])
+
+
+def document_prefixes(rng: np.random.Generator, lengths: list) -> list:
+    """A bidirectional prefix per document, its length ~ U{0 .. document length}."""
+    return [int(rng.integers(0, n + 1)) for n in lengths]
+
+
+def prefix_document(N: int, lengths_per_sample: list, prefixes_per_sample: list) -> Mask:
+    """Documents with a bidirectional prefix each: inside a document every row
+    sees the prefix keys, and the keys after the prefix causally; nothing
+    across documents (no causal flag)."""
+    B = len(lengths_per_sample)
+    lts = np.zeros((B, 1, N), np.int32)
+    lte = np.full((B, 1, N), N, np.int32)
+    uts = np.zeros((B, 1, N), np.int32)
+    ute = np.zeros((B, 1, N), np.int32)
+    j = np.arange(N, dtype=np.int32)
+    for b, (lengths, prefixes) in enumerate(zip(lengths_per_sample, prefixes_per_sample)):
+        assert sum(lengths) == N and len(prefixes) == len(lengths)
+        start, end = _doc_bounds(N, lengths)
+        pref_end = np.repeat(np.cumsum(lengths) - np.asarray(lengths) + np.asarray(prefixes),
+                             lengths).astype(np.int32)
+        lts[b, 0] = end
+        ute[b, 0] = np.where(j < pref_end, start, j)
+    return Mask(N, False, lts=lts, lte=lte, uts=uts, ute=ute, family="prefix_document",
+                meta=[{"lengths": list(map(int, x)), "prefixes": list(map(int, y))}
+                      for x, y in zip(lengths_per_sample, prefixes_per_sample)])
+
+
+def bidirectional_window(N: int, w: int, B: int = 1) -> Mask:
+    """Symmetric local window (no causal flag): row i sees the keys j with
+    |i - j| < w."""
+    j = np.arange(N, dtype=np.int64)
+    lts = np.minimum(j + w, N).astype(np.int32)
+    lte = np.full(N, N, np.int32)
+    uts = np.zeros(N, np.int32)
+    ute = np.maximum(j - w + 1, 0).astype(np.int32)
+    rep = lambda x: np.repeat(x[None, None], B, axis=0)
+    return Mask(N, False, lts=rep(lts), lte=rep(lte), uts=rep(uts), ute=rep(ute),
+                family="bidirectional_window", meta=[{"w": w} for _ in range(B)])
+
+
+def eviction_rows(rng: np.random.Generator, N: int, keep: float = 0.5) -> np.ndarray:
+    """Per key j the first row that no longer sees it: N (never evicted) with
+    probability `keep`, otherwise ~ U{j+1 .. N}."""
+    j = np.arange(N, dtype=np.int64)
+    ev = j + 1 + np.floor(rng.random(N) * (N - j)).astype(np.int64)
+    never = rng.random(N) < keep
+    return np.where(never, N, np.minimum(ev, N)).astype(np.int32)
+
+
+def random_eviction(N: int, rng: np.random.Generator, B: int = 1, keep: float = 0.5) -> Mask:
+    """Causal, and key j is evicted from row e_j on (a key-value cache that
+    drops keys at random times; the diagonal always stays visible)."""
+    lts = np.zeros((B, 1, N), np.int32)
+    lte = np.full((B, 1, N), N, np.int32)
+    meta = []
+    for b in range(B):
+        ev = eviction_rows(rng, N, keep)
+        lts[b, 0] = ev
+        meta.append({"evict": ev})
+    return Mask(N, True, lts=lts, lte=lte, family="random_eviction", meta=meta)
 
 
 def share_question_groups(rng, N, q_len=(1024, 4096), n_ans=(2, 4), a_len=(512, 2048)):
@@ -270,6 +358,19 @@ def dense_semantic(mask: Mask, b: int = 0) -> np.ndarray:
     if fam == "global_sliding":
         g, w = meta["n_global"], meta["w"]
         return (i < j) | ((j >= g) & (i - j >= w))
+    if fam == "document":
+        doc = np.repeat(np.arange(len(meta["lengths"])), meta["lengths"])
+        return doc[:, None] != doc[None, :]
+    if fam == "prefix_document":
+        lengths = meta["lengths"]
+        doc = np.repeat(np.arange(len(lengths)), lengths)
+        offset = np.arange(N) - np.repeat(np.cumsum(lengths) - np.asarray(lengths), lengths)
+        in_prefix = offset < np.repeat(meta["prefixes"], lengths)
+        return (doc[:, None] != doc[None, :]) | (~in_prefix[None, :] & (i < j))
+    if fam == "bidirectional_window":
+        return np.abs(i - j) >= meta["w"]
+    if fam == "random_eviction":
+        return (i < j) | (i >= np.asarray(meta["evict"])[None, :])
     raise ValueError(f"no semantic definition for family {fam!r}")
 
 
@@ -292,6 +393,14 @@ CONFIGS = {
                               passes="fwd+bwd"),
     "long_global_sliding": dict(B=1, H=8, N=131072, d=128, dv=128, mask="global_sliding",
                                 n_global=512, w=4096, passes="fwd+bwd"),
+    "std_document": dict(B=1, H=32, N=8192, d=128, dv=128, mask="document",
+                         doc_len=(512, 4096), passes="fwd"),
+    "std_prefix_document": dict(B=1, H=32, N=8192, d=128, dv=128, mask="prefix_document",
+                                doc_len=(512, 4096), passes="fwd"),
+    "std_bidirectional_window": dict(B=1, H=32, N=8192, d=128, dv=128,
+                                     mask="bidirectional_window", w=1024, passes="fwd"),
+    "std_random_eviction": dict(B=1, H=32, N=8192, d=128, dv=128, mask="random_eviction",
+                                passes="fwd"),
     "large_head_d192": dict(B=1, H=16, N=16384, d=192, dv=128, mask="causal_document",
                             doc_len=(1024, 8192), passes="fwd+bwd", deterministic=True),
     "large_head_d256": dict(B=1, H=16, N=16384, d=256, dv=256, mask="causal_document",
@@ -324,6 +433,17 @@ def make_mask(cfg: dict, seed: int = 0, N: Optional[int] = None, B: Optional[int
         return block_sparse(N, rng, B)
     if kind == "global_sliding":
         return global_sliding(N, cfg["n_global"], cfg["w"], B)
+    if kind == "document":
+        lo, hi = cfg["doc_len"]
+        return document(N, [uniform_lengths(rng, lo, hi, N) for _ in range(B)])
+    if kind == "prefix_document":
+        lo, hi = cfg["doc_len"]
+        lengths = [uniform_lengths(rng, lo, hi, N) for _ in range(B)]
+        return prefix_document(N, lengths, [document_prefixes(rng, x) for x in lengths])
+    if kind == "bidirectional_window":
+        return bidirectional_window(N, cfg["w"], B)
+    if kind == "random_eviction":
+        return random_eviction(N, rng, B)
     raise ValueError(kind)
 
 

@@ -43,11 +43,21 @@ def _family(name, N, B, seed):
         return W.global_sliding(N, 64, 300, B)
     if name == "random":
         return W.random_vectors(N, rng, B, 1, causal_flag=bool(seed % 2))
+    if name == "document":
+        return W.document(N, [W.uniform_lengths(rng, 50, 300, N) for _ in range(B)])
+    if name == "prefix_document":
+        lengths = [W.uniform_lengths(rng, 50, 300, N) for _ in range(B)]
+        return W.prefix_document(N, lengths, [W.document_prefixes(rng, x) for x in lengths])
+    if name == "bidirectional_window":
+        return W.bidirectional_window(N, 100, B)
+    if name == "random_eviction":
+        return W.random_eviction(N, rng, B)
     raise ValueError(name)
 
 
 FAMILIES = ["causal", "full", "sliding", "causal_document", "prefix_lm", "share_question",
-            "block_sparse", "global_sliding", "random"]
+            "block_sparse", "global_sliding", "random", "document", "prefix_document",
+            "bidirectional_window", "random_eviction"]
 
 
 @pytest.mark.parametrize("family", FAMILIES)

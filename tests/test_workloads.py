@@ -54,3 +54,55 @@ def test_inputs_are_seeded():
     for x, y in zip(a, b):
         assert x.dtype.is_floating_point and x.shape[-1] == 8
         assert bool((x == y).all())
+
+
+def _dense(mask, b=0):
+    cls, _ = oracle.tilemap(mask.N, mask.slice(b), mask.causal, tq=1, tk=1)
+    return cls == oracle.TILE_SKIP
+
+
+def test_prefix_document_reduces_to_its_limits():
+    """No prefix: causal documents; a prefix as long as the document: plain
+    bidirectional documents."""
+    rng = np.random.default_rng(3)
+    N = 700
+    lengths = W.uniform_lengths(rng, 40, 200, N)
+    none = W.prefix_document(N, [lengths], [[0] * len(lengths)])
+    whole = W.prefix_document(N, [lengths], [list(lengths)])
+    np.testing.assert_array_equal(_dense(none), _dense(W.causal_document(N, [lengths])))
+    np.testing.assert_array_equal(_dense(whole), _dense(W.document(N, [lengths])))
+
+
+def test_document_is_block_diagonal_and_symmetric():
+    rng = np.random.default_rng(4)
+    N = 500
+    lengths = W.uniform_lengths(rng, 30, 150, N)
+    m = _dense(W.document(N, [lengths]))
+    np.testing.assert_array_equal(m, m.T)
+    ends = np.cumsum(lengths)
+    starts = ends - np.asarray(lengths)
+    for s0, e0 in zip(starts, ends):
+        assert not m[s0:e0, s0:e0].any()
+        assert m[s0:e0, :s0].all() and m[s0:e0, e0:].all()
+
+
+def test_bidirectional_window_limits():
+    N = 300
+    assert not _dense(W.bidirectional_window(N, N)).any()          # window covers all: no mask
+    one = _dense(W.bidirectional_window(N, 1))                      # only the diagonal
+    np.testing.assert_array_equal(~one, np.eye(N, dtype=bool))
+    m = _dense(W.bidirectional_window(N, 37))
+    np.testing.assert_array_equal(m, m.T)
+    assert (~m).sum(axis=1).max() == 2 * 37 - 1
+
+
+def test_random_eviction_limits():
+    """Keys never evicted give plain causal attention; every row keeps its
+    diagonal, and the causal part is always masked."""
+    N = 400
+    kept = _dense(W.random_eviction(N, np.random.default_rng(5), keep=1.0))
+    np.testing.assert_array_equal(kept, _dense(W.causal(N)))
+    m = _dense(W.random_eviction(N, np.random.default_rng(6)))
+    assert not np.diag(m).any()
+    assert m[np.triu(np.ones((N, N), bool), 1)].all()
+    assert m.sum() > kept.sum()  # some keys were evicted
