@@ -215,3 +215,37 @@ def count_unmasked(N, mask=None, causal=False):
     """Brute-force number of unmasked (i, j) pairs of one mask."""
     vec, _keep = _vecs(mask, N)
     return int(_load().oracle_tilemap(int(N), int(bool(causal)), *vec, 128, 128, None))
+
+
+# ------------------------------------------------ context-parallel chunks
+def localize(mask, N, causal, q0, k0, length):
+    """Column-wise vectors of the local problem of one (query chunk, key chunk)
+    pair, the sequence being cut into chunks of `length` rows and keys that
+    start at multiples of `length` (FlashMask-3 abstract: under a multi-chunk
+    context-parallel assignment, mask localization is a zero-communication
+    clip-shift-max on the boundary vectors).
+
+    Local row i' = i - q0 and local key j' = j - k0.  Each interval of key
+    column j, clamped to [0, N] as everywhere, is clipped to the query chunk,
+    shifted by its start and kept non-negative:
+    ``x' = max(min(x, q0 + length) - q0, 0)``.  The causal flag ``i < j``:
+    on the diagonal pair (q0 == k0) it is the local flag ``i' < j'``; a key
+    chunk before the query chunk has ``i > j`` everywhere, so no flag; a key
+    chunk after it is masked everywhere.
+
+    Returns (dict of four [length] int32 arrays, local causal flag), or
+    (None, None) when every element of the pair is masked."""
+    assert 0 <= q0 and q0 + length <= N and 0 <= k0 and k0 + length <= N
+    assert (q0 - k0) % length == 0
+    if causal and k0 > q0:
+        return None, None
+    local_causal = bool(causal) and k0 == q0
+    mask = mask or {}
+    empty = {"lts": N, "lte": N, "uts": 0, "ute": 0}
+    out = {}
+    for name in ("lts", "lte", "uts", "ute"):
+        x = mask.get(name)
+        x = (np.full(length, empty[name], np.int64) if x is None
+             else np.clip(np.asarray(x, np.int64)[k0:k0 + length], 0, N))
+        out[name] = np.maximum(np.minimum(x, q0 + length) - q0, 0).astype(np.int32)
+    return out, local_causal
