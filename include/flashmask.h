@@ -176,6 +176,67 @@ fm_status flashmask_fwd_noalloc(const fm_problem *p, const fm_options *opt,
                                 const int32_t *uts, const int32_t *ute,
                                 void *o, float *lse, void *stream);
 
+/*
+ * Context-parallel chunks on one GPU ("FlashMask-3: Efficient and Expressive
+ * Mask-Aware Distributed Attention", abstract: under any multi-chunk
+ * context-parallel assignment, per-rank mask localization is a
+ * zero-communication clip-shift-max on the boundary vectors, compatible with
+ * the single-GPU kernel).  The sequence is cut into chunks of `len` rows and
+ * keys starting at multiples of `len`; every (query chunk, key chunk) pair is
+ * a local problem of size len that runs through flashmask_fwd / flashmask_bwd,
+ * and a query chunk's partial results are merged by log-sum-exp.
+ */
+
+/*
+ * Local boundary vectors of the pair (query chunk at row q0, key chunk at key
+ * k0): for local key j' = j - k0, every boundary x of column j, clamped to
+ * [0, N], becomes  x' = max(min(x, q0 + len) - q0, 0)  (clip to the query
+ * chunk, shift by its start, max with 0).  *local_causal receives the causal
+ * flag of the local problem: 1 on the diagonal pair (q0 == k0) of a causal
+ * mask, 0 when the mask is not causal or the key chunk lies before the query
+ * chunk, and -1 when it is causal and the key chunk lies after the query chunk:
+ * then every element is masked, the pair is to be skipped and nothing is
+ * written or enqueued.
+ *  - In: the problem's B, Hm, H, N and causal (other fields unused); global
+ *    vectors [B, Hm, N] int32 (a NULL pair is an empty interval).
+ *  - Out: four [B, Hm, len] int32 device arrays (absent intervals are written
+ *    empty).  Requires 1 <= len, 0 <= q0, k0 <= N - len, (q0 - k0) % len == 0;
+ *    else FM_ERR_INVALID_ARG.
+ */
+fm_status flashmask_localize(const fm_problem *p, const int32_t *lts, const int32_t *lte,
+                             const int32_t *uts, const int32_t *ute, int q0, int k0, int len,
+                             int32_t *out_lts, int32_t *out_lte, int32_t *out_uts,
+                             int32_t *out_ute, int *local_causal, void *stream);
+
+/*
+ * Log-sum-exp merge of one query chunk's partial results.  A chunk of one
+ * batch: O [L, H, dv] (the rows q0 .. q0 + L - 1 of a [1, N, H, dv] tensor, or a
+ * local problem's output), LSE [H, L]; running values o_acc [L, H, dv] fp32
+ * and lse_acc [H, L] fp32.  dv a multiple of 8; O pointers 16-byte aligned.
+ *  - merge_init: o_acc = 0, lse_acc = -inf.
+ *  - merge: lse = log(exp(lse_acc) + exp(lse_part)),
+ *           o_acc = o_acc * exp(lse_acc - lse) + o_part * exp(lse_part - lse)
+ *    (rows where both are -inf stay O = 0, LSE = -inf).
+ *  - merge_finish: o_out [L, H, dv] bf16 = o_acc (round to nearest even), and
+ *    head h's LSE to lse_out + h * lse_stride (lse_stride >= L; N for the
+ *    chunk's rows inside a [1, H, N] LSE).
+ */
+fm_status flashmask_merge_init(int L, int H, int dv, float *o_acc, float *lse_acc,
+                               void *stream);
+fm_status flashmask_merge(int L, int H, int dv, const void *o_part, const float *lse_part,
+                          float *o_acc, float *lse_acc, void *stream);
+fm_status flashmask_merge_finish(int L, int H, int dv, const float *o_acc, const float *lse_acc,
+                                 void *o_out, float *lse_out, long long lse_stride,
+                                 void *stream);
+
+/*
+ * Sums of partial gradients over chunk pairs: acc[i] += part[i] (n bf16 values
+ * into fp32), and dst = bf16(src) (round to nearest even).  n a multiple of 8,
+ * pointers 16-byte aligned.
+ */
+fm_status flashmask_accumulate(long long n, const void *part, float *acc, void *stream);
+fm_status flashmask_to_bf16(long long n, const float *src, void *dst, void *stream);
+
 /* Static text for a status code. */
 const char *flashmask_error_string(fm_status s);
 

@@ -206,3 +206,133 @@ def flashmask_attention(q, k, v, lts=None, lte=None, uts=None, ute=None, causal=
 
 def default_scale(d: int) -> float:
     return 1.0 / math.sqrt(d)
+
+
+# --------------------------------------------------- context-parallel chunks
+def zigzag_assignment(chunks: int, ranks: int) -> list:
+    """Query chunks per rank of the usual causal load-balancing assignment:
+    with 2R chunks, rank r owns chunks r and 2R - 1 - r."""
+    if chunks != 2 * ranks:
+        raise FlashMaskError("the zigzag assignment needs chunks == 2 * ranks")
+    return [[r, chunks - 1 - r] for r in range(ranks)]
+
+
+def localize(lts, lte, uts, ute, B, H, N, causal, q0, k0, length, stream=None):
+    """Boundary vectors of the local problem of the pair (query chunk at q0, key
+    chunk at k0) of chunks of `length` (clip to the query chunk, shift by its
+    start, max with 0).  Returns ([lts, lte, uts, ute] as [B, Hm, length] int32
+    tensors, local causal flag), or (None, -1) when every element of the pair is
+    masked."""
+    device = next(t.device for t in (lts, lte, uts, ute) if t is not None) \
+        if any(t is not None for t in (lts, lte, uts, ute)) else torch.device("cuda")
+    Hm, mp, _keep = _mask_args((lts, lte, uts, ute), B, H, N, device)
+    prob = make_problem(B, H, Hm, N, 64, 64, None, causal)
+    out = [torch.empty((B, Hm, length), dtype=torch.int32, device=device) for _ in range(4)]
+    st, flag = _b.flashmask_localize(prob, *mp, int(q0), int(k0), int(length),
+                                     *(t.data_ptr() for t in out), _stream(stream))
+    _check(st, "flashmask_localize")
+    return (None, -1) if flag < 0 else (out, flag)
+
+
+def _chunk_plan(N, chunks, ranks):
+    if chunks < 1 or N % chunks != 0:
+        raise FlashMaskError("chunks must divide N")
+    L = N // chunks
+    owned = zigzag_assignment(chunks, ranks) if ranks else [[c] for c in range(chunks)]
+    return L, owned
+
+
+def fwd_chunked(q, k, v, lts=None, lte=None, uts=None, ute=None, causal=False, scale=None,
+                chunks=2, ranks=None, stream=None):
+    """The forward of the whole sequence as a context-parallel run emulated on
+    this GPU: the sequence is cut into `chunks` equal chunks; each rank (the
+    zigzag assignment when `ranks` is given, one chunk per rank otherwise)
+    takes its query chunks against every key chunk, each pair a local problem
+    with localized vectors, and merges the pairs of a query chunk by
+    log-sum-exp.  Returns (o [B,N,H,dv] bf16, lse [B,H,N] fp32), equal to fwd()
+    up to rounding."""
+    B, N, H, d, dv = _check_qkv(q, k, v)
+    L, owned = _chunk_plan(N, chunks, ranks)
+    dev = q.device
+    s = _stream(stream)
+    o = torch.empty((B, N, H, dv), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    o_part = torch.empty((1, L, H, dv), dtype=torch.bfloat16, device=dev)
+    lse_part = torch.empty((1, H, L), dtype=torch.float32, device=dev)
+    o_acc = torch.empty((L, H, dv), dtype=torch.float32, device=dev)
+    lse_acc = torch.empty((H, L), dtype=torch.float32, device=dev)
+    vecs = (lts, lte, uts, ute)
+    ws = None
+    for b in range(B):
+        vb = [None if t is None else t[b:b + 1] for t in vecs]
+        for rank_chunks in owned:
+            for qc in rank_chunks:
+                q0 = qc * L
+                _check(_b.flashmask_merge_init(L, H, dv, o_acc.data_ptr(), lse_acc.data_ptr(),
+                                               s), "flashmask_merge_init")
+                for kc in range(chunks):
+                    k0 = kc * L
+                    local, lc = localize(*vb, 1, H, N, causal, q0, k0, L, stream)
+                    if local is None:
+                        continue
+                    if ws is None:
+                        Hm = local[0].shape[1]
+                        ws = torch.empty(workspace_size(1, H, Hm, L, d, dv, False),
+                                         dtype=torch.uint8, device=dev)
+                    fwd(q[b:b + 1, q0:q0 + L], k[b:b + 1, k0:k0 + L], v[b:b + 1, k0:k0 + L],
+                        *local, causal=bool(lc), scale=scale if scale is not None
+                        else default_scale(d), out=o_part, lse=lse_part, workspace=ws,
+                        stream=stream)
+                    _check(_b.flashmask_merge(L, H, dv, o_part.data_ptr(), lse_part.data_ptr(),
+                                              o_acc.data_ptr(), lse_acc.data_ptr(), s),
+                           "flashmask_merge")
+                lse_out = lse.data_ptr() + (b * H * N + q0) * 4
+                _check(_b.flashmask_merge_finish(L, H, dv, o_acc.data_ptr(), lse_acc.data_ptr(),
+                                                 o[b:b + 1, q0:q0 + L].data_ptr(), lse_out, N, s),
+                       "flashmask_merge_finish")
+    return o, lse
+
+
+def bwd_chunked(q, k, v, o, lse, dout, lts=None, lte=None, uts=None, ute=None, causal=False,
+                scale=None, deterministic=False, chunks=2, ranks=None, stream=None):
+    """The backward as the same emulated context-parallel run: every pair's
+    local backward (with the whole sequence's O and LSE rows of its query
+    chunk) gives partial dQ for the query chunk and partial dK, dV for the key
+    chunk; the partials are summed in fp32 and rounded to bf16 once."""
+    B, N, H, d, dvd = _check_qkv(q, k, v)
+    L, owned = _chunk_plan(N, chunks, ranks)
+    dev = q.device
+    s = _stream(stream)
+    acc = [torch.zeros((B, N, H, c), dtype=torch.float32, device=dev) for c in (d, d, dvd)]
+    parts = [torch.empty((1, L, H, c), dtype=torch.bfloat16, device=dev) for c in (d, d, dvd)]
+    vecs = (lts, lte, uts, ute)
+    ws = None
+    for b in range(B):
+        vb = [None if t is None else t[b:b + 1] for t in vecs]
+        for rank_chunks in owned:
+            for qc in rank_chunks:
+                q0 = qc * L
+                lse_c = lse[b:b + 1, :, q0:q0 + L].contiguous()
+                for kc in range(chunks):
+                    k0 = kc * L
+                    local, lc = localize(*vb, 1, H, N, causal, q0, k0, L, stream)
+                    if local is None:
+                        continue
+                    if ws is None:
+                        Hm = local[0].shape[1]
+                        ws = torch.empty(workspace_size(1, H, Hm, L, d, dvd, True, deterministic),
+                                         dtype=torch.uint8, device=dev)
+                    bwd(q[b:b + 1, q0:q0 + L], k[b:b + 1, k0:k0 + L], v[b:b + 1, k0:k0 + L],
+                        o[b:b + 1, q0:q0 + L], lse_c, dout[b:b + 1, q0:q0 + L], *local,
+                        causal=bool(lc), scale=scale if scale is not None else default_scale(d),
+                        deterministic=deterministic, dq=parts[0], dk=parts[1], dv=parts[2],
+                        workspace=ws, stream=stream)
+                    for part, a, r0 in zip(parts, acc, (q0, k0, k0)):
+                        dst = a[b:b + 1, r0:r0 + L]
+                        _check(_b.flashmask_accumulate(part.numel(), part.data_ptr(),
+                                                       dst.data_ptr(), s), "flashmask_accumulate")
+    outs = [torch.empty((B, N, H, c), dtype=torch.bfloat16, device=dev) for c in (d, d, dvd)]
+    for a, out in zip(acc, outs):
+        _check(_b.flashmask_to_bf16(a.numel(), a.data_ptr(), out.data_ptr(), s),
+               "flashmask_to_bf16")
+    return tuple(outs)

@@ -41,7 +41,9 @@ class fm_options(ctypes.Structure):
 
 EXPORTS = ("flashmask_workspace_size", "flashmask_fwd", "flashmask_bwd", "flashmask_classify",
            "flashmask_count_unmasked", "flashmask_get_error", "flashmask_error_string",
-           "flashmask_last_error_detail", "flashmask_fwd_noalloc")
+           "flashmask_last_error_detail", "flashmask_fwd_noalloc", "flashmask_localize",
+           "flashmask_merge_init", "flashmask_merge", "flashmask_merge_finish",
+           "flashmask_accumulate", "flashmask_to_bf16")
 
 FM_NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024
 
@@ -81,6 +83,17 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.flashmask_error_string.restype = ctypes.c_char_p
         lib.flashmask_fwd_noalloc.argtypes = [prob, opt, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
         lib.flashmask_fwd_noalloc.restype = ctypes.c_int
+        ci, ll = ctypes.c_int, ctypes.c_longlong
+        lib.flashmask_localize.argtypes = [prob, vp, vp, vp, vp, ci, ci, ci, vp, vp, vp, vp,
+                                           P(ci), vp]
+        lib.flashmask_merge_init.argtypes = [ci, ci, ci, vp, vp, vp]
+        lib.flashmask_merge.argtypes = [ci, ci, ci, vp, vp, vp, vp, vp]
+        lib.flashmask_merge_finish.argtypes = [ci, ci, ci, vp, vp, vp, vp, ll, vp]
+        lib.flashmask_accumulate.argtypes = [ll, vp, vp, vp]
+        lib.flashmask_to_bf16.argtypes = [ll, vp, vp, vp]
+        for name in ("flashmask_localize", "flashmask_merge_init", "flashmask_merge",
+                     "flashmask_merge_finish", "flashmask_accumulate", "flashmask_to_bf16"):
+            getattr(lib, name).restype = ctypes.c_int
         lib.flashmask_last_error_detail.argtypes = []
         lib.flashmask_last_error_detail.restype = ctypes.c_char_p
         _lib = lib
@@ -133,3 +146,34 @@ def flashmask_last_error_detail() -> str:
 def flashmask_fwd_noalloc(problem, options, q, k, v, lts, lte, uts, ute, o, lse, stream) -> int:
     return int(load().flashmask_fwd_noalloc(ctypes.byref(problem), _ref(options), q, k, v, lts,
                                             lte, uts, ute, o, lse, stream))
+
+
+def flashmask_localize(problem, lts, lte, uts, ute, q0, k0, length, out_lts, out_lte, out_uts,
+                       out_ute, stream):
+    """Returns (status, local causal flag: 1, 0, or -1 for a fully masked pair)."""
+    flag = ctypes.c_int(0)
+    st = int(load().flashmask_localize(ctypes.byref(problem), lts, lte, uts, ute, q0, k0, length,
+                                       out_lts, out_lte, out_uts, out_ute, ctypes.byref(flag),
+                                       stream))
+    return st, int(flag.value)
+
+
+def flashmask_merge_init(L, H, dv, o_acc, lse_acc, stream) -> int:
+    return int(load().flashmask_merge_init(L, H, dv, o_acc, lse_acc, stream))
+
+
+def flashmask_merge(L, H, dv, o_part, lse_part, o_acc, lse_acc, stream) -> int:
+    return int(load().flashmask_merge(L, H, dv, o_part, lse_part, o_acc, lse_acc, stream))
+
+
+def flashmask_merge_finish(L, H, dv, o_acc, lse_acc, o_out, lse_out, lse_stride, stream) -> int:
+    return int(load().flashmask_merge_finish(L, H, dv, o_acc, lse_acc, o_out, lse_out,
+                                             lse_stride, stream))
+
+
+def flashmask_accumulate(n, part, acc, stream) -> int:
+    return int(load().flashmask_accumulate(n, part, acc, stream))
+
+
+def flashmask_to_bf16(n, src, dst, stream) -> int:
+    return int(load().flashmask_to_bf16(n, src, dst, stream))

@@ -234,6 +234,8 @@ cudaError_t map_and_lists(const Geometry &g, const MaskPtrs &m, const Workspace 
 namespace fm {
 // Sets the text flashmask_last_error_detail returns on this thread.
 void set_error_detail(const char *msg) { snprintf(g_detail, sizeof(g_detail), "%s", msg); }
+// Makes the device owning `anchor` current for this thread and checks it.
+bool bind_device(const void *anchor) { return device_ok(anchor); }
 }  // namespace fm
 
 extern "C" {

@@ -82,6 +82,9 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
 
 // Text returned by flashmask_last_error_detail on this thread (api.cu).
 void set_error_detail(const char *msg);
+// Makes the device that owns `anchor` (device memory) current for this
+// thread and checks that it is an sm_103 part (api.cu).
+bool bind_device(const void *anchor);
 
 // Lays the workspace out from `base` (may be nullptr to size it); returns bytes.
 size_t carve_workspace(const Geometry &g, bool bwd, void *base, Workspace *ws);

@@ -1,0 +1,115 @@
+"""Context-parallel chunks on one GPU, through the C ABI.
+
+- flashmask_localize writes, bit for bit, the local vectors the oracle's
+  localization gives (clip to the query chunk, shift, max with 0), and flags
+  the pairs a causal mask masks entirely.
+- The forward and backward of the whole sequence, run as the emulated
+  context-parallel job (each rank's query chunks against every key chunk,
+  log-sum-exp merge, fp32 sums of partial gradients), match the fp64 oracle
+  element by element.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from sparse_masked_attention_gb300 import attention as fm
+from sparse_masked_attention_gb300 import workloads as W
+
+from gpu_util import MAX_ABS, assert_close, assert_lse, cuda_mask, head, mask_slice
+
+pytestmark = pytest.mark.gpu
+
+
+def _family(name, N, B, rng, Hm=1):
+    if name == "causal":
+        return W.causal(N, B)
+    if name == "causal_document":
+        return W.causal_document(N, [W.uniform_lengths(rng, 60, 400, N) for _ in range(B)])
+    if name == "document":
+        return W.document(N, [W.uniform_lengths(rng, 60, 400, N) for _ in range(B)])
+    if name == "share_question":
+        return W.share_question(
+            N, [W.share_question_groups(rng, N, (100, 300), (2, 4), (50, 200)) for _ in range(B)])
+    if name == "block_sparse":
+        return W.block_sparse(N, rng, B)
+    if name == "random_causal":
+        return W.random_vectors(N, rng, B, Hm, causal_flag=True)
+    if name == "random":
+        return W.random_vectors(N, rng, B, Hm, causal_flag=False)
+    raise ValueError(name)
+
+
+@pytest.mark.parametrize("family", ["causal_document", "share_question", "block_sparse",
+                                    "random_causal", "random"])
+@pytest.mark.parametrize("chunks", [2, 4])
+def test_localize_matches_oracle(family, chunks):
+    B, H, N = 2, 3, 1024
+    rng = np.random.default_rng(chunks)
+    Hm = H if family.startswith("random") else 1
+    mask = _family(family, N, B, rng, Hm)
+    vec = cuda_mask(mask)
+    L = N // chunks
+    for qc in range(chunks):
+        for kc in range(chunks):
+            local, flag = fm.localize(*vec, B, H, N, mask.causal, qc * L, kc * L, L)
+            for b in range(B):
+                for hm in range(Hm):
+                    want, wc = oracle.localize(mask.slice(b, hm), N, mask.causal, qc * L,
+                                               kc * L, L)
+                    if want is None:
+                        assert local is None and flag == -1
+                        continue
+                    assert flag == int(wc)
+                    for i, name in enumerate(("lts", "lte", "uts", "ute")):
+                        np.testing.assert_array_equal(local[i][b, hm].cpu().numpy(), want[name])
+    torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("family", ["causal", "causal_document", "document", "share_question",
+                                    "block_sparse", "random_causal"])
+@pytest.mark.parametrize("d", [64, 128])
+def test_chunked_fwd_bwd_parity(family, d):
+    B, H, N, C, R = 2, 2, 1024, 4, 2
+    rng = np.random.default_rng(11)
+    q, k, v, do = W.make_inputs(B, N, H, d, d, seed=3, device="cuda")
+    mask = _family(family, N, B, rng)
+    vec = cuda_mask(mask)
+    o, lse = fm.fwd_chunked(q, k, v, *vec, causal=mask.causal, chunks=C, ranks=R)
+    grads = fm.bwd_chunked(q, k, v, o, lse, do, *vec, causal=mask.causal, chunks=C, ranks=R)
+    fm.get_error()
+    scale = 1 / np.sqrt(d)
+    for b in range(B):
+        for h in range(H):
+            qh, kh, vh, doh = head(q, b, h), head(k, b, h), head(v, b, h), head(do, b, h)
+            ms = mask_slice(mask, b, h)
+            ro, rl = oracle.attention_fwd(qh, kh, vh, ms, mask.causal, scale)
+            assert_close("O", head(o, b, h), ro)
+            assert_lse(lse[b, h].cpu().numpy(), rl)
+            refs = oracle.attention_bwd(qh, kh, vh, doh, ms, mask.causal, scale)
+            for name, g, ref in zip(("dQ", "dK", "dV"), grads, refs):
+                # Every pair's partial gradient leaves the backward kernel as
+                # bf16 (half an ulp: 2^-9 relative) before the fp32 sum, and
+                # an element sums at most C partials: on top of the single-call
+                # tolerance, C roundings at the scale of the tensor (max|ref|
+                # taken as the partials' scale).
+                tol = MAX_ABS + C * 2.0 ** -9 * float(np.max(np.abs(ref)))
+                assert_close(name, head(g, b, h), ref, max_abs=tol)
+
+
+def test_chunked_equals_single_call_forward():
+    """The emulated context-parallel forward and the single call agree to bf16
+    rounding of O and fp32 rounding of LSE."""
+    B, H, N, d = 1, 4, 2048, 128
+    rng = np.random.default_rng(5)
+    q, k, v, _ = W.make_inputs(B, N, H, d, d, seed=9, device="cuda", with_dout=False)
+    mask = _family("share_question", N, B, rng)
+    vec = cuda_mask(mask)
+    o1, l1 = fm.fwd(q, k, v, *vec, causal=mask.causal)
+    o2, l2 = fm.fwd_chunked(q, k, v, *vec, causal=mask.causal, chunks=8, ranks=4)
+    fm.get_error()
+    diff = (o1.float() - o2.float()).abs().max().item()
+    assert diff <= 2.0 ** -6 * max(1.0, o1.float().abs().max().item()), diff
+    fin = torch.isfinite(l1)
+    assert torch.equal(torch.isneginf(l1), torch.isneginf(l2))
+    assert (l1[fin] - l2[fin]).abs().max().item() <= 1e-4
