@@ -45,6 +45,9 @@ def parse():
     ap.add_argument("--N", type=int, default=None, help="override the workload's N (profiling)")
     ap.add_argument("--B", type=int, default=None, help="override the workload's B (profiling)")
     ap.add_argument("--H", type=int, default=None, help="override the workload's H (profiling)")
+    ap.add_argument("--chunks", type=int, default=0,
+                    help="time the step as an emulated context-parallel run over this many "
+                         "equal chunks (zigzag over chunks/2 ranks) instead of one call")
     return ap.parse_args()
 
 
@@ -235,6 +238,10 @@ def run_ours(args, rank, world, local_rank):
             fm.bwd(q, k, v, o, lse, do, *vec, causal=mask.causal, deterministic=det, dq=dq,
                    dk=dk, dv=dvv, workspace=ws_b, options=plain_b if i is None else opt_b[i])
 
+    if args.chunks:
+        return run_chunked(args, cfg, q, k, v, do, mask, vec, has_bwd, det, step_flops, world,
+                           device, rank)
+
     # The clock sampler starts first, so that the GPU goes from the warm-up
     # steps straight into the timed ones.
     sampler = ClockSampler(local_rank) if rank == 0 else None
@@ -328,6 +335,55 @@ def run_ours(args, rank, world, local_rank):
         "e2e": e2e,
     }
     return result
+
+
+def run_chunked(args, cfg, q, k, v, do, mask, vec, has_bwd, det, step_flops, world, device,
+                rank):
+    """The step as an emulated context-parallel run on this GPU: the sequence in
+    `args.chunks` equal chunks, zigzag over chunks / 2 ranks, every (query
+    chunk, key chunk) pair a local problem with localized vectors, log-sum-exp
+    merge and fp32 gradient sums.  The same unmasked pairs and FLOPs as the
+    single call; many launches per step, so no per-kernel split."""
+    import torch
+    from sparse_masked_attention_gb300 import attention as fm
+    C = args.chunks
+    R = C // 2 if C % 2 == 0 else None
+
+    def step():
+        o, lse = fm.fwd_chunked(q, k, v, *vec, causal=mask.causal, chunks=C, ranks=R)
+        if has_bwd:
+            fm.bwd_chunked(q, k, v, o, lse, do, *vec, causal=mask.causal, deterministic=det,
+                           chunks=C, ranks=R)
+
+    for _ in range(args.warmup):
+        step()
+    fm.get_error()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    start.record()
+    for _ in range(args.steps):
+        step()
+    end.record()
+    torch.cuda.synchronize()
+    fm.get_error()
+    ms = start.elapsed_time(end) / args.steps
+    value = step_flops / (ms * 1e-3) / 1e12 * world
+    pk, _src = peaks()
+    return {
+        "metric": "masked-attn effective TFLOP/s fwd+bwd" if has_bwd else
+                  "masked-attn effective TFLOP/s fwd",
+        "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": args.workload, "B": cfg["B"], "H": cfg["H"], "N": cfg["N"],
+                   "d": cfg["d"], "dv": cfg["dv"], "mask": cfg["mask"],
+                   "passes": "fwd+bwd" if has_bwd else "fwd",
+                   "context_parallel_emulation": {"chunks": C, "ranks": R,
+                                                  "assignment": "zigzag" if R else "one chunk each"},
+                   "parallelism": f"replicas x{world}"},
+        "frac_of_peak": round(value / world / pk["bf16_tflops"], 4),
+        "roofline": None, "kernel_ms": None, "gpu_launches": None, "e2e": None, "clocks": None,
+    }
 
 
 def run_e2e(q, k, v, do, vec, mask, cfg, has_bwd, det, args, step_flops, world, device):
