@@ -15,6 +15,12 @@ numpy arrays.  What it computes, with the passages it follows:
   ``[UTS_j, UTE_j)``; ``causal`` also masks ``i < j``.
 * Fully masked rows give ``O = 0``, ``LSE = -inf`` and no gradient (stated
   convention; the pages are silent).
+* Attention-sink bias (FlashMask README, "News", which names it without a
+  formula; reading taken): a per-head logit ``sink`` joins every row's
+  softmax denominator as a term ``exp(sink)`` with no value, so
+  ``O_i = sum_j exp(s_ij) v_j / (exp(sink) + sum_j exp(s_ij))`` and
+  ``LSE_i = log(exp(sink) + sum_j exp(s_ij))``; its gradient is
+  ``-sum_i P_sink,i D_i`` with ``P_sink,i = exp(sink - LSE_i)``.
 * The backward pass is the plain derivative of the formula.
 * The tile map is a brute-force count of masked elements per tile.
 """
@@ -66,11 +72,11 @@ def _load():
         lp = ctypes.POINTER(ctypes.c_int64)
         i8p = ctypes.POINTER(ctypes.c_int8)
         head = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_int,
-                dp, dp, dp]
+                ctypes.c_double, dp, dp, dp]
         vec = [ip, ip, ip, ip]
         lib.oracle_fwd.argtypes = head + vec + [ctypes.c_long, lp, dp, dp]
         lib.oracle_fwd.restype = ctypes.c_int
-        lib.oracle_bwd_dq.argtypes = head + [dp] + vec + [ctypes.c_long, lp, dp, dp]
+        lib.oracle_bwd_dq.argtypes = head + [dp] + vec + [ctypes.c_long, lp, dp, dp, dp]
         lib.oracle_bwd_dq.restype = ctypes.c_int
         lib.oracle_bwd_dkdv.argtypes = head + [dp] + vec + [ctypes.c_long, lp, dp, dp]
         lib.oracle_bwd_dkdv.restype = ctypes.c_int
@@ -123,8 +129,14 @@ def _dptr(a):
     return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
 
 
-def attention_fwd(q, k, v, mask=None, causal=False, scale=None, rows=None):
-    """One (batch, head) slice.  q, k: [N, d]; v: [N, dv].
+def _sink(sink):
+    return -np.inf if sink is None else float(sink)
+
+
+def attention_fwd(q, k, v, mask=None, causal=False, scale=None, rows=None, sink=None):
+    """One (batch, head) slice.  q, k: [N, d]; v: [N, dv].  `sink`: the head's
+    attention-sink logit (None: no sink), a term exp(sink) of every row's
+    softmax denominator that carries no value.
 
     Returns (o [n_rows, dv], lse [n_rows]) in float64.
     """
@@ -140,15 +152,17 @@ def attention_fwd(q, k, v, mask=None, causal=False, scale=None, rows=None):
     n = N if rows_a is None else len(rows_a)
     o = np.zeros((n, dv), np.float64)
     lse = np.zeros((n,), np.float64)
-    rc = _load().oracle_fwd(N, d, dv, float(scale), int(bool(causal)), _dptr(q), _dptr(k),
-                            _dptr(v), *vec, n, rows_p, _dptr(o), _dptr(lse))
+    rc = _load().oracle_fwd(N, d, dv, float(scale), int(bool(causal)), _sink(sink), _dptr(q),
+                            _dptr(k), _dptr(v), *vec, n, rows_p, _dptr(o), _dptr(lse))
     if rc:
         raise MemoryError("oracle_fwd: allocation failed")
     return o, lse
 
 
-def attention_bwd_dq(q, k, v, dout, mask=None, causal=False, scale=None, rows=None):
-    """Returns (dq [n_rows, d], delta [n_rows]) for one (batch, head) slice."""
+def attention_bwd_dq(q, k, v, dout, mask=None, causal=False, scale=None, rows=None, sink=None,
+                     with_dsink=False):
+    """Returns (dq [n_rows, d], delta [n_rows]) for one (batch, head) slice, and
+    with `with_dsink` also the rows' terms of the sink logit's gradient."""
     q = _f64(q)
     N, d = q.shape
     k = _f64(k, (N, d))
@@ -162,15 +176,17 @@ def attention_bwd_dq(q, k, v, dout, mask=None, causal=False, scale=None, rows=No
     n = N if rows_a is None else len(rows_a)
     dq = np.zeros((n, d), np.float64)
     delta = np.zeros((n,), np.float64)
-    rc = _load().oracle_bwd_dq(N, d, dv, float(scale), int(bool(causal)), _dptr(q), _dptr(k),
-                               _dptr(v), _dptr(dout), *vec, n, rows_p, _dptr(dq),
-                               _dptr(delta))
+    dsink = np.zeros((n,), np.float64)
+    rc = _load().oracle_bwd_dq(N, d, dv, float(scale), int(bool(causal)), _sink(sink), _dptr(q),
+                               _dptr(k), _dptr(v), _dptr(dout), *vec, n, rows_p, _dptr(dq),
+                               _dptr(delta), _dptr(dsink))
     if rc:
         raise MemoryError("oracle_bwd_dq: allocation failed")
-    return dq, delta
+    return (dq, delta, dsink) if with_dsink else (dq, delta)
 
 
-def attention_bwd_dkdv(q, k, v, dout, mask=None, causal=False, scale=None, cols=None):
+def attention_bwd_dkdv(q, k, v, dout, mask=None, causal=False, scale=None, cols=None,
+                       sink=None):
     """Returns (dk [n_cols, d], dv [n_cols, dv]) for one (batch, head) slice."""
     q = _f64(q)
     N, d = q.shape
@@ -185,19 +201,20 @@ def attention_bwd_dkdv(q, k, v, dout, mask=None, causal=False, scale=None, cols=
     n = N if cols_a is None else len(cols_a)
     dk = np.zeros((n, d), np.float64)
     dvv = np.zeros((n, dv), np.float64)
-    rc = _load().oracle_bwd_dkdv(N, d, dv, float(scale), int(bool(causal)), _dptr(q),
-                                 _dptr(k), _dptr(v), _dptr(dout), *vec, n, cols_p,
+    rc = _load().oracle_bwd_dkdv(N, d, dv, float(scale), int(bool(causal)), _sink(sink),
+                                 _dptr(q), _dptr(k), _dptr(v), _dptr(dout), *vec, n, cols_p,
                                  _dptr(dk), _dptr(dvv))
     if rc:
         raise MemoryError("oracle_bwd_dkdv: allocation failed")
     return dk, dvv
 
 
-def attention_bwd(q, k, v, dout, mask=None, causal=False, scale=None):
-    """Full backward of one (batch, head) slice: (dq, dk, dv)."""
-    dq, _ = attention_bwd_dq(q, k, v, dout, mask, causal, scale)
-    dk, dvv = attention_bwd_dkdv(q, k, v, dout, mask, causal, scale)
-    return dq, dk, dvv
+def attention_bwd(q, k, v, dout, mask=None, causal=False, scale=None, sink=None):
+    """Full backward of one (batch, head) slice: (dq, dk, dv), and with a sink
+    also the gradient of its logit: (dq, dk, dv, dsink)."""
+    dq, _, ds = attention_bwd_dq(q, k, v, dout, mask, causal, scale, sink=sink, with_dsink=True)
+    dk, dvv = attention_bwd_dkdv(q, k, v, dout, mask, causal, scale, sink=sink)
+    return (dq, dk, dvv) if sink is None else (dq, dk, dvv, float(ds.sum()))
 
 
 def tilemap(N, mask=None, causal=False, tq=128, tk=128):

@@ -96,22 +96,31 @@ static double oracle_row_scores(const oracle_mask *m, int d, double scale,
     return mx;
 }
 
-/* Softmax of one row in place: s_j <- P_ij.  Returns LSE_i = log sum_j exp(s_j).
- * A fully masked row gives P = 0 and LSE = -inf. */
-static double oracle_row_softmax(long N, double mx, double *s)
+/* Softmax of one row in place: s_j <- P_ij.  Returns LSE_i = log(exp(sink) +
+ * sum_j exp(s_j)).  `sink` is the row's attention-sink logit, a term of the
+ * denominator that carries no value (-inf: none); *p_sink (optional) receives
+ * its probability exp(sink - LSE_i).  A row with every key masked and no sink
+ * gives P = 0 and LSE = -inf. */
+static double oracle_row_softmax(long N, double mx, double sink, double *s, double *p_sink)
 {
+    if (sink > mx)
+        mx = sink;
     if (mx == -INFINITY) {
         for (long j = 0; j < N; ++j)
             s[j] = 0.0;
+        if (p_sink)
+            *p_sink = 0.0;
         return -INFINITY;
     }
-    double l = 0.0;
+    double l = (sink == -INFINITY) ? 0.0 : exp(sink - mx);
     for (long j = 0; j < N; ++j) {
         s[j] = (s[j] == -INFINITY) ? 0.0 : exp(s[j] - mx);
         l += s[j];
     }
     for (long j = 0; j < N; ++j)
         s[j] /= l;
+    if (p_sink)
+        *p_sink = (sink == -INFINITY) ? 0.0 : exp(sink - mx) / l;
     return mx + log(l);
 }
 
@@ -121,7 +130,7 @@ static double oracle_row_softmax(long N, double mx, double *s)
  *   rows: n_rows query indices, or NULL for all N rows
  *   o: [n_rows, dv]; lse: [n_rows] (natural log)
  */
-int oracle_fwd(int N, int d, int dv, double scale, int causal,
+int oracle_fwd(int N, int d, int dv, double scale, int causal, double sink,
                const double *q, const double *k, const double *v,
                const int32_t *lts, const int32_t *lte,
                const int32_t *uts, const int32_t *ute,
@@ -144,7 +153,7 @@ int oracle_fwd(int N, int d, int dv, double scale, int causal,
                 continue;
             long i = rows ? (long)rows[r] : r;
             double mx = oracle_row_scores(&m, d, scale, q, k, i, p);
-            lse[r] = oracle_row_softmax(N, mx, p);
+            lse[r] = oracle_row_softmax(N, mx, sink, p, NULL);
             for (int c = 0; c < dv; ++c) {
                 double acc = 0.0;
                 for (long j = 0; j < N; ++j)
@@ -160,15 +169,18 @@ int oracle_fwd(int N, int d, int dv, double scale, int causal,
 
 /*
  * Backward, query side, for selected rows of one (batch, head) slice.
- *   dout: [N, dv];  dq: [n_rows, d];  delta (optional): [n_rows], D_i.
- * dQ_i = scale * sum_j P_ij (dP_ij - D_i) k_j, dP_ij = <dO_i, v_j>.
+ *   dout: [N, dv];  dq: [n_rows, d];  delta (optional): [n_rows], D_i;
+ *   dsink (optional): [n_rows], the row's term of the sink logit's gradient.
+ * dQ_i = scale * sum_j P_ij (dP_ij - D_i) k_j, dP_ij = <dO_i, v_j>.  The sink
+ * carries no value, so its dP is 0 and its gradient term is -P_sink,i D_i.
  */
-int oracle_bwd_dq(int N, int d, int dv, double scale, int causal,
+int oracle_bwd_dq(int N, int d, int dv, double scale, int causal, double sink,
                   const double *q, const double *k, const double *v,
                   const double *dout,
                   const int32_t *lts, const int32_t *lte,
                   const int32_t *uts, const int32_t *ute,
-                  long n_rows, const int64_t *rows, double *dq, double *delta)
+                  long n_rows, const int64_t *rows, double *dq, double *delta,
+                  double *dsink)
 {
     oracle_mask m = {N, causal, lts, lte, uts, ute};
     if (!rows)
@@ -188,7 +200,8 @@ int oracle_bwd_dq(int N, int d, int dv, double scale, int causal,
                 continue;
             long i = rows ? (long)rows[r] : r;
             double mx = oracle_row_scores(&m, d, scale, q, k, i, p);
-            oracle_row_softmax(N, mx, p);
+            double p_sink = 0.0;
+            oracle_row_softmax(N, mx, sink, p, &p_sink);
             double D = 0.0;
             for (long j = 0; j < N; ++j) {
                 dp[j] = (p[j] != 0.0) ? oracle_dot(dout + i * dv, v + j * dv, dv) : 0.0;
@@ -196,6 +209,8 @@ int oracle_bwd_dq(int N, int d, int dv, double scale, int causal,
             }
             if (delta)
                 delta[r] = D;
+            if (dsink)
+                dsink[r] = -p_sink * D;
             for (int c = 0; c < d; ++c)
                 dq[r * d + c] = 0.0;
             for (long j = 0; j < N; ++j) {
@@ -220,7 +235,7 @@ int oracle_bwd_dq(int N, int d, int dv, double scale, int causal,
  * Every row that sees one of the columns first gets its LSE_i and D_i from a
  * full pass over that row; the columns are then summed over rows in order.
  */
-int oracle_bwd_dkdv(int N, int d, int dv, double scale, int causal,
+int oracle_bwd_dkdv(int N, int d, int dv, double scale, int causal, double sink,
                     const double *q, const double *k, const double *v,
                     const double *dout,
                     const int32_t *lts, const int32_t *lte,
@@ -264,7 +279,7 @@ int oracle_bwd_dkdv(int N, int d, int dv, double scale, int causal,
             if (!p || !need[i])
                 continue;
             double mx = oracle_row_scores(&m, d, scale, q, k, i, p);
-            row_lse[i] = oracle_row_softmax(N, mx, p);
+            row_lse[i] = oracle_row_softmax(N, mx, sink, p, NULL);
             double D = 0.0;
             for (long j = 0; j < N; ++j)
                 if (p[j] != 0.0)

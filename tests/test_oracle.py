@@ -298,3 +298,55 @@ def test_count_closed_forms():
     m = W.global_sliding(N, g, w)
     want = sum(N - j for j in range(g)) + sum(min(w, N - j) for j in range(g, N))
     assert oracle.count_unmasked(N, m.slice(0), m.causal) == want
+
+
+# ---------------------------------------------------------- attention sink
+def _torch_sink_reference(q, k, v, do, mask, causal, scale, sink):
+    """The sink as one more key column whose logit is `sink` and whose value is
+    zero, through fp64 torch softmax and autograd (independent of the oracle)."""
+    import torch
+    N = q.shape[0]
+    dense = torch.from_numpy(oracle.tilemap(N, mask, causal, tq=1, tk=1)[0] == oracle.TILE_SKIP)
+    qt, kt, vt = (torch.tensor(x, dtype=torch.float64, requires_grad=True) for x in (q, k, v))
+    st = torch.tensor(sink, dtype=torch.float64, requires_grad=True)
+    s = (qt @ kt.T) * scale
+    s = s.masked_fill(dense, float("-inf"))
+    logits = torch.cat([s, st.expand(N, 1)], dim=1)
+    p = torch.softmax(logits, dim=1)
+    o = p[:, :N] @ vt
+    lse = torch.logsumexp(logits, dim=1)
+    o.backward(torch.from_numpy(do))
+    return (o.detach().numpy(), lse.detach().numpy(), qt.grad.numpy(), kt.grad.numpy(),
+            vt.grad.numpy(), float(st.grad))
+
+
+@pytest.mark.parametrize("sink", [-2.0, 0.5, 3.0])
+def test_sink_is_an_extra_zero_value_key(sink):
+    rng = np.random.default_rng(21)
+    N, d = 96, 16
+    q, k, v, do = (rng.standard_normal((N, d)) for _ in range(4))
+    mask = W.causal_document(N, [W.uniform_lengths(rng, 10, 40, N)]).slice(0)
+    scale = 1 / np.sqrt(d)
+    o, lse = oracle.attention_fwd(q, k, v, mask, True, scale, sink=sink)
+    dq, dk, dv, ds = oracle.attention_bwd(q, k, v, do, mask, True, scale, sink=sink)
+    ro, rl, rdq, rdk, rdv, rds = _torch_sink_reference(q, k, v, do, mask, True, scale, sink)
+    for got, ref in ((o, ro), (lse, rl), (dq, rdq), (dk, rdk), (dv, rdv)):
+        np.testing.assert_allclose(got, ref, atol=1e-12, rtol=1e-12)
+    assert abs(ds - rds) <= 1e-12 * max(1.0, abs(rds))
+
+
+def test_sink_limits():
+    """A vanishing sink is no sink; a row whose keys are all masked gives O = 0,
+    LSE = sink and adds nothing to the sink's gradient."""
+    rng = np.random.default_rng(22)
+    N, d = 64, 8
+    q, k, v, do = (rng.standard_normal((N, d)) for _ in range(4))
+    mask = {"lts": np.full(N, 20, np.int32), "lte": np.full(N, 30, np.int32)}
+    o0, l0 = oracle.attention_fwd(q, k, v, mask, False)
+    o1, l1 = oracle.attention_fwd(q, k, v, mask, False, sink=-1e4)
+    np.testing.assert_allclose(o1, o0, atol=1e-15)
+    np.testing.assert_allclose(l1[np.isfinite(l0)], l0[np.isfinite(l0)], atol=1e-15)
+    o2, l2 = oracle.attention_fwd(q, k, v, mask, False, sink=1.25)
+    assert (o2[20:30] == 0).all() and np.allclose(l2[20:30], 1.25)
+    _, _, terms = oracle.attention_bwd_dq(q, k, v, do, mask, False, sink=1.25, with_dsink=True)
+    assert (terms[20:30] == 0).all() and (terms[:20] != 0).all()
