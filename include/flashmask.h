@@ -67,6 +67,19 @@ typedef struct {
  * order, so dQ/dK/dV are bit-identical from run to run.  debug_bounds is
  * reserved and must be 0.  wait_timeout_ns bounds every wait on the device;
  * 0 selects 1 s.
+ * sink (optional, may be NULL): per-head attention-sink logits, [H] fp32 on
+ * the device (FlashMask README, "News", names sink bias without a formula;
+ * reading taken): head h's logit joins every row's softmax denominator as a
+ * term exp(sink[h]) that carries no value, so
+ *     O_i = sum_j exp(s_ij) v_j / (exp(sink[h]) + sum_j exp(s_ij)),
+ *     LSE_i = log(exp(sink[h]) + sum_j exp(s_ij));
+ * a row whose keys are all masked gets O = 0 and LSE = sink[h].  Pass the same
+ * logits to flashmask_fwd and flashmask_bwd.
+ * dsink (optional, flashmask_bwd only, may be NULL): [H] fp32 on the device,
+ * receives the gradient of the sink logits, -sum_i exp(sink[h] - LSE_i) D_i
+ * over the batch and rows of head h (D_i = sum_c dO_ic O_ic), summed in a
+ * fixed order.  With a sink, a sink-gradient kernel runs after the preprocess
+ * kernel; kernel_events do not record it.
  * kernel_events (optional, may be NULL): an array of n_kernel_events
  * cudaEvent_t handles owned by the caller.  The call records
  * kernel_events[2i] on `stream` just before its i-th kernel launch and
@@ -80,6 +93,8 @@ typedef struct {
     unsigned long long wait_timeout_ns;
     void **kernel_events;
     int n_kernel_events;
+    const float *sink;
+    float *dsink;
 } fm_options;
 
 /* Tile classes written by flashmask_classify (128 x 128 tiles). */

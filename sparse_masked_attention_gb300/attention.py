@@ -69,10 +69,15 @@ def make_problem(B, H, Hm, N, d, dv, scale, causal) -> _b.fm_problem:
                          int(bool(causal)))
 
 
-def make_options(deterministic=False, wait_timeout_ns=0, kernel_events=None) -> _b.fm_options:
+def make_options(deterministic=False, wait_timeout_ns=0, kernel_events=None, sink=None,
+                 dsink=None) -> _b.fm_options:
     """kernel_events: optional list of raw cudaEvent_t handles (ints), recorded in
-    pairs around each kernel launch of the call."""
-    opt = _b.fm_options(int(bool(deterministic)), 0, int(wait_timeout_ns), None, 0)
+    pairs around each kernel launch of the call.  sink / dsink: optional [H]
+    fp32 CUDA tensors, the attention-sink logits and (backward) their gradient."""
+    opt = _b.fm_options(int(bool(deterministic)), 0, int(wait_timeout_ns), None, 0,
+                        None if sink is None else sink.data_ptr(),
+                        None if dsink is None else dsink.data_ptr())
+    opt._tensors = (sink, dsink)
     if kernel_events:
         arr = (ctypes.c_void_p * len(kernel_events))(*kernel_events)
         opt.kernel_events = ctypes.cast(arr, ctypes.POINTER(ctypes.c_void_p))
@@ -99,13 +104,24 @@ def workspace_size(B, H, Hm, N, d, dv, is_bwd: bool, deterministic=False) -> int
     return n
 
 
+def _check_sink(sink, H, device):
+    if sink is not None and (sink.dtype != torch.float32 or tuple(sink.shape) != (H,) or
+                             not sink.is_contiguous() or not _same_device(sink.device, device)):
+        raise FlashMaskError(f"sink must be a contiguous float32 tensor of shape ({H},) on "
+                             f"{device}")
+
+
 def fwd(q, k, v, lts=None, lte=None, uts=None, ute=None, causal=False, scale=None,
-        out=None, lse=None, workspace=None, stream=None, options=None):
-    """Masked attention forward; returns (o [B,N,H,dv] bf16, lse [B,H,N] fp32)."""
+        out=None, lse=None, workspace=None, stream=None, options=None, sink=None):
+    """Masked attention forward; returns (o [B,N,H,dv] bf16, lse [B,H,N] fp32).
+    sink: optional [H] fp32 attention-sink logits (see flashmask.h)."""
     B, N, H, d, dv = _check_qkv(q, k, v)
     Hm, mp, _keep = _mask_args((lts, lte, uts, ute), B, H, N, q.device)
     prob = make_problem(B, H, Hm, N, d, dv, scale, causal)
-    opt = make_options() if options is None else options
+    _check_sink(sink, H, q.device)
+    if options is not None and sink is not None:
+        raise FlashMaskError("pass the sink either in options or as sink=, not both")
+    opt = make_options(sink=sink) if options is None else options
     if out is None:
         out = torch.empty((B, N, H, dv), dtype=torch.bfloat16, device=q.device)
     if lse is None:
@@ -122,9 +138,13 @@ def fwd(q, k, v, lts=None, lte=None, uts=None, ute=None, causal=False, scale=Non
 
 def bwd(q, k, v, o, lse, dout, lts=None, lte=None, uts=None, ute=None, causal=False,
         scale=None, deterministic=False, dq=None, dk=None, dv=None, workspace=None,
-        stream=None, options=None):
-    """Masked attention backward; returns (dq, dk, dv) in bf16."""
+        stream=None, options=None, sink=None):
+    """Masked attention backward; returns (dq, dk, dv) in bf16, and with a sink
+    (the forward's [H] fp32 logits) also their gradient: (dq, dk, dv, dsink)."""
     B, N, H, d, dvd = _check_qkv(q, k, v)
+    _check_sink(sink, H, q.device)
+    if options is not None and sink is not None:
+        raise FlashMaskError("pass the sink either in options or as sink=, not both")
     for name, t, shape in (("o", o, (B, N, H, dvd)), ("dout", dout, (B, N, H, dvd))):
         if t.dtype != torch.bfloat16 or not t.is_contiguous() or tuple(t.shape) != shape:
             raise FlashMaskError(f"{name} must be contiguous bf16 {shape}")
@@ -132,7 +152,8 @@ def bwd(q, k, v, o, lse, dout, lts=None, lte=None, uts=None, ute=None, causal=Fa
         raise FlashMaskError("lse must be contiguous fp32 [B, H, N]")
     Hm, mp, _keep = _mask_args((lts, lte, uts, ute), B, H, N, q.device)
     prob = make_problem(B, H, Hm, N, d, dvd, scale, causal)
-    opt = make_options(deterministic) if options is None else options
+    dsink = None if sink is None else torch.empty(H, dtype=torch.float32, device=q.device)
+    opt = make_options(deterministic, sink=sink, dsink=dsink) if options is None else options
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
@@ -144,7 +165,7 @@ def bwd(q, k, v, o, lse, dout, lts=None, lte=None, uts=None, ute=None, causal=Fa
                           dv.data_ptr(), workspace.data_ptr(), workspace.numel(),
                           _stream(stream))
     _check(st, "flashmask_bwd")
-    return dq, dk, dv
+    return (dq, dk, dv) if sink is None else (dq, dk, dv, dsink)
 
 
 def classify(N, B=1, H=1, lts=None, lte=None, uts=None, ute=None, causal=False, device="cuda",
@@ -184,24 +205,27 @@ class FlashMaskAttention(torch.autograd.Function):
     """Autograd wrapper: forward and backward both run in the CUDA library."""
 
     @staticmethod
-    def forward(ctx, q, k, v, lts, lte, uts, ute, causal, scale, deterministic):
-        o, lse = fwd(q, k, v, lts, lte, uts, ute, causal, scale)
-        ctx.save_for_backward(q, k, v, o, lse, lts, lte, uts, ute)
+    def forward(ctx, q, k, v, lts, lte, uts, ute, causal, scale, deterministic, sink):
+        o, lse = fwd(q, k, v, lts, lte, uts, ute, causal, scale, sink=sink)
+        ctx.save_for_backward(q, k, v, o, lse, lts, lte, uts, ute, sink)
         ctx.causal, ctx.scale, ctx.deterministic = causal, scale, deterministic
         return o
 
     @staticmethod
     def backward(ctx, do):
-        q, k, v, o, lse, lts, lte, uts, ute = ctx.saved_tensors
-        dq, dk, dv = bwd(q, k, v, o, lse, do.contiguous(), lts, lte, uts, ute, ctx.causal,
-                         ctx.scale, ctx.deterministic)
-        return dq, dk, dv, None, None, None, None, None, None, None
+        q, k, v, o, lse, lts, lte, uts, ute, sink = ctx.saved_tensors
+        g = bwd(q, k, v, o, lse, do.contiguous(), lts, lte, uts, ute, ctx.causal, ctx.scale,
+                ctx.deterministic, sink=sink)
+        dsink = g[3] if sink is not None else None
+        return g[0], g[1], g[2], None, None, None, None, None, None, None, dsink
 
 
 def flashmask_attention(q, k, v, lts=None, lte=None, uts=None, ute=None, causal=False,
-                        scale=None, deterministic=False):
-    """O = softmax(Q K^T * scale + M) V with the column-wise mask; differentiable."""
-    return FlashMaskAttention.apply(q, k, v, lts, lte, uts, ute, causal, scale, deterministic)
+                        scale=None, deterministic=False, sink=None):
+    """O = softmax(Q K^T * scale + M) V with the column-wise mask; differentiable.
+    sink: optional [H] fp32 attention-sink logits (differentiable as well)."""
+    return FlashMaskAttention.apply(q, k, v, lts, lte, uts, ute, causal, scale, deterministic,
+                                    sink)
 
 
 def default_scale(d: int) -> float:

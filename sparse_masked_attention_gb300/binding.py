@@ -36,7 +36,8 @@ class fm_options(ctypes.Structure):
     _fields_ = [("deterministic", ctypes.c_int), ("debug_bounds", ctypes.c_int),
                 ("wait_timeout_ns", ctypes.c_ulonglong),
                 ("kernel_events", ctypes.POINTER(ctypes.c_void_p)),
-                ("n_kernel_events", ctypes.c_int)]
+                ("n_kernel_events", ctypes.c_int),
+                ("sink", ctypes.c_void_p), ("dsink", ctypes.c_void_p)]
 
 
 EXPORTS = ("flashmask_workspace_size", "flashmask_fwd", "flashmask_bwd", "flashmask_classify",

@@ -51,6 +51,9 @@ fm_status make_geometry(const fm_problem *p, const fm_options *opt, Geometry *g)
     g->timeout_ns =
         (opt && opt->wait_timeout_ns) ? static_cast<uint64_t>(opt->wait_timeout_ns) : DEFAULT_TIMEOUT_NS;
     g->deterministic = opt ? opt->deterministic : 0;
+    g->sink = opt ? opt->sink : nullptr;
+    g->dsink = opt ? opt->dsink : nullptr;
+    if (g->dsink && !g->sink) return FM_ERR_INVALID_ARG;  // a gradient needs its logits
     // The list and map sizes must fit the int indexing of the kernels.
     const double entries = static_cast<double>(g->B) * g->Hm * g->T * g->T;
     if (entries > 2.0e9) return FM_ERR_INVALID_ARG;
@@ -165,6 +168,7 @@ size_t carve_workspace(const Geometry &g, bool bwd, void *base, Workspace *ws) {
     w.delta = nullptr;
     w.v16 = nullptr;
     w.do16 = nullptr;
+    w.sink_part = nullptr;
     if (bwd) {
         const size_t rows = static_cast<size_t>(g.B) * g.H * g.Npad;
         w.lse2 = static_cast<float *>(take(rows * sizeof(float)));
@@ -172,6 +176,7 @@ size_t carve_workspace(const Geometry &g, bool bwd, void *base, Workspace *ws) {
         const size_t vbytes = static_cast<size_t>(g.B) * g.N * g.H * g.dv * 2;
         w.v16 = take(vbytes);
         w.do16 = take(vbytes);
+        w.sink_part = static_cast<float *>(take(rows / 16 * sizeof(float)));
     }
     if (ws) *ws = w;
     return off;

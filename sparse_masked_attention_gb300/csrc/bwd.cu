@@ -83,7 +83,9 @@ __global__ void __launch_bounds__(256) preprocess_kernel(
     int N, int H, int dv, int Npad, int rows_total, const __nv_bfloat16 *__restrict__ o,
     const __nv_bfloat16 *__restrict__ dout, const __nv_bfloat16 *__restrict__ v,
     const float *__restrict__ lse, float *__restrict__ lse2, float *__restrict__ delta,
-    uint4 *__restrict__ v16, uint4 *__restrict__ do16) {
+    uint4 *__restrict__ v16, uint4 *__restrict__ do16, const float *__restrict__ sink,
+    float *__restrict__ sink_part) {
+    __shared__ float sink_rows[16];
     pdl_wait();  // orders it after the kernels before (it rewrites their inputs' copies)
     pdl_trigger();
     const int r0 = blockIdx.x * 16 + (threadIdx.x >> 4);  // over B*H*Npad
@@ -114,15 +116,53 @@ __global__ void __launch_bounds__(256) preprocess_kernel(
     }
 #pragma unroll
     for (int off = 8; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off, 16);
+    float sink_term = 0.f;  // the row's term of the sink-logit gradient
     if (valid && t == 0) {
         float l2 = INFINITY;
         if (i < N) {
             const float l = lse[static_cast<size_t>(bh) * N + i];
             l2 = (l == -INFINITY) ? INFINITY : l * 1.4426950408889634f;
+            if (sink && l != -INFINITY) sink_term = -expf(sink[h] - l) * acc;
         }
         lse2[r] = l2;
         delta[r] = i < N ? acc : 0.f;
     }
+    // The block's 16 rows belong to one (batch, head) (Npad is a multiple of
+    // 16): their terms are summed in row order into the block's slot.
+    if (sink_part) {
+        if (t == 0) sink_rows[threadIdx.x >> 4] = sink_term;
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            float s = 0.f;
+#pragma unroll
+            for (int k = 0; k < 16; ++k) s += sink_rows[k];
+            sink_part[blockIdx.x] = s;
+        }
+    }
+}
+
+// Gradient of head h's sink logit: the per-block sums of every (batch, head h)
+// row block, added in a fixed order (threads stride the blocks, then a fixed
+// tree), so the result is the same from run to run.
+__global__ void __launch_bounds__(256) sink_grad_kernel(int B, int H, int blocks_per_head,
+                                                        const float *__restrict__ sink_part,
+                                                        float *__restrict__ dsink) {
+    __shared__ float red[256];
+    pdl_wait();  // the preprocess kernel's block sums
+    pdl_trigger();
+    const int h = blockIdx.x;
+    float s = 0.f;
+    for (int b = 0; b < B; ++b) {
+        const float *part = sink_part + (static_cast<size_t>(b) * H + h) * blocks_per_head;
+        for (int j = threadIdx.x; j < blocks_per_head; j += 256) s += part[j];
+    }
+    red[threadIdx.x] = s;
+    __syncthreads();
+    for (int w = 128; w > 0; w >>= 1) {
+        if (static_cast<int>(threadIdx.x) < w) red[threadIdx.x] += red[threadIdx.x + w];
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) dsink[h] = red[0];
 }
 
 struct BwdParams {
@@ -1093,8 +1133,11 @@ cudaError_t launch_bwd(const Geometry &g, const Workspace &ws, const BwdArgs &a,
         rows_total, static_cast<const __nv_bfloat16 *>(a.o),
         static_cast<const __nv_bfloat16 *>(a.dout), static_cast<const __nv_bfloat16 *>(a.v),
         static_cast<const float *>(a.lse), ws.lse2, ws.delta, static_cast<uint4 *>(ws.v16),
-        static_cast<uint4 *>(ws.do16));
+        static_cast<uint4 *>(ws.do16), g.sink, g.dsink ? ws.sink_part : nullptr);
     rec.after(st);
+    if (e == cudaSuccess && g.dsink)
+        e = launch_pdl(sink_grad_kernel, dim3(g.H), dim3(256), 0, st, g.B, g.H, g.Npad / 16,
+                       static_cast<const float *>(ws.sink_part), g.dsink);
     if (e != cudaSuccess) return e;
     // DkdvCfg<d, dv, query sub-tile, Q stages, dK, dV, groups>;
     // DqCfg<d, dv, key sub-tile, K stages, groups>

@@ -21,6 +21,8 @@ struct Geometry {
     int causal;
     uint64_t timeout_ns;
     int deterministic;
+    const float *sink;  // [H] attention-sink logits, or nullptr
+    float *dsink;       // [H] their gradient (backward), or nullptr
 };
 
 // Normalised mask boundaries per key column: (LTS, LTE, UTS, UTE) clamped to
@@ -42,6 +44,7 @@ struct Workspace {
     float *delta;      // [B*H][Npad] D_i = sum_c dO_ic O_ic
     void *v16;         // [B,N,H,dv] fp16 copy of V   (backward)
     void *do16;        // [B,N,H,dv] fp16 copy of dO  (backward)
+    float *sink_part;  // [B*H*Npad/16] per-block sink-gradient sums (backward)
 };
 
 // Optional per-kernel event recording (fm_options.kernel_events).

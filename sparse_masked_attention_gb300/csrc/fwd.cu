@@ -41,6 +41,7 @@ struct FwdParams {
     const int *cnt;
     const int *order;  // pair kernel: pairs by decreasing key-tile count
     float *lse;
+    const float *sink;  // [H] attention-sink logits, or nullptr
     int N, H, Hm, T, B, Npad, causal;
     float sl2;  // scale * log2(e)
     uint64_t timeout_ns;
@@ -75,6 +76,32 @@ struct FwdCfg {
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
     static_assert(KS % NWG == 0 && VS % NWG == 0, "per-group ring stages");
 };
+
+// Row normalisation.  O_acc and the row sum l are relative to the row's
+// reference max m (log2 units); O = O_acc * factor.  An attention-sink logit
+// sink2 (log2 units, -inf for none) adds exp2(sink2 - m) to the denominator,
+// a term with no value.  Returns the factor (0 when the row saw no key) and
+// writes the row's LSE in log2 units (-inf when it saw neither a key nor a
+// sink).
+__device__ __forceinline__ float row_finish(float m, float l, float sink2, float &lse2) {
+    if (!(l > 0.f)) {  // every key of the row masked
+        lse2 = sink2;
+        return 0.f;
+    }
+    if (sink2 == -INFINITY) {
+        lse2 = m + lg2(l);
+        return 1.0f / l;
+    }
+    if (sink2 <= m) {
+        const float lt = l + ex2(sink2 - m);
+        lse2 = m + lg2(lt);
+        return 1.0f / lt;
+    }
+    const float r = ex2(m - sink2);  // the sink dominates: rescale to it
+    const float lt = fmaf(l, r, 1.0f);
+    lse2 = sink2 + lg2(lt);
+    return r / lt;
+}
 
 // Warp-uniform bounded wait: every lane polls, the warp agrees on the result.
 __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, uint64_t tmo,
@@ -570,7 +597,9 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             c_begin = wg * (C::DV / 64);
             c_end = c_begin + C::DV / 64;
         }
-        const float inv = l_all > 0.f ? 1.0f / l_all : 0.f;
+        float lse2_row;
+        const float sink2 = p.sink ? p.sink[h] * 1.4426950408889634f : NEG_INF;
+        const float inv = row_finish(m_all, l_all, sink2, lse2_row);
         // The normalised bf16 row goes to shared memory in the 128B-swizzled
         // layout of the output tensor map (64-column boxes of 128 rows; K
         // stages 1.. are idle by now); TMA then stores whole boxes, clipping
@@ -610,8 +639,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         }
         if (wg == 0 && store) {
             const float ln2 = 0.69314718055994530942f;
-            p.lse[(static_cast<size_t>(b) * p.H + h) * p.N + grow] =
-                l_all > 0.f ? (m_all + lg2(l_all)) * ln2 : NEG_INF;
+            p.lse[(static_cast<size_t>(b) * p.H + h) * p.N + grow] = lse2_row * ln2;
         }
     }
 
@@ -632,6 +660,7 @@ cudaError_t launch_cfg(const Geometry &g, const Workspace &ws, const FwdArgs &a,
     p.list = ws.fwd_list;
     p.cnt = ws.fwd_cnt;
     p.order = nullptr;
+    p.sink = g.sink;
     p.B = g.B;
     p.lse = a.lse;
     p.N = g.N;
@@ -942,7 +971,9 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         // (its last S has run) stages the normalised bf16 rows for TMA.
         if (n > 0 && !failed) failed = !warp_wait(&o_done[wg], 0, tmo, abort);
         tc_fence_after();
-        const float inv = l_sum > 0.f ? 1.0f / l_sum : 0.f;
+        float lse2_row;
+        const float sink2 = p.sink ? p.sink[h] * 1.4426950408889634f : NEG_INF;
+        const float inv = row_finish(m_ref, l_sum, sink2, lse2_row);
         uint8_t *stage = sQ + wg * C::Q_BYTES;
         for (int c = 0; c < C::DV / 32; ++c) {
             float o[32];
@@ -977,8 +1008,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         }
         if (grow < p.N && !failed) {
             const float ln2 = 0.69314718055994530942f;
-            p.lse[(static_cast<size_t>(b) * p.H + h) * p.N + grow] =
-                l_sum > 0.f ? (m_ref + lg2(l_sum)) * ln2 : NEG_INF;
+            p.lse[(static_cast<size_t>(b) * p.H + h) * p.N + grow] = lse2_row * ln2;
         }
     }
 
@@ -999,6 +1029,7 @@ cudaError_t launch_pair(const Geometry &g, const Workspace &ws, const FwdArgs &a
     p.list = ws.pair_list;
     p.cnt = ws.pair_cnt;
     p.order = ws.pair_order;
+    p.sink = g.sink;
     p.B = g.B;
     p.lse = a.lse;
     p.N = g.N;
