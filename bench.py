@@ -355,18 +355,40 @@ def run_chunked(args, cfg, q, k, v, do, mask, vec, has_bwd, det, step_flops, wor
             fm.bwd_chunked(q, k, v, o, lse, do, *vec, causal=mask.causal, deterministic=det,
                            chunks=C, ranks=R)
 
+    def timed(fn):
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        start.record()
+        for _ in range(args.steps):
+            fn()
+        end.record()
+        torch.cuda.synchronize()
+        fm.get_error()
+        return start.elapsed_time(end) / args.steps
+
     for _ in range(args.warmup):
         step()
     fm.get_error()
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    torch.cuda.synchronize()
-    start.record()
-    for _ in range(args.steps):
-        step()
-    end.record()
-    torch.cuda.synchronize()
-    fm.get_error()
-    ms = start.elapsed_time(end) / args.steps
+    ms_eager = timed(step)
+    # The same step captured once in a CUDA graph and replayed: the emulation
+    # issues every pair from Python, and the graph takes that host work out.
+    ms_graph, graph_note = None, None
+    try:
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            step()
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g, capture_error_mode="relaxed"):
+            step()
+        for _ in range(args.warmup):
+            g.replay()
+        ms_graph = timed(g.replay)
+    except Exception as ex:  # capture refused: report the eager figure only
+        graph_note = f"graph capture failed: {type(ex).__name__}"
+    ms = ms_graph if ms_graph is not None else ms_eager
     value = step_flops / (ms * 1e-3) / 1e12 * world
     pk, _src = peaks()
     return {
@@ -382,6 +404,10 @@ def run_chunked(args, cfg, q, k, v, do, mask, vec, has_bwd, det, step_flops, wor
                                                   "assignment": "zigzag" if R else "one chunk each"},
                    "parallelism": f"replicas x{world}"},
         "frac_of_peak": round(value / world / pk["bf16_tflops"], 4),
+        "timing": "CUDA graph replay of one captured step" if ms_graph is not None else
+                  "eager (" + str(graph_note) + ")",
+        "eager": {"value": round(step_flops / (ms_eager * 1e-3) / 1e12 * world, 3),
+                  "ms_per_step": round(ms_eager, 4)},
         "roofline": None, "kernel_ms": None, "gpu_launches": None, "e2e": None, "clocks": None,
     }
 
