@@ -190,6 +190,23 @@ def setup(cfg, seed, device):
     return q, k, v, do, mask, vec, u_heads
 
 
+def max_over_ranks(ms: float, world: int, device) -> float:
+    """The slowest rank's time: every rank contributes its own, all get the max."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_value(step_flops: float, ms_step: float, world: int) -> float:
+    """Effective TFLOP/s of the whole job: every rank runs one replica's step
+    (`step_flops` each) in the slowest rank's time `ms_step`."""
+    return step_flops / (ms_step * 1e-3) / 1e12 * world
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     import torch.distributed as dist
@@ -272,11 +289,7 @@ def run_ours(args, rank, world, local_rank):
         dist.barrier()
     clocks = sampler.stop() if sampler else None
     fm.get_error()
-    ms_total = start.elapsed_time(end)
-    if world > 1:
-        t = torch.tensor([ms_total], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = max_over_ranks(start.elapsed_time(end), world, device)
     ms_step = ms_total / K
 
     # per-kernel durations from the library's event pairs
@@ -304,7 +317,7 @@ def run_ours(args, rank, world, local_rank):
 
     # forward alone, same inputs (event pairs of the forward calls)
     fwd_ms = sum(avg[f"fwd:{n}"] for n in fwd_names)
-    value = step_flops / (ms_step * 1e-3) / 1e12 * world
+    value = whole_job_value(step_flops, ms_step, world)
     launches = K * (len(fwd_names) + (len(bwd_names) if has_bwd else 0))
 
     e2e = None
