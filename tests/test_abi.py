@@ -91,3 +91,31 @@ def test_invalid_args_rejected_before_cuda(lib):
     st = B.flashmask_fwd(p, opt, 256, 256, 256, None, None, None, None, 256, 256, 256, 1 << 30,
                          None)
     assert st == B.FM_ERR_INVALID_ARG
+
+
+def test_chunk_entry_points_reject_bad_arguments_before_cuda(lib):
+    p = _prob(N=1024)
+    out = [256, 512, 768, 1024]
+    # chunk length 0, chunks that overrun N, chunks not on a common grid
+    for q0, k0, ln in ((0, 0, 0), (900, 0, 256), (0, 100, 256), (-256, 0, 256)):
+        st, _ = B.flashmask_localize(p, None, None, None, None, q0, k0, ln, *out, None)
+        assert st == B.FM_ERR_INVALID_ARG, (q0, k0, ln)
+    st, _ = B.flashmask_localize(p, 256, None, None, None, 0, 0, 256, *out, None)  # half pair
+    assert st == B.FM_ERR_INVALID_ARG
+    # a causal key chunk after the query chunk: skipped, nothing enqueued
+    st, flag = B.flashmask_localize(_prob(N=1024, causal=1), None, None, None, None, 0, 256, 256,
+                                    *out, None)
+    assert st == B.FM_OK and flag == -1
+    assert B.flashmask_merge_init(0, 2, 64, 256, 512, None) == B.FM_ERR_INVALID_ARG
+    assert B.flashmask_merge(16, 2, 12, 256, 512, 768, 1024, None) == B.FM_ERR_INVALID_ARG
+    assert B.flashmask_merge(16, 2, 64, 8, 512, 768, 1024, None) == B.FM_ERR_INVALID_ARG
+    assert B.flashmask_merge_finish(16, 2, 64, 256, 512, 768, 1024, 8, None) == \
+        B.FM_ERR_INVALID_ARG  # LSE row stride below the chunk length
+    assert B.flashmask_accumulate(12, 256, 512, None) == B.FM_ERR_INVALID_ARG
+    assert B.flashmask_to_bf16(16, 8, 512, None) == B.FM_ERR_INVALID_ARG
+    assert B.flashmask_accumulate(0, 256, 512, None) == B.FM_OK  # nothing to do
+
+
+def test_sink_gradient_needs_its_logits(lib):
+    opt = B.fm_options(0, 0, 0, None, 0, None, 256)
+    assert B.flashmask_workspace_size(_prob(), opt, 1) == 0

@@ -113,3 +113,26 @@ def test_chunked_equals_single_call_forward():
     fin = torch.isfinite(l1)
     assert torch.equal(torch.isneginf(l1), torch.isneginf(l2))
     assert (l1[fin] - l2[fin]).abs().max().item() <= 1e-4
+
+
+def test_chunked_odd_chunk_count_one_chunk_per_rank():
+    """Three chunks, no zigzag: every rank (here, loop step) owns one chunk."""
+    B, H, N, d = 1, 2, 768, 64
+    rng = np.random.default_rng(12)
+    q, k, v, do = W.make_inputs(B, N, H, d, d, seed=4, device="cuda")
+    mask = _family("share_question", N, B, rng)
+    vec = cuda_mask(mask)
+    o, lse = fm.fwd_chunked(q, k, v, *vec, causal=mask.causal, chunks=3)
+    grads = fm.bwd_chunked(q, k, v, o, lse, do, *vec, causal=mask.causal, chunks=3)
+    fm.get_error()
+    scale = 1 / np.sqrt(d)
+    for h in range(H):
+        qh, kh, vh, doh = head(q, 0, h), head(k, 0, h), head(v, 0, h), head(do, 0, h)
+        ms = mask_slice(mask, 0, h)
+        ro, rl = oracle.attention_fwd(qh, kh, vh, ms, mask.causal, scale)
+        assert_close("O", head(o, 0, h), ro)
+        assert_lse(lse[0, h].cpu().numpy(), rl)
+        for name, g, ref in zip(("dQ", "dK", "dV"), grads,
+                                oracle.attention_bwd(qh, kh, vh, doh, ms, mask.causal, scale)):
+            assert_close(name, head(g, 0, h), ref,
+                         max_abs=MAX_ABS + 3 * 2.0 ** -9 * float(np.max(np.abs(ref))))
