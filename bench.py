@@ -159,8 +159,11 @@ def flops_per_pair(d, dv):
 
 
 def kernel_names(d, dv):
+    """Kernels of the step's forward and backward calls, in launch order.  The
+    backward reuses the tile map and lists the forward built in the shared
+    workspace, so it starts at the preprocess kernel."""
     fwd = ["classify", "lists", "fwd"]
-    bwd = ["classify", "lists", "bwd_preprocess"]
+    bwd = ["bwd_preprocess"]
     bwd += ["bwd_dkdv_dv", "bwd_dkdv_dk"] if (d == 256 and dv == 256) else ["bwd_dkdv"]
     bwd += ["bwd_dq"]
     return fwd, bwd
@@ -227,10 +230,12 @@ def run_ours(args, rank, world, local_rank):
     o = torch.empty((B, N, H, dv), dtype=torch.bfloat16, device=device)
     lse = torch.empty((B, H, N), dtype=torch.float32, device=device)
     dq, dk, dvv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    ws_f = torch.empty(fm.workspace_size(B, H, 1, N, d, dv, False), dtype=torch.uint8,
-                       device=device)
+    # One workspace, sized for the backward, serves both calls: the backward
+    # reuses the tile map and lists the forward writes into it.
     ws_b = torch.empty(fm.workspace_size(B, H, 1, N, d, dv, True, det), dtype=torch.uint8,
                        device=device)
+    ws_f = ws_b if has_bwd else torch.empty(fm.workspace_size(B, H, 1, N, d, dv, False),
+                                            dtype=torch.uint8, device=device)
     stream = torch.cuda.current_stream()
 
     def make_events(n):
@@ -244,9 +249,10 @@ def run_ours(args, rank, world, local_rank):
     ev_b = [make_events(2 * len(bwd_names)) for _ in range(K)] if has_bwd else []
     torch.cuda.synchronize()
     opt_f = [fm.make_options(kernel_events=[e.cuda_event for e in evs]) for evs in ev_f]
-    opt_b = [fm.make_options(det, kernel_events=[e.cuda_event for e in evs]) for evs in ev_b]
+    opt_b = [fm.make_options(det, kernel_events=[e.cuda_event for e in evs], reuse_tile_map=True)
+             for evs in ev_b]
     plain_f = fm.make_options()
-    plain_b = fm.make_options(det)
+    plain_b = fm.make_options(det, reuse_tile_map=True)
 
     def step(i=None):
         fm.fwd(q, k, v, *vec, causal=mask.causal, out=o, lse=lse, workspace=ws_f,
@@ -451,10 +457,11 @@ def run_e2e(q, k, v, do, vec, mask, cfg, has_bwd, det, args, step_flops, world, 
     lse = torch.empty((B, H, N), dtype=torch.float32, device=device)
     host_out = [torch.empty(s_, dtype=torch.bfloat16).pin_memory() for s_ in out_shapes]
     d2h = sum(t.numel() * t.element_size() for t in host_out)
-    ws_f = torch.empty(fm.workspace_size(B, H, 1, N, d, dv, False), dtype=torch.uint8,
-                       device=device)
     ws_b = torch.empty(fm.workspace_size(B, H, 1, N, d, dv, True, det), dtype=torch.uint8,
                        device=device) if has_bwd else None
+    ws_f = ws_b if has_bwd else torch.empty(fm.workspace_size(B, H, 1, N, d, dv, False),
+                                            dtype=torch.uint8, device=device)
+    opt_b = fm.make_options(det, reuse_tile_map=True)
     s_comp = torch.cuda.current_stream(device)
     s_in, s_out = torch.cuda.Stream(device), torch.cuda.Stream(device)
     ev = lambda: torch.cuda.Event()
@@ -481,7 +488,7 @@ def run_e2e(q, k, v, do, vec, mask, cfg, has_bwd, det, args, step_flops, world, 
                workspace=ws_f)
         if has_bwd:
             fm.bwd(x[0], x[1], x[2], o[0], lse, x[3], *dev_vec[sl], causal=mask.causal,
-                   deterministic=det, dq=o[1], dk=o[2], dv=o[3], workspace=ws_b)
+                   dq=o[1], dk=o[2], dv=o[3], workspace=ws_b, options=opt_b)
         comp_done[sl].record(s_comp)
         with torch.cuda.stream(s_out):
             s_out.wait_event(comp_done[sl])

@@ -80,6 +80,15 @@ typedef struct {
  * over the batch and rows of head h (D_i = sum_c dO_ic O_ic), summed in a
  * fixed order.  With a sink, a sink-gradient kernel runs after the preprocess
  * kernel; kernel_events do not record it.
+ * reuse_tile_map (0 or 1): the workspace already holds the tile map and tile
+ * lists of this very problem and mask, written by an earlier flashmask_fwd or
+ * flashmask_bwd on the same workspace (every call writes all of them), and
+ * the call skips the classify and lists kernels (kernel_events then start at
+ * the next kernel).  A forward and the backward of one layer, or layers that
+ * share one mask, can share them this way; the workspace must then be sized
+ * for the backward (is_bwd = 1) in every call, since the backward's own parts
+ * follow the shared ones.  The library cannot check that the contents match:
+ * stale contents give wrong results.
  * kernel_events (optional, may be NULL): an array of n_kernel_events
  * cudaEvent_t handles owned by the caller.  The call records
  * kernel_events[2i] on `stream` just before its i-th kernel launch and
@@ -95,6 +104,7 @@ typedef struct {
     int n_kernel_events;
     const float *sink;
     float *dsink;
+    int reuse_tile_map;
 } fm_options;
 
 /* Tile classes written by flashmask_classify (128 x 128 tiles). */

@@ -70,13 +70,15 @@ def make_problem(B, H, Hm, N, d, dv, scale, causal) -> _b.fm_problem:
 
 
 def make_options(deterministic=False, wait_timeout_ns=0, kernel_events=None, sink=None,
-                 dsink=None) -> _b.fm_options:
+                 dsink=None, reuse_tile_map=False) -> _b.fm_options:
     """kernel_events: optional list of raw cudaEvent_t handles (ints), recorded in
     pairs around each kernel launch of the call.  sink / dsink: optional [H]
-    fp32 CUDA tensors, the attention-sink logits and (backward) their gradient."""
+    fp32 CUDA tensors, the attention-sink logits and (backward) their gradient.
+    reuse_tile_map: the workspace already holds this problem's tile map and
+    lists from an earlier call on it (see flashmask.h)."""
     opt = _b.fm_options(int(bool(deterministic)), 0, int(wait_timeout_ns), None, 0,
                         None if sink is None else sink.data_ptr(),
-                        None if dsink is None else dsink.data_ptr())
+                        None if dsink is None else dsink.data_ptr(), int(bool(reuse_tile_map)))
     opt._tensors = (sink, dsink)
     if kernel_events:
         arr = (ctypes.c_void_p * len(kernel_events))(*kernel_events)
@@ -112,16 +114,20 @@ def _check_sink(sink, H, device):
 
 
 def fwd(q, k, v, lts=None, lte=None, uts=None, ute=None, causal=False, scale=None,
-        out=None, lse=None, workspace=None, stream=None, options=None, sink=None):
+        out=None, lse=None, workspace=None, stream=None, options=None, sink=None,
+        reuse_tile_map=False):
     """Masked attention forward; returns (o [B,N,H,dv] bf16, lse [B,H,N] fp32).
-    sink: optional [H] fp32 attention-sink logits (see flashmask.h)."""
+    sink: optional [H] fp32 attention-sink logits (see flashmask.h).
+    reuse_tile_map: `workspace` already holds this problem's tile map and lists."""
     B, N, H, d, dv = _check_qkv(q, k, v)
     Hm, mp, _keep = _mask_args((lts, lte, uts, ute), B, H, N, q.device)
     prob = make_problem(B, H, Hm, N, d, dv, scale, causal)
     _check_sink(sink, H, q.device)
     if options is not None and sink is not None:
         raise FlashMaskError("pass the sink either in options or as sink=, not both")
-    opt = make_options(sink=sink) if options is None else options
+    if reuse_tile_map and workspace is None:
+        raise FlashMaskError("reuse_tile_map needs the workspace that holds the tile map")
+    opt = make_options(sink=sink, reuse_tile_map=reuse_tile_map) if options is None else options
     if out is None:
         out = torch.empty((B, N, H, dv), dtype=torch.bfloat16, device=q.device)
     if lse is None:
@@ -138,9 +144,11 @@ def fwd(q, k, v, lts=None, lte=None, uts=None, ute=None, causal=False, scale=Non
 
 def bwd(q, k, v, o, lse, dout, lts=None, lte=None, uts=None, ute=None, causal=False,
         scale=None, deterministic=False, dq=None, dk=None, dv=None, workspace=None,
-        stream=None, options=None, sink=None):
+        stream=None, options=None, sink=None, reuse_tile_map=False):
     """Masked attention backward; returns (dq, dk, dv) in bf16, and with a sink
-    (the forward's [H] fp32 logits) also their gradient: (dq, dk, dv, dsink)."""
+    (the forward's [H] fp32 logits) also their gradient: (dq, dk, dv, dsink).
+    reuse_tile_map: `workspace` (sized for the backward) already holds this
+    problem's tile map and lists, e.g. from the forward call on it."""
     B, N, H, d, dvd = _check_qkv(q, k, v)
     _check_sink(sink, H, q.device)
     if options is not None and sink is not None:
@@ -153,7 +161,10 @@ def bwd(q, k, v, o, lse, dout, lts=None, lte=None, uts=None, ute=None, causal=Fa
     Hm, mp, _keep = _mask_args((lts, lte, uts, ute), B, H, N, q.device)
     prob = make_problem(B, H, Hm, N, d, dvd, scale, causal)
     dsink = None if sink is None else torch.empty(H, dtype=torch.float32, device=q.device)
-    opt = make_options(deterministic, sink=sink, dsink=dsink) if options is None else options
+    if reuse_tile_map and workspace is None:
+        raise FlashMaskError("reuse_tile_map needs the workspace that holds the tile map")
+    opt = make_options(deterministic, sink=sink, dsink=dsink,
+                       reuse_tile_map=reuse_tile_map) if options is None else options
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv

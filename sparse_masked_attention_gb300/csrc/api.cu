@@ -54,6 +54,8 @@ fm_status make_geometry(const fm_problem *p, const fm_options *opt, Geometry *g)
     g->sink = opt ? opt->sink : nullptr;
     g->dsink = opt ? opt->dsink : nullptr;
     if (g->dsink && !g->sink) return FM_ERR_INVALID_ARG;  // a gradient needs its logits
+    g->reuse_map = opt ? opt->reuse_tile_map : 0;
+    if (g->reuse_map != 0 && g->reuse_map != 1) return FM_ERR_INVALID_ARG;
     // The list and map sizes must fit the int indexing of the kernels.
     const double entries = static_cast<double>(g->B) * g->Hm * g->T * g->T;
     if (entries > 2.0e9) return FM_ERR_INVALID_ARG;
@@ -303,7 +305,7 @@ fm_status flashmask_fwd(const fm_problem *p, const fm_options *opt, const void *
         return fail(cudaErrorInvalidValue, g_encode_detail);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     Recorder rec = recorder(opt);
-    cudaError_t e = map_and_lists(g, m, ws, st, rec);
+    cudaError_t e = g.reuse_map ? cudaSuccess : map_and_lists(g, m, ws, st, rec);
     if (e == cudaSuccess) {
         FwdArgs a{&tq, &tk, &tv, kr, &to, o, lse};
         rec.before(st);
@@ -346,7 +348,7 @@ fm_status flashmask_bwd(const fm_problem *p, const fm_options *opt, const void *
         return fail(cudaErrorInvalidValue, g_encode_detail);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     Recorder rec = recorder(opt);
-    cudaError_t e = map_and_lists(g, m, ws, st, rec);
+    cudaError_t e = g.reuse_map ? cudaSuccess : map_and_lists(g, m, ws, st, rec);
     if (e == cudaSuccess) {
         BwdArgs a;
         a.dq_k_rows = dq_kr;

@@ -23,6 +23,7 @@ struct Geometry {
     int deterministic;
     const float *sink;  // [H] attention-sink logits, or nullptr
     float *dsink;       // [H] their gradient (backward), or nullptr
+    int reuse_map;      // the workspace already holds this problem's tile map and lists
 };
 
 // Normalised mask boundaries per key column: (LTS, LTE, UTS, UTE) clamped to

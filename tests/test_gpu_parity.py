@@ -207,3 +207,27 @@ def test_rescale_paths(causal):
     o, lse, _ = run_fwd_bwd(q, k, v, do, mask, bwd=False)
     for h in range(H):
         check_head_full(q, k, v, do, mask, o, lse, None, 0, h)
+
+
+def test_backward_reuses_the_forward_tile_map():
+    """A forward and a backward sharing one workspace (sized for the backward):
+    the backward that reuses the tile map and lists the forward wrote gives
+    the same bits as one that builds them again, and so does a second forward
+    that reuses them."""
+    B, H, N, d = 2, 2, 900, 128
+    rng = np.random.default_rng(17)
+    q, k, v, do = W.make_inputs(B, N, H, d, d, seed=13, device="cuda")
+    mask = _family("share_question", N, B, seed=5)
+    vec = cuda_mask(mask)
+    ws = torch.empty(fm.workspace_size(B, H, 1, N, d, d, True, True), dtype=torch.uint8,
+                     device="cuda")
+    o, lse = fm.fwd(q, k, v, *vec, causal=mask.causal, workspace=ws)
+    g_reuse = fm.bwd(q, k, v, o, lse, do, *vec, causal=mask.causal, deterministic=True,
+                     workspace=ws, reuse_tile_map=True)
+    g_fresh = fm.bwd(q, k, v, o, lse, do, *vec, causal=mask.causal, deterministic=True)
+    o2, lse2 = fm.fwd(q, k, v, *vec, causal=mask.causal, workspace=ws, reuse_tile_map=True)
+    fm.get_error()
+    for a, b in zip(g_reuse, g_fresh):
+        assert torch.equal(a, b)
+    assert torch.equal(o, o2) and torch.equal(lse, lse2)
+    check_head_full(q, k, v, do, mask, o, lse, g_reuse, 1, 1)
