@@ -51,7 +51,7 @@ __device__ __forceinline__ int warp_min(int v) {
 }
 
 // One CTA per (key tile, chunk of at most kClassifyChunk query tiles, mask head).
-// Per query tile qt, one word of `state` collects the CTA's verdict:
+// Per query tile qt, one word of `state` collects the CTA's decision:
 //   bits 0..3  column test "every column of warp w covers the tile"
 //   bits 4..7  column test "some column of warp w reaches into the tile"
 //   bit  8     the column test ran (the tile map's min/max left the tile open)
