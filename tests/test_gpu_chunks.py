@@ -136,3 +136,27 @@ def test_chunked_odd_chunk_count_one_chunk_per_rank():
                                 oracle.attention_bwd(qh, kh, vh, doh, ms, mask.causal, scale)):
             assert_close(name, head(g, 0, h), ref,
                          max_abs=MAX_ABS + 3 * 2.0 ** -9 * float(np.max(np.abs(ref))))
+
+
+def test_chunked_ragged_chunk_length():
+    """N = 1000 in 4 chunks of 250 rows: every local problem ends in a ragged
+    tile, and chunk boundaries cut through tiles of the whole sequence."""
+    B, H, N, d, C = 1, 2, 1000, 128, 4
+    rng = np.random.default_rng(19)
+    q, k, v, do = W.make_inputs(B, N, H, d, d, seed=16, device="cuda")
+    mask = _family("causal_document", N, B, rng)
+    vec = cuda_mask(mask)
+    o, lse = fm.fwd_chunked(q, k, v, *vec, causal=mask.causal, chunks=C, ranks=C // 2)
+    grads = fm.bwd_chunked(q, k, v, o, lse, do, *vec, causal=mask.causal, chunks=C, ranks=C // 2)
+    fm.get_error()
+    scale = 1 / np.sqrt(d)
+    for h in range(H):
+        qh, kh, vh, doh = head(q, 0, h), head(k, 0, h), head(v, 0, h), head(do, 0, h)
+        ms = mask_slice(mask, 0, h)
+        ro, rl = oracle.attention_fwd(qh, kh, vh, ms, mask.causal, scale)
+        assert_close("O", head(o, 0, h), ro)
+        assert_lse(lse[0, h].cpu().numpy(), rl)
+        for name, g, ref in zip(("dQ", "dK", "dV"), grads,
+                                oracle.attention_bwd(qh, kh, vh, doh, ms, mask.causal, scale)):
+            assert_close(name, head(g, 0, h), ref,
+                         max_abs=MAX_ABS + C * 2.0 ** -9 * float(np.max(np.abs(ref))))

@@ -231,3 +231,34 @@ def test_backward_reuses_the_forward_tile_map():
         assert torch.equal(a, b)
     assert torch.equal(o, o2) and torch.equal(lse, lse2)
     check_head_full(q, k, v, do, mask, o, lse, g_reuse, 1, 1)
+
+
+@pytest.mark.parametrize("d,dv", DIMS)
+def test_per_head_masks_every_head_dim(d, dv):
+    """Hm = H: every head has its own vectors, at every supported (d, dv)."""
+    B, H, N = 2, 2, 640
+    rng = np.random.default_rng(23 + d)
+    q, k, v, do = W.make_inputs(B, N, H, d, dv, seed=14, device="cuda")
+    mask = W.random_vectors(N, rng, B, Hm=H, causal_flag=bool(d % 128), lo=0, hi=N)
+    o, lse, grads = run_fwd_bwd(q, k, v, do, mask)
+    for b in range(B):
+        for h in range(H):
+            check_head_full(q, k, v, do, mask, o, lse, grads, b, h)
+
+
+@pytest.mark.parametrize("d,dv", [(192, 128), (256, 256)])
+def test_tile_map_reuse_large_heads(d, dv):
+    B, H, N = 1, 2, 700
+    q, k, v, do = W.make_inputs(B, N, H, d, dv, seed=15, device="cuda")
+    mask = _family("causal_document", N, B, seed=9)
+    vec = cuda_mask(mask)
+    ws = torch.empty(fm.workspace_size(B, H, 1, N, d, dv, True, True), dtype=torch.uint8,
+                     device="cuda")
+    o, lse = fm.fwd(q, k, v, *vec, causal=mask.causal, workspace=ws)
+    g1 = fm.bwd(q, k, v, o, lse, do, *vec, causal=mask.causal, deterministic=True,
+                workspace=ws, reuse_tile_map=True)
+    g2 = fm.bwd(q, k, v, o, lse, do, *vec, causal=mask.causal, deterministic=True)
+    fm.get_error()
+    for a, b in zip(g1, g2):
+        assert torch.equal(a, b)
+    check_head_full(q, k, v, do, mask, o, lse, g1, 0, 1)

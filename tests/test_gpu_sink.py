@@ -105,3 +105,16 @@ def test_sink_gradient_deterministic_and_autograd():
     assert torch.equal(out, o)
     for a, b_ in zip((qq.grad, kk.grad, vv.grad, ss.grad), g1):
         assert torch.equal(a, b_)
+
+
+def test_sink_with_per_head_masks():
+    B, H, N, d = 1, 3, 500, 128
+    rng = np.random.default_rng(41)
+    q, k, v, do = W.make_inputs(B, N, H, d, d, seed=17, device="cuda")
+    mask = W.random_vectors(N, rng, B, Hm=H, causal_flag=True, lo=0, hi=N)
+    vec = cuda_mask(mask)
+    sink = torch.tensor([-0.5, 0.0, 2.5], dtype=torch.float32, device="cuda")
+    o, lse = fm.fwd(q, k, v, *vec, causal=True, sink=sink)
+    grads = fm.bwd(q, k, v, o, lse, do, *vec, causal=True, sink=sink)
+    fm.get_error()
+    _check(q, k, v, do, mask, sink.cpu().numpy(), o, lse, grads)
