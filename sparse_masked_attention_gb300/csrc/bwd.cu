@@ -171,6 +171,7 @@ struct BwdParams {
     const int *cnt;
     const float *lse2;
     const float *delta;
+    const void *do16;  // [B, N, H, dv] fp16 copy of dO
     __nv_bfloat16 *dq, *dk, *dv;
     int N, H, Hm, T, Npad, causal;
     float sl2;    // scale * log2(e)
@@ -188,13 +189,21 @@ struct BwdParams {
 // stage per group (dP reads it).  The MMA thread serves whichever group is
 // ready, so one group's late operand never stalls the other group's work;
 // only the dQ accumulation keeps tile order (bit-reproducible sums).
-template <int D_, int DV_, int BN_, int KS_, int NWG_>
+// DO_TM: the query tile's dO, the same for every key sub-tile, is put into
+// TMEM once by compute group 0 (from the fp16 copy), and dP = dO V^T reads it
+// from there (TS MMA).  Shared memory then holds only Q, the K ring and the V
+// stages, which lets d = 192 run 128-key sub-tiles (N = 128 MMAs for S and
+// dP instead of N = 64 ones, which take the pipe as long); at d <= 128, where
+// the sub-tiles are 128 keys anyway, the extra TMEM reads made the kernel
+// slower, so there dO stays in shared memory.
+template <int D_, int DV_, int BN_, int KS_, int NWG_, bool DO_TM_ = false>
 struct DqCfg {
     static constexpr int D = D_, DV = DV_, BN = BN_, KS = KS_, NWG = NWG_;
+    static constexpr bool DO_TM = DO_TM_;
     static constexpr int BM = 128;
     static constexpr int SUB = TILE / BN;
     static constexpr int Q_BYTES = BM * D * 2;
-    static constexpr int DO_BYTES = BM * DV * 2;
+    static constexpr int DO_BYTES = DO_TM ? 0 : BM * DV * 2;  // dO in shared memory
     static constexpr int K_BYTES = BN * D * 2;
     static constexpr int V_BYTES = BN * DV * 2;
     static constexpr int OFF_Q = 0;
@@ -203,14 +212,16 @@ struct DqCfg {
     static constexpr int OFF_V = OFF_K + KS * K_BYTES;
     static constexpr int OFF_BAR = OFF_V + NWG * V_BYTES;
     // q_full, k_full[KS], k_empty[KS], v_full[NWG], v_empty[NWG],
-    // s_full[NWG], p_full[NWG], dp_full[NWG], ds_full[NWG], dq_done
-    static constexpr int NBAR = 1 + 2 * KS + 6 * NWG + 1;
+    // s_full[NWG], p_full[NWG], dp_full[NWG], ds_full[NWG], dq_done, do_ready
+    static constexpr int NBAR = 1 + 2 * KS + 6 * NWG + 2;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int SMEM_BYTES = OFF_MISC + 16;
     static constexpr int TM_DQ = NWG * BN;  // group w's region: columns [w*BN, (w+1)*BN)
+    static constexpr int TM_DO = TM_DQ + D;  // dO as fp16 pairs (DO_TM)
     static constexpr int TM_COLS = 512;
     static constexpr int THREADS = 64 + NWG * 128;
-    static_assert(TM_DQ + D <= TM_COLS, "TMEM budget");
+    static_assert(TM_DQ + D + (DO_TM ? DV / 2 : 0) <= TM_COLS, "TMEM budget");
+    static_assert(!DO_TM || DV % 64 == 0, "dO columns in 32-column stores");
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
     static_assert(BN == 64 || BN == 128, "key sub-tile");
     static_assert(KS >= NWG, "ring depth");
@@ -244,6 +255,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     uint64_t *v_full = k_empty + C::KS, *v_empty = v_full + C::NWG;
     uint64_t *s_full = v_empty + C::NWG, *p_full = s_full + C::NWG, *dp_full = p_full + C::NWG;
     uint64_t *ds_full = dp_full + C::NWG, *dq_done = ds_full + C::NWG;
+    uint64_t *do_ready = dq_done + 1;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
     volatile int *abort = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
 
@@ -274,6 +286,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             mbar_init(&ds_full[i], 128);
         }
         mbar_init(dq_done, 1);
+        mbar_init(do_ready, 128);
         *abort = 0;
         fence_barrier_init();
         if (n > 0) {  // Q and dO before the CTA-wide barrier: latency overlaps the setup
@@ -281,9 +294,11 @@ __global__ void __launch_bounds__(C::THREADS, 1)
 #pragma unroll
             for (int c = 0; c < C::D / 64; ++c)
                 tma_load_4d(sQ + c * C::BM * 128, &tm_q, q_full, c * 64, h, qt * TILE, b);
+            if constexpr (!C::DO_TM) {
 #pragma unroll
-            for (int c = 0; c < C::DV / 64; ++c)
-                tma_load_4d(sDO + c * C::BM * 128, &tm_do, q_full, c * 64, h, qt * TILE, b);
+                for (int c = 0; c < C::DV / 64; ++c)
+                    tma_load_4d(sDO + c * C::BM * 128, &tm_do, q_full, c * 64, h, qt * TILE, b);
+            }
         }
     }
     if (warp == 1) {
@@ -399,13 +414,19 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     } else if (st_[w] == 1) {  // dP = dO V^T, once the group has read S
                         if (!mbar_test(&p_full[w], lu & 1) || !mbar_test(&v_full[w], lu & 1))
                             continue;
+                        if (C::DO_TM && !mbar_test(do_ready, 0)) continue;
                         tc_fence_after();
                         const uint64_t vsd = v_desc + static_cast<uint64_t>((w * C::V_BYTES) >> 4);
 #pragma unroll
                         for (int k = 0; k < C::DV / 16; ++k) {
                             const uint32_t a_off = ((k / 4) * (C::BM * 128) + (k % 4) * 32) >> 4;
                             const uint32_t b_off = ((k / 4) * (C::BN * 128) + (k % 4) * 32) >> 4;
-                            mma_ss(t_r, do_desc + a_off, vsd + b_off, IDESC_DP, k > 0 ? 1u : 0u);
+                            if constexpr (C::DO_TM)  // A = dO from TMEM, 16 fp16 = 8 columns
+                                mma_ts(t_r, tmem + C::TM_DO + k * 8, vsd + b_off, IDESC_DP,
+                                       k > 0 ? 1u : 0u);
+                            else
+                                mma_ss(t_r, do_desc + a_off, vsd + b_off, IDESC_DP,
+                                       k > 0 ? 1u : 0u);
                         }
                         mma_commit(&dp_full[w]);
                         st_[w] = 2;
@@ -466,6 +487,32 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         const float sl2 = p.sl2;
         const int n_my = n_of(wg);
         const int4 *vec = p.vec + static_cast<size_t>(bm) * p.Npad;
+        if constexpr (C::DO_TM) {
+            // Group 0 puts the query tile's dO rows (fp16 pairs; zeros past N)
+            // into TMEM, where every dP of the CTA reads them.
+            if (wg == 0 && n > 0) {
+                const uint4 *src = reinterpret_cast<const uint4 *>(
+                    static_cast<const __half *>(p.do16) +
+                    ((static_cast<size_t>(b) * p.N + (grow < p.N ? grow : 0)) * p.H + h) *
+                        C::DV);
+#pragma unroll 1
+                for (int c = 0; c < C::DV / 64; ++c) {
+                    uint32_t r[32];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const uint4 w4 = grow < p.N ? src[c * 8 + i] : make_uint4(0u, 0u, 0u, 0u);
+                        r[4 * i] = w4.x;
+                        r[4 * i + 1] = w4.y;
+                        r[4 * i + 2] = w4.z;
+                        r[4 * i + 3] = w4.w;
+                    }
+                    tmem_st32(lane_base + C::TM_DO + c * 32, r);
+                }
+                tmem_st_wait();
+                tc_fence_before();
+                mbar_arrive(do_ready);
+            }
+        }
         // The next tile's list entry and mask boundaries are read one tile ahead.
         int4 cv_next[C::BN / 64][2];
         auto load_bounds = [&](int u, int entry) {
@@ -1063,6 +1110,7 @@ BwdParams make_params(const Geometry &g, const Workspace &ws, const BwdArgs &a, 
     p.cnt = dq_side ? ws.fwd_cnt : ws.bwd_cnt;
     p.lse2 = ws.lse2;
     p.delta = ws.delta;
+    p.do16 = ws.do16;
     p.dq = static_cast<__nv_bfloat16 *>(a.dq);
     p.dk = static_cast<__nv_bfloat16 *>(a.dk);
     p.dv = static_cast<__nv_bfloat16 *>(a.dv);
@@ -1119,9 +1167,10 @@ cudaError_t launch_pair(const Geometry &g, const Workspace &ws, const BwdArgs &a
 
 }  // namespace
 
-// Key sub-tile of the query-side kernel and query sub-tile of the key-side
-// kernel: 128 (full-rate N = 128 MMAs) up to d = 128, 64 above (shared memory).
-int dq_key_rows(int d, int) { return d <= 128 ? 128 : 64; }
+// Key sub-tile of the query-side kernel (128 up to d = 192, with dO in TMEM at
+// d = 192) and query sub-tile of the key-side kernel (128 up to d = 128): 128
+// gives full-rate N = 128 MMAs, 64 is what shared memory holds above.
+int dq_key_rows(int d, int) { return d <= 192 ? 128 : 64; }
 int dkdv_query_rows(int d, int) { return d <= 128 ? 128 : 64; }
 
 cudaError_t launch_bwd(const Geometry &g, const Workspace &ws, const BwdArgs &a,
@@ -1148,7 +1197,8 @@ cudaError_t launch_bwd(const Geometry &g, const Workspace &ws, const BwdArgs &a,
         return launch_pair<DkdvCfg<128, 128, 128, 3, true, true, 2>, DqCfg<128, 128, 128, 3, 2>>(
             g, ws, a, st, rec);
     if (g.d == 192 && g.dv == 128)
-        return launch_pair<DkdvCfg<192, 128, 64, 3, true, true, 2>, DqCfg<192, 128, 64, 3, 2>>(
+        return launch_pair<DkdvCfg<192, 128, 64, 3, true, true, 2>,
+                           DqCfg<192, 128, 128, 2, 2, true>>(
             g, ws, a, st, rec);
     if (g.d == 256 && g.dv == 256) {
         rec.before(st);
