@@ -1205,7 +1205,8 @@ cudaError_t launch_bwd(const Geometry &g, const Workspace &ws, const BwdArgs &a,
         e = launch_dkdv<DkdvCfg<256, 256, 64, 3, false, true, 2>>(g, ws, a, st);
         rec.after(st);
         if (e != cudaSuccess) return e;
-        return launch_pair<DkdvCfg<256, 256, 64, 1, true, false, 1>, DqCfg<256, 256, 64, 2, 1>>(
+        return launch_pair<DkdvCfg<256, 256, 64, 1, true, false, 1>,
+                           DqCfg<256, 256, 64, 3, 2, true>>(
             g, ws, a, st, rec);
     }
     return cudaErrorInvalidValue;
