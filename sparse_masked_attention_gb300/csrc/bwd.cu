@@ -172,6 +172,7 @@ struct BwdParams {
     const float *lse2;
     const float *delta;
     const void *do16;  // [B, N, H, dv] fp16 copy of dO
+    const void *v16;   // [B, N, H, dv] fp16 copy of V
     __nv_bfloat16 *dq, *dk, *dv;
     int N, H, Hm, T, Npad, causal;
     float sl2;    // scale * log2(e)
@@ -648,15 +649,20 @@ __global__ void __launch_bounds__(C::THREADS, 1)
 // the tile's LSE2 and D in one stage per group (dV, dP^T and the compute read
 // them).  The MMA thread serves whichever group is ready; the dV and dK
 // accumulations keep tile order (bit-reproducible sums).
-template <int D_, int DV_, int BM_, int QS_, bool DK_, bool DV_ON_, int NWG_>
+// V_TM: the CTA's V tile, the same for every query sub-tile, is put into TMEM
+// once by compute group 0 (from the fp16 copy) and dP^T = V dO^T reads it from
+// there (TS MMA); its shared memory goes to a second compute group at
+// d = dv = 256, where only the dK pass needs V.
+template <int D_, int DV_, int BM_, int QS_, bool DK_, bool DV_ON_, int NWG_,
+          bool V_TM_ = false>
 struct DkdvCfg {
     static constexpr int D = D_, DV = DV_, BM = BM_, QS = QS_, NWG = NWG_;
-    static constexpr bool DO_DK = DK_, DO_DV = DV_ON_;
+    static constexpr bool DO_DK = DK_, DO_DV = DV_ON_, V_TM = V_TM_;
     static constexpr int BN = 128;            // keys per CTA (TMEM lanes)
     static constexpr int SUB = TILE / BM;     // query sub-tiles per list entry
     static constexpr bool NEED_V = DO_DK;     // V only feeds dP^T
     static constexpr int K_BYTES = BN * D * 2;
-    static constexpr int V_BYTES = NEED_V ? BN * DV * 2 : 0;
+    static constexpr int V_BYTES = (NEED_V && !V_TM) ? BN * DV * 2 : 0;  // V in shared memory
     static constexpr int Q_BYTES = BM * D * 2;
     static constexpr int DO_BYTES = BM * DV * 2;
     static constexpr int LD_BYTES = 2 * BM * 4;  // LSE2 then D of the sub-tile's rows
@@ -667,17 +673,19 @@ struct DkdvCfg {
     static constexpr int OFF_LD = OFF_DO + NWG * DO_BYTES;
     static constexpr int OFF_BAR = OFF_LD + NWG * LD_BYTES;
     // kv_full, q_full[QS], q_empty[QS], o_full[NWG], o_empty[NWG],
-    // s_full[NWG], p_full[NWG], dp_full[NWG], ds_full[NWG], done
-    static constexpr int NBAR = 1 + 2 * QS + 6 * NWG + 1;
+    // s_full[NWG], p_full[NWG], dp_full[NWG], ds_full[NWG], done, v_ready
+    static constexpr int NBAR = 1 + 2 * QS + 6 * NWG + 2;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int SMEM_BYTES = OFF_MISC + 16;
     static constexpr int TM_DK = 0;
     static constexpr int TM_DV = DO_DK ? D : 0;
     static constexpr int TM_W0 = TM_DV + (DO_DV ? DV : 0);  // group w: [TM_W0 + w*BM, +BM)
     static constexpr int TM_END = TM_W0 + NWG * BM;
+    static constexpr int TM_V = TM_END;      // V as fp16 pairs (V_TM)
     static constexpr int TM_COLS = 512;
     static constexpr int THREADS = 64 + NWG * 128;
-    static_assert(TM_END <= TM_COLS, "TMEM budget");
+    static_assert(TM_END + (V_TM ? DV / 2 : 0) <= TM_COLS, "TMEM budget");
+    static_assert(!V_TM || (NEED_V && DV % 64 == 0), "V in TMEM only feeds dP^T");
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
     static_assert(D <= 256 && DV <= 256 && (BM == 64 || BM == 128), "MMA shape");
     static_assert(QS >= NWG, "ring depth");
@@ -710,6 +718,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     uint64_t *o_full = q_empty + C::QS, *o_empty = o_full + C::NWG;
     uint64_t *s_full = o_empty + C::NWG, *p_full = s_full + C::NWG, *dp_full = p_full + C::NWG,
              *ds_full = dp_full + C::NWG, *done = ds_full + C::NWG;
+    uint64_t *v_ready = done + 1;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
     volatile int *abort = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
 
@@ -741,6 +750,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             mbar_init(&ds_full[i], 128);
         }
         mbar_init(done, 1);
+        mbar_init(v_ready, 128);
         *abort = 0;
         fence_barrier_init();
         if (n > 0) {  // K and V before the CTA-wide barrier: latency overlaps the setup
@@ -748,7 +758,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
 #pragma unroll
             for (int c = 0; c < C::D / 64; ++c)
                 tma_load_4d(sK + c * C::BN * 128, &tm_k, kv_full, c * 64, h, kt * TILE, b);
-            if constexpr (C::NEED_V) {
+            if constexpr (C::NEED_V && !C::V_TM) {
 #pragma unroll
                 for (int c = 0; c < C::DV / 64; ++c)
                     tma_load_4d(sV + c * C::BN * 128, &tm_v, kv_full, c * 64, h, kt * TILE, b);
@@ -878,6 +888,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                         if ((p.ordered && u != next_v) || !mbar_test(&p_full[w], lu & 1) ||
                             !mbar_test(&o_full[w], lu & 1))
                             continue;
+                        if (C::V_TM && !mbar_test(v_ready, 0)) continue;
                         tc_fence_after();
                         const bool acc_v = next_v > 0;  // the first dV product initialises
                         ++next_v;
@@ -898,7 +909,12 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                                     ((k / 4) * (C::BN * 128) + (k % 4) * 32) >> 4;
                                 const uint32_t b_off =
                                     ((k / 4) * (C::BM * 128) + (k % 4) * 32) >> 4;
-                                mma_ss(t_r, v_desc + a_off, dd + b_off, IDESC_DP, k > 0 ? 1u : 0u);
+                                if constexpr (C::V_TM)  // A = V from TMEM, 16 fp16 = 8 columns
+                                    mma_ts(t_r, tmem + C::TM_V + k * 8, dd + b_off, IDESC_DP,
+                                           k > 0 ? 1u : 0u);
+                                else
+                                    mma_ss(t_r, v_desc + a_off, dd + b_off, IDESC_DP,
+                                           k > 0 ? 1u : 0u);
                             }
                             mma_commit(&dp_full[w]);
                         } else {
@@ -966,6 +982,32 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         const int n_my = n_of(wg);
         const float *slse = reinterpret_cast<const float *>(sLD + wg * C::LD_BYTES);
         const float *sd = slse + C::BM;
+        if constexpr (C::V_TM) {
+            // Group 0 puts the key tile's V rows (fp16 pairs; zeros past N) into
+            // TMEM, where every dP^T of the CTA reads them.
+            if (wg == 0 && n > 0) {
+                const uint4 *src = reinterpret_cast<const uint4 *>(
+                    static_cast<const __half *>(p.v16) +
+                    ((static_cast<size_t>(b) * p.N + (gkey < p.N ? gkey : 0)) * p.H + h) *
+                        C::DV);
+#pragma unroll 1
+                for (int c = 0; c < C::DV / 64; ++c) {
+                    uint32_t r[32];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const uint4 w4 = gkey < p.N ? src[c * 8 + i] : make_uint4(0u, 0u, 0u, 0u);
+                        r[4 * i] = w4.x;
+                        r[4 * i + 1] = w4.y;
+                        r[4 * i + 2] = w4.z;
+                        r[4 * i + 3] = w4.w;
+                    }
+                    tmem_st32(lane_base + C::TM_V + c * 32, r);
+                }
+                tmem_st_wait();
+                tc_fence_before();
+                mbar_arrive(v_ready);
+            }
+        }
         int entry_next = n_my > 0 ? entries[wg / C::SUB] : 0;
         for (int lu = 0; lu < n_my; ++lu) {
             const int u = lu * C::NWG + wg;
@@ -1111,6 +1153,7 @@ BwdParams make_params(const Geometry &g, const Workspace &ws, const BwdArgs &a, 
     p.lse2 = ws.lse2;
     p.delta = ws.delta;
     p.do16 = ws.do16;
+    p.v16 = ws.v16;
     p.dq = static_cast<__nv_bfloat16 *>(a.dq);
     p.dk = static_cast<__nv_bfloat16 *>(a.dk);
     p.dv = static_cast<__nv_bfloat16 *>(a.dv);
@@ -1205,7 +1248,7 @@ cudaError_t launch_bwd(const Geometry &g, const Workspace &ws, const BwdArgs &a,
         e = launch_dkdv<DkdvCfg<256, 256, 64, 3, false, true, 2>>(g, ws, a, st);
         rec.after(st);
         if (e != cudaSuccess) return e;
-        return launch_pair<DkdvCfg<256, 256, 64, 1, true, false, 1>,
+        return launch_pair<DkdvCfg<256, 256, 64, 2, true, false, 2, true>,
                            DqCfg<256, 256, 64, 3, 2, true>>(
             g, ws, a, st, rec);
     }
