@@ -651,8 +651,9 @@ __global__ void __launch_bounds__(C::THREADS, 1)
 // accumulations keep tile order (bit-reproducible sums).
 // V_TM: the CTA's V tile, the same for every query sub-tile, is put into TMEM
 // once by compute group 0 (from the fp16 copy) and dP^T = V dO^T reads it from
-// there (TS MMA); its shared memory goes to a second compute group at
-// d = dv = 256, where only the dK pass needs V.
+// there (TS MMA).  Its shared memory goes to a second compute group and a
+// deeper Q ring at d = dv = 256 (where only the dK pass needs V), and to a
+// deeper Q ring at d = 192.
 template <int D_, int DV_, int BM_, int QS_, bool DK_, bool DV_ON_, int NWG_,
           bool V_TM_ = false>
 struct DkdvCfg {
@@ -1240,7 +1241,7 @@ cudaError_t launch_bwd(const Geometry &g, const Workspace &ws, const BwdArgs &a,
         return launch_pair<DkdvCfg<128, 128, 128, 3, true, true, 2>, DqCfg<128, 128, 128, 3, 2>>(
             g, ws, a, st, rec);
     if (g.d == 192 && g.dv == 128)
-        return launch_pair<DkdvCfg<192, 128, 64, 3, true, true, 2>,
+        return launch_pair<DkdvCfg<192, 128, 64, 4, true, true, 2, true>,
                            DqCfg<192, 128, 128, 2, 2, true>>(
             g, ws, a, st, rec);
     if (g.d == 256 && g.dv == 256) {
@@ -1248,7 +1249,7 @@ cudaError_t launch_bwd(const Geometry &g, const Workspace &ws, const BwdArgs &a,
         e = launch_dkdv<DkdvCfg<256, 256, 64, 3, false, true, 2>>(g, ws, a, st);
         rec.after(st);
         if (e != cudaSuccess) return e;
-        return launch_pair<DkdvCfg<256, 256, 64, 2, true, false, 2, true>,
+        return launch_pair<DkdvCfg<256, 256, 64, 3, true, false, 2, true>,
                            DqCfg<256, 256, 64, 3, 2, true>>(
             g, ws, a, st, rec);
     }
