@@ -45,6 +45,8 @@ def parse():
     ap.add_argument("--N", type=int, default=None, help="override the workload's N (profiling)")
     ap.add_argument("--B", type=int, default=None, help="override the workload's B (profiling)")
     ap.add_argument("--H", type=int, default=None, help="override the workload's H (profiling)")
+    ap.add_argument("--deterministic", type=int, choices=[0, 1], default=None,
+                    help="override the workload's deterministic-backward flag")
     ap.add_argument("--chunks", type=int, default=0,
                     help="time the step as an emulated context-parallel run over this many "
                          "equal chunks (zigzag over chunks/2 ranks) instead of one call")
@@ -151,6 +153,8 @@ def workload_cfg(args):
     for key in ("N", "B", "H"):
         if getattr(args, key, None):
             cfg[key] = getattr(args, key)
+    if getattr(args, "deterministic", None) is not None:
+        cfg["deterministic"] = bool(args.deterministic)
     return cfg
 
 
@@ -173,9 +177,11 @@ def kernel_alg_flops_per_pair(name, d, dv):
     """Algorithmic FLOPs per unmasked pair credited to each kernel.  The
     key-side kernel does the S/dP recomputation and the dK/dV products the
     backward needs once; the query-side kernel is credited with dQ only (its S
-    and dP are a second recomputation)."""
+    and dP are a second recomputation).  Where the key side runs as two passes
+    (d = dv = 256), the dV pass is credited with S and dV, the dK pass with dP
+    and dK (its S is a recomputation), so the two add up to the one kernel."""
     return {"fwd": 2 * (d + dv), "bwd_dkdv": 2 * (2 * d + 2 * dv), "bwd_dq": 2 * d,
-            "bwd_dkdv_dv": 2 * (d + dv) + 2 * dv, "bwd_dkdv_dk": 2 * d + 2 * dv + 2 * d}.get(name, 0)
+            "bwd_dkdv_dv": 2 * d + 2 * dv, "bwd_dkdv_dk": 2 * dv + 2 * d}.get(name, 0)
 
 
 def setup(cfg, seed, device):
