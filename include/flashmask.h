@@ -53,7 +53,9 @@ typedef enum {
     FM_ERR_UNSUPPORTED = 2,     /* (d, dv) pair or device not supported            */
     FM_ERR_WORKSPACE = 3,       /* workspace NULL, unaligned or smaller than needed */
     FM_ERR_CUDA = 4,            /* a CUDA runtime/driver call failed               */
-    FM_ERR_DEVICE_TIMEOUT = 5   /* a kernel gave up on a bounded wait              */
+    FM_ERR_DEVICE_TIMEOUT = 5,  /* a kernel gave up on a bounded wait              */
+    FM_ERR_DEVICE_BOUNDS = 6    /* debug_bounds: a kernel found its work list out of
+                                 * range (for example a stale reused tile map)     */
 } fm_status;
 
 /* Problem shape.  scale <= 0 selects the default 1/sqrt(d). */
@@ -64,9 +66,18 @@ typedef struct {
 } fm_problem;
 
 /* Options.  deterministic: the backward adds every partial sum in a fixed
- * order, so dQ/dK/dV are bit-identical from run to run.  debug_bounds is
- * reserved and must be 0.  wait_timeout_ns bounds every wait on the device;
- * 0 selects 1 s.
+ * order, so dQ/dK/dV are bit-identical from run to run.  wait_timeout_ns
+ * bounds every wait on the device; 0 selects 1 s.
+ * debug_bounds (0 or 1): before the attention kernels, a check kernel reads
+ * every work list in the workspace: each list's length must lie in [0, T]
+ * and each of its tile indices in [0, T), T = ceil(N / 128), and each entry
+ * of the forward's pair order in [0, ceil(T / 2)).  A list that fails is
+ * emptied (length 0) and an order entry that fails is replaced by a valid
+ * one, so no kernel after it reads out of range; flashmask_get_error then
+ * returns FM_ERR_DEVICE_BOUNDS, and the outputs are not meaningful.  The
+ * lists the library builds itself always pass (results are bit-identical
+ * with and without the check); it is meant for workspaces reused with
+ * reuse_tile_map.  kernel_events do not record the check kernel.
  * sink (optional, may be NULL): per-head attention-sink logits, [H] fp32 on
  * the device (FlashMask README, "News", names sink bias without a formula;
  * reading taken): head h's logit joins every row's softmax denominator as a
@@ -171,8 +182,10 @@ fm_status flashmask_count_unmasked(const fm_problem *p,
 
 /*
  * Synchronises `stream`, then reads and clears the library's device error
- * word.  Returns FM_ERR_DEVICE_TIMEOUT if a kernel gave up on a bounded wait
- * since the last call, FM_ERR_CUDA if the stream itself failed, else FM_OK.
+ * words.  Since the last call: FM_ERR_DEVICE_BOUNDS if a kernel found its
+ * work list out of range (debug_bounds), else FM_ERR_DEVICE_TIMEOUT if a
+ * kernel gave up on a bounded wait.  FM_ERR_CUDA if the stream itself
+ * failed, else FM_OK.
  */
 fm_status flashmask_get_error(void *stream);
 

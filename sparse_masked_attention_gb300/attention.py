@@ -17,14 +17,19 @@ from . import binding as _b
 
 
 class FlashMaskError(RuntimeError):
-    pass
+    """An error of the library or of its arguments; `status` is the library's
+    fm_status code, or None for a check made in Python."""
+
+    def __init__(self, message, status=None):
+        super().__init__(message)
+        self.status = status
 
 
 def _check(status: int, what: str):
     if status != _b.FM_OK:
         detail = _b.flashmask_last_error_detail() if status == _b.FM_ERR_CUDA else ""
         raise FlashMaskError(f"{what}: {_b.flashmask_error_string(status)} (status {status})"
-                             + (f" [{detail}]" if detail else ""))
+                             + (f" [{detail}]" if detail else ""), status)
 
 
 def _ptr(t: Optional[torch.Tensor]):
@@ -70,13 +75,16 @@ def make_problem(B, H, Hm, N, d, dv, scale, causal) -> _b.fm_problem:
 
 
 def make_options(deterministic=False, wait_timeout_ns=0, kernel_events=None, sink=None,
-                 dsink=None, reuse_tile_map=False) -> _b.fm_options:
+                 dsink=None, reuse_tile_map=False, debug_bounds=False) -> _b.fm_options:
     """kernel_events: optional list of raw cudaEvent_t handles (ints), recorded in
     pairs around each kernel launch of the call.  sink / dsink: optional [H]
     fp32 CUDA tensors, the attention-sink logits and (backward) their gradient.
     reuse_tile_map: the workspace already holds this problem's tile map and
-    lists from an earlier call on it (see flashmask.h)."""
-    opt = _b.fm_options(int(bool(deterministic)), 0, int(wait_timeout_ns), None, 0,
+    lists from an earlier call on it (see flashmask.h).  debug_bounds: every
+    attention CTA checks its work list first; a bad one makes get_error()
+    raise (status FM_ERR_DEVICE_BOUNDS) instead of reading out of range."""
+    opt = _b.fm_options(int(bool(deterministic)), int(bool(debug_bounds)), int(wait_timeout_ns),
+                        None, 0,
                         None if sink is None else sink.data_ptr(),
                         None if dsink is None else dsink.data_ptr(), int(bool(reuse_tile_map)))
     opt._tensors = (sink, dsink)
@@ -208,7 +216,8 @@ def count_unmasked(N, B=1, H=1, lts=None, lte=None, uts=None, ute=None, causal=F
 
 
 def get_error(stream=None):
-    """Synchronise the stream and raise if a kernel gave up on a bounded wait."""
+    """Synchronise the stream and raise if a kernel gave up on a bounded wait or
+    (debug_bounds) found its work list out of range."""
     _check(_b.flashmask_get_error(_stream(stream)), "device")
 
 

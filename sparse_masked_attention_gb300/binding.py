@@ -20,6 +20,7 @@ FM_ERR_UNSUPPORTED = 2
 FM_ERR_WORKSPACE = 3
 FM_ERR_CUDA = 4
 FM_ERR_DEVICE_TIMEOUT = 5
+FM_ERR_DEVICE_BOUNDS = 6
 
 FM_TILE_SKIP = 0
 FM_TILE_PARTIAL = 1

@@ -34,7 +34,7 @@ fm_status make_geometry(const fm_problem *p, const fm_options *opt, Geometry *g)
     if (!(p->Hm == 1 || p->Hm == p->H)) return FM_ERR_INVALID_ARG;
     if (p->causal != 0 && p->causal != 1) return FM_ERR_INVALID_ARG;
     if (!isfinite(p->scale)) return FM_ERR_INVALID_ARG;
-    if (opt && opt->debug_bounds != 0) return FM_ERR_INVALID_ARG;
+    if (opt && opt->debug_bounds != 0 && opt->debug_bounds != 1) return FM_ERR_INVALID_ARG;
     if (!supported_dims(p->d, p->dv)) return FM_ERR_UNSUPPORTED;
     // Grid limits: H and B are grid dimensions y and z.
     if (p->H > 65535 || p->B > 65535) return FM_ERR_INVALID_ARG;
@@ -56,6 +56,7 @@ fm_status make_geometry(const fm_problem *p, const fm_options *opt, Geometry *g)
     if (g->dsink && !g->sink) return FM_ERR_INVALID_ARG;  // a gradient needs its logits
     g->reuse_map = opt ? opt->reuse_tile_map : 0;
     if (g->reuse_map != 0 && g->reuse_map != 1) return FM_ERR_INVALID_ARG;
+    g->debug_bounds = opt ? opt->debug_bounds : 0;
     // The list and map sizes must fit the int indexing of the kernels.
     const double entries = static_cast<double>(g->B) * g->Hm * g->T * g->T;
     if (entries > 2.0e9) return FM_ERR_INVALID_ARG;
@@ -306,6 +307,7 @@ fm_status flashmask_fwd(const fm_problem *p, const fm_options *opt, const void *
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     Recorder rec = recorder(opt);
     cudaError_t e = g.reuse_map ? cudaSuccess : map_and_lists(g, m, ws, st, rec);
+    if (e == cudaSuccess && g.debug_bounds) e = launch_validate_lists(g, ws, st);
     if (e == cudaSuccess) {
         FwdArgs a{&tq, &tk, &tv, kr, &to, o, lse};
         rec.before(st);
@@ -349,6 +351,7 @@ fm_status flashmask_bwd(const fm_problem *p, const fm_options *opt, const void *
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     Recorder rec = recorder(opt);
     cudaError_t e = g.reuse_map ? cudaSuccess : map_and_lists(g, m, ws, st, rec);
+    if (e == cudaSuccess && g.debug_bounds) e = launch_validate_lists(g, ws, st);
     if (e == cudaSuccess) {
         BwdArgs a;
         a.dq_k_rows = dq_kr;
@@ -380,6 +383,7 @@ fm_status flashmask_get_error(void *stream) {
     cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return fail(e, "cudaStreamSynchronize");
     unsigned err = read_clear_error_classify() | read_clear_error_fwd() | read_clear_error_bwd();
+    if (err & ERR_BOUNDS) return FM_ERR_DEVICE_BOUNDS;
     return err ? FM_ERR_DEVICE_TIMEOUT : FM_OK;
 }
 
@@ -393,6 +397,7 @@ const char *flashmask_error_string(fm_status s) {
         case FM_ERR_WORKSPACE: return "workspace missing, unaligned or too small";
         case FM_ERR_CUDA: return "CUDA call failed";
         case FM_ERR_DEVICE_TIMEOUT: return "a kernel gave up on a bounded wait";
+        case FM_ERR_DEVICE_BOUNDS: return "a kernel found a work list out of bounds";
     }
     return "unknown status";
 }

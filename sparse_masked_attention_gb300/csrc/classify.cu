@@ -260,6 +260,61 @@ __global__ void __launch_bounds__(1024) fwd_lists_kernel(int N, int T, int rows,
     if (lane == 0) pair_cnt[pr] = count;
 }
 
+// debug_bounds: checks every work list the attention kernels will read from
+// the workspace, one warp per job, before they run.  A list row must have a
+// count in [0, T] and entries whose tile index (entry >> shift) lies in
+// [0, T); a pair-order entry must lie in [0, TP).  A failing row gets count 0
+// and a failing order entry its own position (a valid pair index), so the
+// kernels after it read nothing out of range; the error word records
+// ERR_BOUNDS.  Jobs: fwd lists, bwd lists (rows x T entries, shift 1), pair
+// lists (pair_rows x T, shift 2), pair order (pair_rows).
+__global__ void __launch_bounds__(256) validate_lists_kernel(
+    int T, int rows, int pair_rows, int *__restrict__ fwd_list, int *__restrict__ fwd_cnt,
+    int *__restrict__ bwd_list, int *__restrict__ bwd_cnt, int *__restrict__ pair_list,
+    int *__restrict__ pair_cnt, int *__restrict__ pair_order) {
+    pdl_wait();  // the lists of the kernels before
+    pdl_trigger();
+    const int lane = threadIdx.x & 31;
+    const long long job = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int TP = (T + 1) / 2;
+    const int *list;
+    int *cnt;
+    int shift;
+    long long r = job;
+    if (r < rows) {
+        list = fwd_list, cnt = fwd_cnt, shift = 1;
+    } else if ((r -= rows) < rows) {
+        list = bwd_list, cnt = bwd_cnt, shift = 1;
+    } else if ((r -= rows) < pair_rows) {
+        list = pair_list, cnt = pair_cnt, shift = 2;
+    } else if ((r -= pair_rows) < pair_rows) {
+        if (lane == 0) {
+            const int v = pair_order[r];
+            if (v < 0 || v >= TP) {
+                pair_order[r] = static_cast<int>(r % TP);
+                atomicOr(&g_err_classify, ERR_BOUNDS);
+            }
+        }
+        return;
+    } else {
+        return;
+    }
+    const int n = cnt[r];
+    bool ok = n >= 0 && n <= T;
+    if (ok) {
+        const int *row = list + r * T;
+        for (int i = lane; i < n; i += 32) {
+            const int t = row[i] >> shift;
+            ok = ok && t >= 0 && t < T;
+        }
+    }
+    ok = __all_sync(0xffffffffu, ok);
+    if (!ok && lane == 0) {
+        cnt[r] = 0;
+        atomicOr(&g_err_classify, ERR_BOUNDS);
+    }
+}
+
 // Unmasked pairs per mask head: sum over columns of N - |masked rows of j|.
 __global__ void __launch_bounds__(1024) count_kernel(int N, int causal,
                                                      const int32_t *__restrict__ lts,
@@ -325,6 +380,17 @@ cudaError_t launch_fwd_lists(const Geometry &g, const Workspace &ws, cudaStream_
                       g.N, g.T, rows, pair_rows, list_blocks,
                       static_cast<const uint8_t *>(ws.cls), ws.fwd_list, ws.fwd_cnt, ws.bwd_list,
                       ws.bwd_cnt, ws.pair_list, ws.pair_cnt, ws.pair_order);
+}
+
+cudaError_t launch_validate_lists(const Geometry &g, const Workspace &ws, cudaStream_t st) {
+    const long long rows = static_cast<long long>(g.B) * g.Hm * g.T;
+    const long long pair_rows = static_cast<long long>(g.B) * g.Hm * ((g.T + 1) / 2);
+    const long long jobs = 2 * rows + 2 * pair_rows;
+    const unsigned blocks = static_cast<unsigned>((jobs * 32 + 255) / 256);
+    return launch_pdl(validate_lists_kernel, dim3(blocks), dim3(256), 0, st, g.T,
+                      static_cast<int>(rows), static_cast<int>(pair_rows), ws.fwd_list,
+                      ws.fwd_cnt, ws.bwd_list, ws.bwd_cnt, ws.pair_list, ws.pair_cnt,
+                      ws.pair_order);
 }
 
 cudaError_t launch_count(const Geometry &g, const MaskPtrs &m, unsigned long long *counts,

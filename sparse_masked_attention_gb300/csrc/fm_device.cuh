@@ -8,6 +8,8 @@
 #include <cuda_fp16.h>
 #include <stdint.h>
 
+#include "fm_internal.h"
+
 namespace fm {
 
 // ------------------------------------------------------------------ basics
@@ -91,9 +93,6 @@ __device__ __forceinline__ uint32_t mbar_test(uint64_t *bar, uint32_t parity) {
         : "memory");
     return ok;
 }
-
-// Error codes a kernel may leave in its device error word.
-enum : unsigned { ERR_NONE = 0, ERR_TIMEOUT = 1, ERR_SMEM_ALIGN = 2 };
 
 // Bounded wait for the phase of `bar` with the given parity to complete.
 // Returns false when `timeout_ns` elapsed or another role of the CTA already

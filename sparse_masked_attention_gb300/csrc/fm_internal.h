@@ -13,6 +13,9 @@ namespace fm {
 
 constexpr int TILE = 128;  // tile edge of the tile map and of the list entries
 
+// Error codes a kernel may leave in its device error word (bits).
+enum : unsigned { ERR_NONE = 0, ERR_TIMEOUT = 1, ERR_SMEM_ALIGN = 2, ERR_BOUNDS = 4 };
+
 struct Geometry {
     int B, H, Hm, N, d, dv;
     int T;       // ceil(N / 128)
@@ -24,6 +27,7 @@ struct Geometry {
     const float *sink;  // [H] attention-sink logits, or nullptr
     float *dsink;       // [H] their gradient (backward), or nullptr
     int reuse_map;      // the workspace already holds this problem's tile map and lists
+    int debug_bounds;   // attention kernels check their work lists before use
 };
 
 // Normalised mask boundaries per key column: (LTS, LTE, UTS, UTE) clamped to
@@ -101,6 +105,8 @@ struct MaskPtrs {
 cudaError_t launch_classify(const Geometry &g, const MaskPtrs &m, const Workspace &ws,
                             cudaStream_t st);
 cudaError_t launch_fwd_lists(const Geometry &g, const Workspace &ws, cudaStream_t st);
+// debug_bounds: checks (and neutralises) every work list in the workspace.
+cudaError_t launch_validate_lists(const Geometry &g, const Workspace &ws, cudaStream_t st);
 cudaError_t launch_count(const Geometry &g, const MaskPtrs &m, unsigned long long *counts,
                          cudaStream_t st);
 unsigned read_clear_error_classify();

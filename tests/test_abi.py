@@ -37,8 +37,9 @@ def test_exports_every_declared_symbol(lib):
 
 
 def test_error_strings(lib):
-    for s in range(6):
-        assert B.flashmask_error_string(s)
+    for s in range(7):
+        assert B.flashmask_error_string(s) != "unknown status"
+    assert "bounds" in B.flashmask_error_string(B.FM_ERR_DEVICE_BOUNDS)
     assert B.flashmask_error_string(99) == "unknown status"
 
 
@@ -86,11 +87,19 @@ def test_invalid_args_rejected_before_cuda(lib):
     # workspace too small
     st = B.flashmask_fwd(p, None, 256, 256, 256, None, None, None, None, 256, 256, 256, 16, None)
     assert st == B.FM_ERR_WORKSPACE
-    # reserved option
-    opt = B.fm_options(0, 1, 0, None, 0)
+    # debug_bounds is a flag: 0 or 1
+    opt = B.fm_options(0, 2, 0, None, 0)
     st = B.flashmask_fwd(p, opt, 256, 256, 256, None, None, None, None, 256, 256, 256, 1 << 30,
                          None)
     assert st == B.FM_ERR_INVALID_ARG
+
+
+def test_debug_bounds_is_a_flag(lib):
+    p = _prob()
+    base = B.flashmask_workspace_size(p, None, 1)
+    assert B.flashmask_workspace_size(p, B.fm_options(0, 1, 0, None, 0), 1) == base
+    assert B.flashmask_workspace_size(p, B.fm_options(0, 2, 0, None, 0), 1) == 0
+    assert B.flashmask_workspace_size(p, B.fm_options(0, -1, 0, None, 0), 1) == 0
 
 
 def test_chunk_entry_points_reject_bad_arguments_before_cuda(lib):
