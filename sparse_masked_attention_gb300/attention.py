@@ -103,6 +103,8 @@ def _check_qkv(q, k, v):
     B, N, H, d = q.shape
     if k.shape != (B, N, H, d) or v.shape[:3] != (B, N, H):
         raise FlashMaskError("q, k, v shapes disagree")
+    if not (_same_device(k.device, q.device) and _same_device(v.device, q.device)):
+        raise FlashMaskError("q, k, v must be on one device")
     return B, N, H, d, v.shape[3]
 
 
@@ -112,6 +114,21 @@ def workspace_size(B, H, Hm, N, d, dv, is_bwd: bool, deterministic=False) -> int
     if n == 0:
         raise FlashMaskError("invalid problem for workspace query")
     return n
+
+
+def _check_out(name, t, shape, dtype, device):
+    """A caller-supplied output: the kernels write every element of `shape`
+    through its data pointer, so anything else would write out of bounds."""
+    if (t.dtype != dtype or tuple(t.shape) != tuple(shape) or not t.is_contiguous()
+            or not _same_device(t.device, device)):
+        raise FlashMaskError(f"{name} must be a contiguous {dtype} tensor of shape "
+                             f"{tuple(shape)} on {device}")
+
+
+def _check_workspace(ws, device):
+    if ws.dtype != torch.uint8 or ws.dim() != 1 or not ws.is_contiguous() or \
+            not _same_device(ws.device, device):
+        raise FlashMaskError(f"workspace must be a contiguous 1-D uint8 tensor on {device}")
 
 
 def _check_sink(sink, H, device):
@@ -140,9 +157,12 @@ def fwd(q, k, v, lts=None, lte=None, uts=None, ute=None, causal=False, scale=Non
         out = torch.empty((B, N, H, dv), dtype=torch.bfloat16, device=q.device)
     if lse is None:
         lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    _check_out("out", out, (B, N, H, dv), torch.bfloat16, q.device)
+    _check_out("lse", lse, (B, H, N), torch.float32, q.device)
     ws_bytes = _b.flashmask_workspace_size(prob, opt, 0)
     if workspace is None:
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
+    _check_workspace(workspace, q.device)
     st = _b.flashmask_fwd(prob, opt, q.data_ptr(), k.data_ptr(), v.data_ptr(), *mp,
                           out.data_ptr(), lse.data_ptr(), workspace.data_ptr(),
                           workspace.numel(), _stream(stream))
@@ -162,10 +182,12 @@ def bwd(q, k, v, o, lse, dout, lts=None, lte=None, uts=None, ute=None, causal=Fa
     if options is not None and sink is not None:
         raise FlashMaskError("pass the sink either in options or as sink=, not both")
     for name, t, shape in (("o", o, (B, N, H, dvd)), ("dout", dout, (B, N, H, dvd))):
-        if t.dtype != torch.bfloat16 or not t.is_contiguous() or tuple(t.shape) != shape:
-            raise FlashMaskError(f"{name} must be contiguous bf16 {shape}")
-    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, N) or not lse.is_contiguous():
-        raise FlashMaskError("lse must be contiguous fp32 [B, H, N]")
+        if t.dtype != torch.bfloat16 or not t.is_contiguous() or tuple(t.shape) != shape or \
+                not _same_device(t.device, q.device):
+            raise FlashMaskError(f"{name} must be contiguous bf16 {shape} on {q.device}")
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, N) or \
+            not lse.is_contiguous() or not _same_device(lse.device, q.device):
+        raise FlashMaskError(f"lse must be contiguous fp32 [B, H, N] on {q.device}")
     Hm, mp, _keep = _mask_args((lts, lte, uts, ute), B, H, N, q.device)
     prob = make_problem(B, H, Hm, N, d, dvd, scale, causal)
     dsink = None if sink is None else torch.empty(H, dtype=torch.float32, device=q.device)
@@ -176,9 +198,13 @@ def bwd(q, k, v, o, lse, dout, lts=None, lte=None, uts=None, ute=None, causal=Fa
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
+    _check_out("dq", dq, (B, N, H, d), torch.bfloat16, q.device)
+    _check_out("dk", dk, (B, N, H, d), torch.bfloat16, q.device)
+    _check_out("dv", dv, (B, N, H, dvd), torch.bfloat16, q.device)
     ws_bytes = _b.flashmask_workspace_size(prob, opt, 1)
     if workspace is None:
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
+    _check_workspace(workspace, q.device)
     st = _b.flashmask_bwd(prob, opt, q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
                           lse.data_ptr(), dout.data_ptr(), *mp, dq.data_ptr(), dk.data_ptr(),
                           dv.data_ptr(), workspace.data_ptr(), workspace.numel(),
