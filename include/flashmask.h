@@ -190,6 +190,16 @@ fm_status flashmask_count_unmasked(const fm_problem *p,
 fm_status flashmask_get_error(void *stream);
 
 /*
+ * Failure-detection self-test.  Enqueues on `stream` a one-thread kernel that
+ * waits, through the same bounded wait every kernel of the library uses, on
+ * an mbarrier phase that nothing completes.  After timeout_ns nanoseconds the
+ * wait gives up, records a timeout in the device error word and the kernel
+ * returns, so the next flashmask_get_error reports FM_ERR_DEVICE_TIMEOUT and
+ * the context stays usable.  0 < timeout_ns <= 10 s, else FM_ERR_INVALID_ARG.
+ */
+fm_status flashmask_selftest_wait(unsigned long long timeout_ns, void *stream);
+
+/*
  * Forward without a workspace, for callers that cannot allocate device memory
  * (a host that only hands out its own tensors, code where cudaMalloc is not
  * allowed or would stall, an embedding with no allocator).  It computes

@@ -247,6 +247,13 @@ def get_error(stream=None):
     _check(_b.flashmask_get_error(_stream(stream)), "device")
 
 
+def selftest_wait(timeout_ns=20_000_000, stream=None):
+    """Failure-detection self-test: a device wait that nothing completes gives
+    up after `timeout_ns`; the next get_error() raises with status
+    FM_ERR_DEVICE_TIMEOUT, and the context stays usable."""
+    _check(_b.flashmask_selftest_wait(timeout_ns, _stream(stream)), "flashmask_selftest_wait")
+
+
 class FlashMaskAttention(torch.autograd.Function):
     """Autograd wrapper: forward and backward both run in the CUDA library."""
 

@@ -46,7 +46,7 @@ EXPORTS = ("flashmask_workspace_size", "flashmask_fwd", "flashmask_bwd", "flashm
            "flashmask_count_unmasked", "flashmask_get_error", "flashmask_error_string",
            "flashmask_last_error_detail", "flashmask_fwd_noalloc", "flashmask_localize",
            "flashmask_merge_init", "flashmask_merge", "flashmask_merge_finish",
-           "flashmask_accumulate", "flashmask_to_bf16")
+           "flashmask_accumulate", "flashmask_to_bf16", "flashmask_selftest_wait")
 
 FM_NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024
 
@@ -82,6 +82,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.flashmask_count_unmasked.restype = ctypes.c_int
         lib.flashmask_get_error.argtypes = [vp]
         lib.flashmask_get_error.restype = ctypes.c_int
+        lib.flashmask_selftest_wait.argtypes = [ctypes.c_ulonglong, vp]
+        lib.flashmask_selftest_wait.restype = ctypes.c_int
         lib.flashmask_error_string.argtypes = [ctypes.c_int]
         lib.flashmask_error_string.restype = ctypes.c_char_p
         lib.flashmask_fwd_noalloc.argtypes = [prob, opt, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
@@ -136,6 +138,10 @@ def flashmask_count_unmasked(problem, lts, lte, uts, ute, counts, stream) -> int
 
 def flashmask_get_error(stream) -> int:
     return int(load().flashmask_get_error(stream))
+
+
+def flashmask_selftest_wait(timeout_ns, stream) -> int:
+    return int(load().flashmask_selftest_wait(int(timeout_ns), stream))
 
 
 def flashmask_error_string(status: int) -> str:

@@ -17,6 +17,7 @@ namespace {
 
 constexpr uint64_t DEFAULT_TIMEOUT_NS = 1000000000ull;
 constexpr size_t WS_ALIGN = 256;
+constexpr unsigned long long MAX_SELFTEST_NS = 10000000000ull;  // 10 s
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -377,6 +378,12 @@ fm_status flashmask_bwd(const fm_problem *p, const fm_options *opt, const void *
         e = launch_bwd(g, ws, a, st, rec);
     }
     return cuda_status(e);
+}
+
+fm_status flashmask_selftest_wait(unsigned long long timeout_ns, void *stream) {
+    if (timeout_ns == 0 || timeout_ns > MAX_SELFTEST_NS) return FM_ERR_INVALID_ARG;
+    if (!device_ok(nullptr)) return FM_ERR_UNSUPPORTED;
+    return cuda_status(launch_wait_selftest(timeout_ns, static_cast<cudaStream_t>(stream)));
 }
 
 fm_status flashmask_get_error(void *stream) {

@@ -315,6 +315,22 @@ __global__ void __launch_bounds__(256) validate_lists_kernel(
     }
 }
 
+// Failure-detection self-test: one thread waits, with the caller's limit, on
+// the first phase of an mbarrier that nothing arrives at.  The bounded wait
+// gives up and records ERR_TIMEOUT in the error word, as the wait of any
+// kernel of the library would; the kernel then returns normally.
+__global__ void __launch_bounds__(32) wait_selftest_kernel(uint64_t timeout_ns) {
+    __shared__ uint64_t bar;
+    __shared__ int abort;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        abort = 0;
+        fence_barrier_init();
+        (void)mbar_wait(&bar, 0, timeout_ns, reinterpret_cast<volatile int *>(&abort),
+                        &g_err_classify);
+    }
+}
+
 // Unmasked pairs per mask head: sum over columns of N - |masked rows of j|.
 __global__ void __launch_bounds__(1024) count_kernel(int N, int causal,
                                                      const int32_t *__restrict__ lts,
@@ -391,6 +407,11 @@ cudaError_t launch_validate_lists(const Geometry &g, const Workspace &ws, cudaSt
                       static_cast<int>(rows), static_cast<int>(pair_rows), ws.fwd_list,
                       ws.fwd_cnt, ws.bwd_list, ws.bwd_cnt, ws.pair_list, ws.pair_cnt,
                       ws.pair_order);
+}
+
+cudaError_t launch_wait_selftest(uint64_t timeout_ns, cudaStream_t st) {
+    wait_selftest_kernel<<<1, 32, 0, st>>>(timeout_ns);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_count(const Geometry &g, const MaskPtrs &m, unsigned long long *counts,

@@ -107,6 +107,8 @@ cudaError_t launch_classify(const Geometry &g, const MaskPtrs &m, const Workspac
 cudaError_t launch_fwd_lists(const Geometry &g, const Workspace &ws, cudaStream_t st);
 // debug_bounds: checks (and neutralises) every work list in the workspace.
 cudaError_t launch_validate_lists(const Geometry &g, const Workspace &ws, cudaStream_t st);
+// A bounded wait that nothing completes (failure-detection self-test).
+cudaError_t launch_wait_selftest(uint64_t timeout_ns, cudaStream_t st);
 cudaError_t launch_count(const Geometry &g, const MaskPtrs &m, unsigned long long *counts,
                          cudaStream_t st);
 unsigned read_clear_error_classify();

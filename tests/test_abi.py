@@ -128,3 +128,8 @@ def test_chunk_entry_points_reject_bad_arguments_before_cuda(lib):
 def test_sink_gradient_needs_its_logits(lib):
     opt = B.fm_options(0, 0, 0, None, 0, None, 256)
     assert B.flashmask_workspace_size(_prob(), opt, 1) == 0
+
+
+def test_selftest_wait_limits_checked_before_cuda(lib):
+    assert B.flashmask_selftest_wait(0, None) == B.FM_ERR_INVALID_ARG
+    assert B.flashmask_selftest_wait(10_000_000_001, None) == B.FM_ERR_INVALID_ARG
