@@ -42,6 +42,31 @@ def _stream(stream):
     return stream.cuda_stream
 
 
+_nvtx = False
+
+
+def set_nvtx(enabled: bool) -> None:
+    """Wrap every forward and backward launch sequence in an NVTX range
+    ("flashmask_fwd N=... d=..."), so profiler timelines show which kernels
+    belong to which call.  Off by default: a range costs host time per call."""
+    global _nvtx
+    _nvtx = bool(enabled)
+
+
+class _Range:
+    def __init__(self, name):
+        self.name = name
+
+    def __enter__(self):
+        if _nvtx:
+            torch.cuda.nvtx.range_push(self.name)
+
+    def __exit__(self, *exc):
+        if _nvtx:
+            torch.cuda.nvtx.range_pop()
+        return False
+
+
 def _same_device(a: torch.device, b: torch.device) -> bool:
     if a.type != b.type:
         return False
@@ -163,9 +188,10 @@ def fwd(q, k, v, lts=None, lte=None, uts=None, ute=None, causal=False, scale=Non
     if workspace is None:
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
     _check_workspace(workspace, q.device)
-    st = _b.flashmask_fwd(prob, opt, q.data_ptr(), k.data_ptr(), v.data_ptr(), *mp,
-                          out.data_ptr(), lse.data_ptr(), workspace.data_ptr(),
-                          workspace.numel(), _stream(stream))
+    with _Range(f"flashmask_fwd B={B} H={H} N={N} d={d} dv={dv}" if _nvtx else ""):
+        st = _b.flashmask_fwd(prob, opt, q.data_ptr(), k.data_ptr(), v.data_ptr(), *mp,
+                              out.data_ptr(), lse.data_ptr(), workspace.data_ptr(),
+                              workspace.numel(), _stream(stream))
     _check(st, "flashmask_fwd")
     return out, lse
 
@@ -205,10 +231,11 @@ def bwd(q, k, v, o, lse, dout, lts=None, lte=None, uts=None, ute=None, causal=Fa
     if workspace is None:
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
     _check_workspace(workspace, q.device)
-    st = _b.flashmask_bwd(prob, opt, q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
-                          lse.data_ptr(), dout.data_ptr(), *mp, dq.data_ptr(), dk.data_ptr(),
-                          dv.data_ptr(), workspace.data_ptr(), workspace.numel(),
-                          _stream(stream))
+    with _Range(f"flashmask_bwd B={B} H={H} N={N} d={d} dv={dvd}" if _nvtx else ""):
+        st = _b.flashmask_bwd(prob, opt, q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                              o.data_ptr(), lse.data_ptr(), dout.data_ptr(), *mp,
+                              dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                              workspace.data_ptr(), workspace.numel(), _stream(stream))
     _check(st, "flashmask_bwd")
     return (dq, dk, dv) if sink is None else (dq, dk, dv, dsink)
 

@@ -35,3 +35,17 @@ def test_bounded_wait_gives_up_and_the_context_stays_usable():
     grads = fm.bwd(q, k, v, o, lse, do, lts, lte, uts, ute, mask.causal)
     fm.get_error()
     check_head_full(q, k, v, do, mask, o, lse, grads, 0, 1)
+
+
+def test_nvtx_ranges_wrap_the_calls():
+    B, H, N, d = 1, 2, 300, 64
+    q, k, v, do = W.make_inputs(B, N, H, d, d, seed=9, device="cuda")
+    ref_o, ref_lse = fm.fwd(q, k, v, causal=True)
+    fm.set_nvtx(True)
+    try:
+        o, lse = fm.fwd(q, k, v, causal=True)
+        fm.bwd(q, k, v, o, lse, do, causal=True)
+    finally:
+        fm.set_nvtx(False)
+    fm.get_error()
+    assert torch.equal(o, ref_o) and torch.equal(lse, ref_lse)
