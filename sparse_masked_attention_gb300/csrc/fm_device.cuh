@@ -23,8 +23,6 @@ __device__ __forceinline__ uint64_t globaltimer() {
     return t;
 }
 
-__device__ __forceinline__ uint32_t elect_lane0() { return (threadIdx.x & 31) == 0; }
-
 __device__ __forceinline__ float ex2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -287,18 +285,6 @@ __device__ __forceinline__ void tmem_ld64f(uint32_t taddr, float *x) {
         : "memory");
 }
 
-// Two 64-column TMEM loads (this thread's lane) with a single wait.
-__device__ __forceinline__ void tmem_ld64f_x2(uint32_t taddr_x, float *x, uint32_t taddr_y,
-                                              float *y) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%128];\n\t"
-        "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%64, %65, %66, %67, %68, %69, %70, %71, %72, %73, %74, %75, %76, %77, %78, %79, %80, %81, %82, %83, %84, %85, %86, %87, %88, %89, %90, %91, %92, %93, %94, %95, %96, %97, %98, %99, %100, %101, %102, %103, %104, %105, %106, %107, %108, %109, %110, %111, %112, %113, %114, %115, %116, %117, %118, %119, %120, %121, %122, %123, %124, %125, %126, %127}, [%129];\n\t"
-        "tcgen05.wait::ld.sync.aligned;"
-        : "=f"(x[0]), "=f"(x[1]), "=f"(x[2]), "=f"(x[3]), "=f"(x[4]), "=f"(x[5]), "=f"(x[6]), "=f"(x[7]), "=f"(x[8]), "=f"(x[9]), "=f"(x[10]), "=f"(x[11]), "=f"(x[12]), "=f"(x[13]), "=f"(x[14]), "=f"(x[15]), "=f"(x[16]), "=f"(x[17]), "=f"(x[18]), "=f"(x[19]), "=f"(x[20]), "=f"(x[21]), "=f"(x[22]), "=f"(x[23]), "=f"(x[24]), "=f"(x[25]), "=f"(x[26]), "=f"(x[27]), "=f"(x[28]), "=f"(x[29]), "=f"(x[30]), "=f"(x[31]), "=f"(x[32]), "=f"(x[33]), "=f"(x[34]), "=f"(x[35]), "=f"(x[36]), "=f"(x[37]), "=f"(x[38]), "=f"(x[39]), "=f"(x[40]), "=f"(x[41]), "=f"(x[42]), "=f"(x[43]), "=f"(x[44]), "=f"(x[45]), "=f"(x[46]), "=f"(x[47]), "=f"(x[48]), "=f"(x[49]), "=f"(x[50]), "=f"(x[51]), "=f"(x[52]), "=f"(x[53]), "=f"(x[54]), "=f"(x[55]), "=f"(x[56]), "=f"(x[57]), "=f"(x[58]), "=f"(x[59]), "=f"(x[60]), "=f"(x[61]), "=f"(x[62]), "=f"(x[63]), "=f"(y[0]), "=f"(y[1]), "=f"(y[2]), "=f"(y[3]), "=f"(y[4]), "=f"(y[5]), "=f"(y[6]), "=f"(y[7]), "=f"(y[8]), "=f"(y[9]), "=f"(y[10]), "=f"(y[11]), "=f"(y[12]), "=f"(y[13]), "=f"(y[14]), "=f"(y[15]), "=f"(y[16]), "=f"(y[17]), "=f"(y[18]), "=f"(y[19]), "=f"(y[20]), "=f"(y[21]), "=f"(y[22]), "=f"(y[23]), "=f"(y[24]), "=f"(y[25]), "=f"(y[26]), "=f"(y[27]), "=f"(y[28]), "=f"(y[29]), "=f"(y[30]), "=f"(y[31]), "=f"(y[32]), "=f"(y[33]), "=f"(y[34]), "=f"(y[35]), "=f"(y[36]), "=f"(y[37]), "=f"(y[38]), "=f"(y[39]), "=f"(y[40]), "=f"(y[41]), "=f"(y[42]), "=f"(y[43]), "=f"(y[44]), "=f"(y[45]), "=f"(y[46]), "=f"(y[47]), "=f"(y[48]), "=f"(y[49]), "=f"(y[50]), "=f"(y[51]), "=f"(y[52]), "=f"(y[53]), "=f"(y[54]), "=f"(y[55]), "=f"(y[56]), "=f"(y[57]), "=f"(y[58]), "=f"(y[59]), "=f"(y[60]), "=f"(y[61]), "=f"(y[62]), "=f"(y[63])
-        : "r"(taddr_x), "r"(taddr_y)
-        : "memory");
-}
-
 // Registers -> 32 consecutive TMEM columns of this thread's lane (no wait).
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
     asm volatile(
@@ -315,11 +301,6 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
 
 __device__ __forceinline__ void tmem_st_wait() {
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-}
-
-// TMEM address of (lane, column).
-__device__ __forceinline__ uint32_t tmem_addr(uint32_t base, uint32_t lane, uint32_t col) {
-    return base + (lane << 16) + col;
 }
 
 // Named barrier over `nthreads` threads (multiple of 32).
@@ -360,11 +341,6 @@ __device__ __forceinline__ uint32_t warp_transpose32(uint32_t x, int lane) {
         x = (lane & s) ? ((x & ~m) | ((y & ~m) >> s)) : ((x & m) | ((y & m) << s));
     }
     return x;
-}
-
-// Column-wise mask predicate on normalised boundaries c = (LTS, LTE, UTS, UTE).
-__device__ __forceinline__ bool masked_at(int i, int j, int4 c, int causal) {
-    return (causal && i < j) | (c.x <= i && i < c.y) | (c.z <= i && i < c.w);
 }
 
 }  // namespace fm

@@ -56,14 +56,6 @@ class Mask:
         return out
 
 
-def _empty_lower(N):
-    return np.full(N, N, np.int32), np.full(N, N, np.int32)
-
-
-def _empty_upper(N):
-    return np.zeros(N, np.int32), np.zeros(N, np.int32)
-
-
 def uniform_lengths(rng: np.random.Generator, lo: int, hi: int, N: int) -> list:
     """Integer lengths ~ U[lo, hi] drawn until they cover N; the last one is cut."""
     out, tot = [], 0
