@@ -45,6 +45,10 @@ def parse():
     ap.add_argument("--N", type=int, default=None, help="override the workload's N (profiling)")
     ap.add_argument("--B", type=int, default=None, help="override the workload's B (profiling)")
     ap.add_argument("--H", type=int, default=None, help="override the workload's H (profiling)")
+    ap.add_argument("--d", type=int, default=None,
+                    help="override the workload's head dim of Q and K (with --dv; profiling)")
+    ap.add_argument("--dv", type=int, default=None,
+                    help="override the workload's head dim of V (profiling)")
     ap.add_argument("--deterministic", type=int, choices=[0, 1], default=None,
                     help="override the workload's deterministic-backward flag")
     ap.add_argument("--chunks", type=int, default=0,
@@ -150,7 +154,7 @@ class ClockSampler:
 def workload_cfg(args):
     from sparse_masked_attention_gb300 import workloads as W
     cfg = dict(W.CONFIGS[args.workload])
-    for key in ("N", "B", "H"):
+    for key in ("N", "B", "H", "d", "dv"):
         if getattr(args, key, None):
             cfg[key] = getattr(args, key)
     if getattr(args, "deterministic", None) is not None:
@@ -322,8 +326,8 @@ def run_ours(args, rank, world, local_rank):
                 "frac": round(achieved / pk["bf16_tflops"], 4),
                 "frac_sustained": round(achieved / pk["bf16_tflops_sustained"], 4),
                 "peak_source": f"{src} burst bf16 (sustained {pk['bf16_tflops_sustained']})",
-                "traffic": profiled_traffic(dom_name, args.workload) if (B, H, N) == tuple(
-                    W.CONFIGS[args.workload][x] for x in ("B", "H", "N")) else None,
+                "traffic": profiled_traffic(dom_name, args.workload) if (B, H, N, d, dv) == tuple(
+                    W.CONFIGS[args.workload][x] for x in ("B", "H", "N", "d", "dv")) else None,
                 "traffic_unit": "bytes per launch (ncu, profiles/roofline_traffic.txt)",
                 "avg_ms": round(avg[dominant], 4)}
 
@@ -342,8 +346,8 @@ def run_ours(args, rank, world, local_rank):
         "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": args.workload + ("" if (B, H, N) == tuple(
-                       W.CONFIGS[args.workload][x] for x in ("B", "H", "N")) else " (resized)"),
+        "config": {"workload": args.workload + ("" if (B, H, N, d, dv) == tuple(
+                       W.CONFIGS[args.workload][x] for x in ("B", "H", "N", "d", "dv")) else " (resized)"),
                    "B": B, "H": H, "N": N, "d": d, "dv": dv,
                    "mask": cfg["mask"], "passes": "fwd+bwd" if has_bwd else "fwd",
                    "deterministic": det, "unmasked_pairs": U,
