@@ -57,10 +57,39 @@ def parse():
     return ap.parse_args()
 
 
+def code_hash(path: str) -> str:
+    """SHA-1 (first 12 hex digits) of a C/C++/CUDA source with its comments,
+    blank lines and surrounding whitespace removed: a comment edit keeps it,
+    a code edit changes it.  String and character literals are kept whole."""
+    import hashlib
+    src = open(path, encoding="utf-8").read()
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and src[j] != c:
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            while i < n and src[i] != "\n":
+                i += 1
+        elif src.startswith("/*", i):
+            end = src.find("*/", i + 2)
+            i = n if end < 0 else end + 2
+        else:
+            out.append(c)
+            i += 1
+    lines = [ln.strip() for ln in "".join(out).splitlines()]
+    code = "\n".join(ln for ln in lines if ln)
+    return hashlib.sha1(code.encode("utf-8")).hexdigest()[:12]
+
+
 def profiled_traffic(kernel: str, workload: str):
     """DRAM bytes per launch of `kernel` from the committed ncu summary table, or
-    None when there is none or the kernel's source changed since the capture."""
-    import hashlib
+    None when there is none or the kernel's source code (comments aside)
+    changed since the capture."""
     path = os.path.join(ROOT, "profiles", "roofline_traffic.txt")
     try:
         lines = open(path).read().splitlines()
@@ -73,7 +102,7 @@ def profiled_traffic(kernel: str, workload: str):
         if k != kernel or w != workload:
             continue
         try:
-            cur = hashlib.sha1(open(os.path.join(ROOT, src), "rb").read()).hexdigest()[:12]
+            cur = code_hash(os.path.join(ROOT, src))
         except OSError:
             return None
         return int(nbytes) if cur == sha else None

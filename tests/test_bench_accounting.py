@@ -58,3 +58,18 @@ def test_workload_overrides():
     cfg = bench.workload_cfg(args)
     assert cfg["deterministic"] is False and cfg["N"] == 4096 and cfg["H"] == 2
     assert cfg["d"] == base["d"] and cfg["B"] == base["B"]
+
+
+def test_code_hash_ignores_comments_only(tmp_path):
+    base = ('// header\n#include <x.h>\n/* block\n comment */\nint f(int a) {  // tail\n'
+            '    const char *s = "// not a comment /* either */";\n    return a + 1;\n}\n')
+    p = tmp_path / "k.cu"
+    p.write_text(base)
+    h0 = bench.code_hash(str(p))
+    p.write_text(base.replace("// header", "// another header\n\n// more")
+                     .replace("/* block\n comment */", "/* changed */"))
+    assert bench.code_hash(str(p)) == h0
+    p.write_text(base.replace('"// not a comment /* either */"', '"// not a comment"'))
+    assert bench.code_hash(str(p)) != h0  # string literals are code
+    p.write_text(base.replace("a + 1", "a + 2"))
+    assert bench.code_hash(str(p)) != h0
