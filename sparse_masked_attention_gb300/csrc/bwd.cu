@@ -12,17 +12,20 @@
 //                tiles; padding rows and fully masked rows get LSE = +inf, so
 //                their P is 0.
 //   dq kernel    one CTA per 128-row query tile walks its key tiles:
-//                S = Q K^T (bf16), dP = dO V^T (fp16 copies) as SS MMAs;
+//                S = Q K^T (bf16) and dP = dO V^T (fp16 copies) as SS MMAs
+//                (at d = 192 and 256, dO sits in TMEM and dP is a TS MMA);
 //                dS -> TMEM (bf16);
-//                dQ += dS K (TS MMA, dS read from TMEM).  Writes dQ once, in a
-//                fixed order.
+//                dQ += dS K (TS MMA, dS read from TMEM).  Writes dQ once.
 //   dkdv kernel  one CTA per 128-key tile walks its query tiles:
-//                S^T = K Q^T (bf16), dP^T = V dO^T (fp16 copies) as SS MMAs;
+//                S^T = K Q^T (bf16) and dP^T = V dO^T (fp16 copies) as SS MMAs
+//                (at d = 192 and 256, V sits in TMEM and dP^T is a TS MMA);
 //                P^T -> TMEM as fp16, dS^T as bf16; dV += P^T dO (fp16) and
 //                dK += dS^T Q (bf16) as TS MMAs.
-// No atomics are used, so every gradient is bit-reproducible.  For
-// d = dv = 256 the accumulators dK and dV do not fit in TMEM together, so
-// the dkdv kernel runs twice: once for dV, once for dK.
+// No atomics are used.  In deterministic mode the accumulations run in tile
+// order, so every gradient is bit-reproducible; otherwise whichever compute
+// group is ready goes first.  For d = dv = 256 the accumulators dK and dV do
+// not fit in TMEM together, so the dkdv kernel runs twice: once for dV, once
+// for dK.
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
