@@ -10,6 +10,11 @@
 // an exact per-column test: each column's masked rows form the union of at most
 // three intervals ([0, j) for the causal flag, LT, UT).  The map is therefore
 // exact, never just conservative.
+//
+// Also here: the list builder (fwd_lists_kernel), the unmasked-pair count
+// (count_kernel), the debug_bounds check of every work list in a workspace
+// (validate_lists_kernel) and the bounded-wait self-test
+// (wait_selftest_kernel).
 #include <cuda_runtime.h>
 #include <stdint.h>
 
