@@ -133,3 +133,38 @@ def test_sink_gradient_needs_its_logits(lib):
 def test_selftest_wait_limits_checked_before_cuda(lib):
     assert B.flashmask_selftest_wait(0, None) == B.FM_ERR_INVALID_ARG
     assert B.flashmask_selftest_wait(10_000_000_001, None) == B.FM_ERR_INVALID_ARG
+
+
+def _header_struct(name):
+    """Field names and C types of `typedef struct { ... } name;` in flashmask.h."""
+    import re
+    text = open(os.path.join(ROOT, "include", "flashmask.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    m = re.search(r"typedef struct\s*\{([^{}]*)\}\s*" + name + r"\s*;", text)
+    assert m, name
+    fields = []
+    for decl in m.group(1).split(";"):
+        decl = " ".join(decl.split())
+        if not decl:
+            continue
+        ctype, names = re.match(r"((?:const )?(?:unsigned long long|[a-z_]+)\s*\**)\s*(.*)",
+                                decl).groups()
+        for n in names.split(","):
+            n = n.strip()
+            stars = n.count("*")
+            fields.append((n.lstrip("*").strip(), ctype.replace(" ", "") + "*" * stars))
+    return fields
+
+
+_C_SIZES = {"int": 4, "float": 4, "unsignedlonglong": 8}
+
+
+@pytest.mark.parametrize("name", ["fm_problem", "fm_options"])
+def test_ctypes_structs_match_the_header(name):
+    import ctypes
+    fields = _header_struct(name)
+    cls = getattr(B, name)
+    assert [f[0] for f in fields] == [f[0] for f in cls._fields_]
+    for (fname, ctype), (pname, ptype) in zip(fields, cls._fields_):
+        size = 8 if ctype.endswith("*") else _C_SIZES[ctype.replace("const", "")]
+        assert ctypes.sizeof(ptype) == size, (fname, ctype, ptype)
