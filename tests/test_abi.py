@@ -168,3 +168,21 @@ def test_ctypes_structs_match_the_header(name):
     for (fname, ctype), (pname, ptype) in zip(fields, cls._fields_):
         size = 8 if ctype.endswith("*") else _C_SIZES[ctype.replace("const", "")]
         assert ctypes.sizeof(ptype) == size, (fname, ctype, ptype)
+
+
+def _header_functions():
+    """Parameter counts of the functions flashmask.h declares."""
+    text = open(os.path.join(ROOT, "include", "flashmask.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    out = {}
+    for m in re.finditer(r"\b(flashmask_[a-z0-9_]+)\s*\(([^;{]*?)\)\s*;", text):
+        params = " ".join(m.group(2).split())
+        out[m.group(1)] = 0 if params in ("", "void") else params.count(",") + 1
+    return out
+
+
+def test_ctypes_signatures_match_the_header(lib):
+    decl = _header_functions()
+    assert set(decl) == set(B.EXPORTS)
+    for name, n in decl.items():
+        assert len(getattr(lib, name).argtypes) == n, name
