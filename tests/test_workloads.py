@@ -106,3 +106,30 @@ def test_random_eviction_limits():
     assert not np.diag(m).any()
     assert m[np.triu(np.ones((N, N), bool), 1)].all()
     assert m.sum() > kept.sum()  # some keys were evicted
+
+
+# The benchmarked shapes, as the workload definitions state them: batch, heads,
+# sequence length, head dims, passes, and the mask's own parameters.
+STATED = {
+    "tiny_causal_document": dict(B=1, H=2, N=256, d=64, dv=64, passes="fwd+bwd"),
+    "std_causal": dict(B=1, H=32, N=8192, d=128, dv=128, passes="fwd"),
+    "std_sliding": dict(B=1, H=32, N=8192, d=128, dv=128, passes="fwd", w=1024),
+    "std_causal_document": dict(B=1, H=32, N=8192, d=128, dv=128, passes="fwd",
+                                doc_len=(512, 4096)),
+    "std_prefix_lm": dict(B=1, H=32, N=8192, d=128, dv=128, passes="fwd", prefix=2048),
+    "share_question": dict(B=2, H=16, N=32768, d=128, dv=128, passes="fwd+bwd"),
+    "long_block_sparse": dict(B=1, H=8, N=131072, d=128, dv=128, passes="fwd+bwd"),
+    "long_global_sliding": dict(B=1, H=8, N=131072, d=128, dv=128, passes="fwd+bwd",
+                                n_global=512, w=4096),
+    "large_head_d192": dict(B=1, H=16, N=16384, d=192, dv=128, passes="fwd+bwd",
+                            doc_len=(1024, 8192), deterministic=True),
+    "large_head_d256": dict(B=1, H=16, N=16384, d=256, dv=256, passes="fwd+bwd",
+                            doc_len=(1024, 8192), deterministic=True),
+}
+
+
+@pytest.mark.parametrize("name", sorted(STATED))
+def test_benchmarked_shapes_are_the_stated_ones(name):
+    cfg = W.CONFIGS[name]
+    for key, want in STATED[name].items():
+        assert cfg[key] == want, (name, key)
