@@ -22,6 +22,10 @@
  *   - Device pointers are owned by the caller.  The library never allocates,
  *     frees or synchronises, except flashmask_get_error, which synchronises
  *     its stream.
+ *   - An entry point makes the device that owns the caller's memory current
+ *     for its own launches (flashmask_get_error: the stream's device) and,
+ *     before it returns, makes the calling thread's previous context current
+ *     again: the caller's current device is unchanged.
  *   - Work is enqueued on `stream` (a cudaStream_t, NULL = legacy default
  *     stream), and the call returns at once.
  *   - Errors are returned as fm_status; nothing is thrown and nothing is
@@ -209,12 +213,18 @@ fm_status flashmask_selftest_wait(unsigned long long timeout_ns, void *stream);
  *  - Problems whose forward workspace (flashmask_workspace_size, is_bwd = 0)
  *    exceeds FM_NOALLOC_SCRATCH_BYTES are rejected with FM_ERR_WORKSPACE, and
  *    flashmask_last_error_detail says why.
+ *  - fm_options.reuse_tile_map must be 0 (else FM_ERR_INVALID_ARG, before any
+ *    CUDA call): the array may hold the tile map of another problem.  The
+ *    other options (deterministic, debug_bounds, wait_timeout_ns,
+ *    kernel_events, sink) act as in flashmask_fwd.
  *  - The first call on a device looks up the array's device address (a
- *    one-time cudaGetSymbolAddress with that device current); make that first
- *    call before any stream capture.
+ *    cudaGetSymbolAddress with that device current), and so does the first
+ *    call after a cudaDeviceReset of it; make that first call before any
+ *    stream capture.  A failed lookup returns FM_ERR_CUDA and is retried on
+ *    the next call.
  *  - All calls on a device share the array.  Calls that overlap on the GPU
- *    race and give wrong results; order them on one stream.  Nothing in the
- *    array needs clearing between calls.
+ *    race and give wrong results; order them on one stream.  Every call
+ *    rewrites what it reads, so nothing in the array needs clearing.
  *  - The device is the one that owns q.  Allocates nothing and frees nothing.
  */
 #define FM_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)

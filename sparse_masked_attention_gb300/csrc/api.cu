@@ -93,6 +93,33 @@ EncodeTiledFn get_encoder() {
     return fn;
 }
 
+// cuCtxGetCurrent / cuCtxSetCurrent through the same route.
+using CtxGetFn = CUresult (*)(CUcontext *);
+using CtxSetFn = CUresult (*)(CUcontext);
+struct CtxFns {
+    CtxGetFn get = nullptr;
+    CtxSetFn set = nullptr;
+};
+
+const CtxFns &ctx_fns() {
+    static CtxFns fns;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *g = nullptr, *s = nullptr;
+        cudaDriverEntryPointQueryResult qg, qs;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &g, 12000, cudaEnableDefault,
+                                             &qg) == cudaSuccess &&
+            qg == cudaDriverEntryPointSuccess &&
+            cudaGetDriverEntryPointByVersion("cuCtxSetCurrent", &s, 12000, cudaEnableDefault,
+                                             &qs) == cudaSuccess &&
+            qs == cudaDriverEntryPointSuccess) {
+            fns.get = reinterpret_cast<CtxGetFn>(g);
+            fns.set = reinterpret_cast<CtxSetFn>(s);
+        }
+    });
+    return fns;
+}
+
 // Tensor [B, N, H, dim] bf16 seen by TMA as 4-D (dim, H, N, B), box
 // (64, 1, rows, 1), 128-byte swizzle; rows past N read as zeros.
 // Last encoder failure on this thread: which tensor and the driver's code.
@@ -245,6 +272,18 @@ namespace fm {
 void set_error_detail(const char *msg) { snprintf(g_detail, sizeof(g_detail), "%s", msg); }
 // Makes the device owning `anchor` current for this thread and checks it.
 bool bind_device(const void *anchor) { return device_ok(anchor); }
+
+CallerContext::CallerContext() {
+    const CtxFns &f = ctx_fns();
+    valid_ = f.get && f.set && f.get(&saved_) == CUDA_SUCCESS;
+}
+
+CallerContext::~CallerContext() {
+    if (!valid_) return;
+    const CtxFns &f = ctx_fns();
+    CUcontext now = nullptr;
+    if (f.get(&now) == CUDA_SUCCESS && now != saved_) f.set(saved_);
+}
 }  // namespace fm
 
 extern "C" {
@@ -258,6 +297,7 @@ size_t flashmask_workspace_size(const fm_problem *p, const fm_options *opt, int 
 fm_status flashmask_classify(const fm_problem *p, const int32_t *lts, const int32_t *lte,
                              const int32_t *uts, const int32_t *ute, uint8_t *tile_class,
                              void *workspace, size_t ws_bytes, void *stream) {
+    CallerContext keep;
     Geometry g;
     Workspace ws;
     MaskPtrs m{lts, lte, uts, ute};
@@ -275,6 +315,7 @@ fm_status flashmask_classify(const fm_problem *p, const int32_t *lts, const int3
 fm_status flashmask_count_unmasked(const fm_problem *p, const int32_t *lts, const int32_t *lte,
                                    const int32_t *uts, const int32_t *ute,
                                    unsigned long long *counts, void *stream) {
+    CallerContext keep;
     Geometry g;
     fm_status s = make_geometry(p, nullptr, &g);
     if (s != FM_OK) return s;
@@ -290,6 +331,7 @@ fm_status flashmask_fwd(const fm_problem *p, const fm_options *opt, const void *
                         const void *v, const int32_t *lts, const int32_t *lte,
                         const int32_t *uts, const int32_t *ute, void *o, float *lse,
                         void *workspace, size_t ws_bytes, void *stream) {
+    CallerContext keep;
     Geometry g;
     Workspace ws;
     MaskPtrs m{lts, lte, uts, ute};
@@ -323,6 +365,7 @@ fm_status flashmask_bwd(const fm_problem *p, const fm_options *opt, const void *
                         const int32_t *lts, const int32_t *lte, const int32_t *uts,
                         const int32_t *ute, void *dq, void *dk, void *dv, void *workspace,
                         size_t ws_bytes, void *stream) {
+    CallerContext keep;
     Geometry g;
     Workspace ws;
     MaskPtrs m{lts, lte, uts, ute};
@@ -381,13 +424,21 @@ fm_status flashmask_bwd(const fm_problem *p, const fm_options *opt, const void *
 }
 
 fm_status flashmask_selftest_wait(unsigned long long timeout_ns, void *stream) {
+    CallerContext keep;
     if (timeout_ns == 0 || timeout_ns > MAX_SELFTEST_NS) return FM_ERR_INVALID_ARG;
     if (!device_ok(nullptr)) return FM_ERR_UNSUPPORTED;
     return cuda_status(launch_wait_selftest(timeout_ns, static_cast<cudaStream_t>(stream)));
 }
 
 fm_status flashmask_get_error(void *stream) {
-    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    CallerContext keep;
+    // The error words read below are those of the stream's device.
+    int dev = 0;
+    cudaError_t e = cudaStreamGetDevice(static_cast<cudaStream_t>(stream), &dev);
+    if (e != cudaSuccess) return fail(e, "cudaStreamGetDevice");
+    e = cudaSetDevice(dev);
+    if (e != cudaSuccess) return fail(e, "cudaSetDevice");
+    e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return fail(e, "cudaStreamSynchronize");
     unsigned err = read_clear_error_classify() | read_clear_error_fwd() | read_clear_error_bwd();
     if (err & ERR_BOUNDS) return FM_ERR_DEVICE_BOUNDS;

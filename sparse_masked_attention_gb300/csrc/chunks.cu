@@ -195,6 +195,7 @@ fm_status flashmask_localize(const fm_problem *p, const int32_t *lts, const int3
                              const int32_t *uts, const int32_t *ute, int q0, int k0, int len,
                              int32_t *out_lts, int32_t *out_lte, int32_t *out_uts,
                              int32_t *out_ute, int *local_causal, void *stream) {
+    CallerContext keep;
     if (!p || !local_causal || !out_lts || !out_lte || !out_uts || !out_ute)
         return FM_ERR_INVALID_ARG;
     if (p->B < 1 || p->N < 1 || !(p->Hm == 1 || p->Hm == p->H) || p->H < 1)
@@ -221,6 +222,7 @@ fm_status flashmask_localize(const fm_problem *p, const int32_t *lts, const int3
 
 fm_status flashmask_merge_init(int L, int H, int dv, float *o_acc, float *lse_acc,
                                void *stream) {
+    CallerContext keep;
     if (!merge_shape_ok(L, H, dv) || !o_acc || !lse_acc || !aligned16(o_acc))
         return FM_ERR_INVALID_ARG;
     if (!bind_device(o_acc)) return FM_ERR_UNSUPPORTED;
@@ -233,6 +235,7 @@ fm_status flashmask_merge_init(int L, int H, int dv, float *o_acc, float *lse_ac
 
 fm_status flashmask_merge(int L, int H, int dv, const void *o_part, const float *lse_part,
                           float *o_acc, float *lse_acc, void *stream) {
+    CallerContext keep;
     if (!merge_shape_ok(L, H, dv) || !o_part || !lse_part || !o_acc || !lse_acc ||
         !aligned16(o_part) || !aligned16(o_acc))
         return FM_ERR_INVALID_ARG;
@@ -252,6 +255,7 @@ fm_status flashmask_merge(int L, int H, int dv, const void *o_part, const float 
 fm_status flashmask_merge_finish(int L, int H, int dv, const float *o_acc, const float *lse_acc,
                                  void *o_out, float *lse_out, long long lse_stride,
                                  void *stream) {
+    CallerContext keep;
     if (!merge_shape_ok(L, H, dv) || !o_acc || !lse_acc || !o_out || !lse_out ||
         !aligned16(o_acc) || !aligned16(o_out) || lse_stride < L)
         return FM_ERR_INVALID_ARG;
@@ -264,6 +268,7 @@ fm_status flashmask_merge_finish(int L, int H, int dv, const float *o_acc, const
 }
 
 fm_status flashmask_accumulate(long long n, const void *part, float *acc, void *stream) {
+    CallerContext keep;
     if (n < 0 || n % 8 != 0 || !part || !acc || !aligned16(part) || !aligned16(acc))
         return FM_ERR_INVALID_ARG;
     if (n == 0) return FM_OK;
@@ -274,6 +279,7 @@ fm_status flashmask_accumulate(long long n, const void *part, float *acc, void *
 }
 
 fm_status flashmask_to_bf16(long long n, const float *src, void *dst, void *stream) {
+    CallerContext keep;
     if (n < 0 || n % 8 != 0 || !src || !dst || !aligned16(src) || !aligned16(dst))
         return FM_ERR_INVALID_ARG;
     if (n == 0) return FM_OK;

@@ -94,6 +94,23 @@ void set_error_detail(const char *msg);
 // thread and checks that it is an sm_103 part (api.cu).
 bool bind_device(const void *anchor);
 
+// Keeps the calling thread's CUDA context: records the current context when
+// an entry point starts and makes it current again when the entry point
+// returns.  Entry points make the device of the caller's memory current for
+// their own launches; with this guard the caller finds its thread as it left
+// it (api.cu).
+class CallerContext {
+  public:
+    CallerContext();
+    ~CallerContext();
+    CallerContext(const CallerContext &) = delete;
+    CallerContext &operator=(const CallerContext &) = delete;
+
+  private:
+    CUcontext saved_ = nullptr;
+    bool valid_ = false;
+};
+
 // Lays the workspace out from `base` (may be nullptr to size it); returns bytes.
 size_t carve_workspace(const Geometry &g, bool bwd, void *base, Workspace *ws);
 

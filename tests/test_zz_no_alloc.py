@@ -78,3 +78,44 @@ def test_noalloc_rejects_problems_beyond_the_static_scratch(lib):
                                  None)
     assert st == B.FM_ERR_WORKSPACE
     assert "static scratch" in B.flashmask_last_error_detail()
+
+
+def test_noalloc_refuses_a_reused_tile_map(lib):
+    # The static array may hold another problem's tile map, so a call that asks
+    # to reuse it is refused before any CUDA call (this runs without a GPU).
+    prob = fm.make_problem(1, 2, 1, 1000, 128, 128, None, True)
+    opt = fm.make_options(reuse_tile_map=True)
+    st = B.flashmask_fwd_noalloc(prob, opt, 256, 256, 256, None, None, None, None, 256, 256,
+                                 None)
+    assert st == B.FM_ERR_INVALID_ARG
+    assert "reuse_tile_map" in B.flashmask_last_error_detail()
+
+
+@pytest.mark.gpu
+def test_noalloc_passes_options_through(lib):
+    # A sink and the list check (debug_bounds) reach the kernels exactly as they
+    # do through flashmask_fwd: same outputs, and the check reports nothing.
+    rng = np.random.default_rng(9)
+    N, H, d = 900, 3, 128
+    mask = W.causal_document(N, [W.uniform_lengths(rng, 80, 400, N)])
+    q, k, v, _ = W.make_inputs(1, N, H, d, d, seed=31, device="cuda", with_dout=False)
+    vec = cuda_mask(mask)
+    sink = torch.tensor([0.5, -1.0, 2.0], dtype=torch.float32, device="cuda")
+    prob = fm.make_problem(1, H, 1, N, d, d, None, mask.causal)
+    opt = fm.make_options(sink=sink, debug_bounds=True)
+    stream = torch.cuda.current_stream().cuda_stream
+    o_ref = torch.empty((1, N, H, d), dtype=torch.bfloat16, device="cuda")
+    lse_ref = torch.empty((1, H, N), dtype=torch.float32, device="cuda")
+    ws = torch.empty(B.flashmask_workspace_size(prob, opt, 0), dtype=torch.uint8, device="cuda")
+    st = B.flashmask_fwd(prob, opt, q.data_ptr(), k.data_ptr(), v.data_ptr(), *_ptrs(vec),
+                         o_ref.data_ptr(), lse_ref.data_ptr(), ws.data_ptr(), ws.numel(), stream)
+    assert st == B.FM_OK
+    for call in range(2):
+        o = torch.full_like(o_ref, float("nan"))
+        lse = torch.full_like(lse_ref, float("nan"))
+        st = B.flashmask_fwd_noalloc(prob, opt, q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                     *_ptrs(vec), o.data_ptr(), lse.data_ptr(), stream)
+        assert st == B.FM_OK, B.flashmask_last_error_detail()
+        assert B.flashmask_get_error(stream) == B.FM_OK
+        assert torch.equal(o, o_ref), f"call {call}: O differs from flashmask_fwd"
+        assert torch.equal(lse, lse_ref), f"call {call}: LSE differs from flashmask_fwd"
