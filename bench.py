@@ -206,6 +206,11 @@ def kernel_names(d, dv):
     return fwd, bwd
 
 
+# Kernel launches behind one event pair: the preprocess step is the range,
+# scale and preprocess kernels.
+LAUNCHES = {"bwd_preprocess": 3}
+
+
 def kernel_alg_flops_per_pair(name, d, dv):
     """Algorithmic FLOPs per unmasked pair credited to each kernel.  The
     key-side kernel does the S/dP recomputation and the dK/dV products the
@@ -363,7 +368,7 @@ def run_ours(args, rank, world, local_rank):
     # forward alone, same inputs (event pairs of the forward calls)
     fwd_ms = sum(avg[f"fwd:{n}"] for n in fwd_names)
     value = whole_job_value(step_flops, ms_step, world)
-    launches = K * (len(fwd_names) + (len(bwd_names) if has_bwd else 0))
+    launches = K * sum(LAUNCHES.get(n, 1) for n in fwd_names + (bwd_names if has_bwd else []))
 
     e2e = None
     if not args.no_e2e:

@@ -110,6 +110,9 @@ typedef struct {
  * kernel_events[2i+1] just after it.  Events beyond the array are skipped.
  * Kernel order: fwd = classify, lists, attention; bwd = classify, lists,
  * preprocess, key-side gradient (twice when d = dv = 256), query-side gradient.
+ * The backward's preprocess step is three launches under one event pair: the
+ * largest |dO| and |V| per row tile, their per-(batch, head) scales, then D,
+ * the log2 LSE and the scaled fp16 copies of dO and V.
  * A NULL options pointer selects all defaults. */
 typedef struct {
     int deterministic;
@@ -153,6 +156,12 @@ fm_status flashmask_fwd(const fm_problem *p, const fm_options *opt,
  * o and lse must be the forward's outputs for the same inputs.  dout has the
  * layout of o.  Writes dq, dk [B,N,H,d] and dv [B,N,H,dv] bf16.  These are the
  * gradients of sum(dout * O) with respect to q, k and v.
+ * Accuracy holds over the whole bf16 range of dout and v: the products with
+ * dout and v run in fp16 (more mantissa than bf16) on copies scaled by a power
+ * of two per (batch, head) that puts the largest magnitude in [2^14, 2^15),
+ * and the scales are undone in fp32.  Scales are limited to 2^-63 .. 2^63, so
+ * magnitudes below about 2^-49 lose fp16 precision; products and sums are
+ * formed in fp32.
  */
 fm_status flashmask_bwd(const fm_problem *p, const fm_options *opt,
                         const void *q, const void *k, const void *v,

@@ -200,6 +200,8 @@ size_t carve_workspace(const Geometry &g, bool bwd, void *base, Workspace *ws) {
     w.v16 = nullptr;
     w.do16 = nullptr;
     w.sink_part = nullptr;
+    w.range_part = nullptr;
+    w.scales = nullptr;
     if (bwd) {
         const size_t rows = static_cast<size_t>(g.B) * g.H * g.Npad;
         w.lse2 = static_cast<float *>(take(rows * sizeof(float)));
@@ -208,6 +210,9 @@ size_t carve_workspace(const Geometry &g, bool bwd, void *base, Workspace *ws) {
         w.v16 = take(vbytes);
         w.do16 = take(vbytes);
         w.sink_part = static_cast<float *>(take(rows / 16 * sizeof(float)));
+        const size_t bht = static_cast<size_t>(g.B) * g.H * g.T;
+        w.range_part = static_cast<uint2 *>(take(bht * sizeof(uint2)));
+        w.scales = static_cast<float4 *>(take(static_cast<size_t>(g.B) * g.H * sizeof(float4)));
     }
     if (ws) *ws = w;
     return off;

@@ -7,10 +7,22 @@
 // The backward walks the same tile map as the forward: fully masked tiles are
 // skipped, and the mask is applied elementwise only on partial tiles.
 //
-// Three kernels:
-//   preprocess   D (fp32) and the log2-domain LSE per row, padded to whole
-//                tiles; padding rows and fully masked rows get LSE = +inf, so
-//                their P is 0.
+// The dP and dV products run in fp16 (10 mantissa bits against bf16's 7), on
+// copies of dO and V scaled by powers of two, one per (batch, head) and
+// tensor, that put the tensor's largest magnitude in [2^14, 2^15): inside
+// fp16's range, with its precision, over the whole bf16 input range.  D is
+// stored times s_o s_v, so the kernels form dS * s_o s_v (exact: a power of
+// two changes no rounding, and bf16 keeps fp32's exponent range), and the
+// epilogues undo the scales in fp32: dQ and dK times scale / (s_o s_v), dV
+// times 1 / s_o.  |dO s_o|, |V s_v| < 2^15 bound every scaled product by
+// dv * 2^30 and |D s_o s_v| by dv * 2^30 too (|O| <= max |V|).
+//
+// Kernels:
+//   range        largest |dO| and |V| per 128-row tile of each (batch, head)
+//   scale        the per-(batch, head) scales from those maxima
+//   preprocess   D * s_o s_v (fp32) and the log2-domain LSE per row, padded
+//                to whole tiles; padding rows and fully masked rows get
+//                LSE = +inf, so their P is 0; the scaled fp16 copies of dO, V.
 //   dq kernel    one CTA per 128-row query tile walks its key tiles:
 //                S = Q K^T (bf16) and dP = dO V^T (fp16 copies) as SS MMAs
 //                (at d = 192 and 256, dO sits in TMEM and dP is a TS MMA);
@@ -65,19 +77,125 @@ __device__ __forceinline__ void stage_row_bf16(uint8_t *stage, int c, int row,
     }
 }
 
+// --------------------------------------------------------- range and scale
+// Magnitudes of bf16 values compare as the unsigned integers of their low 15
+// bits (sign cleared); NaN patterns sort above infinity, and both above every
+// finite value.
+constexpr uint32_t BF16X2_ABS = 0x7fff7fffu;
+constexpr uint32_t BF16_INF_BITS = 0x7f80u;
+
+__device__ __forceinline__ uint32_t max_abs_bf16x8(uint32_t m, uint4 a) {
+    const uint32_t x = __vmaxu2(a.x & BF16X2_ABS, a.y & BF16X2_ABS);
+    const uint32_t y = __vmaxu2(a.z & BF16X2_ABS, a.w & BF16X2_ABS);
+    return __vmaxu2(m, __vmaxu2(x, y));
+}
+
+// One CTA per (128-row tile, head, batch): the tile's largest |dO| and |V|
+// as bf16 bit patterns (8 values per load).
+__global__ void __launch_bounds__(256) range_kernel(int N, int H, int dv, int T,
+                                                    const uint4 *__restrict__ dout,
+                                                    const uint4 *__restrict__ v,
+                                                    uint2 *__restrict__ range_part) {
+    __shared__ uint32_t red[2][8];
+    pdl_wait();  // dO and V may come from the kernels before
+    pdl_trigger();
+    const int t = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int bh = b * H + h;
+    const int r0 = t * TILE, rows = min(TILE, N - r0);
+    const int vpr = dv / 8;  // 16-byte vectors per row
+    uint32_t mo = 0, mv = 0;
+    for (int idx = threadIdx.x; idx < rows * vpr; idx += 256) {
+        const int r = idx / vpr, c = idx - r * vpr;
+        const size_t off = ((static_cast<size_t>(b) * N + r0 + r) * H + h) * vpr + c;
+        mo = max_abs_bf16x8(mo, dout[off]);
+        mv = max_abs_bf16x8(mv, v[off]);
+    }
+    mo = max(mo & 0xffffu, mo >> 16);
+    mv = max(mv & 0xffffu, mv >> 16);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        mo = max(mo, __shfl_xor_sync(0xffffffffu, mo, off));
+        mv = max(mv, __shfl_xor_sync(0xffffffffu, mv, off));
+    }
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (lane == 0) {
+        red[0][warp] = mo;
+        red[1][warp] = mv;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+#pragma unroll
+        for (int w = 1; w < 8; ++w) {
+            mo = max(mo, red[0][w]);
+            mv = max(mv, red[1][w]);
+        }
+        range_part[static_cast<size_t>(bh) * T + t] = make_uint2(mo, mv);
+    }
+}
+
+// 2^k as a float, for integer k in [-126, 127].
+__device__ __forceinline__ float pow2i(int k) {
+    return __uint_as_float(static_cast<uint32_t>(k + 127) << 23);
+}
+
+// Exponent k of the power of two that puts a largest magnitude (bf16 bits)
+// in [2^14, 2^15), kept in [-63, 63] so that 2^-(k_o + k_v) is a normal fp32;
+// 0 (no scaling) for an all-zero tensor and when infinity or NaN is present,
+// which then propagate as they would unscaled.
+__device__ __forceinline__ int range_exponent(uint32_t amax_bits) {
+    if (amax_bits == 0 || amax_bits >= BF16_INF_BITS) return 0;
+    const int e = static_cast<int>((amax_bits >> 7) & 0xffu);  // biased exponent
+    const int k = 14 - (e - 127);  // a subnormal (e = 0) lands far above 63
+    return max(-63, min(63, k));
+}
+
+// One CTA per (batch, head): the maxima of its row tiles, then the scales.
+__global__ void __launch_bounds__(256) scale_kernel(int T, const uint2 *__restrict__ range_part,
+                                                    float4 *__restrict__ scales) {
+    __shared__ uint32_t red[2][8];
+    pdl_wait();  // the range kernel's maxima
+    pdl_trigger();
+    const int bh = blockIdx.x;
+    uint32_t mo = 0, mv = 0;
+    for (int t = threadIdx.x; t < T; t += 256) {
+        const uint2 m = range_part[static_cast<size_t>(bh) * T + t];
+        mo = max(mo, m.x);
+        mv = max(mv, m.y);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        mo = max(mo, __shfl_xor_sync(0xffffffffu, mo, off));
+        mv = max(mv, __shfl_xor_sync(0xffffffffu, mv, off));
+    }
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (lane == 0) {
+        red[0][warp] = mo;
+        red[1][warp] = mv;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+#pragma unroll
+        for (int w = 1; w < 8; ++w) {
+            mo = max(mo, red[0][w]);
+            mv = max(mv, red[1][w]);
+        }
+        const int ko = range_exponent(mo), kv = range_exponent(mv);
+        scales[bh] = make_float4(pow2i(ko), pow2i(kv), pow2i(-ko), pow2i(-(ko + kv)));
+    }
+}
+
 // ---------------------------------------------------------------- preprocess
 // 16 threads per row; each takes 8 consecutive bf16 of dO, O and V at a time.
-// Besides D and LSE2 it writes fp16 copies of V and dO: the backward's dP and
-// dV products run in fp16 (10 mantissa bits against bf16's 7), which keeps the
-// probabilities' rounding well below the bf16 rounding of the outputs.
-__device__ __forceinline__ uint4 bf16x8_to_fp16x8(uint4 a) {
+// Besides D and LSE2 it writes the fp16 copies of dO and V, times their
+// (batch, head)'s powers of two s_o and s_v.
+__device__ __forceinline__ uint4 bf16x8_to_fp16x8(uint4 a, float mul) {
     const __nv_bfloat162 *a2 = reinterpret_cast<const __nv_bfloat162 *>(&a);
     uint4 r;
     uint32_t *r32 = reinterpret_cast<uint32_t *>(&r);
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
         const float2 f = __bfloat1622float2(a2[e]);
-        r32[e] = pack_fp16(f.x, f.y);
+        r32[e] = pack_fp16(f.x * mul, f.y * mul);
     }
     return r;
 }
@@ -86,10 +204,10 @@ __global__ void __launch_bounds__(256) preprocess_kernel(
     int N, int H, int dv, int Npad, int rows_total, const __nv_bfloat16 *__restrict__ o,
     const __nv_bfloat16 *__restrict__ dout, const __nv_bfloat16 *__restrict__ v,
     const float *__restrict__ lse, float *__restrict__ lse2, float *__restrict__ delta,
-    uint4 *__restrict__ v16, uint4 *__restrict__ do16, const float *__restrict__ sink,
-    float *__restrict__ sink_part) {
+    uint4 *__restrict__ v16, uint4 *__restrict__ do16, const float4 *__restrict__ scales,
+    const float *__restrict__ sink, float *__restrict__ sink_part) {
     __shared__ float sink_rows[16];
-    pdl_wait();  // orders it after the kernels before (it rewrites their inputs' copies)
+    pdl_wait();  // the scales, and the inputs of the kernels before
     pdl_trigger();
     const int r0 = blockIdx.x * 16 + (threadIdx.x >> 4);  // over B*H*Npad
     const int t = threadIdx.x & 15;
@@ -98,14 +216,16 @@ __global__ void __launch_bounds__(256) preprocess_kernel(
     const int bh = r / Npad, i = r % Npad;
     const int b = bh / H, h = bh % H;
     float acc = 0.f;
+    const float4 sc = scales[bh];
+    const float sc_o = sc.x, sc_v = sc.y;
     if (valid && i < N) {
         const size_t base = ((static_cast<size_t>(b) * N + i) * H + h) * dv;
         for (int c = t * 8; c < dv; c += 128) {
             const uint4 a = *reinterpret_cast<const uint4 *>(o + base + c);
             const uint4 g = *reinterpret_cast<const uint4 *>(dout + base + c);
             const uint4 vv = *reinterpret_cast<const uint4 *>(v + base + c);
-            do16[(base + c) / 8] = bf16x8_to_fp16x8(g);
-            v16[(base + c) / 8] = bf16x8_to_fp16x8(vv);
+            do16[(base + c) / 8] = bf16x8_to_fp16x8(g, sc.x);
+            v16[(base + c) / 8] = bf16x8_to_fp16x8(vv, sc.y);
             const __nv_bfloat162 *a2 = reinterpret_cast<const __nv_bfloat162 *>(&a);
             const __nv_bfloat162 *g2 = reinterpret_cast<const __nv_bfloat162 *>(&g);
 #pragma unroll
@@ -128,7 +248,7 @@ __global__ void __launch_bounds__(256) preprocess_kernel(
             if (sink && l != -INFINITY) sink_term = -expf(sink[h] - l) * acc;
         }
         lse2[r] = l2;
-        delta[r] = i < N ? acc : 0.f;
+        delta[r] = i < N ? acc * (sc_o * sc_v) : 0.f;
     }
     // The block's 16 rows belong to one (batch, head) (Npad is a multiple of
     // 16): their terms are summed in row order into the block's slot.
@@ -174,8 +294,9 @@ struct BwdParams {
     const int *cnt;
     const float *lse2;
     const float *delta;
-    const void *do16;  // [B, N, H, dv] fp16 copy of dO
-    const void *v16;   // [B, N, H, dv] fp16 copy of V
+    const void *do16;  // [B, N, H, dv] fp16 copy of dO * s_o
+    const void *v16;   // [B, N, H, dv] fp16 copy of V * s_v
+    const float4 *scales;  // [B*H] (s_o, s_v, 1/s_o, 1/(s_o s_v))
     __nv_bfloat16 *dq, *dk, *dv;
     int N, H, Hm, T, Npad, causal;
     float sl2;    // scale * log2(e)
@@ -487,7 +608,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         const uint32_t t_r = lane_base + wg * C::BN;
         const size_t bh = static_cast<size_t>(b) * p.H + h;
         const float lse2 = p.lse2[bh * p.Npad + grow];
-        const float Drow = p.delta[bh * p.Npad + grow];
+        const float Drow = p.delta[bh * p.Npad + grow];  // D * s_o s_v
         const float sl2 = p.sl2;
         const int n_my = n_of(wg);
         const int4 *vec = p.vec + static_cast<size_t>(bm) * p.Npad;
@@ -612,8 +733,10 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         }
         if (n > 0) warp_wait(dq_done, 0, tmo, abort);
         tc_fence_after();
-        // dQ (scaled) to the 128B-swizzled layout of the output map in the idle
-        // K ring, then TMA stores of its 64-column boxes (rows past N clipped).
+        // dQ (times scale / (s_o s_v)) to the 128B-swizzled layout of the output
+        // map in the idle K ring, then TMA stores of its 64-column boxes (rows
+        // past N clipped).
+        const float dq_mul = p.scale * p.scales[bh].w;
         constexpr int CPW = (C::D / 32) / C::NWG;  // 32-column chunks per group
 #pragma unroll 1
         for (int c = wg * CPW; c < (wg + 1) * CPW; ++c) {
@@ -622,7 +745,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             float v[32];
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] = n > 0 ? __uint_as_float(r[i]) : 0.f;
-            stage_row_bf16(sK, c, row, v, p.scale);
+            stage_row_bf16(sK, c, row, v, dq_mul);
         }
         fence_proxy_async_smem();
         named_bar_sync(1, C::NWG * 128);
@@ -983,6 +1106,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         const uint32_t t_r = lane_base + C::TM_W0 + wg * C::BM;
         const int4 cv = p.vec[static_cast<size_t>(bm) * p.Npad + gkey];
         const float sl2 = p.sl2;
+
         const int n_my = n_of(wg);
         const float *slse = reinterpret_cast<const float *>(sLD + wg * C::LD_BYTES);
         const float *sd = slse + C::BM;
@@ -1098,9 +1222,11 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         }
         if (n > 0) warp_wait(done, 0, tmo, abort);
         tc_fence_after();
-        // dK (scaled) and dV to the 128B-swizzled layouts of the output maps in
-        // the idle Q ring and dO stages, then TMA stores of their 64-column
-        // boxes (rows past N clipped).
+        // dK (times scale / (s_o s_v)) and dV (times 1 / s_o) to the
+        // 128B-swizzled layouts of the output maps in the idle Q ring and dO
+        // stages, then TMA stores of their 64-column boxes (rows past N
+        // clipped).
+        const float4 sc = p.scales[bh];
         uint8_t *stage_dk = sQ;
         uint8_t *stage_dv = sQ + (C::DO_DK ? C::D / 64 : 0) * (128 * 128);
         if constexpr (C::DO_DK) {
@@ -1112,7 +1238,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 float v[32];
 #pragma unroll
                 for (int i = 0; i < 32; ++i) v[i] = n > 0 ? __uint_as_float(r[i]) : 0.f;
-                stage_row_bf16(stage_dk, c, row, v, p.scale);
+                stage_row_bf16(stage_dk, c, row, v, p.scale * sc.w);
             }
         }
         if constexpr (C::DO_DV) {
@@ -1124,7 +1250,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 float v[32];
 #pragma unroll
                 for (int i = 0; i < 32; ++i) v[i] = n > 0 ? __uint_as_float(r[i]) : 0.f;
-                stage_row_bf16(stage_dv, c, row, v, 1.0f);
+                stage_row_bf16(stage_dv, c, row, v, sc.z);  // dV = (P^T dO s_o) / s_o
             }
         }
         fence_proxy_async_smem();
@@ -1158,6 +1284,7 @@ BwdParams make_params(const Geometry &g, const Workspace &ws, const BwdArgs &a, 
     p.delta = ws.delta;
     p.do16 = ws.do16;
     p.v16 = ws.v16;
+    p.scales = ws.scales;
     p.dq = static_cast<__nv_bfloat16 *>(a.dq);
     p.dk = static_cast<__nv_bfloat16 *>(a.dk);
     p.dv = static_cast<__nv_bfloat16 *>(a.dv);
@@ -1223,13 +1350,23 @@ int dkdv_query_rows(int d, int) { return d <= 128 ? 128 : 64; }
 cudaError_t launch_bwd(const Geometry &g, const Workspace &ws, const BwdArgs &a,
                        cudaStream_t st, Recorder &rec) {
     const int rows_total = g.B * g.H * g.Npad;
+    // The preprocess step: input ranges, their scales, then D, LSE2 and the
+    // scaled fp16 copies (one event pair around the three launches).
     rec.before(st);
-    cudaError_t e = launch_pdl(
-        preprocess_kernel, dim3((rows_total + 15) / 16), dim3(256), 0, st, g.N, g.H, g.dv, g.Npad,
-        rows_total, static_cast<const __nv_bfloat16 *>(a.o),
-        static_cast<const __nv_bfloat16 *>(a.dout), static_cast<const __nv_bfloat16 *>(a.v),
-        static_cast<const float *>(a.lse), ws.lse2, ws.delta, static_cast<uint4 *>(ws.v16),
-        static_cast<uint4 *>(ws.do16), g.sink, g.dsink ? ws.sink_part : nullptr);
+    cudaError_t e = launch_pdl(range_kernel, dim3(g.T, g.H, g.B), dim3(256), 0, st, g.N, g.H,
+                               g.dv, g.T, static_cast<const uint4 *>(a.dout),
+                               static_cast<const uint4 *>(a.v), ws.range_part);
+    if (e == cudaSuccess)
+        e = launch_pdl(scale_kernel, dim3(g.B * g.H), dim3(256), 0, st, g.T,
+                       static_cast<const uint2 *>(ws.range_part), ws.scales);
+    if (e == cudaSuccess)
+        e = launch_pdl(preprocess_kernel, dim3((rows_total + 15) / 16), dim3(256), 0, st, g.N,
+                       g.H, g.dv, g.Npad, rows_total, static_cast<const __nv_bfloat16 *>(a.o),
+                       static_cast<const __nv_bfloat16 *>(a.dout),
+                       static_cast<const __nv_bfloat16 *>(a.v), static_cast<const float *>(a.lse),
+                       ws.lse2, ws.delta, static_cast<uint4 *>(ws.v16),
+                       static_cast<uint4 *>(ws.do16), static_cast<const float4 *>(ws.scales),
+                       g.sink, g.dsink ? ws.sink_part : nullptr);
     rec.after(st);
     if (e == cudaSuccess && g.dsink)
         e = launch_pdl(sink_grad_kernel, dim3(g.H), dim3(256), 0, st, g.B, g.H, g.Npad / 16,

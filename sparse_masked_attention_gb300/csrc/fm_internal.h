@@ -47,9 +47,12 @@ struct Workspace {
     int *pair_order;   // [B*Hm][TP] pair indices by decreasing key-tile count
     float *lse2;       // [B*H][Npad] log2-domain LSE, +inf for empty / padding rows
     float *delta;      // [B*H][Npad] D_i = sum_c dO_ic O_ic
-    void *v16;         // [B,N,H,dv] fp16 copy of V   (backward)
-    void *do16;        // [B,N,H,dv] fp16 copy of dO  (backward)
+    void *v16;         // [B,N,H,dv] fp16 copy of V * s_v   (backward)
+    void *do16;        // [B,N,H,dv] fp16 copy of dO * s_o  (backward)
     float *sink_part;  // [B*H*Npad/16] per-block sink-gradient sums (backward)
+    uint2 *range_part; // [B*H][T] largest |dO| and |V| (bf16 bit patterns) per row tile
+    float4 *scales;    // [B*H] (s_o, s_v, 1/s_o, 1/(s_o s_v)): powers of two that put the
+                       // largest |dO| and |V| of the (batch, head) in [2^14, 2^15)
 };
 
 // Optional per-kernel event recording (fm_options.kernel_events).

@@ -55,6 +55,8 @@ def _layout(B, Hm, H, N, dv, bwd):
         take("v16", B * N * H * dv * 2)
         take("do16", B * N * H * dv * 2)
         take("sink_part", rows // 16 * 4)
+        take("range_part", B * H * T * 8)
+        take("scales", B * H * 16)
     return out, off, T, TP
 
 

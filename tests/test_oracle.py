@@ -170,6 +170,29 @@ def test_finite_differences():
         np.testing.assert_allclose(g, num, rtol=1e-6, atol=1e-8, err_msg=name)
 
 
+@pytest.mark.parametrize("f", [1e-9, 3.0, 1e5])
+def test_homogeneity_in_dout_and_v(f):
+    """The derivative is linear in dO, so every gradient scales with it; O and
+    dP are linear in V while P is not affected, so O, dQ and dK scale with V
+    and dV does not.  The GPU tests of extreme input ranges lean on this."""
+    N, d, dv = 40, 8, 6
+    rng = np.random.default_rng(17)
+    mask = W.causal_document(N, [[15, 25]]).slice(0)
+    q, k, v, do = (rng.standard_normal((N, c)) for c in (d, d, dv, dv))
+    o, lse = oracle.attention_fwd(q, k, v, mask, True)
+    g = oracle.attention_bwd(q, k, v, do, mask, True)
+    g_do = oracle.attention_bwd(q, k, v, do * f, mask, True)
+    for a, b in zip(g, g_do):
+        np.testing.assert_allclose(b, a * f, rtol=1e-12, atol=0)
+    o_v, lse_v = oracle.attention_fwd(q, k, v * f, mask, True)
+    np.testing.assert_allclose(o_v, o * f, rtol=1e-12, atol=0)
+    np.testing.assert_array_equal(lse_v, lse)
+    gq, gk, gv = oracle.attention_bwd(q, k, v * f, do, mask, True)
+    np.testing.assert_allclose(gq, g[0] * f, rtol=1e-9, atol=0)
+    np.testing.assert_allclose(gk, g[1] * f, rtol=1e-9, atol=0)
+    np.testing.assert_allclose(gv, g[2], rtol=1e-12, atol=0)
+
+
 def test_softmax_rows_sum_to_one():
     """With V = 1 every visible row of O is sum_j P_ij = 1."""
     N, d = 70, 8
