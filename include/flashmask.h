@@ -113,6 +113,12 @@ typedef struct {
  * The backward's preprocess step is three launches under one event pair: the
  * largest |dO| and |V| per row tile, their per-(batch, head) scales, then D,
  * the log2 LSE and the scaled fp16 copies of dO and V.
+ * accumulate_f32 (0 or 1, flashmask_bwd only): dq, dk and dv are fp32 arrays
+ * of the same shapes ([B,N,H,d], [B,N,H,d], [B,N,H,dv]), and the backward adds
+ * its gradients to them in fp32 instead of writing bf16 (each element is
+ * read and written once, by one thread; no atomics).  Partial gradients of
+ * several calls, such as the (query chunk, key chunk) pairs of a context-
+ * parallel run, are then summed before a single rounding to bf16.
  * A NULL options pointer selects all defaults. */
 typedef struct {
     int deterministic;
@@ -123,6 +129,7 @@ typedef struct {
     const float *sink;
     float *dsink;
     int reuse_tile_map;
+    int accumulate_f32;
 } fm_options;
 
 /* Tile classes written by flashmask_classify (128 x 128 tiles). */
@@ -155,7 +162,8 @@ fm_status flashmask_fwd(const fm_problem *p, const fm_options *opt,
  * Backward, the derivative of the forward above.  P is rebuilt from lse.
  * o and lse must be the forward's outputs for the same inputs.  dout has the
  * layout of o.  Writes dq, dk [B,N,H,d] and dv [B,N,H,dv] bf16.  These are the
- * gradients of sum(dout * O) with respect to q, k and v.
+ * gradients of sum(dout * O) with respect to q, k and v (with
+ * fm_options.accumulate_f32: fp32 arrays that the gradients are added to).
  * Accuracy holds over the whole bf16 range of dout and v: the products with
  * dout and v run in fp16 (more mantissa than bf16) on copies scaled by a power
  * of two per (batch, head) that puts the largest magnitude in [2^14, 2^15),

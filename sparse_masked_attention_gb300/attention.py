@@ -100,18 +100,22 @@ def make_problem(B, H, Hm, N, d, dv, scale, causal) -> _b.fm_problem:
 
 
 def make_options(deterministic=False, wait_timeout_ns=0, kernel_events=None, sink=None,
-                 dsink=None, reuse_tile_map=False, debug_bounds=False) -> _b.fm_options:
+                 dsink=None, reuse_tile_map=False, debug_bounds=False,
+                 accumulate_f32=False) -> _b.fm_options:
     """kernel_events: optional list of raw cudaEvent_t handles (ints), recorded in
     pairs around each kernel launch of the call.  sink / dsink: optional [H]
     fp32 CUDA tensors, the attention-sink logits and (backward) their gradient.
     reuse_tile_map: the workspace already holds this problem's tile map and
     lists from an earlier call on it (see flashmask.h).  debug_bounds: every
     attention CTA checks its work list first; a bad one makes get_error()
-    raise (status FM_ERR_DEVICE_BOUNDS) instead of reading out of range."""
+    raise (status FM_ERR_DEVICE_BOUNDS) instead of reading out of range.
+    accumulate_f32: the backward adds its gradients to fp32 dq, dk, dv instead
+    of writing bf16."""
     opt = _b.fm_options(int(bool(deterministic)), int(bool(debug_bounds)), int(wait_timeout_ns),
                         None, 0,
                         None if sink is None else sink.data_ptr(),
-                        None if dsink is None else dsink.data_ptr(), int(bool(reuse_tile_map)))
+                        None if dsink is None else dsink.data_ptr(), int(bool(reuse_tile_map)),
+                        int(bool(accumulate_f32)))
     opt._tensors = (sink, dsink)
     if kernel_events:
         arr = (ctypes.c_void_p * len(kernel_events))(*kernel_events)
@@ -198,11 +202,13 @@ def fwd(q, k, v, lts=None, lte=None, uts=None, ute=None, causal=False, scale=Non
 
 def bwd(q, k, v, o, lse, dout, lts=None, lte=None, uts=None, ute=None, causal=False,
         scale=None, deterministic=False, dq=None, dk=None, dv=None, workspace=None,
-        stream=None, options=None, sink=None, reuse_tile_map=False):
+        stream=None, options=None, sink=None, reuse_tile_map=False, accumulate_f32=False):
     """Masked attention backward; returns (dq, dk, dv) in bf16, and with a sink
     (the forward's [H] fp32 logits) also their gradient: (dq, dk, dv, dsink).
     reuse_tile_map: `workspace` (sized for the backward) already holds this
-    problem's tile map and lists, e.g. from the forward call on it."""
+    problem's tile map and lists, e.g. from the forward call on it.
+    accumulate_f32: dq, dk, dv are given as fp32 tensors and the gradients
+    are added to them (no bf16 rounding)."""
     B, N, H, d, dvd = _check_qkv(q, k, v)
     _check_sink(sink, H, q.device)
     if options is not None and sink is not None:
@@ -219,14 +225,20 @@ def bwd(q, k, v, o, lse, dout, lts=None, lte=None, uts=None, ute=None, causal=Fa
     dsink = None if sink is None else torch.empty(H, dtype=torch.float32, device=q.device)
     if reuse_tile_map and workspace is None:
         raise FlashMaskError("reuse_tile_map needs the workspace that holds the tile map")
-    opt = make_options(deterministic, sink=sink, dsink=dsink,
-                       reuse_tile_map=reuse_tile_map) if options is None else options
+    if options is not None and accumulate_f32:
+        raise FlashMaskError("pass accumulate_f32 either in options or as an argument")
+    opt = make_options(deterministic, sink=sink, dsink=dsink, reuse_tile_map=reuse_tile_map,
+                       accumulate_f32=accumulate_f32) if options is None else options
+    acc32 = bool(opt.accumulate_f32)
+    if acc32 and (dq is None or dk is None or dv is None):
+        raise FlashMaskError("accumulate_f32 adds to the caller's fp32 dq, dk and dv")
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
-    _check_out("dq", dq, (B, N, H, d), torch.bfloat16, q.device)
-    _check_out("dk", dk, (B, N, H, d), torch.bfloat16, q.device)
-    _check_out("dv", dv, (B, N, H, dvd), torch.bfloat16, q.device)
+    gdt = torch.float32 if acc32 else torch.bfloat16
+    _check_out("dq", dq, (B, N, H, d), gdt, q.device)
+    _check_out("dk", dk, (B, N, H, d), gdt, q.device)
+    _check_out("dv", dv, (B, N, H, dvd), gdt, q.device)
     ws_bytes = _b.flashmask_workspace_size(prob, opt, 1)
     if workspace is None:
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
@@ -401,14 +413,14 @@ def bwd_chunked(q, k, v, o, lse, dout, lts=None, lte=None, uts=None, ute=None, c
                 scale=None, deterministic=False, chunks=2, ranks=None, stream=None):
     """The backward as the same emulated context-parallel run: every pair's
     local backward (with the whole sequence's O and LSE rows of its query
-    chunk) gives partial dQ for the query chunk and partial dK, dV for the key
-    chunk; the partials are summed in fp32 and rounded to bf16 once."""
+    chunk) adds its partial dQ for the query chunk and partial dK, dV for the
+    key chunk, in fp32, straight into the whole sequence's accumulators
+    (fm_options.accumulate_f32); they are rounded to bf16 once."""
     B, N, H, d, dvd = _check_qkv(q, k, v)
     L, owned = _chunk_plan(N, chunks, ranks)
     dev = q.device
     s = _stream(stream)
     acc = [torch.zeros((B, N, H, c), dtype=torch.float32, device=dev) for c in (d, d, dvd)]
-    parts = [torch.empty((1, L, H, c), dtype=torch.bfloat16, device=dev) for c in (d, d, dvd)]
     vecs = (lts, lte, uts, ute)
     ws = None
     for b in range(B):
@@ -429,12 +441,9 @@ def bwd_chunked(q, k, v, o, lse, dout, lts=None, lte=None, uts=None, ute=None, c
                     bwd(q[b:b + 1, q0:q0 + L], k[b:b + 1, k0:k0 + L], v[b:b + 1, k0:k0 + L],
                         o[b:b + 1, q0:q0 + L], lse_c, dout[b:b + 1, q0:q0 + L], *local,
                         causal=bool(lc), scale=scale if scale is not None else default_scale(d),
-                        deterministic=deterministic, dq=parts[0], dk=parts[1], dv=parts[2],
-                        workspace=ws, stream=stream)
-                    for part, a, r0 in zip(parts, acc, (q0, k0, k0)):
-                        dst = a[b:b + 1, r0:r0 + L]
-                        _check(_b.flashmask_accumulate(part.numel(), part.data_ptr(),
-                                                       dst.data_ptr(), s), "flashmask_accumulate")
+                        deterministic=deterministic, dq=acc[0][b:b + 1, q0:q0 + L],
+                        dk=acc[1][b:b + 1, k0:k0 + L], dv=acc[2][b:b + 1, k0:k0 + L],
+                        workspace=ws, stream=stream, accumulate_f32=True)
     outs = [torch.empty((B, N, H, c), dtype=torch.bfloat16, device=dev) for c in (d, d, dvd)]
     for a, out in zip(acc, outs):
         _check(_b.flashmask_to_bf16(a.numel(), a.data_ptr(), out.data_ptr(), s),

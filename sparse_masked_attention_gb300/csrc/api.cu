@@ -58,6 +58,8 @@ fm_status make_geometry(const fm_problem *p, const fm_options *opt, Geometry *g)
     g->reuse_map = opt ? opt->reuse_tile_map : 0;
     if (g->reuse_map != 0 && g->reuse_map != 1) return FM_ERR_INVALID_ARG;
     g->debug_bounds = opt ? opt->debug_bounds : 0;
+    g->acc32 = opt ? opt->accumulate_f32 : 0;
+    if (g->acc32 != 0 && g->acc32 != 1) return FM_ERR_INVALID_ARG;
     // The list and map sizes must fit the int indexing of the kernels.
     const double entries = static_cast<double>(g->B) * g->Hm * g->T * g->T;
     if (entries > 2.0e9) return FM_ERR_INVALID_ARG;
@@ -392,10 +394,16 @@ fm_status flashmask_bwd(const fm_problem *p, const fm_options *opt, const void *
         !encode_bnhd(&tq_k, q, g.B, g.N, g.H, g.d, kv_qr) ||
         !encode_bnhd(&tdo_k, ws.do16, g.B, g.N, g.H, g.dv, kv_qr, true) ||
         !encode_bnhd(&tk_kv, k, g.B, g.N, g.H, g.d, 128) ||
-        !encode_bnhd(&tv_kv, ws.v16, g.B, g.N, g.H, g.dv, 128, true) ||
-        !encode_bnhd(&tdq_o, dq, g.B, g.N, g.H, g.d, 128) ||
-        !encode_bnhd(&tdk_o, dk, g.B, g.N, g.H, g.d, 128) ||
-        !encode_bnhd(&tdv_o, dv, g.B, g.N, g.H, g.dv, 128))
+        !encode_bnhd(&tv_kv, ws.v16, g.B, g.N, g.H, g.dv, 128, true))
+        return fail(cudaErrorInvalidValue, g_encode_detail);
+    // bf16 outputs are stored by TMA; fp32 accumulation (acc32) adds to them
+    // with plain loads and stores, and the maps stay unused.
+    memset(&tdq_o, 0, sizeof(tdq_o));
+    memset(&tdk_o, 0, sizeof(tdk_o));
+    memset(&tdv_o, 0, sizeof(tdv_o));
+    if (!g.acc32 && (!encode_bnhd(&tdq_o, dq, g.B, g.N, g.H, g.d, 128) ||
+                     !encode_bnhd(&tdk_o, dk, g.B, g.N, g.H, g.d, 128) ||
+                     !encode_bnhd(&tdv_o, dv, g.B, g.N, g.H, g.dv, 128)))
         return fail(cudaErrorInvalidValue, g_encode_detail);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     Recorder rec = recorder(opt);

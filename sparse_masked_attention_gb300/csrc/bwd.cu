@@ -184,6 +184,24 @@ __global__ void __launch_bounds__(256) scale_kernel(int T, const uint2 *__restri
     }
 }
 
+// fp32 accumulation (fm_options.accumulate_f32, the ACC32 instantiations of
+// the gradient kernels): 32 values of one output row
+// (columns 32c .. 32c + 31), times `mul`, added to that row of an fp32 array.
+// Each element has one writer per call, so a plain load and store suffice.
+__device__ __forceinline__ void add_row_f32(float *row_ptr, int c, const uint32_t (&r)[32],
+                                            float mul) {
+    float4 *dst = reinterpret_cast<float4 *>(row_ptr + c * 32);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+        float4 a = dst[q];
+        a.x = fmaf(__uint_as_float(r[4 * q + 0]), mul, a.x);
+        a.y = fmaf(__uint_as_float(r[4 * q + 1]), mul, a.y);
+        a.z = fmaf(__uint_as_float(r[4 * q + 2]), mul, a.z);
+        a.w = fmaf(__uint_as_float(r[4 * q + 3]), mul, a.w);
+        dst[q] = a;
+    }
+}
+
 // ---------------------------------------------------------------- preprocess
 // 16 threads per row; each takes 8 consecutive bf16 of dO, O and V at a time.
 // Besides D and LSE2 it writes the fp16 copies of dO and V, times their
@@ -297,7 +315,7 @@ struct BwdParams {
     const void *do16;  // [B, N, H, dv] fp16 copy of dO * s_o
     const void *v16;   // [B, N, H, dv] fp16 copy of V * s_v
     const float4 *scales;  // [B*H] (s_o, s_v, 1/s_o, 1/(s_o s_v))
-    __nv_bfloat16 *dq, *dk, *dv;
+    void *dq, *dk, *dv;  // bf16 outputs, or fp32 accumulators (ACC32 instantiations)
     int N, H, Hm, T, Npad, causal;
     float sl2;    // scale * log2(e)
     float scale;
@@ -357,7 +375,7 @@ struct DqCfg {
     static_assert((D / 32) % NWG == 0, "epilogue column split");
 };
 
-template <class C>
+template <class C, bool ACC32>
 __global__ void __launch_bounds__(C::THREADS, 1)
     dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
               const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -733,26 +751,39 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         }
         if (n > 0) warp_wait(dq_done, 0, tmo, abort);
         tc_fence_after();
-        // dQ (times scale / (s_o s_v)) to the 128B-swizzled layout of the output
-        // map in the idle K ring, then TMA stores of its 64-column boxes (rows
-        // past N clipped).
+        // dQ (times scale / (s_o s_v)): added to the fp32 output (acc32), or as
+        // bf16 to the 128B-swizzled layout of the output map in the idle K ring,
+        // then TMA stores of its 64-column boxes (rows past N clipped).
         const float dq_mul = p.scale * p.scales[bh].w;
         constexpr int CPW = (C::D / 32) / C::NWG;  // 32-column chunks per group
+        if constexpr (ACC32) {
+            // fp32 accumulation: each row adds its own values (rows past N and
+            // CTAs without work add nothing).
+            float *dst = static_cast<float *>(p.dq) +
+                         ((static_cast<size_t>(b) * p.N + grow) * p.H + h) * C::D;
 #pragma unroll 1
-        for (int c = wg * CPW; c < (wg + 1) * CPW; ++c) {
-            uint32_t r[32];
-            tmem_ld32(lane_base + C::TM_DQ + c * 32, r);
-            float v[32];
+            for (int c = wg * CPW; c < (wg + 1) * CPW && n > 0; ++c) {
+                uint32_t r[32];
+                tmem_ld32(lane_base + C::TM_DQ + c * 32, r);
+                if (grow < p.N) add_row_f32(dst, c, r, dq_mul);
+            }
+        } else {
+#pragma unroll 1
+            for (int c = wg * CPW; c < (wg + 1) * CPW; ++c) {
+                uint32_t r[32];
+                tmem_ld32(lane_base + C::TM_DQ + c * 32, r);
+                float v[32];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = n > 0 ? __uint_as_float(r[i]) : 0.f;
-            stage_row_bf16(sK, c, row, v, dq_mul);
-        }
-        fence_proxy_async_smem();
-        named_bar_sync(1, C::NWG * 128);
-        if (threadIdx.x == 64) {
-            for (int box = 0; box < C::D / 64; ++box)
-                tma_store_4d(&tm_dq, sK + box * (128 * 128), box * 64, h, qt * TILE, b);
-            bulk_commit_wait_read();
+                for (int i = 0; i < 32; ++i) v[i] = n > 0 ? __uint_as_float(r[i]) : 0.f;
+                stage_row_bf16(sK, c, row, v, dq_mul);
+            }
+            fence_proxy_async_smem();
+            named_bar_sync(1, C::NWG * 128);
+            if (threadIdx.x == 64) {
+                for (int box = 0; box < C::D / 64; ++box)
+                    tma_store_4d(&tm_dq, sK + box * (128 * 128), box * 64, h, qt * TILE, b);
+                bulk_commit_wait_read();
+            }
         }
     }
 
@@ -825,7 +856,7 @@ struct DkdvCfg {
     static_assert((D / 32) % NWG == 0 && (DV / 32) % NWG == 0, "epilogue column split");
 };
 
-template <class C>
+template <class C, bool ACC32>
 __global__ void __launch_bounds__(C::THREADS, 1)
     dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -1222,47 +1253,75 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         }
         if (n > 0) warp_wait(done, 0, tmo, abort);
         tc_fence_after();
-        // dK (times scale / (s_o s_v)) and dV (times 1 / s_o) to the
-        // 128B-swizzled layouts of the output maps in the idle Q ring and dO
-        // stages, then TMA stores of their 64-column boxes (rows past N
-        // clipped).
+        // dK (times scale / (s_o s_v)) and dV (times 1 / s_o): added to the fp32
+        // outputs (acc32), or as bf16 to the 128B-swizzled layouts of the output
+        // maps in the idle Q ring and dO stages, then TMA stores of their
+        // 64-column boxes (rows past N clipped).
         const float4 sc = p.scales[bh];
-        uint8_t *stage_dk = sQ;
-        uint8_t *stage_dv = sQ + (C::DO_DK ? C::D / 64 : 0) * (128 * 128);
-        if constexpr (C::DO_DK) {
-            constexpr int CPW = (C::D / 32) / C::NWG;
+        if constexpr (ACC32) {
+            // fp32 accumulation: each key row adds its own values (rows past N
+            // and CTAs without work add nothing).
+            const size_t grow_off = (static_cast<size_t>(b) * p.N + gkey) * p.H + h;
+            if constexpr (C::DO_DK) {
+                constexpr int CPW = (C::D / 32) / C::NWG;
+                float *dst = static_cast<float *>(p.dk) + grow_off * C::D;
 #pragma unroll 1
-            for (int c = wg * CPW; c < (wg + 1) * CPW; ++c) {
-                uint32_t r[32];
-                tmem_ld32(lane_base + C::TM_DK + c * 32, r);
-                float v[32];
-#pragma unroll
-                for (int i = 0; i < 32; ++i) v[i] = n > 0 ? __uint_as_float(r[i]) : 0.f;
-                stage_row_bf16(stage_dk, c, row, v, p.scale * sc.w);
+                for (int c = wg * CPW; c < (wg + 1) * CPW && n > 0; ++c) {
+                    uint32_t r[32];
+                    tmem_ld32(lane_base + C::TM_DK + c * 32, r);
+                    if (gkey < p.N) add_row_f32(dst, c, r, p.scale * sc.w);
+                }
             }
-        }
-        if constexpr (C::DO_DV) {
-            constexpr int CPW = (C::DV / 32) / C::NWG;
+            if constexpr (C::DO_DV) {
+                constexpr int CPW = (C::DV / 32) / C::NWG;
+                float *dst = static_cast<float *>(p.dv) + grow_off * C::DV;
 #pragma unroll 1
-            for (int c = wg * CPW; c < (wg + 1) * CPW; ++c) {
-                uint32_t r[32];
-                tmem_ld32(lane_base + C::TM_DV + c * 32, r);
-                float v[32];
-#pragma unroll
-                for (int i = 0; i < 32; ++i) v[i] = n > 0 ? __uint_as_float(r[i]) : 0.f;
-                stage_row_bf16(stage_dv, c, row, v, sc.z);  // dV = (P^T dO s_o) / s_o
+                for (int c = wg * CPW; c < (wg + 1) * CPW && n > 0; ++c) {
+                    uint32_t r[32];
+                    tmem_ld32(lane_base + C::TM_DV + c * 32, r);
+                    if (gkey < p.N) add_row_f32(dst, c, r, sc.z);
+                }
             }
-        }
-        fence_proxy_async_smem();
-        named_bar_sync(1, C::NWG * 128);
-        if (threadIdx.x == 64) {
-            if constexpr (C::DO_DK)
-                for (int box = 0; box < C::D / 64; ++box)
-                    tma_store_4d(&tm_dk, stage_dk + box * (128 * 128), box * 64, h, kt * TILE, b);
-            if constexpr (C::DO_DV)
-                for (int box = 0; box < C::DV / 64; ++box)
-                    tma_store_4d(&tm_dv, stage_dv + box * (128 * 128), box * 64, h, kt * TILE, b);
-            bulk_commit_wait_read();
+        } else {
+            uint8_t *stage_dk = sQ;
+            uint8_t *stage_dv = sQ + (C::DO_DK ? C::D / 64 : 0) * (128 * 128);
+            if constexpr (C::DO_DK) {
+                constexpr int CPW = (C::D / 32) / C::NWG;
+#pragma unroll 1
+                for (int c = wg * CPW; c < (wg + 1) * CPW; ++c) {
+                    uint32_t r[32];
+                    tmem_ld32(lane_base + C::TM_DK + c * 32, r);
+                    float v[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) v[i] = n > 0 ? __uint_as_float(r[i]) : 0.f;
+                    stage_row_bf16(stage_dk, c, row, v, p.scale * sc.w);
+                }
+            }
+            if constexpr (C::DO_DV) {
+                constexpr int CPW = (C::DV / 32) / C::NWG;
+#pragma unroll 1
+                for (int c = wg * CPW; c < (wg + 1) * CPW; ++c) {
+                    uint32_t r[32];
+                    tmem_ld32(lane_base + C::TM_DV + c * 32, r);
+                    float v[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) v[i] = n > 0 ? __uint_as_float(r[i]) : 0.f;
+                    stage_row_bf16(stage_dv, c, row, v, sc.z);  // dV = (P^T dO s_o) / s_o
+                }
+            }
+            fence_proxy_async_smem();
+            named_bar_sync(1, C::NWG * 128);
+            if (threadIdx.x == 64) {
+                if constexpr (C::DO_DK)
+                    for (int box = 0; box < C::D / 64; ++box)
+                        tma_store_4d(&tm_dk, stage_dk + box * (128 * 128), box * 64, h,
+                                     kt * TILE, b);
+                if constexpr (C::DO_DV)
+                    for (int box = 0; box < C::DV / 64; ++box)
+                        tma_store_4d(&tm_dv, stage_dv + box * (128 * 128), box * 64, h,
+                                     kt * TILE, b);
+                bulk_commit_wait_read();
+            }
         }
     }
 
@@ -1285,9 +1344,9 @@ BwdParams make_params(const Geometry &g, const Workspace &ws, const BwdArgs &a, 
     p.do16 = ws.do16;
     p.v16 = ws.v16;
     p.scales = ws.scales;
-    p.dq = static_cast<__nv_bfloat16 *>(a.dq);
-    p.dk = static_cast<__nv_bfloat16 *>(a.dk);
-    p.dv = static_cast<__nv_bfloat16 *>(a.dv);
+    p.dq = a.dq;
+    p.dk = a.dk;
+    p.dv = a.dv;
     p.N = g.N;
     p.H = g.H;
     p.Hm = g.Hm;
@@ -1304,7 +1363,9 @@ BwdParams make_params(const Geometry &g, const Workspace &ws, const BwdArgs &a, 
 template <class C>
 cudaError_t launch_dq(const Geometry &g, const Workspace &ws, const BwdArgs &a, cudaStream_t st) {
     if (a.dq_k_rows != C::BN) return cudaErrorInvalidValue;  // map boxes must match the tile
-    auto kern = dq_kernel<C>;
+    // fp32 accumulation is a separate instantiation: its epilogue would add
+    // registers to kernels that sit at their register cap.
+    auto kern = g.acc32 ? dq_kernel<C, true> : dq_kernel<C, false>;
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
@@ -1317,7 +1378,7 @@ template <class C>
 cudaError_t launch_dkdv(const Geometry &g, const Workspace &ws, const BwdArgs &a,
                         cudaStream_t st) {
     if (a.kv_q_rows != C::BM) return cudaErrorInvalidValue;  // map boxes must match the tile
-    auto kern = dkdv_kernel<C>;
+    auto kern = g.acc32 ? dkdv_kernel<C, true> : dkdv_kernel<C, false>;
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (e != cudaSuccess) return e;

@@ -28,6 +28,7 @@ struct Geometry {
     float *dsink;       // [H] their gradient (backward), or nullptr
     int reuse_map;      // the workspace already holds this problem's tile map and lists
     int debug_bounds;   // attention kernels check their work lists before use
+    int acc32;          // backward: add the gradients to fp32 outputs instead of writing bf16
 };
 
 // Normalised mask boundaries per key column: (LTS, LTE, UTS, UTE) clamped to
