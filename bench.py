@@ -205,12 +205,21 @@ def flops_per_pair(d, dv):
     return {"fwd": 2 * (d + dv), "bwd": 2 * (3 * d + 2 * dv), "fwd+bwd": 8 * d + 6 * dv}
 
 
-def kernel_names(d, dv):
+def fused_backward(d, dv, deterministic):
+    """The library's backward runs one key-side pass that also reduces dQ
+    (fp32 red.add into a buffer, then a conversion kernel) at d = dv <= 128
+    outside the deterministic mode; otherwise the atomic-free split."""
+    return not deterministic and d == dv and d <= 128
+
+
+def kernel_names(d, dv, deterministic=False):
     """Kernels of the step's forward and backward calls, in launch order.  The
     backward reuses the tile map and lists the forward built in the shared
     workspace, so it starts at the preprocess kernel."""
     fwd = ["classify", "lists", "fwd"]
     bwd = ["bwd_preprocess"]
+    if fused_backward(d, dv, deterministic):
+        return fwd, bwd + ["bwd_dkdvq", "bwd_dq_convert"]
     bwd += ["bwd_dkdv_dv", "bwd_dkdv_dk"] if (d == 256 and dv == 256) else ["bwd_dkdv"]
     bwd += ["bwd_dq"]
     return fwd, bwd
@@ -227,9 +236,11 @@ def kernel_alg_flops_per_pair(name, d, dv):
     backward needs once; the query-side kernel is credited with dQ only (its S
     and dP are a second recomputation).  Where the key side runs as two passes
     (d = dv = 256), the dV pass is credited with S and dV, the dK pass with dP
-    and dK (its S is a recomputation), so the two add up to the one kernel."""
+    and dK (its S is a recomputation), so the two add up to the one kernel.
+    The fused key-side kernel does every product of the backward once."""
     return {"fwd": 2 * (d + dv), "bwd_dkdv": 2 * (2 * d + 2 * dv), "bwd_dq": 2 * d,
-            "bwd_dkdv_dv": 2 * d + 2 * dv, "bwd_dkdv_dk": 2 * dv + 2 * d}.get(name, 0)
+            "bwd_dkdv_dv": 2 * d + 2 * dv, "bwd_dkdv_dk": 2 * dv + 2 * d,
+            "bwd_dkdvq": 2 * (3 * d + 2 * dv)}.get(name, 0)
 
 
 def setup(cfg, seed, device):
@@ -280,7 +291,7 @@ def run_ours(args, rank, world, local_rank):
     fpp = flops_per_pair(d, dv)
     step_flops = U * (fpp["fwd+bwd"] if has_bwd else fpp["fwd"])
     in_bytes = B * N * H * (2 * d + dv + (dv if has_bwd else 0)) * 2
-    fwd_names, bwd_names = kernel_names(d, dv)
+    fwd_names, bwd_names = kernel_names(d, dv, det)
 
     o = torch.empty((B, N, H, dv), dtype=torch.bfloat16, device=device)
     lse = torch.empty((B, H, N), dtype=torch.float32, device=device)

@@ -204,6 +204,7 @@ size_t carve_workspace(const Geometry &g, bool bwd, void *base, Workspace *ws) {
     w.sink_part = nullptr;
     w.range_part = nullptr;
     w.scales = nullptr;
+    w.dqacc = nullptr;
     if (bwd) {
         const size_t rows = static_cast<size_t>(g.B) * g.H * g.Npad;
         w.lse2 = static_cast<float *>(take(rows * sizeof(float)));
@@ -215,6 +216,8 @@ size_t carve_workspace(const Geometry &g, bool bwd, void *base, Workspace *ws) {
         const size_t bht = static_cast<size_t>(g.B) * g.H * g.T;
         w.range_part = static_cast<uint2 *>(take(bht * sizeof(uint2)));
         w.scales = static_cast<float4 *>(take(static_cast<size_t>(g.B) * g.H * sizeof(float4)));
+        if (fused_dq(g))
+            w.dqacc = static_cast<float4 *>(take(rows * g.d * sizeof(float)));
     }
     if (ws) *ws = w;
     return off;

@@ -223,7 +223,8 @@ __global__ void __launch_bounds__(256) preprocess_kernel(
     const __nv_bfloat16 *__restrict__ dout, const __nv_bfloat16 *__restrict__ v,
     const float *__restrict__ lse, float *__restrict__ lse2, float *__restrict__ delta,
     uint4 *__restrict__ v16, uint4 *__restrict__ do16, const float4 *__restrict__ scales,
-    const float *__restrict__ sink, float *__restrict__ sink_part) {
+    const float *__restrict__ sink, float *__restrict__ sink_part, float4 *__restrict__ dqacc,
+    int dq4) {
     __shared__ float sink_rows[16];
     pdl_wait();  // the scales, and the inputs of the kernels before
     pdl_trigger();
@@ -255,6 +256,10 @@ __global__ void __launch_bounds__(256) preprocess_kernel(
             }
         }
     }
+    // fused dQ: the row's entries of the fp32 buffer [B*H][d/4][Npad] start at 0
+    if (dqacc && valid)
+        for (int c4 = t; c4 < dq4; c4 += 16)
+            dqacc[(static_cast<size_t>(bh) * dq4 + c4) * Npad + i] = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int off = 8; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off, 16);
     float sink_term = 0.f;  // the row's term of the sink-logit gradient
@@ -306,6 +311,47 @@ __global__ void __launch_bounds__(256) sink_grad_kernel(int B, int H, int blocks
     if (threadIdx.x == 0) dsink[h] = red[0];
 }
 
+// Fused dQ: the fp32 buffer [B*H][d/4][Npad] (float4) to dQ [B, N, H, d] bf16,
+// times scale / (s_o s_v); or (ACC32) added to an fp32 dQ of that layout.
+// One thread per row, 8 columns per store.
+template <bool ACC32>
+__global__ void __launch_bounds__(256) dq_convert_kernel(int N, int H, int d, int Npad,
+                                                         const float4 *__restrict__ dqacc,
+                                                         const float4 *__restrict__ scales,
+                                                         float scale, void *__restrict__ dq) {
+    pdl_wait();  // the fused kernel's sums
+    pdl_trigger();
+    const int i = blockIdx.x * 256 + threadIdx.x;
+    const int h = blockIdx.y, b = blockIdx.z;
+    if (i >= N) return;
+    const size_t bh = static_cast<size_t>(b) * H + h;
+    const float mul = scale * scales[bh].w;
+    const int d4 = d / 4;
+    const float4 *src = dqacc + bh * d4 * static_cast<size_t>(Npad) + i;
+    const size_t row = ((static_cast<size_t>(b) * N + i) * H + h) * d;
+    for (int c8 = 0; c8 < d / 8; ++c8) {
+        const float4 x = src[static_cast<size_t>(2 * c8) * Npad];
+        const float4 y = src[static_cast<size_t>(2 * c8 + 1) * Npad];
+        if constexpr (ACC32) {
+            float4 *o = reinterpret_cast<float4 *>(static_cast<float *>(dq) + row) + 2 * c8;
+            float4 a = o[0], c = o[1];
+            a.x = fmaf(x.x, mul, a.x); a.y = fmaf(x.y, mul, a.y);
+            a.z = fmaf(x.z, mul, a.z); a.w = fmaf(x.w, mul, a.w);
+            c.x = fmaf(y.x, mul, c.x); c.y = fmaf(y.y, mul, c.y);
+            c.z = fmaf(y.z, mul, c.z); c.w = fmaf(y.w, mul, c.w);
+            o[0] = a;
+            o[1] = c;
+        } else {
+            uint4 w;
+            w.x = pack_bf16(x.x * mul, x.y * mul);
+            w.y = pack_bf16(x.z * mul, x.w * mul);
+            w.z = pack_bf16(y.x * mul, y.y * mul);
+            w.w = pack_bf16(y.z * mul, y.w * mul);
+            reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(dq) + row)[c8] = w;
+        }
+    }
+}
+
 struct BwdParams {
     const int4 *vec;
     const int *list;  // fwd list (dq kernel) or bwd list (dkdv kernel)
@@ -315,6 +361,7 @@ struct BwdParams {
     const void *do16;  // [B, N, H, dv] fp16 copy of dO * s_o
     const void *v16;   // [B, N, H, dv] fp16 copy of V * s_v
     const float4 *scales;  // [B*H] (s_o, s_v, 1/s_o, 1/(s_o s_v))
+    float4 *dqacc;         // fused dQ: fp32 [B*H][d/4][Npad] (float4), zeroed by preprocess
     void *dq, *dk, *dv;  // bf16 outputs, or fp32 accumulators (ACC32 instantiations)
     int N, H, Hm, T, Npad, causal;
     float sl2;    // scale * log2(e)
@@ -811,11 +858,19 @@ __global__ void __launch_bounds__(C::THREADS, 1)
 // there (TS MMA).  Its shared memory goes to a second compute group and a
 // deeper Q ring at d = dv = 256 (where only the dK pass needs V), and to a
 // deeper Q ring at d = 192.
+// FDQ (fused dQ, the default backward at d <= 128): each sub-tile also gives
+// dQ_tile = dS K.  The compute writes dS^T, besides TMEM, to shared memory as
+// the MN-major A operand of that product (over the group's dO stage, spent
+// once dP^T ran, when it is large enough); the product lands in the group's
+// TMEM region after dK has read dS^T from it (the pipe runs them in order);
+// the group then adds the tile to the fp32 dQ buffer (coalesced red.add, the
+// buffer laid out [B*H][d/4][Npad] in float4) before the region takes the
+// group's next S^T.  S and dP are computed once per pair.
 template <int D_, int DV_, int BM_, int QS_, bool DK_, bool DV_ON_, int NWG_,
-          bool V_TM_ = false>
+          bool V_TM_ = false, bool FDQ_ = false>
 struct DkdvCfg {
     static constexpr int D = D_, DV = DV_, BM = BM_, QS = QS_, NWG = NWG_;
-    static constexpr bool DO_DK = DK_, DO_DV = DV_ON_, V_TM = V_TM_;
+    static constexpr bool DO_DK = DK_, DO_DV = DV_ON_, V_TM = V_TM_, FDQ = FDQ_;
     static constexpr int BN = 128;            // keys per CTA (TMEM lanes)
     static constexpr int SUB = TILE / BM;     // query sub-tiles per list entry
     static constexpr bool NEED_V = DO_DK;     // V only feeds dP^T
@@ -829,10 +884,16 @@ struct DkdvCfg {
     static constexpr int OFF_Q = OFF_V + V_BYTES;
     static constexpr int OFF_DO = OFF_Q + QS * Q_BYTES;
     static constexpr int OFF_LD = OFF_DO + NWG * DO_BYTES;
-    static constexpr int OFF_BAR = OFF_LD + NWG * LD_BYTES;
+    // FDQ: dS tile per group, bf16 [BN keys][BM queries], 64-query blocks
+    static constexpr int DS_BYTES = FDQ ? BN * BM * 2 : 0;
+    static constexpr bool DS_IN_DO = FDQ && DO_BYTES >= DS_BYTES;
+    static constexpr int OFF_DS = OFF_LD + NWG * LD_BYTES;
+    static constexpr int DS_STRIDE = DS_IN_DO ? DO_BYTES : DS_BYTES;  // between groups' tiles
+    static constexpr int OFF_BAR = OFF_DS + ((FDQ && !DS_IN_DO) ? NWG * DS_BYTES : 0);
     // kv_full, q_full[QS], q_empty[QS], o_full[NWG], o_empty[NWG],
-    // s_full[NWG], p_full[NWG], dp_full[NWG], ds_full[NWG], done, v_ready
-    static constexpr int NBAR = 1 + 2 * QS + 6 * NWG + 2;
+    // s_full[NWG], p_full[NWG], dp_full[NWG], ds_full[NWG], done, v_ready,
+    // FDQ: dq_full[NWG], dq_free[NWG]
+    static constexpr int NBAR = 1 + 2 * QS + 6 * NWG + 2 + (FDQ ? 2 * NWG : 0);
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int SMEM_BYTES = OFF_MISC + 16;
     static constexpr int TM_DK = 0;
@@ -854,6 +915,9 @@ struct DkdvCfg {
     // must not need the stage itself.
     static constexpr bool RELAY_Q = QS > NWG;
     static_assert((D / 32) % NWG == 0 && (DV / 32) % NWG == 0, "epilogue column split");
+    static_assert(!FDQ || (DO_DK && DO_DV && !V_TM && BM == 128 && D <= BM),
+                  "fused dQ: one pass, 128-query sub-tiles, dQ tile within a group region");
+    static_assert(OFF_DS % 1024 == 0, "swizzled dS tiles need 1024-byte alignment");
 };
 
 template <class C, bool ACC32>
@@ -877,6 +941,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     uint64_t *s_full = o_empty + C::NWG, *p_full = s_full + C::NWG, *dp_full = p_full + C::NWG,
              *ds_full = dp_full + C::NWG, *done = ds_full + C::NWG;
     uint64_t *v_ready = done + 1;
+    uint64_t *dq_full = v_ready + 1, *dq_free = dq_full + C::NWG;  // FDQ only
+    uint8_t *sDS = C::DS_IN_DO ? sDO : smem + C::OFF_DS;             // FDQ only
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
     volatile int *abort = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
 
@@ -909,6 +975,12 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         }
         mbar_init(done, 1);
         mbar_init(v_ready, 128);
+        if constexpr (C::FDQ) {
+            for (int i = 0; i < C::NWG; ++i) {
+                mbar_init(&dq_full[i], 1);
+                mbar_init(&dq_free[i], 128);
+            }
+        }
         *abort = 0;
         fence_barrier_init();
         if (n > 0) {  // K and V before the CTA-wide barrier: latency overlaps the setup
@@ -955,8 +1027,11 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 // The stage is free once the group's previous tile no longer
                 // needs it: with dK, when its compute has written dS^T (the dV
                 // and dP^T MMAs, the last readers of dO, completed before dP^T
-                // was handed over); without dK, when the dV MMA has completed.
-                uint64_t *free_bar = C::DO_DK ? &ds_full[w] : &o_empty[w];
+                // was handed over); without dK, when the dV MMA has completed;
+                // with fused dQ, when the dQ MMA has read the dS tile (written
+                // over the spent dO, or beside it).
+                uint64_t *free_bar =
+                    C::FDQ ? &dq_full[w] : (C::DO_DK ? &ds_full[w] : &o_empty[w]);
                 if (lw >= 1 && !mbar_wait(free_bar, (lw - 1) & 1, tmo, abort, &g_err_bwd))
                     break;
                 mbar_arrive_expect_tx(&o_full[w], C::DO_BYTES + C::LD_BYTES);
@@ -976,9 +1051,14 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             constexpr uint32_t IDESC_DP = idesc_fp16(128, C::BM, false, false);
             constexpr uint32_t IDESC_DV = idesc_fp16(128, C::DV, false, true);
             constexpr uint32_t IDESC_DK = idesc_bf16(128, C::D, false, true);
+            // fused dQ = dS K: A = dS, MN-major over the 128 queries of the
+            // sub-tile; B = K, MN-major over d
+            constexpr uint32_t IDESC_DQ = idesc_bf16(128, C::D, true, true);
             // Descriptors are built once; an MMA step only adds its byte offset
             // (in 16-byte units) to the start-address field.
             const uint64_t k_desc = sdesc_sw128(smem_u32(sK), 16, 1024);
+            const uint64_t k_desc_mn = sdesc_sw128(smem_u32(sK), C::BN * 128, 1024);
+            const uint64_t ds_desc = sdesc_sw128(smem_u32(sDS), C::BN * 128, 1024);
             const uint64_t v_desc = sdesc_sw128(smem_u32(sV), 16, 1024);
             const uint64_t q_desc = sdesc_sw128(smem_u32(sQ), 16, 1024);
             const uint64_t q_desc_mn = sdesc_sw128(smem_u32(sQ), C::BM * 128, 1024);
@@ -1036,6 +1116,9 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     const uint32_t t_r = tmem + C::TM_W0 + w * C::BM;
                     if (st_[w] == 0) {  // S^T = K Q^T
                         if (!s_ready(u)) continue;
+                        // fused dQ: the region holds the group's previous dQ tile
+                        // until the group has added it to the buffer
+                        if (C::FDQ && lu > 0 && !mbar_test(&dq_free[w], (lu - 1) & 1)) continue;
                         tc_fence_after();
                         issue_s(w, u);
                         st_[w] = 1;
@@ -1095,6 +1178,16 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                                 mma_ts(tmem + C::TM_DK, t_r + k * 8, qmn + ((k * 2048) >> 4),
                                        IDESC_DK, (acc_k || k > 0) ? 1u : 0u);
                         }
+                        if constexpr (C::FDQ) {
+                            // dQ_tile = dS K into the region dK has just read
+                            const uint64_t dsd =
+                                ds_desc + static_cast<uint64_t>((w * C::DS_STRIDE) >> 4);
+#pragma unroll
+                            for (int k = 0; k < C::BN / 16; ++k)
+                                mma_ss(t_r, dsd + ((k * 2048) >> 4), k_desc_mn + ((k * 2048) >> 4),
+                                       IDESC_DQ, k > 0 ? 1u : 0u);
+                            mma_commit(&dq_full[w]);
+                        }
                         lu_[w] = lu + 1;
                         st_[w] = 0;
                         // no later S^T of this group frees the stage (or, with no
@@ -1102,7 +1195,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                         if (!C::RELAY_Q || lu + 1 >= n_of(w)) mma_commit(&q_empty[s]);
                         if (lu + 1 >= n_of(w)) {
                             --remaining;
-                        } else if (s_ready(u + C::NWG)) {
+                        } else if (!C::FDQ && s_ready(u + C::NWG)) {
                             issue_s(w, u + C::NWG);
                             st_[w] = 1;
                         }
@@ -1245,11 +1338,42 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                         r[i] = pack_bf16(ds.x, ds.y);
                     }
                     tmem_st32(t_r + c * 32, r);  // columns already read
+                    if constexpr (C::FDQ) {
+                        // this key's row of the dS tile: queries 64c .. 64c + 63 in
+                        // block c, 16-byte units swizzled by the row (128B pattern)
+                        uint8_t *ds_row = sDS + wg * C::DS_STRIDE + c * (C::BN * 128) + row * 128;
+#pragma unroll
+                        for (int q = 0; q < 8; ++q)
+                            *reinterpret_cast<uint4 *>(ds_row + ((q ^ (row & 7)) * 16)) =
+                                make_uint4(r[4 * q], r[4 * q + 1], r[4 * q + 2], r[4 * q + 3]);
+                    }
                 }
+                if constexpr (C::FDQ) fence_proxy_async_smem();  // dS tile -> the MMA
                 tmem_st_wait();
                 tc_fence_before();
             }
             mbar_arrive(&ds_full[wg]);
+            if constexpr (C::FDQ) {
+                // phase 3: the tile's dQ rows (TMEM lane = query row q0 + row)
+                // added to the fp32 buffer; then the region is free
+                if (!warp_wait(&dq_full[wg], lu & 1, tmo, abort)) break;
+                tc_fence_after();
+                float4 *dst = p.dqacc + bh * (C::D / 4) * static_cast<size_t>(p.Npad) + q0 + row;
+#pragma unroll 1
+                for (int c = 0; c < C::D / 32; ++c) {
+                    uint32_t r[32];
+                    tmem_ld32(t_r + c * 32, r);
+#pragma unroll
+                    for (int q = 0; q < 8; ++q)
+                        atomicAdd(dst + static_cast<size_t>(c * 8 + q) * p.Npad,
+                                  make_float4(__uint_as_float(r[4 * q]),
+                                              __uint_as_float(r[4 * q + 1]),
+                                              __uint_as_float(r[4 * q + 2]),
+                                              __uint_as_float(r[4 * q + 3])));
+                }
+                tc_fence_before();
+                mbar_arrive(&dq_free[wg]);
+            }
         }
         if (n > 0) warp_wait(done, 0, tmo, abort);
         tc_fence_after();
@@ -1344,6 +1468,7 @@ BwdParams make_params(const Geometry &g, const Workspace &ws, const BwdArgs &a, 
     p.do16 = ws.do16;
     p.v16 = ws.v16;
     p.scales = ws.scales;
+    p.dqacc = ws.dqacc;
     p.dq = a.dq;
     p.dk = a.dk;
     p.dv = a.dv;
@@ -1427,12 +1552,31 @@ cudaError_t launch_bwd(const Geometry &g, const Workspace &ws, const BwdArgs &a,
                        static_cast<const __nv_bfloat16 *>(a.v), static_cast<const float *>(a.lse),
                        ws.lse2, ws.delta, static_cast<uint4 *>(ws.v16),
                        static_cast<uint4 *>(ws.do16), static_cast<const float4 *>(ws.scales),
-                       g.sink, g.dsink ? ws.sink_part : nullptr);
+                       g.sink, g.dsink ? ws.sink_part : nullptr, ws.dqacc, g.d / 4);
     rec.after(st);
     if (e == cudaSuccess && g.dsink)
         e = launch_pdl(sink_grad_kernel, dim3(g.H), dim3(256), 0, st, g.B, g.H, g.Npad / 16,
                        static_cast<const float *>(ws.sink_part), g.dsink);
     if (e != cudaSuccess) return e;
+    if (fused_dq(g)) {
+        // One key-side pass with dQ reduced into the fp32 buffer, then dQ out.
+        rec.before(st);
+        e = g.d == 64 ? launch_dkdv<DkdvCfg<64, 64, 128, 3, true, true, 2, false, true>>(g, ws, a, st)
+                      : launch_dkdv<DkdvCfg<128, 128, 128, 3, true, true, 2, false, true>>(g, ws,
+                                                                                            a, st);
+        rec.after(st);
+        if (e != cudaSuccess) return e;
+        rec.before(st);
+        const dim3 cgrid((g.N + 255) / 256, g.H, g.B);
+        e = g.acc32 ? launch_pdl(dq_convert_kernel<true>, cgrid, dim3(256), 0, st, g.N, g.H, g.d,
+                                 g.Npad, static_cast<const float4 *>(ws.dqacc),
+                                 static_cast<const float4 *>(ws.scales), g.scale, a.dq)
+                    : launch_pdl(dq_convert_kernel<false>, cgrid, dim3(256), 0, st, g.N, g.H, g.d,
+                                 g.Npad, static_cast<const float4 *>(ws.dqacc),
+                                 static_cast<const float4 *>(ws.scales), g.scale, a.dq);
+        rec.after(st);
+        return e;
+    }
     // DkdvCfg<d, dv, query sub-tile, Q stages, dK, dV, groups>;
     // DqCfg<d, dv, key sub-tile, K stages, groups>
     if (g.d == 64 && g.dv == 64)

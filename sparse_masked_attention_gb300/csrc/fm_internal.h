@@ -54,7 +54,15 @@ struct Workspace {
     uint2 *range_part; // [B*H][T] largest |dO| and |V| (bf16 bit patterns) per row tile
     float4 *scales;    // [B*H] (s_o, s_v, 1/s_o, 1/(s_o s_v)): powers of two that put the
                        // largest |dO| and |V| of the (batch, head) in [2^14, 2^15)
+    float4 *dqacc;     // fused backward: fp32 dQ sums [B*H][d/4][Npad] (float4)
 };
+
+// The backward reduces dQ inside its key-side kernel (one pass, fp32 red.add
+// into Workspace::dqacc) at d = dv <= 128 unless the deterministic mode asks
+// for the atomic-free split (key side, then query side).
+inline bool fused_dq(const Geometry &g) {
+    return !g.deterministic && g.d == g.dv && g.d <= 128;
+}
 
 // Optional per-kernel event recording (fm_options.kernel_events).
 struct Recorder {

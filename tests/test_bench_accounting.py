@@ -30,22 +30,31 @@ def test_step_flops_per_pair(d, dv):
 
 
 @pytest.mark.parametrize("d,dv", HEADS)
-def test_kernel_credits_add_up(d, dv):
+@pytest.mark.parametrize("det", [False, True])
+def test_kernel_credits_add_up(d, dv, det):
     credit = lambda n: bench.kernel_alg_flops_per_pair(n, d, dv)  # noqa: E731
     f = bench.flops_per_pair(d, dv)
-    fwd_names, bwd_names = bench.kernel_names(d, dv)
+    fwd_names, bwd_names = bench.kernel_names(d, dv, det)
     assert sum(credit(n) for n in fwd_names) == f["fwd"]
     assert sum(credit(n) for n in bwd_names) == f["bwd"]
     # the two-pass key side is credited exactly like the one-pass kernel
     assert credit("bwd_dkdv_dv") + credit("bwd_dkdv_dk") == credit("bwd_dkdv")
+    # the fused pass is the key side and the query side's dQ together
+    assert credit("bwd_dkdvq") == credit("bwd_dkdv") + credit("bwd_dq")
 
 
-def test_kernel_names_split_only_at_256():
+def test_kernel_names_follow_the_backward_variant():
     for d, dv in HEADS:
-        _, bwd = bench.kernel_names(d, dv)
-        split = "bwd_dkdv_dv" in bwd
-        assert split == (d == 256 and dv == 256)
-        assert bwd[0] == "bwd_preprocess" and bwd[-1] == "bwd_dq"
+        for det in (False, True):
+            _, bwd = bench.kernel_names(d, dv, det)
+            fused = not det and d == dv and d <= 128
+            assert bwd[0] == "bwd_preprocess"
+            if fused:
+                assert bwd[1:] == ["bwd_dkdvq", "bwd_dq_convert"]
+                continue
+            split = "bwd_dkdv_dv" in bwd
+            assert split == (d == 256 and dv == 256)
+            assert bwd[-1] == "bwd_dq"
 
 
 def test_workload_overrides():
