@@ -890,10 +890,16 @@ struct DkdvCfg {
     static constexpr int OFF_DS = OFF_LD + NWG * LD_BYTES;
     static constexpr int DS_STRIDE = DS_IN_DO ? DO_BYTES : DS_BYTES;  // between groups' tiles
     static constexpr int OFF_BAR = OFF_DS + ((FDQ && !DS_IN_DO) ? NWG * DS_BYTES : 0);
+    // FDQ: the first DQ_TMA_COLS columns of a dQ tile leave through a TMA bulk
+    // reduction, staged as fp32 [column / 4][128 rows] float4 in the sub-tile's
+    // Q stage (spent once dK ran: dQ does not read Q); the rest through red.add
+    // from registers.  The bulk path moves its bytes without the compute warps.
+    static constexpr int DQ_TMA_COLS = FDQ ? Q_BYTES / (BM * 4) : 0;
+    static constexpr bool Q_BY_REDUCER = DQ_TMA_COLS > 0;  // Q stages freed by the reducer
     // kv_full, q_full[QS], q_empty[QS], o_full[NWG], o_empty[NWG],
     // s_full[NWG], p_full[NWG], dp_full[NWG], ds_full[NWG], done, v_ready,
-    // FDQ: dq_full[NWG], dq_free[NWG]
-    static constexpr int NBAR = 1 + 2 * QS + 6 * NWG + 2 + (FDQ ? 2 * NWG : 0);
+    // FDQ: dq_full[NWG], dq_free[NWG], staged[NWG], red_done
+    static constexpr int NBAR = 1 + 2 * QS + 6 * NWG + 2 + (FDQ ? 3 * NWG + 1 : 0);
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int SMEM_BYTES = OFF_MISC + 16;
     static constexpr int TM_DK = 0;
@@ -918,6 +924,7 @@ struct DkdvCfg {
     static_assert(!FDQ || (DO_DK && DO_DV && !V_TM && BM == 128 && D <= BM),
                   "fused dQ: one pass, 128-query sub-tiles, dQ tile within a group region");
     static_assert(OFF_DS % 1024 == 0, "swizzled dS tiles need 1024-byte alignment");
+    static_assert(DQ_TMA_COLS % 32 == 0 && DQ_TMA_COLS <= D, "dQ columns staged in 32s");
 };
 
 template <class C, bool ACC32>
@@ -942,6 +949,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
              *ds_full = dp_full + C::NWG, *done = ds_full + C::NWG;
     uint64_t *v_ready = done + 1;
     uint64_t *dq_full = v_ready + 1, *dq_free = dq_full + C::NWG;  // FDQ only
+    uint64_t *staged = dq_free + C::NWG, *red_done = staged + C::NWG;  // FDQ only
     uint8_t *sDS = C::DS_IN_DO ? sDO : smem + C::OFF_DS;             // FDQ only
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
     volatile int *abort = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
@@ -979,7 +987,9 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             for (int i = 0; i < C::NWG; ++i) {
                 mbar_init(&dq_full[i], 1);
                 mbar_init(&dq_free[i], 128);
+                mbar_init(&staged[i], 128);
             }
+            mbar_init(red_done, 1);
         }
         *abort = 0;
         fence_barrier_init();
@@ -1044,6 +1054,26 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 bulk_load(ld, p.lse2 + bh * p.Npad + q0, C::BM * 4, &o_full[w]);
                 bulk_load(ld + C::BM * 4, p.delta + bh * p.Npad + q0, C::BM * 4, &o_full[w]);
             }
+        } else if (lane == 2 && n > 0 && C::Q_BY_REDUCER) {
+            // dQ reducer: once a group has staged a tile's first DQ_TMA_COLS
+            // columns in the tile's Q stage, add them to the fp32 buffer with
+            // bulk reductions (2 KB: 128 rows of one float4 column), wait until
+            // the engine has read the stage, and hand the stage back to the Q
+            // producer.
+            for (int u = 0; u < n; ++u) {
+                const int w = u % C::NWG, lw = u / C::NWG;
+                if (!mbar_wait(&staged[w], lw & 1, tmo, abort, &g_err_bwd)) break;
+                float4 *g = p.dqacc + bh * (C::D / 4) * static_cast<size_t>(p.Npad) + q0_of(u);
+                const uint8_t *src = sQ + (u % C::QS) * C::Q_BYTES;
+#pragma unroll 1
+                for (int c4 = 0; c4 < C::DQ_TMA_COLS / 4; ++c4)
+                    bulk_reduce_add_f32(g + static_cast<size_t>(c4) * p.Npad, src + c4 * 2048, 2048);
+                bulk_commit();
+                bulk_wait_read_all();
+                mbar_arrive(&q_empty[u % C::QS]);
+            }
+            bulk_wait_all();
+            mbar_arrive(red_done);
         }
     } else if (warp == 1) {
         if (lane == 0 && n > 0) {
@@ -1192,7 +1222,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                         st_[w] = 0;
                         // no later S^T of this group frees the stage (or, with no
                         // more stages than groups, that S^T would need it first)
-                        if (!C::RELAY_Q || lu + 1 >= n_of(w)) mma_commit(&q_empty[s]);
+                        if (!C::Q_BY_REDUCER && (!C::RELAY_Q || lu + 1 >= n_of(w)))
+                            mma_commit(&q_empty[s]);
                         if (lu + 1 >= n_of(w)) {
                             --remaining;
                         } else if (!C::FDQ && s_ready(u + C::NWG)) {
@@ -1271,7 +1302,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             if (!warp_wait(&o_full[wg], lu & 1, tmo, abort)) break;
             tc_fence_after();
             // S^T of this tile ran after the group's previous dK: that Q stage is free.
-            if (C::RELAY_Q && ((warp - 2) & 3) == 0 && lane == 0 && lu > 0)
+            if (C::RELAY_Q && !C::Q_BY_REDUCER && ((warp - 2) & 3) == 0 && lane == 0 && lu > 0)
                 mbar_arrive(&q_empty[(u - C::NWG) % C::QS]);
             // phase 1: P^T = exp2(S^T * scale * log2e - LSE2), masked; fp16 pairs
             uint32_t pk[C::BM / 2];
@@ -1358,24 +1389,43 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 // added to the fp32 buffer; then the region is free
                 if (!warp_wait(&dq_full[wg], lu & 1, tmo, abort)) break;
                 tc_fence_after();
+                if constexpr (C::DQ_TMA_COLS > 0) {
+                    // the first columns to the tile's spent Q stage, for the reducer
+                    float4 *stg = reinterpret_cast<float4 *>(sQ + (u % C::QS) * C::Q_BYTES) + row;
+#pragma unroll 1
+                    for (int c = 0; c < C::DQ_TMA_COLS / 32; ++c) {
+                        uint32_t r[32];
+                        tmem_ld32(t_r + c * 32, r);
+#pragma unroll
+                        for (int q = 0; q < 8; ++q)
+                            stg[(c * 8 + q) * 128] =
+                                make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
+                                            __uint_as_float(r[4 * q + 2]),
+                                            __uint_as_float(r[4 * q + 3]));
+                    }
+                    fence_proxy_async_smem();
+                    mbar_arrive(&staged[wg]);  // release: the engine reads these writes
+                }
                 float4 *dst = p.dqacc + bh * (C::D / 4) * static_cast<size_t>(p.Npad) + q0 + row;
 #pragma unroll 1
-                for (int c = 0; c < C::D / 32; ++c) {
+                for (int c = C::DQ_TMA_COLS / 32; c < C::D / 32; ++c) {
                     uint32_t r[32];
                     tmem_ld32(t_r + c * 32, r);
 #pragma unroll
                     for (int q = 0; q < 8; ++q)
-                        atomicAdd(dst + static_cast<size_t>(c * 8 + q) * p.Npad,
-                                  make_float4(__uint_as_float(r[4 * q]),
-                                              __uint_as_float(r[4 * q + 1]),
-                                              __uint_as_float(r[4 * q + 2]),
-                                              __uint_as_float(r[4 * q + 3])));
+                        red_add_v4(dst + static_cast<size_t>(c * 8 + q) * p.Npad,
+                                   __uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
+                                   __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
                 }
+                // Only the TMEM reads (complete at tcgen05.wait::ld) must precede
+                // the next S^T; the reductions need no ordering inside the CTA.
                 tc_fence_before();
-                mbar_arrive(&dq_free[wg]);
+                mbar_arrive_relaxed(&dq_free[wg]);
             }
         }
         if (n > 0) warp_wait(done, 0, tmo, abort);
+        // the epilogue stages dK and dV over the Q ring: the reducer must be done
+        if (C::Q_BY_REDUCER && n > 0) warp_wait(red_done, 0, tmo, abort);
         tc_fence_after();
         // dK (times scale / (s_o s_v)) and dV (times 1 / s_o): added to the fp32
         // outputs (acc32), or as bf16 to the 128B-swizzled layouts of the output
