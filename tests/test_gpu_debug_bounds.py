@@ -26,7 +26,7 @@ WS_ALIGN = 256
 SLACK = 1 << 20
 
 
-def _layout(B, Hm, H, N, dv, bwd):
+def _layout(B, Hm, H, N, dv, bwd, fused_d=None):
     """Byte offsets of the workspace's tile map and lists, in the order the
     library lays them out, and the total size (pinned below against
     flashmask_workspace_size and the lists' contents)."""
@@ -57,6 +57,8 @@ def _layout(B, Hm, H, N, dv, bwd):
         take("sink_part", rows // 16 * 4)
         take("range_part", B * H * T * 8)
         take("scales", B * H * 16)
+        if fused_d:  # the one-pass backward's fp32 dQ sums (not in deterministic mode)
+            take("dqacc", rows * fused_d * 4)
     return out, off, T, TP
 
 
@@ -99,7 +101,11 @@ def test_damaged_reused_lists_are_reported_and_emptied():
     vec = cuda_mask(mask)
     N, H = q.shape[1], q.shape[2]
     lay, total, T, TP = _layout(1, 1, H, N, dv, bwd=True)
-    assert total == fm.workspace_size(1, H, 1, N, d, dv, True)
+    # the steps below run the deterministic backward, whose workspace has no
+    # dQ buffer; the default backward's adds one at the end
+    assert total == fm.workspace_size(1, H, 1, N, d, dv, True, deterministic=True)
+    assert _layout(1, 1, H, N, dv, bwd=True, fused_d=d)[1] == \
+        fm.workspace_size(1, H, 1, N, d, dv, True)
     ws = torch.zeros(total + SLACK, dtype=torch.uint8, device="cuda")
     _step(q, k, v, do, vec, mask.causal, ws, debug=False)
     fm.get_error()
