@@ -313,41 +313,65 @@ __global__ void __launch_bounds__(256) sink_grad_kernel(int B, int H, int blocks
 
 // Fused dQ: the fp32 buffer [B*H][d/4][Npad] (float4) to dQ [B, N, H, d] bf16,
 // times scale / (s_o s_v); or (ACC32) added to an fp32 dQ of that layout.
-// One thread per row, 8 columns per store.
-template <bool ACC32>
-__global__ void __launch_bounds__(256) dq_convert_kernel(int N, int H, int d, int Npad,
+// A CTA takes 32 rows of one (batch, head): coalesced float4 reads down the
+// buffer's columns into a padded shared tile, then coalesced 16-byte writes
+// along the output rows.
+constexpr int CONV_ROWS = 32;
+
+template <bool ACC32, int D>
+__global__ void __launch_bounds__(256) dq_convert_kernel(int N, int H, int Npad,
                                                          const float4 *__restrict__ dqacc,
                                                          const float4 *__restrict__ scales,
                                                          float scale, void *__restrict__ dq) {
+    constexpr int LD = D + 4;  // row stride in floats: consecutive rows 16 bytes apart in banks
+    __shared__ __align__(16) float tile[CONV_ROWS * LD];
     pdl_wait();  // the fused kernel's sums
     pdl_trigger();
-    const int i = blockIdx.x * 256 + threadIdx.x;
+    const int i0 = blockIdx.x * CONV_ROWS;
     const int h = blockIdx.y, b = blockIdx.z;
-    if (i >= N) return;
     const size_t bh = static_cast<size_t>(b) * H + h;
     const float mul = scale * scales[bh].w;
-    const int d4 = d / 4;
-    const float4 *src = dqacc + bh * d4 * static_cast<size_t>(Npad) + i;
-    const size_t row = ((static_cast<size_t>(b) * N + i) * H + h) * d;
-    for (int c8 = 0; c8 < d / 8; ++c8) {
-        const float4 x = src[static_cast<size_t>(2 * c8) * Npad];
-        const float4 y = src[static_cast<size_t>(2 * c8 + 1) * Npad];
-        if constexpr (ACC32) {
-            float4 *o = reinterpret_cast<float4 *>(static_cast<float *>(dq) + row) + 2 * c8;
-            float4 a = o[0], c = o[1];
-            a.x = fmaf(x.x, mul, a.x); a.y = fmaf(x.y, mul, a.y);
-            a.z = fmaf(x.z, mul, a.z); a.w = fmaf(x.w, mul, a.w);
-            c.x = fmaf(y.x, mul, c.x); c.y = fmaf(y.y, mul, c.y);
-            c.z = fmaf(y.z, mul, c.z); c.w = fmaf(y.w, mul, c.w);
-            o[0] = a;
-            o[1] = c;
-        } else {
+    const float4 *src = dqacc + bh * (D / 4) * static_cast<size_t>(Npad) + i0;
+#pragma unroll
+    for (int k = 0; k < (D / 4) * CONV_ROWS / 256; ++k) {
+        const int idx = threadIdx.x + 256 * k;
+        const int c4 = idx / CONV_ROWS, r = idx % CONV_ROWS;  // i0 + r < Npad always
+        *reinterpret_cast<float4 *>(&tile[r * LD + c4 * 4]) = src[static_cast<size_t>(c4) * Npad + r];
+    }
+    __syncthreads();
+    if constexpr (ACC32) {
+        constexpr int CH = D / 4;  // float4 chunks per row
+#pragma unroll
+        for (int k = 0; k < CH * CONV_ROWS / 256; ++k) {
+            const int idx = threadIdx.x + 256 * k;
+            const int r = idx / CH, ch = idx % CH;
+            if (i0 + r >= N) continue;
+            const float4 x = *reinterpret_cast<const float4 *>(&tile[r * LD + ch * 4]);
+            float4 *o = reinterpret_cast<float4 *>(static_cast<float *>(dq) +
+                                                   ((static_cast<size_t>(b) * N + i0 + r) * H + h) * D) + ch;
+            float4 a = *o;
+            a.x = fmaf(x.x, mul, a.x);
+            a.y = fmaf(x.y, mul, a.y);
+            a.z = fmaf(x.z, mul, a.z);
+            a.w = fmaf(x.w, mul, a.w);
+            *o = a;
+        }
+    } else {
+        constexpr int CH = D / 8;  // 16-byte chunks (8 bf16) per row
+#pragma unroll
+        for (int k = 0; k < (CH * CONV_ROWS + 255) / 256; ++k) {
+            const int idx = threadIdx.x + 256 * k;
+            const int r = idx / CH, ch = idx % CH;
+            if (idx >= CH * CONV_ROWS || i0 + r >= N) continue;
+            const float4 x = *reinterpret_cast<const float4 *>(&tile[r * LD + ch * 8]);
+            const float4 y = *reinterpret_cast<const float4 *>(&tile[r * LD + ch * 8 + 4]);
             uint4 w;
             w.x = pack_bf16(x.x * mul, x.y * mul);
             w.y = pack_bf16(x.z * mul, x.w * mul);
             w.z = pack_bf16(y.x * mul, y.y * mul);
             w.w = pack_bf16(y.z * mul, y.w * mul);
-            reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(dq) + row)[c8] = w;
+            reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(dq) +
+                                      ((static_cast<size_t>(b) * N + i0 + r) * H + h) * D)[ch] = w;
         }
     }
 }
@@ -1617,13 +1641,13 @@ cudaError_t launch_bwd(const Geometry &g, const Workspace &ws, const BwdArgs &a,
         rec.after(st);
         if (e != cudaSuccess) return e;
         rec.before(st);
-        const dim3 cgrid((g.N + 255) / 256, g.H, g.B);
-        e = g.acc32 ? launch_pdl(dq_convert_kernel<true>, cgrid, dim3(256), 0, st, g.N, g.H, g.d,
-                                 g.Npad, static_cast<const float4 *>(ws.dqacc),
-                                 static_cast<const float4 *>(ws.scales), g.scale, a.dq)
-                    : launch_pdl(dq_convert_kernel<false>, cgrid, dim3(256), 0, st, g.N, g.H, g.d,
-                                 g.Npad, static_cast<const float4 *>(ws.dqacc),
-                                 static_cast<const float4 *>(ws.scales), g.scale, a.dq);
+        const dim3 cgrid((g.N + CONV_ROWS - 1) / CONV_ROWS, g.H, g.B);
+        auto conv = g.d == 64 ? (g.acc32 ? dq_convert_kernel<true, 64> : dq_convert_kernel<false, 64>)
+                              : (g.acc32 ? dq_convert_kernel<true, 128>
+                                         : dq_convert_kernel<false, 128>);
+        e = launch_pdl(conv, cgrid, dim3(256), 0, st, g.N, g.H, g.Npad,
+                       static_cast<const float4 *>(ws.dqacc), static_cast<const float4 *>(ws.scales),
+                       g.scale, a.dq);
         rec.after(st);
         return e;
     }
