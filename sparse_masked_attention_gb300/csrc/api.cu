@@ -210,7 +210,7 @@ size_t carve_workspace(const Geometry &g, bool bwd, void *base, Workspace *ws) {
         w.lse2 = static_cast<float *>(take(rows * sizeof(float)));
         w.delta = static_cast<float *>(take(rows * sizeof(float)));
         const size_t vbytes = static_cast<size_t>(g.B) * g.N * g.H * g.dv * 2;
-        w.v16 = take(vbytes);
+        w.v16 = fused_dq(g) ? nullptr : take(vbytes);  // the one-pass kernel converts V itself
         w.do16 = take(vbytes);
         w.sink_part = static_cast<float *>(take(rows / 16 * sizeof(float)));
         const size_t bht = static_cast<size_t>(g.B) * g.H * g.T;
@@ -389,15 +389,19 @@ fm_status flashmask_bwd(const fm_problem *p, const fm_options *opt, const void *
     CUtensorMap tdq_o, tdk_o, tdv_o;        // the gradients, stored by TMA
     const int dq_kr = dq_key_rows(g.d, g.dv), kv_qr = dkdv_query_rows(g.d, g.dv);
     // dO and V enter the dP and dV products through their fp16 copies (made by
-    // the preprocess kernel); Q and K stay bf16.
+    // the preprocess kernel); Q and K stay bf16.  The one-pass backward loads
+    // the bf16 V instead and converts its tile in shared memory (its query-side
+    // maps go unused).
+    const bool fused = fused_dq(g);
+    const void *v_src = fused ? v : ws.v16;
     if (!encode_bnhd(&tq_q, q, g.B, g.N, g.H, g.d, 128) ||
         !encode_bnhd(&tdo_q, ws.do16, g.B, g.N, g.H, g.dv, 128, true) ||
         !encode_bnhd(&tk_k, k, g.B, g.N, g.H, g.d, dq_kr) ||
-        !encode_bnhd(&tv_k, ws.v16, g.B, g.N, g.H, g.dv, dq_kr, true) ||
+        !encode_bnhd(&tv_k, v_src, g.B, g.N, g.H, g.dv, dq_kr, !fused) ||
         !encode_bnhd(&tq_k, q, g.B, g.N, g.H, g.d, kv_qr) ||
         !encode_bnhd(&tdo_k, ws.do16, g.B, g.N, g.H, g.dv, kv_qr, true) ||
         !encode_bnhd(&tk_kv, k, g.B, g.N, g.H, g.d, 128) ||
-        !encode_bnhd(&tv_kv, ws.v16, g.B, g.N, g.H, g.dv, 128, true))
+        !encode_bnhd(&tv_kv, v_src, g.B, g.N, g.H, g.dv, 128, !fused))
         return fail(cudaErrorInvalidValue, g_encode_detail);
     // bf16 outputs are stored by TMA; fp32 accumulation (acc32) adds to them
     // with plain loads and stores, and the maps stay unused.

@@ -205,7 +205,8 @@ __device__ __forceinline__ void add_row_f32(float *row_ptr, int c, const uint32_
 // ---------------------------------------------------------------- preprocess
 // 16 threads per row; each takes 8 consecutive bf16 of dO, O and V at a time.
 // Besides D and LSE2 it writes the fp16 copies of dO and V, times their
-// (batch, head)'s powers of two s_o and s_v.
+// (batch, head)'s powers of two s_o and s_v (V only for the split backward:
+// the one-pass kernel converts its resident V tile itself).
 __device__ __forceinline__ uint4 bf16x8_to_fp16x8(uint4 a, float mul) {
     const __nv_bfloat162 *a2 = reinterpret_cast<const __nv_bfloat162 *>(&a);
     uint4 r;
@@ -242,9 +243,11 @@ __global__ void __launch_bounds__(256) preprocess_kernel(
         for (int c = t * 8; c < dv; c += 128) {
             const uint4 a = *reinterpret_cast<const uint4 *>(o + base + c);
             const uint4 g = *reinterpret_cast<const uint4 *>(dout + base + c);
-            const uint4 vv = *reinterpret_cast<const uint4 *>(v + base + c);
             do16[(base + c) / 8] = bf16x8_to_fp16x8(g, sc.x);
-            v16[(base + c) / 8] = bf16x8_to_fp16x8(vv, sc.y);
+            if (v16) {  // the one-pass backward converts V in its own kernel
+                const uint4 vv = *reinterpret_cast<const uint4 *>(v + base + c);
+                v16[(base + c) / 8] = bf16x8_to_fp16x8(vv, sc.y);
+            }
             const __nv_bfloat162 *a2 = reinterpret_cast<const __nv_bfloat162 *>(&a);
             const __nv_bfloat162 *g2 = reinterpret_cast<const __nv_bfloat162 *>(&g);
 #pragma unroll
@@ -1183,7 +1186,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                         if ((p.ordered && u != next_v) || !mbar_test(&p_full[w], lu & 1) ||
                             !mbar_test(&o_full[w], lu & 1))
                             continue;
-                        if (C::V_TM && !mbar_test(v_ready, 0)) continue;
+                        if ((C::V_TM || C::FDQ) && !mbar_test(v_ready, 0)) continue;
                         tc_fence_after();
                         const bool acc_v = next_v > 0;  // the first dV product initialises
                         ++next_v;
@@ -1289,6 +1292,21 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         const int n_my = n_of(wg);
         const float *slse = reinterpret_cast<const float *>(sLD + wg * C::LD_BYTES);
         const float *sd = slse + C::BM;
+        if constexpr (C::FDQ) {
+            // Group 0 turns the key tile's V (bf16, loaded once) into the scaled
+            // fp16 operand of dP^T in place: 8 values per 16-byte unit, so the
+            // swizzled layout is unchanged.
+            if (wg == 0 && n > 0) {
+                if (warp_wait(kv_full, 0, tmo, abort)) {
+                    const float sv = p.scales[bh].y;
+                    uint4 *vb = reinterpret_cast<uint4 *>(sV);
+#pragma unroll 4
+                    for (int k = row; k < C::V_BYTES / 16; k += 128) vb[k] = bf16x8_to_fp16x8(vb[k], sv);
+                    fence_proxy_async_smem();
+                }
+                mbar_arrive(v_ready);
+            }
+        }
         if constexpr (C::V_TM) {
             // Group 0 puts the key tile's V rows (fp16 pairs; zeros past N) into
             // TMEM, where every dP^T of the CTA reads them.

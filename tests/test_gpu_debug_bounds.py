@@ -52,7 +52,8 @@ def _layout(B, Hm, H, N, dv, bwd, fused_d=None):
         rows = B * H * Npad
         take("lse2", rows * 4)
         take("delta", rows * 4)
-        take("v16", B * N * H * dv * 2)
+        if not fused_d:  # the one-pass backward converts V in its own kernel
+            take("v16", B * N * H * dv * 2)
         take("do16", B * N * H * dv * 2)
         take("sink_part", rows // 16 * 4)
         take("range_part", B * H * T * 8)
