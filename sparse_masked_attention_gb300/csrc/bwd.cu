@@ -455,14 +455,15 @@ __global__ void __launch_bounds__(C::THREADS, 1)
               const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
               const __grid_constant__ CUtensorMap tm_dq, const BwdParams p) {
     extern __shared__ __align__(1024) uint8_t smem[];
-    // Launched behind the key-side kernel, which it does not depend on: it can
-    // start only once every key-side CTA has passed its own pdl_wait(), so the
-    // lists, LSE2, D and the fp16 copies are complete.  It waits for the
-    // key-side grid before it exits, so that its completion implies both.
+    // Launched behind the key-side kernel.  The lists, LSE2, D and the fp16
+    // copies it reads were written before that kernel, but a grid sees another
+    // grid's writes only once it has executed griddepcontrol.wait itself: it
+    // waits here, before any read (its CTAs still launch during the key-side
+    // kernel's tail and hide their launch latency).
+    pdl_wait();
     pdl_trigger();
     if (smem_u32(smem) & 1023u) {  // swizzled tiles need 1024-byte alignment
         if (threadIdx.x == 0) atomicExch(&g_err_bwd, ERR_SMEM_ALIGN);
-        pdl_wait();
         return;
     }
     uint8_t *sQ = smem + C::OFF_Q, *sDO = smem + C::OFF_DO;
@@ -868,7 +869,6 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         tc_fence_after();
         tmem_dealloc(tmem, C::TM_COLS);
     }
-    pdl_wait();
 }
 
 // ---------------------------------------------------------------- dkdv kernel

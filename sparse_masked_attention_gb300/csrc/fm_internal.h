@@ -81,9 +81,8 @@ struct Recorder {
 // Launches `kern` with programmatic stream serialization: its CTAs may start
 // while the previous kernel in the stream drains.  Every kernel launched this
 // way calls pdl_wait() before it touches memory an earlier kernel in the
-// stream may write or read (the query-side backward kernel, whose inputs are
-// complete by the time it can launch, waits before it exits instead), so the
-// stream order of all results is that of plain launches.
+// stream may write or read, so the stream order of all results is that of
+// plain launches.
 template <typename... KArgs, typename... Args>
 cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
                        cudaStream_t st, Args &&...args) {
