@@ -119,6 +119,12 @@ typedef struct {
  * read and written once, by one thread; no atomics).  Partial gradients of
  * several calls, such as the (query chunk, key chunk) pairs of a context-
  * parallel run, are then summed before a single rounding to bf16.
+ * debug_drop_load (>= 0; 0 = off; failure-detection tests only): with k > 0
+ * the forward kernel at d <= 128 never issues the k-th key-tile load of each
+ * CTA, so the waits for it run out after wait_timeout_ns: the CTA stops, waits
+ * for its own loads and MMAs already in flight, frees its tensor memory and
+ * returns; flashmask_get_error then reports FM_ERR_DEVICE_TIMEOUT and the
+ * outputs are not meaningful.  No memory is touched out of place.
  * A NULL options pointer selects all defaults. */
 typedef struct {
     int deterministic;
@@ -130,6 +136,7 @@ typedef struct {
     float *dsink;
     int reuse_tile_map;
     int accumulate_f32;
+    int debug_drop_load;
 } fm_options;
 
 /* Tile classes written by flashmask_classify (128 x 128 tiles). */

@@ -101,7 +101,7 @@ def make_problem(B, H, Hm, N, d, dv, scale, causal) -> _b.fm_problem:
 
 def make_options(deterministic=False, wait_timeout_ns=0, kernel_events=None, sink=None,
                  dsink=None, reuse_tile_map=False, debug_bounds=False,
-                 accumulate_f32=False) -> _b.fm_options:
+                 accumulate_f32=False, debug_drop_load=0) -> _b.fm_options:
     """kernel_events: optional list of raw cudaEvent_t handles (ints), recorded in
     pairs around each kernel launch of the call.  sink / dsink: optional [H]
     fp32 CUDA tensors, the attention-sink logits and (backward) their gradient.
@@ -110,12 +110,13 @@ def make_options(deterministic=False, wait_timeout_ns=0, kernel_events=None, sin
     attention CTA checks its work list first; a bad one makes get_error()
     raise (status FM_ERR_DEVICE_BOUNDS) instead of reading out of range.
     accumulate_f32: the backward adds its gradients to fp32 dq, dk, dv instead
-    of writing bf16."""
+    of writing bf16.  debug_drop_load: failure-detection tests only (see
+    flashmask.h): the forward skips one key-tile load so its waits run out."""
     opt = _b.fm_options(int(bool(deterministic)), int(bool(debug_bounds)), int(wait_timeout_ns),
                         None, 0,
                         None if sink is None else sink.data_ptr(),
                         None if dsink is None else dsink.data_ptr(), int(bool(reuse_tile_map)),
-                        int(bool(accumulate_f32)))
+                        int(bool(accumulate_f32)), int(debug_drop_load))
     opt._tensors = (sink, dsink)
     if kernel_events:
         arr = (ctypes.c_void_p * len(kernel_events))(*kernel_events)

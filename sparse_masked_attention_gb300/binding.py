@@ -39,7 +39,8 @@ class fm_options(ctypes.Structure):
                 ("kernel_events", ctypes.POINTER(ctypes.c_void_p)),
                 ("n_kernel_events", ctypes.c_int),
                 ("sink", ctypes.c_void_p), ("dsink", ctypes.c_void_p),
-                ("reuse_tile_map", ctypes.c_int), ("accumulate_f32", ctypes.c_int)]
+                ("reuse_tile_map", ctypes.c_int), ("accumulate_f32", ctypes.c_int),
+                ("debug_drop_load", ctypes.c_int)]
 
 
 EXPORTS = ("flashmask_workspace_size", "flashmask_fwd", "flashmask_bwd", "flashmask_classify",

@@ -60,6 +60,8 @@ fm_status make_geometry(const fm_problem *p, const fm_options *opt, Geometry *g)
     g->debug_bounds = opt ? opt->debug_bounds : 0;
     g->acc32 = opt ? opt->accumulate_f32 : 0;
     if (g->acc32 != 0 && g->acc32 != 1) return FM_ERR_INVALID_ARG;
+    g->drop_load = opt ? opt->debug_drop_load : 0;
+    if (g->drop_load < 0) return FM_ERR_INVALID_ARG;
     // The list and map sizes must fit the int indexing of the kernels.
     const double entries = static_cast<double>(g->B) * g->Hm * g->T * g->T;
     if (entries > 2.0e9) return FM_ERR_INVALID_ARG;

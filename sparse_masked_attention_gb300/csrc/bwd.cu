@@ -534,7 +534,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     if (warp == 0) {
         if (lane == 0 && n > 0) {
             prefetch_tmap(&tm_k);
-            for (int u = 0; u < n; ++u) {
+            int u = 0;
+            for (; u < n; ++u) {
                 const int s = u % C::KS;
                 if (u >= C::KS &&
                     !mbar_wait(&k_empty[s], ((u / C::KS) - 1) & 1, tmo, abort, &g_err_bwd))
@@ -546,9 +547,13 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     tma_load_4d(sK + s * C::K_BYTES + c * C::BN * 128, &tm_k, &k_full[s], c * 64,
                                 h, key0, b);
             }
+            // loads in flight (and the Q / dO tiles) land before the CTA exits
+            drain_ring(k_full, C::KS, u, -1, tmo, &g_err_bwd);
+            mbar_wait_drain(q_full, 0, tmo, &g_err_bwd);
         } else if (lane == 1 && n > 0) {
             prefetch_tmap(&tm_v);
-            for (int u = 0; u < n; ++u) {
+            int u = 0;
+            for (; u < n; ++u) {
                 const int w = u % C::NWG, lw = u / C::NWG;
                 if (lw >= 1 && !mbar_wait(&v_empty[w], (lw - 1) & 1, tmo, abort, &g_err_bwd))
                     break;
@@ -559,6 +564,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     tma_load_4d(sV + w * C::V_BYTES + c * C::BN * 128, &tm_v, &v_full[w], c * 64,
                                 h, key0, b);
             }
+            drain_ring(v_full, C::NWG, u, -1, tmo, &g_err_bwd);
         }
     } else if (warp == 1) {
         if (lane == 0 && n > 0) {
@@ -690,6 +696,9 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 }
             }
             mma_commit(dq_done);
+            // every MMA has completed before the CTA frees TMEM, also after a
+            // wait gave up early
+            mbar_wait_drain(dq_done, 0, tmo, &g_err_bwd);
         }
     } else {
         // compute warpgroups: thread = query row
@@ -1045,7 +1054,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     if (warp == 0) {
         if (lane == 0 && n > 0) {
             prefetch_tmap(&tm_q);
-            for (int u = 0; u < n; ++u) {
+            int u = 0;
+            for (; u < n; ++u) {
                 const int s = u % C::QS;
                 if (u >= C::QS &&
                     !mbar_wait(&q_empty[s], ((u / C::QS) - 1) & 1, tmo, abort, &g_err_bwd))
@@ -1057,9 +1067,13 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     tma_load_4d(sQ + s * C::Q_BYTES + c * C::BM * 128, &tm_q, &q_full[s], c * 64,
                                 h, q0, b);
             }
+            // loads in flight (and the K / V tiles) land before the CTA exits
+            drain_ring(q_full, C::QS, u, -1, tmo, &g_err_bwd);
+            mbar_wait_drain(kv_full, 0, tmo, &g_err_bwd);
         } else if (lane == 1 && n > 0) {
             prefetch_tmap(&tm_do);
-            for (int u = 0; u < n; ++u) {
+            int u = 0;
+            for (; u < n; ++u) {
                 const int w = u % C::NWG, lw = u / C::NWG;
                 // The stage is free once the group's previous tile no longer
                 // needs it: with dK, when its compute has written dS^T (the dV
@@ -1081,6 +1095,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 bulk_load(ld, p.lse2 + bh * p.Npad + q0, C::BM * 4, &o_full[w]);
                 bulk_load(ld + C::BM * 4, p.delta + bh * p.Npad + q0, C::BM * 4, &o_full[w]);
             }
+            drain_ring(o_full, C::NWG, u, -1, tmo, &g_err_bwd);
         } else if (lane == 2 && n > 0 && C::Q_BY_REDUCER) {
             // dQ reducer: once a group has staged a tile's first DQ_TMA_COLS
             // columns in the tile's Q stage, add them to the fp32 buffer with
@@ -1277,6 +1292,9 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 }
             }
             mma_commit(done);
+            // every MMA has completed before the CTA frees TMEM, also after a
+            // wait gave up early
+            mbar_wait_drain(done, 0, tmo, &g_err_bwd);
         }
     } else {
         // compute warpgroups: thread = key column (TMEM lane)

@@ -120,6 +120,34 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint64
     }
 }
 
+// Bounded wait for this CTA's own asynchronous work on the way out (MMAs or
+// TMA loads it issued, which must land before it frees TMEM or exits).
+// Unlike mbar_wait it ignores the abort flag: after another role gave up, the
+// work already in flight still completes, and the CTA waits for it.  On a
+// timeout it records ERR_TIMEOUT and gives up.
+__device__ __forceinline__ bool mbar_wait_drain(uint64_t *bar, uint32_t parity,
+                                                uint64_t timeout_ns, unsigned *err_word) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer();
+    while (!mbar_try_wait(bar, parity)) {
+        if (globaltimer() - t0 > timeout_ns) {
+            atomicExch(err_word, ERR_TIMEOUT);
+            return false;
+        }
+    }
+    return true;
+}
+
+// Waits (mbar_wait_drain) for the last loads a producer issued into a ring of
+// `stages` stages: loads [0, issued), except the one numbered `skipped` (-1:
+// none).  Each stage's latest load is the only one that can still be in
+// flight, and its completion phase is load / stages.
+__device__ __forceinline__ void drain_ring(uint64_t *full, int stages, int issued, int skipped,
+                                           uint64_t timeout_ns, unsigned *err_word) {
+    for (int j = issued > stages ? issued - stages : 0; j < issued; ++j)
+        if (j != skipped) mbar_wait_drain(&full[j % stages], (j / stages) & 1, timeout_ns, err_word);
+}
+
 // -------------------------------------------------------------------- TMA
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap *map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");

@@ -29,6 +29,7 @@ struct Geometry {
     int reuse_map;      // the workspace already holds this problem's tile map and lists
     int debug_bounds;   // attention kernels check their work lists before use
     int acc32;          // backward: add the gradients to fp32 outputs instead of writing bf16
+    int drop_load;      // failure-detection test: the forward skips one K load (0: off)
 };
 
 // Normalised mask boundaries per key column: (LTS, LTE, UTS, UTE) clamped to

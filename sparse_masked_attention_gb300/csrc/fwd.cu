@@ -45,6 +45,7 @@ struct FwdParams {
     int N, H, Hm, T, B, Npad, causal;
     float sl2;  // scale * log2(e)
     uint64_t timeout_ns;
+    int drop_load;  // failure-detection test: k > 0 skips the k-th K load (pair kernel)
 };
 
 template <int D_, int DV_, int BN_, int NWG_, int NSB_, int KS_, int VS_>
@@ -359,7 +360,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         // consumer drains it: lane 0 Q and K, lane 1 V.
         if (lane == 0 && n > 0) {
             prefetch_tmap(&tm_k);
-            for (int u = 0; u < n; ++u) {
+            int u = 0;
+            for (; u < n; ++u) {
                 const int s = u % C::KS;
                 if (u >= C::KS &&
                     !mbar_wait(&k_empty[s], ((u / C::KS) - 1) & 1, tmo, abort, &g_err_fwd))
@@ -371,9 +373,13 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     tma_load_4d(sK + s * C::K_BYTES + c * C::BN * 128, &tm_k, &k_full[s], c * 64,
                                 h, key0, b);
             }
+            // loads in flight (and the Q tile) land before the CTA exits
+            drain_ring(k_full, C::KS, u, -1, tmo, &g_err_fwd);
+            mbar_wait_drain(q_full, 0, tmo, &g_err_fwd);
         } else if (lane == 1 && n > 0) {
             prefetch_tmap(&tm_v);
-            for (int u = 0; u < n; ++u) {
+            int u = 0;
+            for (; u < n; ++u) {
                 const int s = u % C::VS;
                 if (u >= C::VS &&
                     !mbar_wait(&v_empty[s], ((u / C::VS) - 1) & 1, tmo, abort, &g_err_fwd))
@@ -385,6 +391,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     tma_load_4d(sV + s * C::V_BYTES + c * C::BN * 128, &tm_v, &v_full[s], c * 64,
                                 h, key0, b);
             }
+            drain_ring(v_full, C::VS, u, -1, tmo, &g_err_fwd);
         }
     } else if (warp == 1) {
         // --------------------------------------------------- tcgen05 issuer
@@ -503,6 +510,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 }
             }
             mma_commit(mma_done);  // every MMA of the CTA has completed
+            // ... before the CTA frees TMEM, also when a wait gave up early
+            mbar_wait_drain(mma_done, 0, tmo, &g_err_fwd);
         }
     } else {
         // ------------------------------------------------ softmax warpgroups
@@ -671,6 +680,7 @@ cudaError_t launch_cfg(const Geometry &g, const Workspace &ws, const FwdArgs &a,
     p.causal = g.causal;
     p.sl2 = g.scale * 1.4426950408889634f;
     p.timeout_ns = g.timeout_ns;
+    p.drop_load = g.drop_load;
     if (a.k_rows != C::BN) return cudaErrorInvalidValue;  // map boxes must match the tile
     auto kern = fwd_kernel<C>;
     cudaError_t e =
@@ -704,8 +714,8 @@ struct PairCfg {
     static constexpr int OFF_V = OFF_K + KS * K_BYTES;
     static constexpr int OFF_BAR = OFF_V + VS * V_BYTES;
     // q_full, k_full[KS], k_empty[KS], v_full[VS], v_empty[VS], s_full[2],
-    // p_full[2], o_done[2]
-    static constexpr int NBAR = 1 + 2 * KS + 2 * VS + 6;
+    // p_full[2], o_done[2], mma_idle
+    static constexpr int NBAR = 1 + 2 * KS + 2 * VS + 7;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int SMEM_BYTES = OFF_MISC + 16;
     static constexpr int TM_O = 0;
@@ -744,6 +754,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     uint64_t *s_full = v_empty + C::VS;
     uint64_t *p_full = s_full + 2;
     uint64_t *o_done = p_full + 2;
+    uint64_t *mma_idle = o_done + 2;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
     volatile int *abort = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
 
@@ -777,6 +788,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             mbar_init(&p_full[g], 128);
             mbar_init(&o_done[g], 1);
         }
+        mbar_init(mma_idle, 1);
         *abort = 0;
         fence_barrier_init();
         if (n > 0) {  // both Q tiles before the CTA-wide barrier: latency overlaps the setup
@@ -804,12 +816,16 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         if (lane < 2 && n > 0) {
             const bool is_k = lane == 0;
             const int S = is_k ? C::KS : C::VS;
+            // failure-detection test only: this K load is never issued
+            const int skip = is_k ? p.drop_load - 1 : -1;
             if (is_k) prefetch_tmap(&tm_k); else prefetch_tmap(&tm_v);
-            for (int j = 0; j < n; ++j) {
+            int j = 0;
+            for (; j < n; ++j) {
                 const int s = j % S;
                 uint64_t *full = is_k ? &k_full[s] : &v_full[s];
                 uint64_t *empty = is_k ? &k_empty[s] : &v_empty[s];
                 if (j >= S && !mbar_wait(empty, ((j / S) - 1) & 1, tmo, abort, &g_err_fwd)) break;
+                if (j == skip) continue;
                 const int key0 = (entries[j] >> 2) * TILE;
                 if (is_k) {
                     mbar_arrive_expect_tx(full, C::K_BYTES);
@@ -825,6 +841,11 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                                     key0, b);
                 }
             }
+            // Loads still in flight land before the CTA exits, whatever happened
+            // (after a timeout the consumers no longer wait for them); lane 0
+            // also issued the Q tiles.
+            drain_ring(is_k ? k_full : v_full, S, j, skip, tmo, &g_err_fwd);
+            if (is_k) mbar_wait_drain(q_full, 0, tmo, &g_err_fwd);
         }
     } else if (warp == 1) {
         // --------------------------------------------------- tcgen05 issuer
@@ -913,6 +934,10 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     }
                 }
             }
+            // Every MMA issued has completed before the CTA frees TMEM, also
+            // when a wait gave up and the groups stopped early.
+            mma_commit(mma_idle);
+            mbar_wait_drain(mma_idle, 0, tmo, &g_err_fwd);
         }
     } else {
         // ------------------------------------------------ softmax warpgroups
@@ -1040,6 +1065,7 @@ cudaError_t launch_pair(const Geometry &g, const Workspace &ws, const FwdArgs &a
     p.causal = g.causal;
     p.sl2 = g.scale * 1.4426950408889634f;
     p.timeout_ns = g.timeout_ns;
+    p.drop_load = g.drop_load;
     if (a.k_rows != C::BN) return cudaErrorInvalidValue;  // map boxes must match the tile
     auto kern = fwd_pair_kernel<C>;
     cudaError_t e =
