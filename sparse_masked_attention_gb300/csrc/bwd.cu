@@ -476,6 +476,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     uint64_t *do_ready = dq_done + 1;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
     volatile int *abort = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
+    int *issued = reinterpret_cast<int *>(smem + C::OFF_MISC + 8);  // loads per ring
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int qt = p.T - 1 - static_cast<int>(blockIdx.x);
@@ -506,6 +507,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         mbar_init(dq_done, 1);
         mbar_init(do_ready, 128);
         *abort = 0;
+        issued[0] = issued[1] = 0;
         fence_barrier_init();
         if (n > 0) {  // Q and dO before the CTA-wide barrier: latency overlaps the setup
             mbar_arrive_expect_tx(q_full, C::Q_BYTES + C::DO_BYTES);
@@ -547,9 +549,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     tma_load_4d(sK + s * C::K_BYTES + c * C::BN * 128, &tm_k, &k_full[s], c * 64,
                                 h, key0, b);
             }
-            // loads in flight (and the Q / dO tiles) land before the CTA exits
-            drain_ring(k_full, C::KS, u, -1, tmo, &g_err_bwd);
-            mbar_wait_drain(q_full, 0, tmo, &g_err_bwd);
+            issued[0] = u;
         } else if (lane == 1 && n > 0) {
             prefetch_tmap(&tm_v);
             int u = 0;
@@ -564,7 +564,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     tma_load_4d(sV + w * C::V_BYTES + c * C::BN * 128, &tm_v, &v_full[w], c * 64,
                                 h, key0, b);
             }
-            drain_ring(v_full, C::NWG, u, -1, tmo, &g_err_bwd);
+            issued[1] = u;
         }
     } else if (warp == 1) {
         if (lane == 0 && n > 0) {
@@ -696,9 +696,6 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 }
             }
             mma_commit(dq_done);
-            // every MMA has completed before the CTA frees TMEM, also after a
-            // wait gave up early
-            mbar_wait_drain(dq_done, 0, tmo, &g_err_bwd);
         }
     } else {
         // compute warpgroups: thread = query row
@@ -873,6 +870,20 @@ __global__ void __launch_bounds__(C::THREADS, 1)
 
     tc_fence_before();
     __syncthreads();
+    // After a wait gave up, what this CTA still has in flight lands before it
+    // frees TMEM and exits: both rings' loads, the tiles loaded at the start and
+    // the MMAs.  Past the barrier *abort is final and the same for every
+    // thread; on the normal path every load was consumed and every MMA waited
+    // for, and nothing is left to drain.
+    if (*abort) {
+        if (threadIdx.x == 0 && n > 0) {
+            drain_ring(k_full, C::KS, issued[0], -1, tmo, &g_err_bwd);
+            drain_ring(v_full, C::NWG, issued[1], -1, tmo, &g_err_bwd);
+            mbar_wait_drain(q_full, 0, tmo, &g_err_bwd);
+            mbar_wait_drain(dq_done, 0, tmo, &g_err_bwd);
+        }
+        __syncthreads();
+    }
     if (warp == 1) {
         __syncwarp();
         tc_fence_after();
@@ -989,6 +1000,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     uint8_t *sDS = C::DS_IN_DO ? sDO : smem + C::OFF_DS;             // FDQ only
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
     volatile int *abort = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
+    int *issued = reinterpret_cast<int *>(smem + C::OFF_MISC + 8);  // loads per ring
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int kt = blockIdx.x;
@@ -1019,6 +1031,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         }
         mbar_init(done, 1);
         mbar_init(v_ready, 128);
+        issued[0] = issued[1] = 0;
         if constexpr (C::FDQ) {
             for (int i = 0; i < C::NWG; ++i) {
                 mbar_init(&dq_full[i], 1);
@@ -1067,9 +1080,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     tma_load_4d(sQ + s * C::Q_BYTES + c * C::BM * 128, &tm_q, &q_full[s], c * 64,
                                 h, q0, b);
             }
-            // loads in flight (and the K / V tiles) land before the CTA exits
-            drain_ring(q_full, C::QS, u, -1, tmo, &g_err_bwd);
-            mbar_wait_drain(kv_full, 0, tmo, &g_err_bwd);
+            issued[0] = u;
         } else if (lane == 1 && n > 0) {
             prefetch_tmap(&tm_do);
             int u = 0;
@@ -1095,7 +1106,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 bulk_load(ld, p.lse2 + bh * p.Npad + q0, C::BM * 4, &o_full[w]);
                 bulk_load(ld + C::BM * 4, p.delta + bh * p.Npad + q0, C::BM * 4, &o_full[w]);
             }
-            drain_ring(o_full, C::NWG, u, -1, tmo, &g_err_bwd);
+            issued[1] = u;
         } else if (lane == 2 && n > 0 && C::Q_BY_REDUCER) {
             // dQ reducer: once a group has staged a tile's first DQ_TMA_COLS
             // columns in the tile's Q stage, add them to the fp32 buffer with
@@ -1292,9 +1303,6 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 }
             }
             mma_commit(done);
-            // every MMA has completed before the CTA frees TMEM, also after a
-            // wait gave up early
-            mbar_wait_drain(done, 0, tmo, &g_err_bwd);
         }
     } else {
         // compute warpgroups: thread = key column (TMEM lane)
@@ -1561,6 +1569,20 @@ __global__ void __launch_bounds__(C::THREADS, 1)
 
     tc_fence_before();
     __syncthreads();
+    // After a wait gave up, what this CTA still has in flight lands before it
+    // frees TMEM and exits: both rings' loads, the tiles loaded at the start and
+    // the MMAs.  Past the barrier *abort is final and the same for every
+    // thread; on the normal path every load was consumed and every MMA waited
+    // for, and nothing is left to drain.
+    if (*abort) {
+        if (threadIdx.x == 0 && n > 0) {
+            drain_ring(q_full, C::QS, issued[0], -1, tmo, &g_err_bwd);
+            drain_ring(o_full, C::NWG, issued[1], -1, tmo, &g_err_bwd);
+            mbar_wait_drain(kv_full, 0, tmo, &g_err_bwd);
+            mbar_wait_drain(done, 0, tmo, &g_err_bwd);
+        }
+        __syncthreads();
+    }
     if (warp == 1) {
         __syncwarp();
         tc_fence_after();

@@ -303,6 +303,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     uint64_t *mma_done = pv_done + C::NWG * 2;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
     volatile int *abort = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
+    int *issued = reinterpret_cast<int *>(smem + C::OFF_MISC + 8);  // loads per ring
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int qt = p.T - 1 - static_cast<int>(blockIdx.x);  // heaviest query tiles first
@@ -333,6 +334,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         for (int i = 0; i < C::NWG * 2; ++i) mbar_init(&pv_done[i], 1);
         mbar_init(mma_done, 1);
         *abort = 0;
+        issued[0] = issued[1] = 0;
         fence_barrier_init();
         if (n > 0) {  // Q before the CTA-wide barrier: its latency overlaps the setup
             mbar_arrive_expect_tx(q_full, C::Q_BYTES);
@@ -373,9 +375,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     tma_load_4d(sK + s * C::K_BYTES + c * C::BN * 128, &tm_k, &k_full[s], c * 64,
                                 h, key0, b);
             }
-            // loads in flight (and the Q tile) land before the CTA exits
-            drain_ring(k_full, C::KS, u, -1, tmo, &g_err_fwd);
-            mbar_wait_drain(q_full, 0, tmo, &g_err_fwd);
+            issued[0] = u;
         } else if (lane == 1 && n > 0) {
             prefetch_tmap(&tm_v);
             int u = 0;
@@ -391,7 +391,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     tma_load_4d(sV + s * C::V_BYTES + c * C::BN * 128, &tm_v, &v_full[s], c * 64,
                                 h, key0, b);
             }
-            drain_ring(v_full, C::VS, u, -1, tmo, &g_err_fwd);
+            issued[1] = u;
         }
     } else if (warp == 1) {
         // --------------------------------------------------- tcgen05 issuer
@@ -510,8 +510,6 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 }
             }
             mma_commit(mma_done);  // every MMA of the CTA has completed
-            // ... before the CTA frees TMEM, also when a wait gave up early
-            mbar_wait_drain(mma_done, 0, tmo, &g_err_fwd);
         }
     } else {
         // ------------------------------------------------ softmax warpgroups
@@ -654,6 +652,20 @@ __global__ void __launch_bounds__(C::THREADS, 1)
 
     tc_fence_before();
     __syncthreads();
+    // After a wait gave up, what this CTA still has in flight lands before it
+    // frees TMEM and exits: both rings' loads, the tiles loaded at the start and
+    // the MMAs.  Past the barrier *abort is final and the same for every
+    // thread; on the normal path every load was consumed and every MMA waited
+    // for, and nothing is left to drain.
+    if (*abort) {
+        if (threadIdx.x == 0 && n > 0) {
+            drain_ring(k_full, C::KS, issued[0], -1, tmo, &g_err_fwd);
+            drain_ring(v_full, C::VS, issued[1], -1, tmo, &g_err_fwd);
+            mbar_wait_drain(q_full, 0, tmo, &g_err_fwd);
+            mbar_wait_drain(mma_done, 0, tmo, &g_err_fwd);
+        }
+        __syncthreads();
+    }
     if (warp == 1) {
         __syncwarp();
         tc_fence_after();
@@ -757,6 +769,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     uint64_t *mma_idle = o_done + 2;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
     volatile int *abort = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
+    int *issued = reinterpret_cast<int *>(smem + C::OFF_MISC + 8);  // loads per ring
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int TP = (p.T + 1) / 2;
@@ -790,6 +803,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         }
         mbar_init(mma_idle, 1);
         *abort = 0;
+        issued[0] = issued[1] = 0;
         fence_barrier_init();
         if (n > 0) {  // both Q tiles before the CTA-wide barrier: latency overlaps the setup
             mbar_arrive_expect_tx(q_full, 2 * C::Q_BYTES);
@@ -841,11 +855,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                                     key0, b);
                 }
             }
-            // Loads still in flight land before the CTA exits, whatever happened
-            // (after a timeout the consumers no longer wait for them); lane 0
-            // also issued the Q tiles.
-            drain_ring(is_k ? k_full : v_full, S, j, skip, tmo, &g_err_fwd);
-            if (is_k) mbar_wait_drain(q_full, 0, tmo, &g_err_fwd);
+            issued[is_k ? 0 : 1] = j;
         }
     } else if (warp == 1) {
         // --------------------------------------------------- tcgen05 issuer
@@ -934,10 +944,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     }
                 }
             }
-            // Every MMA issued has completed before the CTA frees TMEM, also
-            // when a wait gave up and the groups stopped early.
-            mma_commit(mma_idle);
-            mbar_wait_drain(mma_idle, 0, tmo, &g_err_fwd);
+            mma_commit(mma_idle);  // waited for only after a wait gave up
         }
     } else {
         // ------------------------------------------------ softmax warpgroups
@@ -1039,6 +1046,20 @@ __global__ void __launch_bounds__(C::THREADS, 1)
 
     tc_fence_before();
     __syncthreads();
+    // After a wait gave up, what this CTA still has in flight lands before it
+    // frees TMEM and exits: both rings' loads, the tiles loaded at the start and
+    // the MMAs.  Past the barrier *abort is final and the same for every
+    // thread; on the normal path every load was consumed and every MMA waited
+    // for, and nothing is left to drain.
+    if (*abort) {
+        if (threadIdx.x == 0 && n > 0) {
+            drain_ring(k_full, C::KS, issued[0], p.drop_load - 1, tmo, &g_err_fwd);
+            drain_ring(v_full, C::VS, issued[1], -1, tmo, &g_err_fwd);
+            mbar_wait_drain(q_full, 0, tmo, &g_err_fwd);
+            mbar_wait_drain(mma_idle, 0, tmo, &g_err_fwd);
+        }
+        __syncthreads();
+    }
     if (warp == 1) {
         __syncwarp();
         tc_fence_after();
