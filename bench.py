@@ -220,9 +220,11 @@ def kernel_names(d, dv, deterministic=False):
     bwd = ["bwd_preprocess"]
     if fused_backward(d, dv, deterministic):
         return fwd, bwd + ["bwd_dkdvq", "bwd_dq_convert"]
-    bwd += ["bwd_dkdv_dv", "bwd_dkdv_dk"] if (d == 256 and dv == 256) else ["bwd_dkdv"]
-    bwd += ["bwd_dq"]
-    return fwd, bwd
+    # the split backward: key side and query side in one launch (at
+    # d = dv = 256 after a separate dV pass of the key side)
+    if d == 256 and dv == 256:
+        return fwd, bwd + ["bwd_dkdv_dv", "bwd_split_dk"]
+    return fwd, bwd + ["bwd_split"]
 
 
 # Kernel launches behind one event pair: the preprocess step is the range,
@@ -231,16 +233,17 @@ LAUNCHES = {"bwd_preprocess": 3}
 
 
 def kernel_alg_flops_per_pair(name, d, dv):
-    """Algorithmic FLOPs per unmasked pair credited to each kernel.  The
-    key-side kernel does the S/dP recomputation and the dK/dV products the
-    backward needs once; the query-side kernel is credited with dQ only (its S
-    and dP are a second recomputation).  Where the key side runs as two passes
-    (d = dv = 256), the dV pass is credited with S and dV, the dK pass with dP
-    and dK (its S is a recomputation), so the two add up to the one kernel.
-    The fused key-side kernel does every product of the backward once."""
-    return {"fwd": 2 * (d + dv), "bwd_dkdv": 2 * (2 * d + 2 * dv), "bwd_dq": 2 * d,
-            "bwd_dkdv_dv": 2 * d + 2 * dv, "bwd_dkdv_dk": 2 * dv + 2 * d,
-            "bwd_dkdvq": 2 * (3 * d + 2 * dv)}.get(name, 0)
+    """Algorithmic FLOPs per unmasked pair credited to each kernel launch.
+    The one-pass backward kernel does every product of the backward once:
+    2(3d + 2dv).  The split backward's single launch does the key side (S, dV,
+    dP, dK) and the query side, credited with dQ only (its S and dP are a
+    second recomputation): the same total.  Where the key side runs as two
+    passes (d = dv = 256), the separate dV pass is credited with S and dV, and
+    the launch that holds the dK pass and the query side with dP, dK and dQ,
+    so the two add up to the one kernel."""
+    return {"fwd": 2 * (d + dv), "bwd_dkdvq": 2 * (3 * d + 2 * dv),
+            "bwd_split": 2 * (2 * d + 2 * dv) + 2 * d,
+            "bwd_dkdv_dv": 2 * d + 2 * dv, "bwd_split_dk": 2 * dv + 2 * d + 2 * d}.get(name, 0)
 
 
 def setup(cfg, seed, device):

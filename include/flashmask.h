@@ -70,7 +70,9 @@ typedef struct {
 } fm_problem;
 
 /* Options.  deterministic: the backward adds every partial sum in a fixed
- * order, so dQ/dK/dV are bit-identical from run to run.  wait_timeout_ns
+ * order, so dQ/dK/dV are bit-identical from run to run (without it, at
+ * d = dv <= 128, dQ is summed over key tiles with fp32 reductions whose order
+ * varies, and its last bits with it).  wait_timeout_ns
  * bounds every wait on the device; 0 selects 1 s.
  * debug_bounds (0 or 1): before the attention kernels, a check kernel reads
  * every work list in the workspace: each list's length must lie in [0, T]
@@ -108,11 +110,14 @@ typedef struct {
  * cudaEvent_t handles owned by the caller.  The call records
  * kernel_events[2i] on `stream` just before its i-th kernel launch and
  * kernel_events[2i+1] just after it.  Events beyond the array are skipped.
- * Kernel order: fwd = classify, lists, attention; bwd = classify, lists,
- * preprocess, key-side gradient (twice when d = dv = 256), query-side gradient.
- * The backward's preprocess step is three launches under one event pair: the
- * largest |dO| and |V| per row tile, their per-(batch, head) scales, then D,
- * the log2 LSE and the scaled fp16 copies of dO and V.
+ * Kernel order: fwd = classify, lists, attention.  bwd = classify, lists,
+ * the preprocess step, then: without the deterministic mode at d = dv <= 128,
+ * the one-pass gradient kernel (dK, dV, and dQ sums in fp32) and the dQ
+ * conversion; otherwise one launch of the key-side and query-side gradient
+ * kernels (at d = dv = 256 after a separate dV pass of the key side).  The
+ * preprocess step is three launches under one event pair: the largest |dO|
+ * and |V| per row tile, their per-(batch, head) scales, then D, the log2 LSE
+ * and the scaled fp16 copies of dO (and of V for the split kernels).
  * accumulate_f32 (0 or 1, flashmask_bwd only): dq, dk and dv are fp32 arrays
  * of the same shapes ([B,N,H,d], [B,N,H,d], [B,N,H,dv]), and the backward adds
  * its gradients to them in fp32 instead of writing bf16 (each element is

@@ -449,18 +449,14 @@ struct DqCfg {
     static_assert((D / 32) % NWG == 0, "epilogue column split");
 };
 
+// The query-side work for query tile qt_ of (batch b_, head h_); runs in the
+// split backward's single launch (split_bwd_kernel).
 template <class C, bool ACC32>
-__global__ void __launch_bounds__(C::THREADS, 1)
-    dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-              const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-              const __grid_constant__ CUtensorMap tm_dq, const BwdParams p) {
-    extern __shared__ __align__(1024) uint8_t smem[];
-    // Launched behind the key-side kernel.  The lists, LSE2, D and the fp16
-    // copies it reads were written before that kernel, but a grid sees another
-    // grid's writes only once it has executed griddepcontrol.wait itself: it
-    // waits here, before any read (its CTAs still launch during the key-side
-    // kernel's tail and hide their launch latency).
-    pdl_wait();
+__device__ __forceinline__ void dq_body(uint8_t *smem, const CUtensorMap &tm_q,
+                                        const CUtensorMap &tm_k, const CUtensorMap &tm_v,
+                                        const CUtensorMap &tm_do, const CUtensorMap &tm_dq,
+                                        const BwdParams &p, int qt_, int h_, int b_) {
+    pdl_wait();  // lists, LSE2, D and the fp16 copies of the kernels before
     pdl_trigger();
     if (smem_u32(smem) & 1023u) {  // swizzled tiles need 1024-byte alignment
         if (threadIdx.x == 0) atomicExch(&g_err_bwd, ERR_SMEM_ALIGN);
@@ -479,8 +475,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     int *issued = reinterpret_cast<int *>(smem + C::OFF_MISC + 8);  // loads per ring
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int qt = p.T - 1 - static_cast<int>(blockIdx.x);
-    const int h = blockIdx.y, b = blockIdx.z;
+    const int qt = qt_;
+    const int h = h_, b = b_;
     const int bm = b * p.Hm + (p.Hm == 1 ? 0 : h);
     const int n_entries = p.cnt[static_cast<size_t>(bm) * p.T + qt];
     const int *entries = p.list + (static_cast<size_t>(bm) * p.T + qt) * p.T;
@@ -974,13 +970,14 @@ struct DkdvCfg {
     static_assert(DQ_TMA_COLS % 32 == 0 && DQ_TMA_COLS <= D, "dQ columns staged in 32s");
 };
 
+// The key-side work for key tile kt_ of (batch b_, head h_): the body of
+// dkdv_kernel and of the key-side part of split_bwd_kernel.
 template <class C, bool ACC32>
-__global__ void __launch_bounds__(C::THREADS, 1)
-    dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_dv,
-                const BwdParams p) {
-    extern __shared__ __align__(1024) uint8_t smem[];
+__device__ __forceinline__ void dkdv_body(uint8_t *smem, const CUtensorMap &tm_q,
+                                          const CUtensorMap &tm_k, const CUtensorMap &tm_v,
+                                          const CUtensorMap &tm_do, const CUtensorMap &tm_dk,
+                                          const CUtensorMap &tm_dv, const BwdParams &p, int kt_,
+                                          int h_, int b_) {
     pdl_wait();  // lists, LSE2, D and the fp16 copies of the kernels before
     pdl_trigger();
     if (smem_u32(smem) & 1023u) {  // swizzled tiles need 1024-byte alignment
@@ -1003,8 +1000,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     int *issued = reinterpret_cast<int *>(smem + C::OFF_MISC + 8);  // loads per ring
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int kt = blockIdx.x;
-    const int h = blockIdx.y, b = blockIdx.z;
+    const int kt = kt_;
+    const int h = h_, b = b_;
     const int bm = b * p.Hm + (p.Hm == 1 ? 0 : h);
     const int n_entries = p.cnt[static_cast<size_t>(bm) * p.T + kt];
     const int *entries = p.list + (static_cast<size_t>(bm) * p.T + kt) * p.T;
@@ -1590,6 +1587,49 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     }
 }
 
+// One key tile per CTA: grid (T, H, B).
+template <class C, bool ACC32>
+__global__ void __launch_bounds__(C::THREADS, 1)
+    dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_dv,
+                const BwdParams p) {
+    extern __shared__ __align__(1024) uint8_t smem[];
+    dkdv_body<C, ACC32>(smem, tm_q, tm_k, tm_v, tm_do, tm_dk, tm_dv, p, blockIdx.x, blockIdx.y,
+                        blockIdx.z);
+}
+
+// The split backward (deterministic mode, d >= 192) as one launch: CTAs
+// [0, T H B) take the key side (key tile fastest, then head, then batch), the
+// rest the query side (heaviest query tiles first).  One griddepcontrol.wait
+// orders both after the kernels before, and the query-side CTAs, last in block
+// order, start on the SMs the key side's tail frees.
+template <class KV, class DQ, bool ACC32>
+__global__ void __launch_bounds__(KV::THREADS, 1)
+    split_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                     const __grid_constant__ CUtensorMap tm_dk,
+                     const __grid_constant__ CUtensorMap tm_dv,
+                     const __grid_constant__ CUtensorMap tm_q_dq,
+                     const __grid_constant__ CUtensorMap tm_k_dq,
+                     const __grid_constant__ CUtensorMap tm_v_dq,
+                     const __grid_constant__ CUtensorMap tm_do_dq,
+                     const __grid_constant__ CUtensorMap tm_dq, const BwdParams pkv,
+                     const BwdParams pdq) {
+    static_assert(KV::THREADS == DQ::THREADS, "one block shape for both roles");
+    extern __shared__ __align__(1024) uint8_t smem[];
+    const int half = static_cast<int>(gridDim.x) / 2;  // T H B CTAs per role
+    const int c = static_cast<int>(blockIdx.x);
+    const int TH = pkv.T * pkv.H;
+    if (c < half)
+        dkdv_body<KV, ACC32>(smem, tm_q, tm_k, tm_v, tm_do, tm_dk, tm_dv, pkv, c % pkv.T,
+                             (c / pkv.T) % pkv.H, c / TH);
+    else
+        dq_body<DQ, ACC32>(smem, tm_q_dq, tm_k_dq, tm_v_dq, tm_do_dq, tm_dq, pdq,
+                           pdq.T - 1 - (c - half) % pdq.T, ((c - half) / pdq.T) % pdq.H,
+                           (c - half) / TH);
+}
+
 BwdParams make_params(const Geometry &g, const Workspace &ws, const BwdArgs &a, bool dq_side) {
     BwdParams p;
     p.vec = ws.vec;
@@ -1618,20 +1658,6 @@ BwdParams make_params(const Geometry &g, const Workspace &ws, const BwdArgs &a, 
 }
 
 template <class C>
-cudaError_t launch_dq(const Geometry &g, const Workspace &ws, const BwdArgs &a, cudaStream_t st) {
-    if (a.dq_k_rows != C::BN) return cudaErrorInvalidValue;  // map boxes must match the tile
-    // fp32 accumulation is a separate instantiation: its epilogue would add
-    // registers to kernels that sit at their register cap.
-    auto kern = g.acc32 ? dq_kernel<C, true> : dq_kernel<C, false>;
-    cudaError_t e =
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    return launch_pdl(kern, dim3(g.T, g.H, g.B), dim3(C::THREADS), C::SMEM_BYTES, st,
-                      *a.tm_q_dq, *a.tm_k_dq, *a.tm_v_dq, *a.tm_do_dq, *a.tm_dq_out,
-                      make_params(g, ws, a, true));
-}
-
-template <class C>
 cudaError_t launch_dkdv(const Geometry &g, const Workspace &ws, const BwdArgs &a,
                         cudaStream_t st) {
     if (a.kv_q_rows != C::BM) return cudaErrorInvalidValue;  // map boxes must match the tile
@@ -1647,12 +1673,17 @@ cudaError_t launch_dkdv(const Geometry &g, const Workspace &ws, const BwdArgs &a
 template <class KV, class DQ>
 cudaError_t launch_pair(const Geometry &g, const Workspace &ws, const BwdArgs &a, cudaStream_t st,
                         Recorder &rec) {
-    rec.before(st);
-    cudaError_t e = launch_dkdv<KV>(g, ws, a, st);
-    rec.after(st);
+    if (a.kv_q_rows != KV::BM || a.dq_k_rows != DQ::BN)
+        return cudaErrorInvalidValue;  // map boxes must match the tiles
+    auto kern = g.acc32 ? split_bwd_kernel<KV, DQ, true> : split_bwd_kernel<KV, DQ, false>;
+    constexpr int SMEM = KV::SMEM_BYTES > DQ::SMEM_BYTES ? KV::SMEM_BYTES : DQ::SMEM_BYTES;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
     if (e != cudaSuccess) return e;
     rec.before(st);
-    e = launch_dq<DQ>(g, ws, a, st);
+    e = launch_pdl(kern, dim3(2 * g.T * g.H * g.B), dim3(KV::THREADS), SMEM, st, *a.tm_q, *a.tm_k,
+                   *a.tm_v, *a.tm_do, *a.tm_dk_out, *a.tm_dv_out, *a.tm_q_dq, *a.tm_k_dq,
+                   *a.tm_v_dq, *a.tm_do_dq, *a.tm_dq_out, make_params(g, ws, a, false),
+                   make_params(g, ws, a, true));
     rec.after(st);
     return e;
 }

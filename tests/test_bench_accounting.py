@@ -37,10 +37,9 @@ def test_kernel_credits_add_up(d, dv, det):
     fwd_names, bwd_names = bench.kernel_names(d, dv, det)
     assert sum(credit(n) for n in fwd_names) == f["fwd"]
     assert sum(credit(n) for n in bwd_names) == f["bwd"]
-    # the two-pass key side is credited exactly like the one-pass kernel
-    assert credit("bwd_dkdv_dv") + credit("bwd_dkdv_dk") == credit("bwd_dkdv")
-    # the fused pass is the key side and the query side's dQ together
-    assert credit("bwd_dkdvq") == credit("bwd_dkdv") + credit("bwd_dq")
+    # every form of the backward is credited with the same products
+    assert credit("bwd_dkdv_dv") + credit("bwd_split_dk") == credit("bwd_split")
+    assert credit("bwd_dkdvq") == credit("bwd_split")
 
 
 def test_kernel_names_follow_the_backward_variant():
@@ -51,10 +50,10 @@ def test_kernel_names_follow_the_backward_variant():
             assert bwd[0] == "bwd_preprocess"
             if fused:
                 assert bwd[1:] == ["bwd_dkdvq", "bwd_dq_convert"]
-                continue
-            split = "bwd_dkdv_dv" in bwd
-            assert split == (d == 256 and dv == 256)
-            assert bwd[-1] == "bwd_dq"
+            elif d == 256 and dv == 256:
+                assert bwd[1:] == ["bwd_dkdv_dv", "bwd_split_dk"]
+            else:
+                assert bwd[1:] == ["bwd_split"]
 
 
 def test_workload_overrides():
