@@ -259,10 +259,14 @@ __global__ void __launch_bounds__(256) preprocess_kernel(
             }
         }
     }
-    // fused dQ: the row's entries of the fp32 buffer [B*H][d/4][Npad] start at 0
-    if (dqacc && valid)
-        for (int c4 = t; c4 < dq4; c4 += 16)
-            dqacc[(static_cast<size_t>(bh) * dq4 + c4) * Npad + i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    // fused dQ: the fp32 buffer [B*H][d/4][Npad] starts at 0.  Each block zeroes
+    // one contiguous piece of 16 d/4 float4 (the grid, rows_total / 16 blocks,
+    // covers it exactly): full lines in address order, which the row-wise
+    // pattern (16 bytes in each of d/4 columns) did not give.
+    if (dqacc) {
+        float4 *z = dqacc + static_cast<size_t>(blockIdx.x) * 16 * dq4;
+        for (int k = threadIdx.x; k < 16 * dq4; k += 256) z[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
 #pragma unroll
     for (int off = 8; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off, 16);
     float sink_term = 0.f;  // the row's term of the sink-logit gradient
