@@ -159,7 +159,7 @@ __global__ void __launch_bounds__(128) classify_kernel(
 //   length of that union, ties by index (the forward hands them out heaviest
 //   first).  Its warps count the union lengths from the tile map themselves,
 //   so the job needs no other block's output.
-__global__ void __launch_bounds__(1024) fwd_lists_kernel(int N, int T, int rows, int pair_rows,
+__global__ void __launch_bounds__(1024, 1) fwd_lists_kernel(int N, int T, int rows, int pair_rows,
                                                          int list_blocks,
                                                          const uint8_t *__restrict__ cls,
                                                          int *__restrict__ fwd_list,
