@@ -235,6 +235,15 @@ __global__ void __launch_bounds__(256) preprocess_kernel(
     const int r = valid ? r0 : 0;
     const int bh = r / Npad, i = r % Npad;
     const int b = bh / H, h = bh % H;
+    // fused dQ: the fp32 buffer [B*H][d/4][Npad] starts at 0.  Each block zeroes
+    // one contiguous piece of 16 d/4 float4 (the grid, rows_total / 16 blocks,
+    // covers it exactly): full lines in address order, issued before the loads.
+    if (dqacc) {
+        float4 *z = dqacc + static_cast<size_t>(blockIdx.x) * 16 * dq4;
+        for (int k = threadIdx.x; k < 16 * dq4; k += 256) z[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    // the row's LSE, loaded with the rest rather than after the row sum
+    const float l_row = (valid && t == 0 && i < N) ? lse[static_cast<size_t>(bh) * N + i] : 0.f;
     float acc = 0.f;
     const float4 sc = scales[bh];
     const float sc_o = sc.x, sc_v = sc.y;
@@ -259,21 +268,13 @@ __global__ void __launch_bounds__(256) preprocess_kernel(
             }
         }
     }
-    // fused dQ: the fp32 buffer [B*H][d/4][Npad] starts at 0.  Each block zeroes
-    // one contiguous piece of 16 d/4 float4 (the grid, rows_total / 16 blocks,
-    // covers it exactly): full lines in address order, which the row-wise
-    // pattern (16 bytes in each of d/4 columns) did not give.
-    if (dqacc) {
-        float4 *z = dqacc + static_cast<size_t>(blockIdx.x) * 16 * dq4;
-        for (int k = threadIdx.x; k < 16 * dq4; k += 256) z[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-    }
 #pragma unroll
     for (int off = 8; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off, 16);
     float sink_term = 0.f;  // the row's term of the sink-logit gradient
     if (valid && t == 0) {
         float l2 = INFINITY;
         if (i < N) {
-            const float l = lse[static_cast<size_t>(bh) * N + i];
+            const float l = l_row;
             l2 = (l == -INFINITY) ? INFINITY : l * 1.4426950408889634f;
             if (sink && l != -INFINITY) sink_term = -expf(sink[h] - l) * acc;
         }

@@ -798,7 +798,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         }
         for (int g = 0; g < 2; ++g) {
             mbar_init(&s_full[g], 1);
-            mbar_init(&p_full[g], 128);
+            mbar_init(&p_full[g], 4);  // one arrival per softmax warp
             mbar_init(&o_done[g], 1);
         }
         mbar_init(mma_idle, 1);
@@ -993,9 +993,12 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 failed = true;
                 break;
             }
+            // Every lane's P stores have landed (wait::st) and are fenced; one
+            // lane per warp arrives for the warp, after the warp converges.
             tmem_st_wait();
             tc_fence_before();
-            mbar_arrive(&p_full[wg]);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&p_full[wg]);
         }
 
         // ------------------------------------------------------- epilogue
