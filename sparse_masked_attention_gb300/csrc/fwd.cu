@@ -813,6 +813,18 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 for (int c = 0; c < C::D / 64; ++c)
                     tma_load_4d(sQ + g * C::Q_BYTES + c * C::BM * 128, &tm_q, q_full, c * 64, h,
                                 (2 * pp + g) * TILE, b);
+            // the first K and V tiles too (unless the test drops that K load)
+            const int key0 = (entries[0] >> 2) * TILE;
+            if (p.drop_load != 1) {
+                mbar_arrive_expect_tx(&k_full[0], C::K_BYTES);
+#pragma unroll
+                for (int c = 0; c < C::D / 64; ++c)
+                    tma_load_4d(sK + c * C::BN * 128, &tm_k, &k_full[0], c * 64, h, key0, b);
+            }
+            mbar_arrive_expect_tx(&v_full[0], C::V_BYTES);
+#pragma unroll
+            for (int c = 0; c < C::DV / 64; ++c)
+                tma_load_4d(sV + c * C::BN * 128, &tm_v, &v_full[0], c * 64, h, key0, b);
         }
     }
     if (warp == 1) {
@@ -833,7 +845,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             // failure-detection test only: this K load is never issued
             const int skip = is_k ? p.drop_load - 1 : -1;
             if (is_k) prefetch_tmap(&tm_k); else prefetch_tmap(&tm_v);
-            int j = 0;
+            int j = 1;  // tile 0 was loaded before the CTA-wide barrier
             for (; j < n; ++j) {
                 const int s = j % S;
                 uint64_t *full = is_k ? &k_full[s] : &v_full[s];
