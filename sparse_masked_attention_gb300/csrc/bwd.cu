@@ -946,8 +946,8 @@ struct DkdvCfg {
     static constexpr bool Q_BY_REDUCER = DQ_TMA_COLS > 0;  // Q stages freed by the reducer
     // kv_full, q_full[QS], q_empty[QS], o_full[NWG], o_empty[NWG],
     // s_full[NWG], p_full[NWG], dp_full[NWG], ds_full[NWG], done, v_ready,
-    // FDQ: dq_full[NWG], dq_free[NWG], staged[NWG], red_done
-    static constexpr int NBAR = 1 + 2 * QS + 6 * NWG + 2 + (FDQ ? 3 * NWG + 1 : 0);
+    // FDQ: dq_full[NWG], dq_free[NWG], staged[NWG]
+    static constexpr int NBAR = 1 + 2 * QS + 6 * NWG + 2 + (FDQ ? 3 * NWG : 0);
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int SMEM_BYTES = OFF_MISC + 16;
     static constexpr int TM_DK = 0;
@@ -973,6 +973,9 @@ struct DkdvCfg {
                   "fused dQ: one pass, 128-query sub-tiles, dQ tile within a group region");
     static_assert(OFF_DS % 1024 == 0, "swizzled dS tiles need 1024-byte alignment");
     static_assert(DQ_TMA_COLS % 32 == 0 && DQ_TMA_COLS <= D, "dQ columns staged in 32s");
+    static_assert(!FDQ || NWG * DO_BYTES >= (D / 64 + DV / 64) * 128 * 128,
+                  "fused dQ: dK and dV staging fits the dO stages");
+    static_assert(OFF_DO % 1024 == 0, "swizzled staging needs 1024-byte alignment");
 };
 
 // The key-side work for key tile kt_ of (batch b_, head h_): the body of
@@ -998,7 +1001,7 @@ __device__ __forceinline__ void dkdv_body(uint8_t *smem, const CUtensorMap &tm_q
              *ds_full = dp_full + C::NWG, *done = ds_full + C::NWG;
     uint64_t *v_ready = done + 1;
     uint64_t *dq_full = v_ready + 1, *dq_free = dq_full + C::NWG;  // FDQ only
-    uint64_t *staged = dq_free + C::NWG, *red_done = staged + C::NWG;  // FDQ only
+    uint64_t *staged = dq_free + C::NWG;  // FDQ only
     uint8_t *sDS = C::DS_IN_DO ? sDO : smem + C::OFF_DS;             // FDQ only
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
     volatile int *abort = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
@@ -1040,7 +1043,6 @@ __device__ __forceinline__ void dkdv_body(uint8_t *smem, const CUtensorMap &tm_q
                 mbar_init(&dq_free[i], 128);
                 mbar_init(&staged[i], 128);
             }
-            mbar_init(red_done, 1);
         }
         *abort = 0;
         fence_barrier_init();
@@ -1127,8 +1129,7 @@ __device__ __forceinline__ void dkdv_body(uint8_t *smem, const CUtensorMap &tm_q
                 bulk_wait_read_all();
                 mbar_arrive(&q_empty[u % C::QS]);
             }
-            bulk_wait_all();
-            mbar_arrive(red_done);
+            bulk_wait_all();  // the reductions' global writes, before the CTA exits
         }
     } else if (warp == 1) {
         if (lane == 0 && n > 0) {
@@ -1494,8 +1495,6 @@ __device__ __forceinline__ void dkdv_body(uint8_t *smem, const CUtensorMap &tm_q
             }
         }
         if (n > 0) warp_wait(done, 0, tmo, abort);
-        // the epilogue stages dK and dV over the Q ring: the reducer must be done
-        if (C::Q_BY_REDUCER && n > 0) warp_wait(red_done, 0, tmo, abort);
         tc_fence_after();
         // dK (times scale / (s_o s_v)) and dV (times 1 / s_o): added to the fp32
         // outputs (acc32), or as bf16 to the 128B-swizzled layouts of the output
@@ -1527,8 +1526,11 @@ __device__ __forceinline__ void dkdv_body(uint8_t *smem, const CUtensorMap &tm_q
                 }
             }
         } else {
-            uint8_t *stage_dk = sQ;
-            uint8_t *stage_dv = sQ + (C::DO_DK ? C::D / 64 : 0) * (128 * 128);
+            // Staging: the Q ring, or (fused dQ) the dO stages, spent once every
+            // MMA ran (their dS tiles included), while the dQ reducer may still
+            // be reading its last tile from the Q ring.
+            uint8_t *stage_dk = C::FDQ ? sDO : sQ;
+            uint8_t *stage_dv = stage_dk + (C::DO_DK ? C::D / 64 : 0) * (128 * 128);
             if constexpr (C::DO_DK) {
                 constexpr int CPW = (C::D / 32) / C::NWG;
 #pragma unroll 1
