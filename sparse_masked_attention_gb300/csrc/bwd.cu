@@ -324,7 +324,7 @@ __global__ void __launch_bounds__(256) sink_grad_kernel(int B, int H, int blocks
 // A CTA takes 32 rows of one (batch, head): coalesced float4 reads down the
 // buffer's columns into a padded shared tile, then coalesced 16-byte writes
 // along the output rows.
-constexpr int CONV_ROWS = 32;
+constexpr int CONV_ROWS = 16;
 
 template <bool ACC32, int D>
 __global__ void __launch_bounds__(256) dq_convert_kernel(int N, int H, int Npad,
