@@ -321,7 +321,7 @@ __global__ void __launch_bounds__(256) sink_grad_kernel(int B, int H, int blocks
 
 // Fused dQ: the fp32 buffer [B*H][d/4][Npad] (float4) to dQ [B, N, H, d] bf16,
 // times scale / (s_o s_v); or (ACC32) added to an fp32 dQ of that layout.
-// A CTA takes 32 rows of one (batch, head): coalesced float4 reads down the
+// A CTA takes CONV_ROWS rows of one (batch, head): coalesced float4 reads down the
 // buffer's columns into a padded shared tile, then coalesced 16-byte writes
 // along the output rows.
 constexpr int CONV_ROWS = 16;
@@ -1498,8 +1498,9 @@ __device__ __forceinline__ void dkdv_body(uint8_t *smem, const CUtensorMap &tm_q
         tc_fence_after();
         // dK (times scale / (s_o s_v)) and dV (times 1 / s_o): added to the fp32
         // outputs (acc32), or as bf16 to the 128B-swizzled layouts of the output
-        // maps in the idle Q ring and dO stages, then TMA stores of their
-        // 64-column boxes (rows past N clipped).
+        // maps in idle shared memory (the Q ring, or with fused dQ the dO
+        // stages), then TMA stores of their 64-column boxes (rows past N
+        // clipped).
         const float4 sc = p.scales[bh];
         if constexpr (ACC32) {
             // fp32 accumulation: each key row adds its own values (rows past N

@@ -10,7 +10,8 @@
 // - fwd_kernel (larger heads): one CTA per query tile; with two groups they
 //   take alternate key tiles of that tile and merge their halves at the end.
 // Roles, by warp:
-//   warp 0      TMA producers: lane 0 Q and the K ring, lane 1 the V ring
+//   warp 0      TMA producers: lane 0 Q (and, in the pair kernel, the first K
+//               and V tiles) and the K ring, lane 1 the V ring
 //   warp 1      allocates TMEM; lane 0 issues every tcgen05.mma
 //   warps 2..   softmax warpgroups.  Thread t of a group owns query row t,
 //               which is TMEM lane t.
