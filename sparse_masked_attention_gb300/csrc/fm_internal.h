@@ -61,6 +61,16 @@ struct Workspace {
 // The backward reduces dQ inside its key-side kernel (one pass, fp32 red.add
 // into Workspace::dqacc) at d = dv <= 128 unless the deterministic mode asks
 // for the atomic-free split (key side, then query side).
+// SMs of the current device: with one resident CTA per SM, a kernel's next
+// wave starts this many blocks later.  0 when it cannot be read.
+inline int current_sm_count() {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return 0;
+    return sms;
+}
+
 inline bool fused_dq(const Geometry &g) {
     return !g.deterministic && g.d == g.dv && g.d <= 128;
 }

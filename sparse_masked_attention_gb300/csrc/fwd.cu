@@ -47,6 +47,8 @@ struct FwdParams {
     float sl2;  // scale * log2(e)
     uint64_t timeout_ns;
     int drop_load;  // failure-detection test: k > 0 skips the k-th K load (pair kernel)
+    int next_stride;  // pair kernel: the CTA this many blocks later gets its first tiles
+                      // prefetched into L2 (0: off)
 };
 
 template <int D_, int DV_, int BN_, int NWG_, int NSB_, int KS_, int VS_>
@@ -694,6 +696,7 @@ cudaError_t launch_cfg(const Geometry &g, const Workspace &ws, const FwdArgs &a,
     p.sl2 = g.scale * 1.4426950408889634f;
     p.timeout_ns = g.timeout_ns;
     p.drop_load = g.drop_load;
+    p.next_stride = 0;
     if (a.k_rows != C::BN) return cudaErrorInvalidValue;  // map boxes must match the tile
     auto kern = fwd_kernel<C>;
     cudaError_t e =
@@ -869,6 +872,32 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 }
             }
             issued[is_k ? 0 : 1] = j;
+            // Its last K load issued, this CTA has a few key tiles left: the
+            // CTA about one wave later (about when this one ends) gets its two
+            // Q tiles and its first K and V tiles prefetched into L2, so that
+            // it starts on L2 latency (8K causal-document forward 0.8 % faster,
+            // 32K block-sparse 0.5 % slower).
+            const int nx = static_cast<int>(blockIdx.x) + p.next_stride;
+            if (is_k && p.next_stride > 0 && nx < static_cast<int>(gridDim.x)) {
+                const int hb2 = nx % (p.H * p.B);
+                const int h2 = hb2 % p.H, b2 = hb2 / p.H;
+                const int bm2 = b2 * p.Hm + (p.Hm == 1 ? 0 : h2);
+                const int pp2 = p.order[static_cast<size_t>(bm2) * TP + nx / (p.H * p.B)];
+#pragma unroll
+                for (int g = 0; g < 2; ++g)
+                    if (2 * pp2 + g < p.T)
+#pragma unroll
+                        for (int c = 0; c < C::D / 64; ++c)
+                            tma_prefetch_l2_4d(&tm_q, c * 64, h2, (2 * pp2 + g) * TILE, b2);
+                const size_t r2 = static_cast<size_t>(bm2) * TP + pp2;
+                if (p.cnt[r2] > 0) {
+                    const int k2 = (p.list[r2 * p.T] >> 2) * TILE;
+#pragma unroll
+                    for (int c = 0; c < C::D / 64; ++c) tma_prefetch_l2_4d(&tm_k, c * 64, h2, k2, b2);
+#pragma unroll
+                    for (int c = 0; c < C::DV / 64; ++c) tma_prefetch_l2_4d(&tm_v, c * 64, h2, k2, b2);
+                }
+            }
         }
     } else if (warp == 1) {
         // --------------------------------------------------- tcgen05 issuer
@@ -1103,6 +1132,7 @@ cudaError_t launch_pair(const Geometry &g, const Workspace &ws, const FwdArgs &a
     p.sl2 = g.scale * 1.4426950408889634f;
     p.timeout_ns = g.timeout_ns;
     p.drop_load = g.drop_load;
+    p.next_stride = current_sm_count();
     if (a.k_rows != C::BN) return cudaErrorInvalidValue;  // map boxes must match the tile
     auto kern = fwd_pair_kernel<C>;
     cudaError_t e =
