@@ -58,9 +58,6 @@ struct Workspace {
     float4 *dqacc;     // fused backward: fp32 dQ sums [B*H][d/4][Npad] (float4)
 };
 
-// The backward reduces dQ inside its key-side kernel (one pass, fp32 red.add
-// into Workspace::dqacc) at d = dv <= 128 unless the deterministic mode asks
-// for the atomic-free split (key side, then query side).
 // SMs of the current device: with one resident CTA per SM, a kernel's next
 // wave starts this many blocks later.  0 when it cannot be read.
 inline int current_sm_count() {
@@ -71,6 +68,9 @@ inline int current_sm_count() {
     return sms;
 }
 
+// The backward reduces dQ inside its key-side kernel (one pass, fp32 red.add
+// into Workspace::dqacc) at d = dv <= 128 unless the deterministic mode asks
+// for the atomic-free split (key side, then query side).
 inline bool fused_dq(const Geometry &g) {
     return !g.deterministic && g.d == g.dv && g.d <= 128;
 }
