@@ -729,9 +729,9 @@ struct PairCfg {
     static constexpr int OFF_K = OFF_Q + 2 * Q_BYTES;
     static constexpr int OFF_V = OFF_K + KS * K_BYTES;
     static constexpr int OFF_BAR = OFF_V + VS * V_BYTES;
-    // q_full, k_full[KS], k_empty[KS], v_full[VS], v_empty[VS], s_full[2],
+    // q_full[2], k_full[KS], k_empty[KS], v_full[VS], v_empty[VS], s_full[2],
     // p_full[2], o_done[2], mma_idle
-    static constexpr int NBAR = 1 + 2 * KS + 2 * VS + 7;
+    static constexpr int NBAR = 2 + 2 * KS + 2 * VS + 7;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int SMEM_BYTES = OFF_MISC + 16;
     static constexpr int TM_O = 0;
@@ -762,8 +762,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     uint8_t *sK = smem + C::OFF_K;
     uint8_t *sV = smem + C::OFF_V;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
-    uint64_t *q_full = bars;
-    uint64_t *k_full = q_full + 1;
+    uint64_t *q_full = bars;  // per group
+    uint64_t *k_full = q_full + 2;
     uint64_t *k_empty = k_full + C::KS;
     uint64_t *v_full = k_empty + C::KS;
     uint64_t *v_empty = v_full + C::VS;
@@ -791,7 +791,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     const uint64_t tmo = p.timeout_ns;
 
     if (threadIdx.x == 0) {
-        mbar_init(q_full, 1);
+        mbar_init(&q_full[0], 1);
+        mbar_init(&q_full[1], 1);
         for (int i = 0; i < C::KS; ++i) {
             mbar_init(&k_full[i], 1);
             mbar_init(&k_empty[i], 2);
@@ -810,13 +811,15 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         issued[0] = issued[1] = 0;
         fence_barrier_init();
         if (n > 0) {  // both Q tiles before the CTA-wide barrier: latency overlaps the setup
-            mbar_arrive_expect_tx(q_full, 2 * C::Q_BYTES);
+            // a barrier per group: group 0's first S need not wait for Q_1
 #pragma unroll
-            for (int g = 0; g < 2; ++g)
+            for (int g = 0; g < 2; ++g) {
+                mbar_arrive_expect_tx(&q_full[g], C::Q_BYTES);
 #pragma unroll
                 for (int c = 0; c < C::D / 64; ++c)
-                    tma_load_4d(sQ + g * C::Q_BYTES + c * C::BM * 128, &tm_q, q_full, c * 64, h,
-                                (2 * pp + g) * TILE, b);
+                    tma_load_4d(sQ + g * C::Q_BYTES + c * C::BM * 128, &tm_q, &q_full[g], c * 64,
+                                h, (2 * pp + g) * TILE, b);
+            }
             // the first K and V tiles too (unless the test drops that K load)
             const int key0 = (entries[0] >> 2) * TILE;
             if (p.drop_load != 1) {
@@ -930,11 +933,11 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     mma_ts(o_tmem, p_tmem + k * 8, vsd + ((k * 2048) >> 4), IDESC_PV,
                            (j > 0 || k > 0) ? 1u : 0u);
             };
-            bool ok = mbar_wait(q_full, 0, tmo, abort, &g_err_fwd) &&
-                      mbar_wait(&k_full[0], 0, tmo, abort, &g_err_fwd);
-            if (ok) {
-                tc_fence_after();
-                for (int g = 0; g < 2; ++g) {
+            bool ok = mbar_wait(&k_full[0], 0, tmo, abort, &g_err_fwd);
+            for (int g = 0; g < 2 && ok; ++g) {
+                ok = mbar_wait(&q_full[g], 0, tmo, abort, &g_err_fwd);
+                if (ok) {
+                    tc_fence_after();
                     issue_s(g, 0);
                     mma_commit(&s_full[g]);
                 }
@@ -1100,7 +1103,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         if (threadIdx.x == 0 && n > 0) {
             drain_ring(k_full, C::KS, issued[0], p.drop_load - 1, tmo, &g_err_fwd);
             drain_ring(v_full, C::VS, issued[1], -1, tmo, &g_err_fwd);
-            mbar_wait_drain(q_full, 0, tmo, &g_err_fwd);
+            mbar_wait_drain(&q_full[0], 0, tmo, &g_err_fwd);
+            mbar_wait_drain(&q_full[1], 0, tmo, &g_err_fwd);
             mbar_wait_drain(mma_idle, 0, tmo, &g_err_fwd);
         }
         __syncthreads();
