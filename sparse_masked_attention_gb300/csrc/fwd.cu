@@ -811,7 +811,9 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         issued[0] = issued[1] = 0;
         fence_barrier_init();
         if (n > 0) {  // both Q tiles before the CTA-wide barrier: latency overlaps the setup
-            // a barrier per group: group 0's first S need not wait for Q_1
+            // a barrier per group: group 0's first S need not wait for Q_1;
+            // issued Q_0, K_0, Q_1, V_0, in the order the first MMAs need them
+            const int key0 = (entries[0] >> 2) * TILE;
 #pragma unroll
             for (int g = 0; g < 2; ++g) {
                 mbar_arrive_expect_tx(&q_full[g], C::Q_BYTES);
@@ -819,14 +821,13 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 for (int c = 0; c < C::D / 64; ++c)
                     tma_load_4d(sQ + g * C::Q_BYTES + c * C::BM * 128, &tm_q, &q_full[g], c * 64,
                                 h, (2 * pp + g) * TILE, b);
-            }
-            // the first K and V tiles too (unless the test drops that K load)
-            const int key0 = (entries[0] >> 2) * TILE;
-            if (p.drop_load != 1) {
-                mbar_arrive_expect_tx(&k_full[0], C::K_BYTES);
+                // the first K tile (unless the test drops that load)
+                if (g == 0 && p.drop_load != 1) {
+                    mbar_arrive_expect_tx(&k_full[0], C::K_BYTES);
 #pragma unroll
-                for (int c = 0; c < C::D / 64; ++c)
-                    tma_load_4d(sK + c * C::BN * 128, &tm_k, &k_full[0], c * 64, h, key0, b);
+                    for (int c = 0; c < C::D / 64; ++c)
+                        tma_load_4d(sK + c * C::BN * 128, &tm_k, &k_full[0], c * 64, h, key0, b);
+                }
             }
             mbar_arrive_expect_tx(&v_full[0], C::V_BYTES);
 #pragma unroll
