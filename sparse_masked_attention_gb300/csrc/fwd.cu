@@ -784,10 +784,13 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     const int bm = b * p.Hm + (p.Hm == 1 ? 0 : h);
     const int pp = p.order[static_cast<size_t>(bm) * TP + static_cast<int>(blockIdx.x) / (p.H * p.B)];
     const int *entries = p.list + (static_cast<size_t>(bm) * TP + pp) * p.T;
+    // The pair's key-tile count and first entry are read together, both right
+    // after its index (the row holds T entries, so entry 0 is in bounds even
+    // for an empty list).
+    const int cnt = p.cnt[static_cast<size_t>(bm) * TP + pp];
+    const int entry0 = entries[0];
     // key tiles; none after a bounded wait gave up anywhere
-    const int n = (*reinterpret_cast<volatile unsigned *>(&g_err_fwd) != 0)
-                      ? 0
-                      : p.cnt[static_cast<size_t>(bm) * TP + pp];
+    const int n = (*reinterpret_cast<volatile unsigned *>(&g_err_fwd) != 0) ? 0 : cnt;
     const uint64_t tmo = p.timeout_ns;
 
     if (threadIdx.x == 0) {
@@ -813,7 +816,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         if (n > 0) {  // both Q tiles before the CTA-wide barrier: latency overlaps the setup
             // a barrier per group: group 0's first S need not wait for Q_1;
             // issued Q_0, K_0, Q_1, V_0, in the order the first MMAs need them
-            const int key0 = (entries[0] >> 2) * TILE;
+            const int key0 = (entry0 >> 2) * TILE;
 #pragma unroll
             for (int g = 0; g < 2; ++g) {
                 mbar_arrive_expect_tx(&q_full[g], C::Q_BYTES);
@@ -1008,7 +1011,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         float m_ref = NEG_INF, l_sum = 0.f;
         bool failed = false;
         // The list entry of the next tile is read one tile ahead.
-        int entry_next = n > 0 ? entries[0] : 0;
+        int entry_next = entry0;
         for (int j = 0; j < n; ++j) {
             const int entry = entry_next;
             if (j + 1 < n) entry_next = entries[j + 1];
