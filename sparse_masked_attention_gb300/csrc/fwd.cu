@@ -1160,7 +1160,7 @@ cudaError_t launch_fwd(const Geometry &g, const Workspace &ws, const FwdArgs &a,
                        cudaStream_t st) {
     // <d, dv, key tile, softmax groups, S buffers per group, K / V ring stages>
     // d <= 128: a pair of query tiles per CTA, <d, dv, K / V ring stages>
-    if (g.d == 64 && g.dv == 64) return launch_pair<PairCfg<64, 64, 4, 4>>(g, ws, a, st);
+    if (g.d == 64 && g.dv == 64) return launch_pair<PairCfg<64, 64, 2, 2>>(g, ws, a, st);
     if (g.d == 128 && g.dv == 128) return launch_pair<PairCfg<128, 128, 2, 2>>(g, ws, a, st);
     if (g.d == 192 && g.dv == 128)
         return launch_cfg<FwdCfg<192, 128, 128, 2, 1, 2, 2>>(g, ws, a, st);
