@@ -1775,7 +1775,7 @@ cudaError_t launch_bwd(const Geometry &g, const Workspace &ws, const BwdArgs &a,
     if (fused_dq(g)) {
         // One key-side pass with dQ reduced into the fp32 buffer, then dQ out.
         rec.before(st);
-        e = g.d == 64 ? launch_dkdv<DkdvCfg<64, 64, 128, 3, true, true, 2, false, true>>(g, ws, a, st)
+        e = g.d == 64 ? launch_dkdv<DkdvCfg<64, 64, 128, 5, true, true, 2, false, true>>(g, ws, a, st)
                       : launch_dkdv<DkdvCfg<128, 128, 128, 3, true, true, 2, false, true>>(g, ws,
                                                                                             a, st);
         rec.after(st);
