@@ -1805,7 +1805,7 @@ cudaError_t launch_bwd(const Geometry &g, const Workspace &ws, const BwdArgs &a,
             g, ws, a, st, rec);
     if (g.d == 256 && g.dv == 256) {
         rec.before(st);
-        e = launch_dkdv<DkdvCfg<256, 256, 64, 3, false, true, 2>>(g, ws, a, st);
+        e = launch_dkdv<DkdvCfg<256, 256, 64, 2, false, true, 2>>(g, ws, a, st);
         rec.after(st);
         if (e != cudaSuccess) return e;
         return launch_pair<DkdvCfg<256, 256, 64, 3, true, false, 2, true>,
