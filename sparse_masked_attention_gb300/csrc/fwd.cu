@@ -79,6 +79,9 @@ struct FwdCfg {
     static_assert((KS - 1) * K_BYTES >= BM * DV * 2, "output tile staging aliases K stages 1..");
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
     static_assert(KS % NWG == 0 && VS % NWG == 0, "per-group ring stages");
+    // A V stage is freed only once the group has seen a later tile's S, so a
+    // single stage would wait on itself.
+    static_assert(VS >= 2, "ring depth");
 };
 
 // Row normalisation.  O_acc and the row sum l are relative to the row's
